@@ -1,0 +1,192 @@
+"""CPU oracle for the deterministic, batch-invariant BF16 GEMM.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import this package.  The
+product path (``deterministic_invariant_gemm_gb300``) never imports it and
+shares no code with it; the two meet only on inputs drawn from ``workloads``.
+
+The arithmetic lives in ``oracle.c`` (plain C, binary64); this module compiles
+it with gcc on first use and wraps it with ctypes.  Every function states the
+passage of the pages it follows in ``oracle.c``'s header:
+
+* :func:`gemm_rows` -- C_ij = sum_k A_ik B_kj in binary64, k ascending, plus
+  D_ij = sum_k |A_ik B_kj| (Tencent AI-infra article, "Batch Invariance の由来").
+* :func:`decode` / :func:`encode_rne` -- IEEE-754 binary16 / bfloat16 codecs
+  with round-to-nearest-even (same article, "背景": 2048 + 1 in FP16).
+* :func:`ulp` -- ULP(x) = 2^(E - M) (same section).
+* :func:`splitk_reduce_f32` -- the split-K workspace reduction in serial order
+  (same article, "Split-K").
+
+Pins (tests/test_oracle.py) tie each function to something other than itself:
+identity and permutation products, small-integer products checked against
+exact integer arithmetic, brute force with exact rationals, the FP16 worked
+example, exhaustive codec round trips and hand-computed binary32 sums.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import shutil
+import subprocess
+import tempfile
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+FMT_FP16 = 0
+FMT_BF16 = 1
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so beside it (gcc, OpenMP when present)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        raise RuntimeError("oracle: no C compiler (gcc) on PATH")
+    base = [cc, "-O2", "-std=c99", "-ffp-contract=off", "-fno-fast-math",
+            "-fPIC", "-shared"]
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_HERE)
+    os.close(fd)
+    try:
+        last = None
+        for extra in (["-fopenmp"], []):
+            r = subprocess.run(base + extra + ["-o", tmp, _SRC, "-lm"],
+                               capture_output=True, text=True)
+            if r.returncode == 0:
+                os.replace(tmp, _LIB)   # atomic: concurrent builders are safe
+                return _LIB
+            last = r.stderr
+        raise RuntimeError("oracle: gcc failed:\n" + (last or ""))
+    finally:
+        if os.path.exists(tmp):
+            os.unlink(tmp)
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB)
+    i64, u32, dbl = ctypes.c_int64, ctypes.c_uint32, ctypes.c_double
+    vp = ctypes.c_void_p
+    lib.oracle_decode.argtypes = [ctypes.c_int, u32]
+    lib.oracle_decode.restype = dbl
+    lib.oracle_encode_rne.argtypes = [ctypes.c_int, dbl]
+    lib.oracle_encode_rne.restype = u32
+    lib.oracle_ulp.argtypes = [ctypes.c_int, dbl]
+    lib.oracle_ulp.restype = dbl
+    lib.oracle_gemm_rows.argtypes = [vp, vp, i64, i64, i64, i64, i64, vp, i64, vp, vp]
+    lib.oracle_gemm_rows.restype = ctypes.c_int
+    lib.oracle_splitk_reduce_f32.argtypes = [vp, i64, i64, vp]
+    lib.oracle_splitk_reduce_f32.restype = ctypes.c_int
+    lib.oracle_decode_array.argtypes = [ctypes.c_int, vp, i64, vp]
+    lib.oracle_decode_array.restype = None
+    lib.oracle_encode_rne_array.argtypes = [ctypes.c_int, vp, i64, vp]
+    lib.oracle_encode_rne_array.restype = None
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _bits16(x) -> np.ndarray:
+    """Accept a numpy uint16/int16 array or a torch bf16/fp16 tensor (CPU)."""
+    if hasattr(x, "detach"):                     # torch tensor
+        import torch
+        t = x.detach()
+        if t.device.type != "cpu":
+            raise ValueError("oracle: inputs must live in host memory")
+        if t.dtype in (torch.bfloat16, torch.float16):
+            t = t.view(torch.int16)
+        x = t.contiguous().numpy()
+    a = np.ascontiguousarray(x)
+    if a.dtype == np.int16:
+        a = a.view(np.uint16)
+    if a.dtype != np.uint16:
+        raise TypeError("oracle: expected 16-bit patterns, got %s" % a.dtype)
+    return a
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def decode(fmt: int, bits) -> np.ndarray:
+    b = _bits16(np.asarray(bits, dtype=np.uint16) if not hasattr(bits, "detach") else bits)
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().oracle_decode_array(fmt, _ptr(b), b.size, _ptr(out))
+    return out
+
+
+def encode_rne(fmt: int, x) -> np.ndarray:
+    v = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.empty(v.shape, dtype=np.uint16)
+    _load().oracle_encode_rne_array(fmt, _ptr(v), v.size, _ptr(out))
+    return out
+
+
+def ulp(fmt: int, x: float) -> float:
+    return float(_load().oracle_ulp(fmt, float(x)))
+
+
+def fp16_add(a: float, b: float) -> float:
+    """a + b rounded once to binary16 (a, b themselves first rounded to binary16)."""
+    qa = decode(FMT_FP16, encode_rne(FMT_FP16, [a]))[0]
+    qb = decode(FMT_FP16, encode_rne(FMT_FP16, [b]))[0]
+    return float(decode(FMT_FP16, encode_rne(FMT_FP16, [qa + qb]))[0])
+
+
+def gemm_rows(A, B, M: int, N: int, K: int, lda: int | None = None,
+              ldb: int | None = None, rows=None):
+    """(C, D) for the selected rows of A (all rows when ``rows`` is None).
+
+    A: bf16 patterns [M, lda]; B: bf16 patterns [K, ldb].  Returns binary64
+    arrays C, D of shape [len(rows), N].
+    """
+    a = _bits16(A).reshape(-1)
+    b = _bits16(B).reshape(-1)
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    if rows is None:
+        r = None
+        nrows = M
+    else:
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = r.size
+    C = np.empty((nrows, N), dtype=np.float64)
+    D = np.empty((nrows, N), dtype=np.float64)
+    rc = _load().oracle_gemm_rows(_ptr(a), _ptr(b), M, N, K, lda, ldb,
+                                  None if r is None else _ptr(r), nrows,
+                                  _ptr(C), _ptr(D))
+    if rc != 0:
+        raise ValueError("oracle_gemm_rows: bad arguments")
+    return C, D
+
+
+def splitk_reduce_f32(W: np.ndarray) -> np.ndarray:
+    """Serial binary32 reduction over the leading axis of W ([S, ...])."""
+    w = np.ascontiguousarray(W, dtype=np.float32)
+    S = w.shape[0]
+    count = w.size // S
+    out = np.empty(w.shape[1:], dtype=np.float32)
+    rc = _load().oracle_splitk_reduce_f32(_ptr(w), S, count, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_splitk_reduce_f32: bad arguments")
+    return out
+
+
+def bf16_round(x) -> np.ndarray:
+    """Round binary64 values to bfloat16 (ties to even); returns binary64 values."""
+    return decode(FMT_BF16, encode_rne(FMT_BF16, x))

@@ -1,0 +1,236 @@
+/*
+ * oracle.c -- plain, slow, obviously correct CPU reference for the
+ * deterministic batch-invariant BF16 GEMM.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library
+ * and its Python binding) may include, link, load or call this file; only the
+ * tests, the package's smoke() check and the benchmark's CPU-baseline leg do.
+ * It shares no code, header, table or constant with the GPU path.
+ *
+ * What it computes, and the passage each function follows:
+ *
+ *   oracle_gemm_rows      C_ij = sum_{k=0}^{K-1} A_ik * B_kj, the plain
+ *                         definition of the matrix product (Tencent AI-infra
+ *                         article "腾讯エンジニア：大規模モデルの出力を確定させる
+ *                         ための AI インフラ手法", section "Batch Invariance の由来",
+ *                         and the i/j/k triple loop in "GEMM の最適化戦略"),
+ *                         evaluated in binary64 with k ascending.  Every
+ *                         bf16 x bf16 product is exact in binary64 (8 + 8 <= 53
+ *                         significand bits), so only the additions round.
+ *                         It also returns D_ij = sum_k |A_ik * B_kj|, the scale
+ *                         the error criterion |C - C_ref| <= 1e-5 * D uses.
+ *   oracle_decode         value of an IEEE-754 binary16 / bfloat16 bit pattern,
+ *                         written from the field definitions (sign, biased
+ *                         exponent, fraction; subnormals; inf/nan).
+ *   oracle_encode_rne     round a binary64 value to the nearest binary16 /
+ *                         bfloat16, ties to even (the rounding rule the same
+ *                         article's "背景" section applies to 2048 + 1 in FP16).
+ *   oracle_ulp            ULP(x) = 2^(E - M): E the unbiased exponent of x,
+ *                         M the number of stored fraction bits ("背景").
+ *   oracle_splitk_reduce_f32
+ *                         the split-K workspace reduction of the same article's
+ *                         "Split-K" section: out = w_0, then out = out + w_s for
+ *                         s = 1 .. S-1, every addition rounded to binary32
+ *                         (round to nearest even), in that serial order.
+ *
+ * Build: a C99 compiler with -O2 -ffp-contract=off (no fused multiply-add, no
+ * fast-math); OpenMP is optional and only splits the rows between threads --
+ * each output element is still one thread's serial loop.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* IEEE-754 small formats.  A format is (exponent bits, fraction bits):       */
+/*   binary16 (FP16): 5, 10     bfloat16 (BF16): 8, 7                         */
+/* ------------------------------------------------------------------------ */
+
+#define ORACLE_FMT_FP16 0
+#define ORACLE_FMT_BF16 1
+
+static void fmt_fields(int fmt, int *ebits, int *fbits) {
+    if (fmt == ORACLE_FMT_FP16) { *ebits = 5; *fbits = 10; }
+    else                        { *ebits = 8; *fbits = 7; }
+}
+
+/* Decode one bit pattern of the given format to its exact binary64 value. */
+double oracle_decode(int fmt, uint32_t bits) {
+    int ebits, fbits;
+    fmt_fields(fmt, &ebits, &fbits);
+    const uint32_t nbits = 1u + (uint32_t)ebits + (uint32_t)fbits;
+    bits &= (nbits == 32u) ? 0xFFFFFFFFu : ((1u << nbits) - 1u);
+    const uint32_t sign = (bits >> (ebits + fbits)) & 1u;
+    const uint32_t e = (bits >> fbits) & ((1u << ebits) - 1u);
+    const uint32_t f = bits & ((1u << fbits) - 1u);
+    const int bias = (1 << (ebits - 1)) - 1;
+    const uint32_t emax_field = (1u << ebits) - 1u;
+    double mag;
+    if (e == emax_field) {
+        mag = (f == 0) ? INFINITY : NAN;
+    } else if (e == 0) {
+        /* subnormal: 0.f * 2^(1 - bias) */
+        mag = ldexp((double)f, 1 - bias - fbits);
+    } else {
+        /* normal: 1.f * 2^(e - bias) */
+        mag = ldexp((double)((1u << fbits) | f), (int)e - bias - fbits);
+    }
+    return sign ? -mag : mag;
+}
+
+/* Round a binary64 value to the nearest representable value of the format,
+ * ties to even; overflow goes to infinity; NaN to the canonical quiet NaN. */
+uint32_t oracle_encode_rne(int fmt, double x) {
+    int ebits, fbits;
+    fmt_fields(fmt, &ebits, &fbits);
+    const int bias = (1 << (ebits - 1)) - 1;
+    const int emin = 1 - bias;          /* smallest normal exponent */
+    const int emax = bias;              /* largest finite exponent */
+    const uint32_t sign_bit = 1u << (ebits + fbits);
+    const uint32_t exp_all = ((1u << ebits) - 1u) << fbits;
+    if (isnan(x)) return exp_all | (1u << (fbits - 1));
+    const uint32_t sign = signbit(x) ? sign_bit : 0u;
+    double a = fabs(x);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return sign | exp_all;
+    /* a = fr * 2^ex with fr in [0.5, 1): the unbiased exponent is ex - 1 */
+    int ex;
+    (void)frexp(a, &ex);
+    int E = ex - 1;
+    if (E < emin) E = emin;             /* subnormal range shares emin's quantum */
+    /* quantum (one unit in the last place) of the binade [2^E, 2^(E+1)) */
+    const int qexp = E - fbits;
+    const double n = ldexp(a, -qexp);   /* exact: scaling by a power of two */
+    double r = floor(n);
+    const double rem = n - r;           /* exact: n and r share the binade */
+    if (rem > 0.5 || (rem == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+    /* r is an integer in [0, 2^(fbits+1)]; rounding up may carry into the
+     * next binade, which the re-normalisation below absorbs. */
+    if (r == 0.0) return sign;
+    double v = ldexp(r, qexp);
+    if (v >= ldexp(2.0 - ldexp(1.0, -fbits - 1), emax)) {
+        /* at or beyond the halfway point past the largest finite value */
+        return sign | exp_all;
+    }
+    (void)frexp(v, &ex);
+    int Ev = ex - 1;
+    if (Ev < emin) {
+        /* subnormal: fraction = v / 2^(emin - fbits), exponent field 0 */
+        const uint32_t f = (uint32_t)ldexp(v, -(emin - fbits));
+        return sign | f;
+    }
+    const uint32_t f = (uint32_t)(ldexp(v, -(Ev - fbits)) - ldexp(1.0, fbits));
+    return sign | ((uint32_t)(Ev + bias) << fbits) | f;
+}
+
+/* ULP(x) = 2^(E - M): E the unbiased exponent of |x| (clamped to the smallest
+ * normal exponent for subnormals), M the stored fraction bits of the format. */
+double oracle_ulp(int fmt, double x) {
+    int ebits, fbits;
+    fmt_fields(fmt, &ebits, &fbits);
+    const int emin = 2 - (1 << (ebits - 1));
+    double a = fabs(x);
+    int E = emin;
+    if (a != 0.0) {
+        int ex;
+        (void)frexp(a, &ex);
+        E = ex - 1;
+        if (E < emin) E = emin;
+    }
+    return ldexp(1.0, E - fbits);
+}
+
+/* ------------------------------------------------------------------------ */
+/* The matrix product.                                                        */
+/* ------------------------------------------------------------------------ */
+
+static double g_bf16_value[65536];
+static int g_bf16_ready = 0;
+
+static void bf16_table_init(void) {
+    if (g_bf16_ready) return;
+    for (uint32_t h = 0; h < 65536u; ++h) g_bf16_value[h] = oracle_decode(ORACLE_FMT_BF16, h);
+    g_bf16_ready = 1;
+}
+
+/*
+ * A: bf16 bit patterns, row-major [M][lda] (row i, column k at A[i*lda + k]).
+ * B: bf16 bit patterns, row-major [K][ldb] (row k, column j at B[k*ldb + j]).
+ * rows: the nrows row indices of A to evaluate (NULL: rows 0 .. nrows-1).
+ * C, D: binary64 outputs, [nrows][N] dense (row r of C holds row rows[r]).
+ *
+ * For every (i, j) the K terms are added to a binary64 accumulator that starts
+ * at +0.0, in ascending k.  The loop nest walks k outside j so that B is read
+ * row by row; that changes nothing about any single element's sum, whose
+ * terms still arrive in ascending k into its own accumulator.
+ *
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_gemm_rows(const uint16_t *A, const uint16_t *B,
+                     int64_t M, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldb,
+                     const int64_t *rows, int64_t nrows,
+                     double *C, double *D) {
+    if (M < 0 || N < 0 || K < 0 || nrows < 0) return -1;
+    if (nrows > 0 && N > 0 && (C == NULL || D == NULL)) return -1;
+    if (K > 0 && (lda < K || ldb < N)) return -1;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t i = rows ? rows[r] : r;
+        if (i < 0 || i >= M) return -1;
+    }
+    bf16_table_init();
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t i = rows ? rows[r] : r;
+        double *c = C + r * N;
+        double *d = D + r * N;
+        for (int64_t j = 0; j < N; ++j) { c[j] = 0.0; d[j] = 0.0; }
+        for (int64_t k = 0; k < K; ++k) {
+            const double a = g_bf16_value[A[i * lda + k]];
+            const uint16_t *brow = B + k * ldb;
+            for (int64_t j = 0; j < N; ++j) {
+                const double p = a * g_bf16_value[brow[j]];   /* exact */
+                c[j] = c[j] + p;
+                d[j] = d[j] + fabs(p);
+            }
+        }
+    }
+    return 0;
+}
+
+/* Serial split-K reduction in binary32: W is [S][count] dense; out[e] =
+ * (((W[0][e] + W[1][e]) + W[2][e]) + ...), each '+' one binary32 addition. */
+int oracle_splitk_reduce_f32(const float *W, int64_t S, int64_t count, float *out) {
+    if (S < 1 || count < 0) return -1;
+    for (int64_t e = 0; e < count; ++e) {
+        float acc = W[e];
+        for (int64_t s = 1; s < S; ++s) acc = acc + W[s * count + e];
+        out[e] = acc;
+    }
+    return 0;
+}
+
+/* Batch helpers for the Python side: decode / encode whole arrays. */
+void oracle_decode_array(int fmt, const uint16_t *bits, int64_t n, double *out) {
+    for (int64_t e = 0; e < n; ++e) out[e] = oracle_decode(fmt, bits[e]);
+}
+
+void oracle_encode_rne_array(int fmt, const double *x, int64_t n, uint16_t *out) {
+    for (int64_t e = 0; e < n; ++e) out[e] = (uint16_t)oracle_encode_rne(fmt, x[e]);
+}
+
+/* Threads the row loop may use (1 without OpenMP). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
