@@ -1,0 +1,266 @@
+"""Deterministic, batch-invariant BF16 GEMM for NVIDIA GB300 (sm_103a).
+
+A thin ctypes binding over ``libbigemm.so`` (declared in ``include/bigemm.h``).
+Every computation runs in that library's CUDA kernels; this module only turns
+torch tensors (or raw integers) into pointers, sizes and a stream handle, and
+uses torch to allocate outputs and workspaces.  There is no fallback: if the
+library is missing or the device is not sm_103, calls raise.
+
+The operation is C = A * B with A [M, K] and B [K, N] in bf16 and FP32
+accumulation; row i of C is bit-for-bit a function of (row i of A, B, K,
+split_k, output dtype) only -- independent of M, of the rest of the batch and
+of the run (Tencent AI-infra article "腾讯エンジニア：大規模モデルの出力を確定
+させるための AI インフラ手法", sections "Batch Invariance の由来" and "Split-K").
+
+Low-level functions keep the C names and argument order::
+
+    bigemm_run(A, B, C, M, N, K, lda, ldb, ldc, split_k, workspace, workspace_bytes, stream)
+
+where the pointer arguments accept a torch tensor, an integer address or None
+and ``stream`` accepts a ``torch.cuda.Stream``, an integer handle or None (the
+current torch stream).  :func:`matmul` is the convenience wrapper.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH, build as build_library  # noqa: F401
+
+__all__ = [
+    "BigemmError", "load", "library_path", "BLOCK_K", "TILE_M", "TILE_N",
+    "bigemm_version", "bigemm_status_string", "bigemm_max_split_k",
+    "bigemm_default_split_k", "bigemm_effective_split_k", "bigemm_workspace_ld",
+    "bigemm_workspace_bytes", "bigemm_partial_workspace_bytes", "bigemm_run",
+    "bigemm_run_bf16out", "bigemm_run_partial", "bigemm_splitk_reduce",
+    "bigemm_run_atomic_splitk", "bigemm_device_status", "bigemm_last_launch_count",
+    "matmul", "EXPORTED_SYMBOLS",
+]
+
+BLOCK_K = 64
+TILE_M = 128
+TILE_N = 256
+
+STATUS_NAMES = {
+    0: "BIGEMM_OK", 1: "BIGEMM_ERR_ARG", 2: "BIGEMM_ERR_ALIGN", 3: "BIGEMM_ERR_WORKSPACE",
+    4: "BIGEMM_ERR_UNSUPPORTED", 5: "BIGEMM_ERR_CUDA", 6: "BIGEMM_ERR_TIMEOUT",
+}
+
+EXPORTED_SYMBOLS = (
+    "bigemm_version", "bigemm_status_string", "bigemm_max_split_k", "bigemm_default_split_k",
+    "bigemm_effective_split_k", "bigemm_workspace_ld", "bigemm_workspace_bytes",
+    "bigemm_partial_workspace_bytes", "bigemm_run", "bigemm_run_bf16out", "bigemm_run_partial",
+    "bigemm_splitk_reduce", "bigemm_run_atomic_splitk", "bigemm_device_status",
+    "bigemm_last_launch_count",
+)
+
+
+class BigemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__("%s: %s" % (where, bigemm_status_string(status)))
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load():
+    """Load libbigemm.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            "libbigemm.so is not built; run `python -m deterministic_invariant_gemm_gb300.build` "
+            "(needs nvcc) -- there is no fallback implementation")
+    lib = ctypes.CDLL(LIB_PATH)
+    i64, vp, i32, sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "bigemm_version": ([], i32),
+        "bigemm_status_string": ([i32], ctypes.c_char_p),
+        "bigemm_max_split_k": ([i64], i32),
+        "bigemm_default_split_k": ([i64], i32),
+        "bigemm_effective_split_k": ([i64, i32], i32),
+        "bigemm_workspace_ld": ([i64], i64),
+        "bigemm_workspace_bytes": ([i64, i64, i64, i32], sz),
+        "bigemm_partial_workspace_bytes": ([i64, i64, i64, i32], sz),
+        "bigemm_run": ([vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, vp, sz, vp], i32),
+        "bigemm_run_bf16out": ([vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, vp, sz, vp], i32),
+        "bigemm_run_partial": ([vp, vp, i64, i64, i64, i64, i64, i32, vp, sz, vp], i32),
+        "bigemm_splitk_reduce": ([vp, i32, i64, i64, vp, i64, i32, vp], i32),
+        "bigemm_run_atomic_splitk": ([vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, vp], i32),
+        "bigemm_device_status": ([i32], i32),
+        "bigemm_last_launch_count": ([], i32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+# ------------------------------------------------------------ marshalling --
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr())
+    raise TypeError("expected a tensor, an integer address or None, got %r" % type(x))
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(s, int):
+        return s
+    if hasattr(s, "cuda_stream"):
+        return int(s.cuda_stream)
+    raise TypeError("expected a torch.cuda.Stream, an integer handle or None")
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise BigemmError(status, where)
+
+
+# ------------------------------------------------------ C functions, same names --
+
+def bigemm_version() -> int:
+    return int(load().bigemm_version())
+
+
+def bigemm_status_string(status: int) -> str:
+    if _lib is None and not os.path.exists(LIB_PATH):
+        return STATUS_NAMES.get(int(status), "BIGEMM_ERR_UNKNOWN")
+    return load().bigemm_status_string(int(status)).decode()
+
+
+def bigemm_max_split_k(K: int) -> int:
+    return int(load().bigemm_max_split_k(K))
+
+
+def bigemm_default_split_k(K: int) -> int:
+    return int(load().bigemm_default_split_k(K))
+
+
+def bigemm_effective_split_k(K: int, split_k: int) -> int:
+    return int(load().bigemm_effective_split_k(K, split_k))
+
+
+def bigemm_workspace_ld(N: int) -> int:
+    return int(load().bigemm_workspace_ld(N))
+
+
+def bigemm_workspace_bytes(M: int, N: int, K: int, split_k: int) -> int:
+    return int(load().bigemm_workspace_bytes(M, N, K, split_k))
+
+
+def bigemm_partial_workspace_bytes(M: int, N: int, K: int, split_k: int) -> int:
+    return int(load().bigemm_partial_workspace_bytes(M, N, K, split_k))
+
+
+def bigemm_run(A, B, C, M, N, K, lda, ldb, ldc, split_k, workspace=None, workspace_bytes=0,
+               stream=None, check=True) -> int:
+    st = load().bigemm_run(_ptr(A), _ptr(B), _ptr(C), M, N, K, lda, ldb, ldc, split_k,
+                           _ptr(workspace), workspace_bytes, _stream(stream))
+    if check:
+        _check(st, "bigemm_run")
+    return st
+
+
+def bigemm_run_bf16out(A, B, C, M, N, K, lda, ldb, ldc, split_k, workspace=None,
+                       workspace_bytes=0, stream=None, check=True) -> int:
+    st = load().bigemm_run_bf16out(_ptr(A), _ptr(B), _ptr(C), M, N, K, lda, ldb, ldc, split_k,
+                                   _ptr(workspace), workspace_bytes, _stream(stream))
+    if check:
+        _check(st, "bigemm_run_bf16out")
+    return st
+
+
+def bigemm_run_partial(A, B, M, N, K, lda, ldb, split_k, workspace, workspace_bytes,
+                       stream=None, check=True) -> int:
+    st = load().bigemm_run_partial(_ptr(A), _ptr(B), M, N, K, lda, ldb, split_k,
+                                   _ptr(workspace), workspace_bytes, _stream(stream))
+    if check:
+        _check(st, "bigemm_run_partial")
+    return st
+
+
+def bigemm_splitk_reduce(workspace, splits, M, N, C, ldc, c_is_bf16, stream=None,
+                         check=True) -> int:
+    st = load().bigemm_splitk_reduce(_ptr(workspace), splits, M, N, _ptr(C), ldc,
+                                     int(bool(c_is_bf16)), _stream(stream))
+    if check:
+        _check(st, "bigemm_splitk_reduce")
+    return st
+
+
+def bigemm_run_atomic_splitk(A, B, C, M, N, K, lda, ldb, ldc, split_k, stream=None,
+                             check=True) -> int:
+    st = load().bigemm_run_atomic_splitk(_ptr(A), _ptr(B), _ptr(C), M, N, K, lda, ldb, ldc,
+                                         split_k, _stream(stream))
+    if check:
+        _check(st, "bigemm_run_atomic_splitk")
+    return st
+
+
+def bigemm_device_status(reset: bool = True) -> int:
+    return int(load().bigemm_device_status(int(bool(reset))))
+
+
+def bigemm_last_launch_count() -> int:
+    return int(load().bigemm_last_launch_count())
+
+
+# ----------------------------------------------------------- convenience --
+
+def matmul(A, B, out_dtype=None, split_k: int = 1, out=None, workspace=None, stream=None,
+           atomic: bool = False):
+    """C = A @ B for bf16 CUDA tensors A [M, K] and B [K, N] (row-major, unit
+    column stride; leading dimensions may be padded).  ``out_dtype`` is
+    torch.float32 (default) or torch.bfloat16.  ``split_k``: 1 = none, 0 = the
+    K-only default, S > 1 = S segments through a workspace (allocated here
+    with torch when not given).  ``atomic=True`` runs the nondeterministic
+    atomic-add contrast instead (fp32 only)."""
+    import torch
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("A and B must be bfloat16")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError("shapes do not compose: %s x %s" % (tuple(A.shape), tuple(B.shape)))
+    if A.stride(1) != 1 or B.stride(1) != 1:
+        raise ValueError("A and B need unit column stride (row-major)")
+    out_dtype = torch.float32 if out_dtype is None else out_dtype
+    M, K = A.shape
+    N = B.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    if out.dtype != out_dtype or out.stride(1) != 1 or tuple(out.shape) != (M, N):
+        raise ValueError("bad output tensor")
+    lda = A.stride(0) if M > 1 else max(K, 8 * ((K + 7) // 8))
+    ldb = B.stride(0) if K > 1 else max(N, 8 * ((N + 7) // 8))
+    ldc = out.stride(0) if M > 1 else max(N, 8 * ((N + 7) // 8))
+    if atomic:
+        if out_dtype != torch.float32:
+            raise ValueError("the atomic contrast writes fp32")
+        bigemm_run_atomic_splitk(A, B, out, M, N, K, lda, ldb, ldc, split_k, stream)
+        return out
+    need = bigemm_workspace_bytes(M, N, K, split_k)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=A.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if out_dtype == torch.float32:
+        bigemm_run(A, B, out, M, N, K, lda, ldb, ldc, split_k, workspace, wbytes, stream)
+    elif out_dtype == torch.bfloat16:
+        bigemm_run_bf16out(A, B, out, M, N, K, lda, ldb, ldc, split_k, workspace, wbytes, stream)
+    else:
+        raise TypeError("out_dtype must be float32 or bfloat16")
+    return out

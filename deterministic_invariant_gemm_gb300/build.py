@@ -1,0 +1,68 @@
+"""Build step for libbigemm.so (sm_103a), in-tree.
+
+    python -m deterministic_invariant_gemm_gb300.build [--force]
+
+Compiles ``csrc/bigemm.cu`` with nvcc for ``sm_103a`` only and writes
+``libbigemm.so`` beside this file.  The output is replaced atomically, so
+concurrent builders never observe a half-written library.
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+import tempfile
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(HERE, "csrc")
+LIB_PATH = os.path.join(HERE, "libbigemm.so")
+INCLUDE = os.path.join(os.path.dirname(HERE), "include")
+
+SOURCES = [os.path.join(CSRC, "bigemm.cu")]
+DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("kernels.cuh", "ptx.cuh")] + \
+    [os.path.join(INCLUDE, "bigemm.h")]
+
+NVCC_FLAGS = [
+    "-gencode", "arch=compute_103a,code=sm_103a",
+    "-O3", "-lineinfo", "-std=c++17",
+    "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+    "-shared",
+]
+
+
+def nvcc_path() -> str:
+    for cand in (shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libbigemm.so")
+
+
+def up_to_date() -> bool:
+    if not os.path.exists(LIB_PATH):
+        return False
+    t = os.path.getmtime(LIB_PATH)
+    return all(os.path.getmtime(d) <= t for d in DEPENDS if os.path.exists(d))
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    if not force and up_to_date():
+        return LIB_PATH
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=HERE)
+    os.close(fd)
+    try:
+        cmd = [nvcc_path()] + NVCC_FLAGS + ["-o", tmp] + SOURCES
+        if verbose:
+            print(" ".join(cmd), flush=True)
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("nvcc failed building libbigemm.so:\n" + r.stdout + r.stderr)
+        os.replace(tmp, LIB_PATH)
+    finally:
+        if os.path.exists(tmp):
+            os.unlink(tmp)
+    return LIB_PATH
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose=True))

@@ -1,0 +1,405 @@
+// bigemm.cu -- host side of libbigemm.so: argument checks, tensor-map
+// encoding, launches, and the C ABI declared in include/bigemm.h.
+//
+// The library allocates no device memory and never synchronises (except in
+// bigemm_device_status, which exists to read the device error word).
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/bigemm.h"
+#include "kernels.cuh"
+
+namespace bigemm {
+
+// Device-side error word: bits set by a kernel whose bounded wait expired.
+__device__ unsigned g_device_status = 0;
+
+static_assert(kBK == BIGEMM_BLOCK_K, "header and kernel disagree on BLOCK_K");
+static_assert(kBM == BIGEMM_TILE_M && kBN == BIGEMM_TILE_N, "header and kernel disagree on tiles");
+
+namespace {
+
+thread_local int g_last_launches = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int sm_count = 0;
+    unsigned* status = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Per-device set-up with that device current: capability check, the shared
+// memory opt-in of every kernel, and the address of the device error word.
+bigemm_status device_info(const DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BIGEMM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return BIGEMM_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return BIGEMM_ERR_CUDA;
+        d.supported = (major == 10 && minor == 3);
+        d.sm_count = sms;
+        if (d.supported) {
+            const int smem = static_cast<int>(kSmemBytes);
+            if (cudaFuncSetAttribute(bigemm_tc_kernel<kOutF32>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+                cudaFuncSetAttribute(bigemm_tc_kernel<kOutBF16>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+                cudaFuncSetAttribute(bigemm_tc_kernel<kOutSlices>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+                cudaFuncSetAttribute(bigemm_tc_kernel<kOutAtomic>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+                return BIGEMM_ERR_CUDA;
+            void* sym = nullptr;
+            if (cudaGetSymbolAddress(&sym, g_device_status) != cudaSuccess) return BIGEMM_ERR_CUDA;
+            d.status = static_cast<unsigned*>(sym);
+        }
+        d.ready = true;
+    }
+    if (!d.supported) return BIGEMM_ERR_UNSUPPORTED;
+    *out = &d;
+    return BIGEMM_OK;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int max_split(int64_t K) {
+    if (K <= 0) return 1;
+    const int64_t kb = ceil_div(K, kBK);
+    return kb > INT_MAX ? INT_MAX : static_cast<int>(kb);
+}
+
+int default_split(int64_t K) {
+    int64_t cap = K / 512;
+    if (cap > 16) cap = 16;
+    int s = 1;
+    while (2 * s <= cap) s *= 2;
+    return s;
+}
+
+// Effective split and blocks per segment; 0 when split_k is invalid.
+int effective_split(int64_t K, int split_k, int* blocks_per_split) {
+    if (K < 0) return 0;
+    if (split_k == 0) split_k = default_split(K);
+    if (split_k < 1 || split_k > max_split(K)) return 0;
+    if (K == 0) {
+        if (blocks_per_split) *blocks_per_split = 0;
+        return 1;
+    }
+    const int64_t kb = ceil_div(K, kBK);
+    const int64_t L = ceil_div(kb, split_k);
+    if (blocks_per_split) *blocks_per_split = static_cast<int>(L);
+    return static_cast<int>(ceil_div(kb, L));
+}
+
+int64_t ws_ld_of(int64_t N) { return ceil_div(N, 4) * 4; }
+
+// Bytes of `slices` workspace slices, or SIZE_MAX on overflow.
+size_t slice_bytes(int64_t M, int64_t N, int slices) {
+    const unsigned __int128 b = static_cast<unsigned __int128>(slices) *
+                                static_cast<unsigned __int128>(M) *
+                                static_cast<unsigned __int128>(ws_ld_of(N)) * 4u;
+    if (b > static_cast<unsigned __int128>(SIZE_MAX)) return SIZE_MAX;
+    return static_cast<size_t>(b);
+}
+
+bool encode_bf16_2d(CUtensorMap* map, const void* ptr, int64_t inner, int64_t outer, int64_t ld,
+                    uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+enum Mode { kModeF32, kModeBF16, kModePartial, kModeAtomic };
+
+bigemm_status launch_reduce(const DeviceInfo& d, const float* ws, int splits, int64_t M, int64_t N,
+                            void* C, int64_t ldc, bool bf16, cudaStream_t stream) {
+    const int64_t ws_ld = ws_ld_of(N);
+    const int64_t items = M * (ws_ld / 4);
+    int64_t blocks = ceil_div(items, 256);
+    const int64_t cap = static_cast<int64_t>(d.sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    cudaError_t e;
+    if (bf16)
+        e = launch_pdl(splitk_reduce_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                       stream, ws, C, static_cast<int>(M), static_cast<int>(N), ldc, ws_ld, splits);
+    else
+        e = launch_pdl(splitk_reduce_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                       stream, ws, C, static_cast<int>(M), static_cast<int>(N), ldc, ws_ld, splits);
+    return e == cudaSuccess ? BIGEMM_OK : BIGEMM_ERR_CUDA;
+}
+
+bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t M, int64_t N,
+                       int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int split_k, void* ws,
+                       size_t ws_bytes, cudaStream_t stream) {
+    g_last_launches = 0;
+    // ---- sizes and the split
+    if (M < 0 || N < 0 || K < 0) return BIGEMM_ERR_ARG;
+    if (M > INT_MAX || N > INT_MAX || K > INT_MAX) return BIGEMM_ERR_ARG;
+    int kb_per_split = 0;
+    const int splits = effective_split(K, split_k, &kb_per_split);
+    if (splits == 0) return BIGEMM_ERR_ARG;
+    const bool want_c = (mode != kModePartial);
+    // ---- pointers and strides (checked even for empty products)
+    if (K > 0 && (A == nullptr || B == nullptr)) return BIGEMM_ERR_ARG;
+    if (K > 0 && (lda < K || ldb < N)) return BIGEMM_ERR_ARG;
+    if (want_c && (C == nullptr || ldc < N)) return BIGEMM_ERR_ARG;
+    if (K > 0 && (!aligned16(A) || !aligned16(B) || lda % 8 != 0 || ldb % 8 != 0))
+        return BIGEMM_ERR_ALIGN;
+    if (want_c) {
+        if (!aligned16(C)) return BIGEMM_ERR_ALIGN;
+        if (ldc % (mode == kModeBF16 ? 8 : 4) != 0) return BIGEMM_ERR_ALIGN;
+    }
+    // ---- workspace
+    const bool need_ws = (mode == kModePartial) || ((mode == kModeF32 || mode == kModeBF16) && splits > 1);
+    if (need_ws) {
+        const size_t need = slice_bytes(M, N, splits);
+        if (need == SIZE_MAX) return BIGEMM_ERR_ARG;
+        if (need > 0 && (ws == nullptr || !aligned16(ws) || ws_bytes < need))
+            return BIGEMM_ERR_WORKSPACE;
+    }
+    if (M == 0 || N == 0) return BIGEMM_OK;
+    const int64_t m_tiles = ceil_div(M, kBM);
+    const int64_t n_tiles = ceil_div(N, kBN);
+    const int64_t units = m_tiles * n_tiles * splits;
+    if (units > INT_MAX) return BIGEMM_ERR_ARG;
+
+    const DeviceInfo* d = nullptr;
+    bigemm_status st = device_info(&d);
+    if (st != BIGEMM_OK) return st;
+
+    // ---- K == 0: the empty sum is +0.0 everywhere
+    if (K == 0) {
+        cudaError_t e;
+        if (mode == kModePartial) {
+            e = cudaMemsetAsync(ws, 0, slice_bytes(M, N, 1), stream);
+        } else {
+            const size_t es = (mode == kModeBF16) ? 2 : 4;
+            e = cudaMemset2DAsync(C, static_cast<size_t>(ldc) * es, 0, static_cast<size_t>(N) * es,
+                                  static_cast<size_t>(M), stream);
+        }
+        return e == cudaSuccess ? BIGEMM_OK : BIGEMM_ERR_CUDA;
+    }
+
+    CUtensorMap tmA, tmB;
+    if (!encode_bf16_2d(&tmA, A, K, M, lda, kBK, kBM)) return BIGEMM_ERR_CUDA;
+    if (!encode_bf16_2d(&tmB, B, N, K, ldb, kBChunkCols, kBK)) return BIGEMM_ERR_CUDA;
+
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.status = d->status;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.m_tiles = static_cast<int>(m_tiles);
+    p.n_tiles = static_cast<int>(n_tiles);
+    p.splits = splits;
+    p.kb_total = static_cast<int>(ceil_div(K, kBK));
+    p.kb_per_split = kb_per_split;
+    p.units = static_cast<int>(units);
+
+    const int grid = static_cast<int>(units < d->sm_count ? units : d->sm_count);
+    const dim3 g(static_cast<unsigned>(grid)), blk(kNumThreads);
+    cudaError_t e = cudaSuccess;
+    int launches = 0;
+
+    if (mode == kModeAtomic) {
+        e = cudaMemset2DAsync(C, static_cast<size_t>(ldc) * 4, 0, static_cast<size_t>(N) * 4,
+                              static_cast<size_t>(M), stream);
+        if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
+        p.out = C;
+        p.ld_out = ldc;
+        e = launch_pdl(bigemm_tc_kernel<kOutAtomic>, g, blk, kSmemBytes, stream, tmA, tmB, p);
+        launches = 1;
+    } else if (mode == kModePartial || splits > 1) {
+        p.out = ws;
+        p.ld_out = ws_ld_of(N);
+        p.slice_stride = M * p.ld_out;
+        e = launch_pdl(bigemm_tc_kernel<kOutSlices>, g, blk, kSmemBytes, stream, tmA, tmB, p);
+        launches = 1;
+        if (e == cudaSuccess && mode != kModePartial) {
+            st = launch_reduce(*d, static_cast<const float*>(ws), splits, M, N, C, ldc,
+                               mode == kModeBF16, stream);
+            if (st != BIGEMM_OK) return st;
+            launches = 2;
+        }
+    } else {
+        p.out = C;
+        p.ld_out = ldc;
+        if (mode == kModeBF16)
+            e = launch_pdl(bigemm_tc_kernel<kOutBF16>, g, blk, kSmemBytes, stream, tmA, tmB, p);
+        else
+            e = launch_pdl(bigemm_tc_kernel<kOutF32>, g, blk, kSmemBytes, stream, tmA, tmB, p);
+        launches = 1;
+    }
+    if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
+    g_last_launches = launches;
+    return BIGEMM_OK;
+}
+
+}  // namespace
+}  // namespace bigemm
+
+using namespace bigemm;
+
+extern "C" {
+
+int bigemm_version(void) { return (0 << 16) | 1; }
+
+const char* bigemm_status_string(bigemm_status s) {
+    switch (s) {
+        case BIGEMM_OK: return "BIGEMM_OK";
+        case BIGEMM_ERR_ARG: return "BIGEMM_ERR_ARG: invalid size, pointer, leading dimension or split_k";
+        case BIGEMM_ERR_ALIGN: return "BIGEMM_ERR_ALIGN: pointer or leading dimension not aligned";
+        case BIGEMM_ERR_WORKSPACE: return "BIGEMM_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        case BIGEMM_ERR_UNSUPPORTED: return "BIGEMM_ERR_UNSUPPORTED: current device is not sm_103";
+        case BIGEMM_ERR_CUDA: return "BIGEMM_ERR_CUDA: a CUDA call failed";
+        case BIGEMM_ERR_TIMEOUT: return "BIGEMM_ERR_TIMEOUT: a kernel's bounded wait expired";
+    }
+    return "BIGEMM_ERR_UNKNOWN";
+}
+
+int bigemm_max_split_k(int64_t K) { return K < 0 ? 0 : max_split(K); }
+
+int bigemm_default_split_k(int64_t K) { return K < 0 ? 0 : default_split(K); }
+
+int bigemm_effective_split_k(int64_t K, int split_k) { return effective_split(K, split_k, nullptr); }
+
+int64_t bigemm_workspace_ld(int64_t N) { return N < 0 ? 0 : ws_ld_of(N); }
+
+size_t bigemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {
+    if (M < 0 || N < 0) return 0;
+    const int s = effective_split(K, split_k, nullptr);
+    if (s <= 1) return 0;
+    return slice_bytes(M, N, s);
+}
+
+size_t bigemm_partial_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {
+    if (M < 0 || N < 0) return 0;
+    const int s = effective_split(K, split_k, nullptr);
+    if (s < 1) return 0;
+    return slice_bytes(M, N, s);
+}
+
+bigemm_status bigemm_run(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
+                         int64_t lda, int64_t ldb, int64_t ldc, int split_k, void* workspace,
+                         size_t workspace_bytes, bigemm_stream stream) {
+    return run_impl(kModeF32, A, B, C, M, N, K, lda, ldb, ldc, split_k, workspace, workspace_bytes,
+                    static_cast<cudaStream_t>(stream));
+}
+
+bigemm_status bigemm_run_bf16out(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                                 int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int split_k,
+                                 void* workspace, size_t workspace_bytes, bigemm_stream stream) {
+    return run_impl(kModeBF16, A, B, C, M, N, K, lda, ldb, ldc, split_k, workspace, workspace_bytes,
+                    static_cast<cudaStream_t>(stream));
+}
+
+bigemm_status bigemm_run_partial(const void* A, const void* B, int64_t M, int64_t N, int64_t K,
+                                 int64_t lda, int64_t ldb, int split_k, void* workspace,
+                                 size_t workspace_bytes, bigemm_stream stream) {
+    return run_impl(kModePartial, A, B, nullptr, M, N, K, lda, ldb, 0, split_k, workspace,
+                    workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+bigemm_status bigemm_splitk_reduce(const float* workspace, int splits, int64_t M, int64_t N, void* C,
+                                   int64_t ldc, int c_is_bf16, bigemm_stream stream) {
+    g_last_launches = 0;
+    if (M < 0 || N < 0 || M > INT_MAX || N > INT_MAX || splits < 1) return BIGEMM_ERR_ARG;
+    if (M == 0 || N == 0) return BIGEMM_OK;
+    if (workspace == nullptr || C == nullptr || ldc < N) return BIGEMM_ERR_ARG;
+    if (!aligned16(workspace) || !aligned16(C)) return BIGEMM_ERR_ALIGN;
+    if (ldc % (c_is_bf16 ? 8 : 4) != 0) return BIGEMM_ERR_ALIGN;
+    if (slice_bytes(M, N, splits) == SIZE_MAX) return BIGEMM_ERR_ARG;
+    const DeviceInfo* d = nullptr;
+    bigemm_status st = device_info(&d);
+    if (st != BIGEMM_OK) return st;
+    st = launch_reduce(*d, workspace, splits, M, N, C, ldc, c_is_bf16 != 0,
+                       static_cast<cudaStream_t>(stream));
+    if (st == BIGEMM_OK) g_last_launches = 1;
+    return st;
+}
+
+bigemm_status bigemm_run_atomic_splitk(const void* A, const void* B, float* C, int64_t M, int64_t N,
+                                       int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int split_k,
+                                       bigemm_stream stream) {
+    return run_impl(kModeAtomic, A, B, C, M, N, K, lda, ldb, ldc, split_k, nullptr, 0,
+                    static_cast<cudaStream_t>(stream));
+}
+
+bigemm_status bigemm_device_status(int reset) {
+    const DeviceInfo* d = nullptr;
+    bigemm_status st = device_info(&d);
+    if (st != BIGEMM_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return BIGEMM_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(v)) != cudaSuccess) return BIGEMM_ERR_CUDA;
+    if (reset && v != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero)) != cudaSuccess)
+            return BIGEMM_ERR_CUDA;
+    }
+    return v ? BIGEMM_ERR_TIMEOUT : BIGEMM_OK;
+}
+
+int bigemm_last_launch_count(void) { return g_last_launches; }
+
+}  // extern "C"

@@ -1,0 +1,421 @@
+// kernels.cuh -- the device side of the deterministic, batch-invariant BF16 GEMM.
+//
+// Work decomposition (Tencent AI-infra article "腾讯エンジニア：大規模モデルの出力を
+// 確定させるための AI インフラ手法"):
+//   * "Tiling": one work unit computes a kBM x kBN tile of C over one K segment;
+//     its accumulator lives in tensor memory (TMEM) and is fed by a K loop in
+//     fixed steps of kBK = 64, each step four tcgen05.mma of K = 16, in
+//     ascending k.
+//   * "Split-K": with S > 1 segments the K blocks are dealt into S contiguous
+//     segments; each unit writes its FP32 partial to workspace slice s with plain
+//     stores, and splitk_reduce_kernel adds the slices in the order 0..S-1.
+//   * "GROUP_M - Swizzle L2 Cache": units are ordered in groups of kGroupM tile
+//     rows; a persistent grid of at most one CTA per SM takes units
+//     blockIdx.x, blockIdx.x + gridDim.x, ... -- a static schedule.
+// None of the three changes the order in which any single C element's terms
+// are added, so the bits of row i depend only on (row i of A, B, K, S).  The
+// same MMA instruction shape (M = 128, N = 256, K = 16) and operand roles are
+// used for every M: short batches are padded by the TMA unit's zero fill, never
+// served by a different code path.
+//
+// CTA roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer: fills a kStages-deep shared-memory ring.
+//   warp 1      allocates TMEM; one lane issues the MMAs and commits.
+//   warps 2..5  epilogue: TMEM -> registers -> global, one C row per thread;
+//               two TMEM accumulators let the epilogue of tile t overlap the
+//               mainloop of tile t + 1.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace bigemm {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kUmmaK = 16;
+constexpr int kStages = 4;
+constexpr int kAccStages = 2;
+constexpr int kGroupM = 8;
+constexpr int kTmemCols = kAccStages * kBN;  // 512: all of TMEM, one CTA per SM
+constexpr int kNumThreads = 192;
+constexpr int kEpilogueThreads = 128;
+
+constexpr uint32_t kABytes = kBM * kBK * 2;       // 16 KiB: 128 rows x 128 B
+constexpr uint32_t kBChunkCols = 64;              // one 128-byte swizzle span of N
+constexpr uint32_t kBChunkBytes = kBK * kBChunkCols * 2;  // 8 KiB: 64 k-rows x 128 B
+constexpr uint32_t kBBytes = kBK * kBN * 2;       // 32 KiB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr int kNumBarriers = 2 * kStages + 2 * kAccStages + 1;
+constexpr uint32_t kSmemBytes =
+    1024 /* alignment slack */ + kStages * kStageBytes + kNumBarriers * 8 + 16;
+
+constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, /*A MN-major*/ false, /*B MN-major*/ true);
+
+// A wait that gives up: 2 s of global time, checked every 256 polls.
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+// Bits of the device error word.
+constexpr unsigned kErrWaitProducer = 1u;
+constexpr unsigned kErrWaitMma = 2u;
+constexpr unsigned kErrWaitEpilogue = 4u;
+constexpr unsigned kErrWaitDrain = 8u;
+
+enum OutKind : int {
+    kOutF32 = 0,     // C fp32, plain stores
+    kOutBF16 = 1,    // C bf16 (round to nearest even), plain stores
+    kOutSlices = 2,  // fp32 split-K partial to workspace slice `seg`
+    kOutAtomic = 3,  // fp32 atomic add into C (nondeterministic contrast)
+};
+
+struct GemmParams {
+    void* out;              // C, or the workspace for kOutSlices
+    int64_t ld_out;         // row stride of `out`, elements
+    int64_t slice_stride;   // elements between workspace slices (M * ld_out)
+    unsigned* status;       // device error word
+    int M, N;
+    int m_tiles, n_tiles;
+    int splits;             // effective number of K segments
+    int kb_total;           // ceil(K / kBK)
+    int kb_per_split;       // K blocks per segment
+    int units;              // m_tiles * n_tiles * splits
+};
+
+// Unit u -> (tile row, tile column, K segment).  Segments of one tile are
+// adjacent; tiles follow the GROUP_M swizzle: groups of kGroupM tile rows,
+// column-major inside a group.
+__device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& mt, int& nt,
+                                            int& seg) {
+    const int tile = u / p.splits;
+    seg = u - tile * p.splits;
+    const int per_group = kGroupM * p.n_tiles;
+    const int g = tile / per_group;
+    const int first_m = g * kGroupM;
+    const int gm = min(p.m_tiles - first_m, kGroupM);
+    const int r = tile - g * per_group;
+    mt = first_m + r % gm;
+    nt = r / gm;
+}
+
+// Bounded wait on an mbarrier phase.  Gives up when another role has aborted
+// (shared flag) or after kWaitTimeoutNs; a timeout raises the abort flag and
+// records `why` in the device error word.  Never traps.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag, unsigned* status,
+                                             unsigned why, bool honour_abort = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1; it != 0u; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0u) {
+            if (honour_abort && *abort_flag) return false;
+            if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
+        }
+    }
+    *abort_flag = 1;
+    atomicOr(status, why);
+    return false;
+}
+
+template <int kOut>
+__device__ __forceinline__ void store_row_chunk(const GemmParams& p, int seg, int row, int col,
+                                                const uint32_t (&r)[32]) {
+    const int valid = min(32, p.N - col);
+    if constexpr (kOut == kOutBF16) {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.ld_out + col;
+        if (valid == 32) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                uint32_t w[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[8 * v + 2 * h]),
+                                                              __uint_as_float(r[8 * v + 2 * h + 1]));
+                    w[h] = *reinterpret_cast<uint32_t*>(&b2);
+                }
+                d4[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                if (c < valid) dst[c] = __float2bfloat16_rn(__uint_as_float(r[c]));
+        }
+    } else if constexpr (kOut == kOutAtomic) {
+        float* dst = static_cast<float*>(p.out) + static_cast<int64_t>(row) * p.ld_out + col;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+            if (c < valid) atomicAdd(dst + c, __uint_as_float(r[c]));
+    } else {
+        float* dst = static_cast<float*>(p.out) + static_cast<int64_t>(row) * p.ld_out + col;
+        if constexpr (kOut == kOutSlices) dst += static_cast<int64_t>(seg) * p.slice_stride;
+        if (valid == 32) {
+            float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+                d4[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                    __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+        } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                if (c < valid) dst[c] = __uint_as_float(r[c]);
+        }
+    }
+}
+
+template <int kOut>
+__global__ void __launch_bounds__(kNumThreads, 1)
+    bigemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    // 128-byte-swizzled tiles must start on 1024-byte boundaries.
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t sA = base;                                // stage s: sA + s * kABytes
+    const uint32_t sB = base + kStages * kABytes;            // stage s: sB + s * kBBytes
+    uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kStages * kStageBytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBarriers);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const uint32_t bar0 = smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + kAccStages + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 2 * kAccStages);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < kAccStages; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), kEpilogueThreads);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    // Everything above overlaps the previous kernel in the stream; global
+    // memory is touched only after it has finished.
+    grid_dependency_wait();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer --
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+                int mt, nt, seg;
+                unit_coords(p, u, mt, nt, seg);
+                const int kb0 = seg * p.kb_per_split;
+                const int kb1 = min(kb0 + p.kb_per_split, p.kb_total);
+                const int m0 = mt * kBM, n0 = nt * kBN;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.status,
+                                      kErrWaitProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full_bar(stage);
+                    mbar_arrive_expect_tx(fb, kStageBytes);
+                    tma_load_2d(sA + stage * kABytes, &tmA, fb, kb * kBK, m0);
+#pragma unroll
+                    for (int c = 0; c < kBN / static_cast<int>(kBChunkCols); ++c)
+                        tma_load_2d(sB + stage * kBBytes + c * kBChunkBytes, &tmB, fb,
+                                    n0 + c * static_cast<int>(kBChunkCols), kb * kBK);
+                    issued_mask |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            grid_launch_dependents();
+            // No copy may still be in flight when the CTA exits: wait (bounded)
+            // for the last load issued into every stage.
+            for (int s = 0; s < kStages; ++s)
+                if (issued_mask & (1u << s))
+                    wait_bounded(full_bar(s), (issued_parity >> s) & 1u, abort_flag, p.status,
+                                 kErrWaitDrain, /*honour_abort=*/false);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------- MMA issuer --
+            int stage = 0;
+            uint32_t phase = 0;
+            int t = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x, ++t) {
+                int mt, nt, seg;
+                unit_coords(p, u, mt, nt, seg);
+                const int kb0 = seg * p.kb_per_split;
+                const int kb1 = min(kb0 + p.kb_per_split, p.kb_total);
+                const int acc = t & 1;
+                const uint32_t acc_phase = (t >> 1) & 1;
+                if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status,
+                                  kErrWaitMma)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_bounded(full_bar(stage), phase, abort_flag, p.status, kErrWaitMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sA + stage * kABytes;
+                    const uint32_t b0 = sB + stage * kBBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                        // A: K-major, 128-byte rows; advance 16 elements = 32 bytes.
+                        const uint64_t ad = smem_desc_sw128(a0 + kk * kUmmaK * 2, 16, 1024);
+                        // B: N-major; 16 k-rows of 128 bytes = 2048 bytes per step.
+                        // LBO = distance between 64-column chunks, SBO = 8 k-rows.
+                        const uint64_t bd =
+                            smem_desc_sw128(b0 + kk * kUmmaK * 128, kBChunkBytes, 1024);
+                        mma_bf16(d_tmem, ad, bd, kIdesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(empty_bar(stage));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(tfull_bar(acc));
+            }
+            // Every MMA this thread issued completes before TMEM is released.
+            mma_commit(drain_bar);
+            wait_bounded(drain_bar, 0, abort_flag, p.status, kErrWaitDrain, /*honour_abort=*/false);
+        }
+    } else {
+        // ------------------------------------------------------ epilogue --
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row_in_tile = q * 32 + lane;
+        int t = 0;
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
+            int mt, nt, seg;
+            unit_coords(p, u, mt, nt, seg);
+            const int acc = t & 1;
+            const uint32_t acc_phase = (t >> 1) & 1;
+            if (!wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.status, kErrWaitEpilogue))
+                break;
+            tc_fence_after();
+            const int m0 = mt * kBM, n0 = nt * kBN;
+            const int row = m0 + row_in_tile;
+            const bool warp_has_rows = (m0 + q * 32) < p.M;  // uniform per warp
+            if (warp_has_rows) {
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       static_cast<uint32_t>(acc * kBN);
+#pragma unroll 1
+                for (int ch = 0; ch < kBN / 32; ++ch) {
+                    const int col = n0 + ch * 32;
+                    if (col >= p.N) break;  // uniform
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + ch * 32, r);
+                    tmem_ld_wait();
+                    if (row < p.M) store_row_chunk<kOut>(p, seg, row, col, r);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(tempty_bar(acc));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// Split-K reduction: for every element, acc = w_0, then acc = acc + w_s for
+// s = 1 .. S-1 in that order (FP32, round to nearest even); starting from w_0
+// rather than 0.0f keeps a lone -0.0 partial intact.  One thread handles four
+// adjacent columns of one row (16-byte loads, coalesced along N); the loads of
+// up to eight slices are issued before their additions.
+template <bool kBF16Out>
+__global__ void __launch_bounds__(256)
+    splitk_reduce_kernel(const float* __restrict__ ws, void* __restrict__ C, int M, int N,
+                         int64_t ldc, int64_t ws_ld, int S) {
+    grid_dependency_wait();
+    const int64_t vec_per_row = ws_ld / 4;
+    const int64_t total = static_cast<int64_t>(M) * vec_per_row;
+    const int64_t slice = static_cast<int64_t>(M) * ws_ld;
+    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < total;
+         v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = v / vec_per_row;
+        const int col = static_cast<int>(v - m * vec_per_row) * 4;
+        const float* src = ws + m * ws_ld + col;
+        float4 acc = __ldcs(reinterpret_cast<const float4*>(src));
+        for (int s0 = 1; s0 < S; s0 += 8) {
+            float4 w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (s0 + i < S) w[i] = __ldcs(reinterpret_cast<const float4*>(src + (s0 + i) * slice));
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (s0 + i < S) {
+                    acc.x = __fadd_rn(acc.x, w[i].x);
+                    acc.y = __fadd_rn(acc.y, w[i].y);
+                    acc.z = __fadd_rn(acc.z, w[i].z);
+                    acc.w = __fadd_rn(acc.w, w[i].w);
+                }
+            }
+        }
+        const int valid = min(4, N - col);
+        if (valid <= 0) continue;
+        if constexpr (kBF16Out) {
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(C) + m * ldc + col;
+            if (valid == 4) {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+                uint2 pk = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+                *reinterpret_cast<uint2*>(dst) = pk;
+            } else {
+                const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+                for (int c = 0; c < valid; ++c) dst[c] = __float2bfloat16_rn(a[c]);
+            }
+        } else {
+            float* dst = static_cast<float*>(C) + m * ldc + col;
+            if (valid == 4) {
+                *reinterpret_cast<float4*>(dst) = acc;
+            } else {
+                const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+                for (int c = 0; c < valid; ++c) dst[c] = a[c];
+            }
+        }
+    }
+    grid_launch_dependents();
+}
+
+}  // namespace bigemm

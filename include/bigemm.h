@@ -1,0 +1,196 @@
+/*
+ * bigemm.h -- C ABI of libbigemm.so: a deterministic, batch-invariant BF16
+ * matrix multiply C = A * B with FP32 accumulation, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (Tencent AI-infra article "腾讯エンジニア：大規模モデルの出力を
+ * 確定させるための AI インフラ手法", section "Batch Invariance の由来"):
+ *     A is [M, K], B is [K, N], C is [M, N],   C_ij = sum_{k=0}^{K-1} A_ik * B_kj.
+ * Each output element's K-reduction order is fixed by K and the split-K count
+ * alone: it never depends on M, on the other rows of the batch, on where a row
+ * sits in the batch, or on run-to-run scheduling.  Concretely, for every (i, j):
+ *   - the K axis is cut into blocks of BIGEMM_BLOCK_K = 64 ("Tiling": the
+ *     per-CTA K loop in fixed steps; "Batch Invariance の由来": BLOCK_K fixes the
+ *     reduction tree), consumed in ascending order by one tensor-core
+ *     accumulator in FP32;
+ *   - with split_k = S > 1 the blocks are dealt into S contiguous segments,
+ *     each segment's FP32 partial goes to its own workspace slice, and a
+ *     separate kernel adds the slices in the fixed order s = 0, 1, ..., S-1
+ *     ("Split-K": workspace [split_k, M, N], partial GEMM kernel, reduction
+ *     kernel) -- no atomics;
+ *   - the M and N tile sizes and the order in which tiles run (a GROUP_M
+ *     swizzle, "GROUP_M - Swizzle L2 Cache") change no sum.
+ * So row i of C is bit-for-bit a function of (row i of A, B, K, split_k,
+ * output type) only.
+ *
+ * Layouts.  All matrices are row-major with explicit leading dimensions in
+ * elements: A[i*lda + k] (bf16), B[k*ldb + j] (bf16), C[i*ldc + j].  The
+ * workspace of the split-K path holds S slices of M rows of
+ * bigemm_workspace_ld(N) fp32 values: slice s, row i, column j at
+ * ws[(s*M + i) * bigemm_workspace_ld(N) + j].
+ *
+ * Ownership and synchronisation.  The caller owns every buffer and the stream.
+ * The library allocates no device memory, never synchronises, and returns as
+ * soon as the work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ * default stream).  Buffers must stay valid until that work completes.  Calls
+ * that share a workspace must be ordered (same stream or explicit events).
+ * C must not overlap A, B or the workspace.
+ *
+ * Errors.  Every argument is checked before anything is enqueued; a failed
+ * check returns an error code and enqueues nothing:
+ *   BIGEMM_ERR_ARG        negative size, NULL pointer, ld smaller than the row
+ *                         length, split_k outside [0, ceil(K/64)], sizes past
+ *                         the int32 limits of the tile scheduler
+ *   BIGEMM_ERR_ALIGN      a base pointer not 16-byte aligned, lda or ldb not a
+ *                         multiple of 8 elements (16-byte rows for the tensor
+ *                         memory accelerator), ldc not a multiple of 4 (fp32
+ *                         C) or 8 (bf16 C)
+ *   BIGEMM_ERR_WORKSPACE  workspace NULL, misaligned or smaller than
+ *                         bigemm_workspace_bytes(M, N, K, split_k)
+ *   BIGEMM_ERR_UNSUPPORTED the current device is not sm_103 / sm_100 class
+ *   BIGEMM_ERR_CUDA       a CUDA runtime or driver call failed
+ *   BIGEMM_ERR_TIMEOUT    reported by bigemm_device_status(): a kernel's
+ *                         bounded wait expired; the kernel stopped early,
+ *                         released its tensor memory and returned (its output
+ *                         is then undefined)
+ * Empty products are valid: M == 0 or N == 0 enqueue nothing, K == 0 writes
+ * zeros to C.
+ */
+#ifndef BIGEMM_H
+#define BIGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define BIGEMM_API __attribute__((visibility("default")))
+#else
+#define BIGEMM_API
+#endif
+
+typedef enum {
+    BIGEMM_OK = 0,
+    BIGEMM_ERR_ARG = 1,
+    BIGEMM_ERR_ALIGN = 2,
+    BIGEMM_ERR_WORKSPACE = 3,
+    BIGEMM_ERR_UNSUPPORTED = 4,
+    BIGEMM_ERR_CUDA = 5,
+    BIGEMM_ERR_TIMEOUT = 6
+} bigemm_status;
+
+/* A cudaStream_t passed through the C ABI. */
+typedef void *bigemm_stream;
+
+/* K step of the tensor-core mainloop (elements).  Fixed: it is part of the
+ * reduction order, so it never varies with the shape (Tencent article,
+ * "Batch Invariance の由来": a different BLOCK_K gives a different but still
+ * deterministic result). */
+#define BIGEMM_BLOCK_K 64
+
+/* Output tile of one work unit: BIGEMM_TILE_M rows x BIGEMM_TILE_N columns. */
+#define BIGEMM_TILE_M 128
+#define BIGEMM_TILE_N 256
+
+/* Library version, (major << 16) | minor. */
+BIGEMM_API int bigemm_version(void);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+BIGEMM_API const char *bigemm_status_string(bigemm_status status);
+
+/* max(1, ceil(K / BIGEMM_BLOCK_K)): the number of K blocks (at least 1),
+ * and the largest split_k; 0 for K < 0. */
+BIGEMM_API int bigemm_max_split_k(int64_t K);
+
+/* The split-K count used when split_k = 0 is passed: a function of K alone,
+ * never of M or N ("Split-K" is enabled for long K; "Batch Invariance の由来":
+ * a split that varies with the batch breaks invariance).  It is the largest
+ * power of two <= min(16, floor(K / 512)), and at least 1:
+ * K < 1024 -> 1, K = 4096 -> 8, K >= 8192 -> 16. */
+BIGEMM_API int bigemm_default_split_k(int64_t K);
+
+/* Number of non-empty K segments for (K, split_k): with L = ceil(KB / S)
+ * blocks per segment (KB = ceil(K/64)), this is ceil(KB / L) <= S.  The
+ * reduction order depends on (K, split_k) only through this count and L.
+ * split_k = 0 means bigemm_default_split_k(K).  Returns 0 for an invalid
+ * split_k. */
+BIGEMM_API int bigemm_effective_split_k(int64_t K, int split_k);
+
+/* Row stride (elements) of the fp32 workspace slices: N rounded up to a
+ * multiple of 4, so that every row starts 16-byte aligned. */
+BIGEMM_API int64_t bigemm_workspace_ld(int64_t N);
+
+/* Workspace bytes bigemm_run / bigemm_run_bf16out need for (M, N, K,
+ * split_k): effective_split * M * bigemm_workspace_ld(N) * 4 when the
+ * effective split is > 1, else 0.  Returns 0 for invalid arguments too. */
+BIGEMM_API size_t bigemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
+
+/* Workspace bytes bigemm_run_partial needs: effective_split * M *
+ * bigemm_workspace_ld(N) * 4, also when the effective split is 1. */
+BIGEMM_API size_t bigemm_partial_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
+
+/* C (fp32) = A * B.  A: bf16 [M, K] (lda), B: bf16 [K, N] (ldb), C: fp32
+ * [M, N] (ldc).  split_k: 1 = no split, 0 = bigemm_default_split_k(K), S > 1 =
+ * S segments through the workspace and the fixed-order reduction kernel.
+ * workspace / workspace_bytes may be NULL / 0 when no workspace is needed. */
+BIGEMM_API bigemm_status bigemm_run(const void *A, const void *B, float *C,
+                         int64_t M, int64_t N, int64_t K,
+                         int64_t lda, int64_t ldb, int64_t ldc,
+                         int split_k, void *workspace, size_t workspace_bytes,
+                         bigemm_stream stream);
+
+/* As bigemm_run, but C is bf16: the FP32 result (after the split-K reduction
+ * when split_k > 1) is rounded once to bf16, to nearest even. */
+BIGEMM_API bigemm_status bigemm_run_bf16out(const void *A, const void *B, void *C,
+                                 int64_t M, int64_t N, int64_t K,
+                                 int64_t lda, int64_t ldb, int64_t ldc,
+                                 int split_k, void *workspace, size_t workspace_bytes,
+                                 bigemm_stream stream);
+
+/* The split-K partial-product kernel alone ("Split-K": each segment writes
+ * its partial to workspace[k_idx, m, n] without atomics).  Writes
+ * bigemm_effective_split_k(K, split_k) slices (one slice when that is 1);
+ * workspace_bytes must be >= bigemm_partial_workspace_bytes(M, N, K, split_k). */
+BIGEMM_API bigemm_status bigemm_run_partial(const void *A, const void *B,
+                                 int64_t M, int64_t N, int64_t K,
+                                 int64_t lda, int64_t ldb, int split_k,
+                                 void *workspace, size_t workspace_bytes,
+                                 bigemm_stream stream);
+
+/* The split-K reduction kernel alone ("Split-K": a separate light kernel sums
+ * the workspace along the split axis).  For every (i, j):
+ *     acc = ws[0][i][j];  acc = acc + ws[s][i][j] for s = 1 .. splits-1
+ * each '+' one FP32 addition rounded to nearest even, in exactly that order;
+ * then C[i*ldc + j] = acc (c_is_bf16 = 0) or acc rounded to bf16, nearest
+ * even (c_is_bf16 = 1).  workspace layout as above, splits >= 1. */
+BIGEMM_API bigemm_status bigemm_splitk_reduce(const float *workspace, int splits,
+                                   int64_t M, int64_t N,
+                                   void *C, int64_t ldc, int c_is_bf16,
+                                   bigemm_stream stream);
+
+/* Measured contrast only -- NOT deterministic.  Same arguments as bigemm_run
+ * without a workspace: C (fp32) is zeroed on the stream, then every K
+ * segment's partial is added into C with atomic adds ("Split-K": atomic_add;
+ * "Batch Invariance の由来": the hardware decides the order of the atomic
+ * additions, so the bits vary from run to run). */
+BIGEMM_API bigemm_status bigemm_run_atomic_splitk(const void *A, const void *B, float *C,
+                                       int64_t M, int64_t N, int64_t K,
+                                       int64_t lda, int64_t ldb, int64_t ldc,
+                                       int split_k, bigemm_stream stream);
+
+/* Reads (and, if reset != 0, clears) the device-side error word the kernels
+ * set when a bounded wait expires.  Synchronises the current device.
+ * Returns BIGEMM_OK, BIGEMM_ERR_TIMEOUT or BIGEMM_ERR_CUDA. */
+BIGEMM_API bigemm_status bigemm_device_status(int reset);
+
+/* Number of kernels the most recent successful call on this host thread
+ * enqueued (0, 1 or 2). */
+BIGEMM_API int bigemm_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BIGEMM_H */

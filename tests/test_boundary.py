@@ -1,0 +1,146 @@
+"""The C ABI without a GPU: the library builds, loads and exports every symbol
+include/bigemm.h declares; the host-side helpers (split count, workspace
+sizing) follow their documented formulas; and argument checks return their
+error codes before anything touches CUDA."""
+import os
+import re
+
+import pytest
+
+import deterministic_invariant_gemm_gb300 as dig
+from deterministic_invariant_gemm_gb300 import build as lib_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bigemm.h")
+
+OK, ARG, ALIGN, WS = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    return dig.load()
+
+
+def header_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    return sorted(set(re.findall(r"BIGEMM_API[^;(]*?\b(bigemm_\w+)\s*\(", text)))
+
+
+def test_header_declares_what_the_binding_expects():
+    assert header_functions() == sorted(dig.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+    # and nothing of the implementation leaks (hidden visibility)
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", dig.library_path()],
+                         capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert exported == set(header_functions())
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = dig.bigemm_status_string(code)
+        assert s.startswith(dig.STATUS_NAMES[code])
+    assert dig.bigemm_status_string(99) == "BIGEMM_ERR_UNKNOWN"
+
+
+def test_split_helpers(lib):
+    assert dig.bigemm_max_split_k(0) == 1
+    assert dig.bigemm_max_split_k(1) == 1
+    assert dig.bigemm_max_split_k(64) == 1
+    assert dig.bigemm_max_split_k(65) == 2
+    assert dig.bigemm_max_split_k(4096) == 64
+    # default split: a function of K only
+    assert [dig.bigemm_default_split_k(k) for k in (1, 512, 1023, 1024, 2048, 4096, 8192, 65536)] == \
+        [1, 1, 1, 2, 4, 8, 16, 16]
+    # effective split: ceil(KB / ceil(KB / S))
+    assert dig.bigemm_effective_split_k(4096, 8) == 8
+    assert dig.bigemm_effective_split_k(4096, 0) == 8
+    assert dig.bigemm_effective_split_k(1000, 3) == 3      # KB=16, L=6 -> 6,6,4
+    assert dig.bigemm_effective_split_k(64 * 10, 7) == 5   # KB=10, L=2 -> 5 segments
+    assert dig.bigemm_effective_split_k(4096, 65) == 0     # beyond KB
+    assert dig.bigemm_effective_split_k(4096, -1) == 0
+    assert dig.bigemm_effective_split_k(0, 1) == 1
+    for K in (1, 63, 64, 65, 1000, 4096, 65536):
+        for S in range(1, min(40, dig.bigemm_max_split_k(K)) + 1):
+            kb = -(-K // 64)
+            L = -(-kb // S)
+            assert dig.bigemm_effective_split_k(K, S) == -(-kb // L)
+
+
+def test_workspace_sizes(lib):
+    assert dig.bigemm_workspace_ld(1) == 4
+    assert dig.bigemm_workspace_ld(4096) == 4096
+    assert dig.bigemm_workspace_ld(4097) == 4100
+    assert dig.bigemm_workspace_bytes(16, 4096, 4096, 8) == 8 * 16 * 4096 * 4
+    assert dig.bigemm_workspace_bytes(16, 4096, 4096, 1) == 0
+    assert dig.bigemm_partial_workspace_bytes(16, 4096, 4096, 1) == 16 * 4096 * 4
+    assert dig.bigemm_workspace_bytes(3, 5, 640, 7) == 5 * 3 * 8 * 4
+    assert dig.bigemm_workspace_bytes(-1, 5, 640, 2) == 0
+
+
+A16 = 1 << 20      # fake, 16-byte aligned addresses: never dereferenced
+B16 = 2 << 20
+C16 = 3 << 20
+W16 = 4 << 20
+
+
+@pytest.mark.parametrize("args,code", [
+    # (A, B, C, M, N, K, lda, ldb, ldc, split_k, ws, ws_bytes)
+    ((A16, B16, C16, -1, 8, 8, 8, 8, 8, 1, None, 0), ARG),
+    ((A16, B16, C16, 8, 8, -1, 8, 8, 8, 1, None, 0), ARG),
+    ((None, B16, C16, 8, 8, 8, 8, 8, 8, 1, None, 0), ARG),
+    ((A16, B16, None, 8, 8, 8, 8, 8, 8, 1, None, 0), ARG),
+    ((A16, B16, C16, 8, 8, 16, 8, 8, 8, 1, None, 0), ARG),       # lda < K
+    ((A16, B16, C16, 8, 16, 8, 8, 8, 16, 1, None, 0), ARG),      # ldb < N
+    ((A16, B16, C16, 8, 16, 8, 8, 16, 8, 1, None, 0), ARG),      # ldc < N
+    ((A16, B16, C16, 8, 8, 128, 128, 8, 8, 3, None, 0), ARG),    # split > KB
+    ((A16, B16, C16, 8, 8, 128, 128, 8, 8, -2, None, 0), ARG),
+    ((A16 + 2, B16, C16, 8, 8, 8, 8, 8, 8, 1, None, 0), ALIGN),
+    ((A16, B16 + 8, C16, 8, 8, 8, 8, 8, 8, 1, None, 0), ALIGN),
+    ((A16, B16, C16 + 4, 8, 8, 8, 8, 8, 8, 1, None, 0), ALIGN),
+    ((A16, B16, C16, 8, 8, 12, 12, 8, 8, 1, None, 0), ALIGN),    # lda % 8
+    ((A16, B16, C16, 8, 12, 8, 8, 12, 12, 1, None, 0), ALIGN),   # ldb % 8
+    ((A16, B16, C16, 8, 8, 8, 8, 8, 10, 1, None, 0), ALIGN),     # ldc % 4
+    ((A16, B16, C16, 8, 8, 4096, 4096, 8, 8, 8, None, 0), WS),   # no workspace
+    ((A16, B16, C16, 8, 8, 4096, 4096, 8, 8, 8, W16, 100), WS),  # too small
+    ((A16, B16, C16, 8, 8, 4096, 4096, 8, 8, 8, W16 + 4, 1 << 20), WS),
+    ((A16, B16, C16, 0, 8, 8, 8, 8, 8, 1, None, 0), OK),         # empty: nothing enqueued
+    ((A16, B16, C16, 8, 0, 8, 8, 8, 8, 1, None, 0), OK),
+])
+def test_argument_checks_fp32(lib, args, code):
+    A, B, C, M, N, K, lda, ldb, ldc, s, ws, wb = args
+    assert dig.bigemm_run(A, B, C, M, N, K, lda, ldb, ldc, s, ws, wb, stream=0, check=False) == code
+
+
+def test_argument_checks_other_entry_points(lib):
+    # bf16 output needs ldc % 8 == 0
+    assert dig.bigemm_run_bf16out(A16, B16, C16, 8, 8, 8, 8, 8, 12, 1, None, 0, stream=0,
+                                  check=False) == ALIGN
+    # the partial kernel needs a workspace even for one slice
+    assert dig.bigemm_run_partial(A16, B16, 8, 8, 8, 8, 8, 1, None, 0, stream=0,
+                                  check=False) == WS
+    assert dig.bigemm_splitk_reduce(W16, 0, 8, 8, C16, 8, 0, stream=0, check=False) == ARG
+    assert dig.bigemm_splitk_reduce(W16 + 4, 2, 8, 8, C16, 8, 0, stream=0, check=False) == ALIGN
+    assert dig.bigemm_splitk_reduce(W16, 2, 8, 8, C16, 4, 0, stream=0, check=False) == ARG
+    assert dig.bigemm_splitk_reduce(W16, 2, 0, 8, C16, 8, 0, stream=0, check=False) == OK
+    assert dig.bigemm_run_atomic_splitk(A16, B16, C16, 8, 8, 8, 8, 8, 8, 2, stream=0,
+                                        check=False) == ARG
+    with pytest.raises(dig.BigemmError):
+        dig.bigemm_run(A16, B16, C16, -1, 8, 8, 8, 8, 8, 1, None, 0, stream=0)
+
+
+def test_product_path_has_no_oracle_or_fallback():
+    """The package never imports the oracle and has no CPU code path."""
+    pkg = os.path.join(ROOT, "deterministic_invariant_gemm_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "liboracle" not in text, f
