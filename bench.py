@@ -1,0 +1,560 @@
+"""Benchmark of the deterministic, batch-invariant BF16 GEMM on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  The headline workload is the decode-shaped
+product: M in {1, 4, 16, 64} rows against N = K = 4096 weights drawn N(0, 0.02),
+split_k = 8 chosen from K alone.  One step = the four products, each through
+the split-K partial kernel and the fixed-order reduction kernel; every product
+of a step multiplies a different weight matrix from a rotating pool of 16
+(512 MiB, four times the 129 MB L2), so the weights stream from HBM as they
+do in decoding.  Steps are replayed from a CUDA graph (one per rotation
+period).  The metric is the whole job's TFLOP/s (2 M N K per product).
+
+Also reported (N = 1, rank 0):
+  roofline      the split-K partial kernel (the dominant kernel): algorithmic
+                bytes 2MK + 2KN + 4MN per launch over its measured duration,
+                against the measured HBM copy bandwidth.
+  e2e           the same step through the public API with host buffers:
+                A and B copied from pinned host memory, C read back, every step.
+  cpu_baseline  the CPU oracle (binary64 triple loop) on the same decode step.
+  workloads     the other shapes: large squares (tensor-core bound) and long K.
+  clocks        SM clock and throttle reasons sampled during the timed region.
+
+--impl reference times the CPU oracle (the reference for this build) on the
+same workload and prints its line with "impl": "reference".
+
+For N > 1 (torchrun) every rank runs the same step on its own GPU (replicas:
+the product shards by rows or columns with no exchange); ranks meet at a
+barrier on both sides of the timed region and the slowest rank's time sets
+the job's throughput.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "TFLOP/s and % of dense BF16 peak (HBM % at small M), bit-exact batch-invariant"
+UNIT = "TFLOP/s"
+DECODE = workloads.WORKLOADS["decode"]
+MS = tuple(DECODE["Ms"])
+N_DEC = DECODE["N"]
+K_DEC = DECODE["K"]
+POOL = 16
+L2_BYTES = 129 * 1000 * 1000
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------- helpers --
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def decode_flops_per_step() -> float:
+    return float(sum(2.0 * M * N_DEC * K_DEC for M in MS))
+
+
+def decode_alg_bytes(M: int) -> float:
+    """Algorithmic bytes of one decode product: read A and B once (bf16), write
+    C once (fp32).  The split-K workspace round trip is overhead, not counted."""
+    return 2.0 * M * K_DEC + 2.0 * K_DEC * N_DEC + 4.0 * M * N_DEC
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Largest value over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job TFLOP/s: the work of every rank over the slowest rank's time."""
+    return flops_per_rank * world / max_seconds / 1e12
+
+
+class ClockSampler:
+    """Samples the SM clock and the clock-event (throttle) reasons of one GPU
+    while the timed region runs: NVML through ctypes every 2 ms, else
+    nvidia-smi every 200 ms.  Read-only: it changes no setting."""
+
+    REASONS = {
+        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+        0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+        0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+        0x100: "display_clock_setting",
+    }
+    REJECT = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []          # (mhz, mask)
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+        self._proc = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() == 0:
+                h = ctypes.c_void_p()
+                if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) == 0:
+                    self._nvml, self._handle = lib, h
+                    mx = ctypes.c_uint()
+                    if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                        self.max_mhz = float(mx.value)
+        except OSError:
+            self._nvml = None
+
+    def _poll_nvml(self):
+        lib, h = self._nvml, self._handle
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mhz = ctypes.c_uint()
+        mask = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0 and \
+                    reasons_fn(h, ctypes.byref(mask)) == 0:
+                self.samples.append((float(mhz.value), int(mask.value)))
+            time.sleep(0.002)
+
+    def start(self):
+        self.samples = []
+        self._stop.clear()
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._poll_nvml, daemon=True)
+            self._thread.start()
+        else:
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index),
+                     "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "200"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self._proc = None
+
+    def stop(self) -> dict:
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join()
+        if self._proc is not None:
+            self._proc.terminate()
+            out, _ = self._proc.communicate()
+            for line in out.splitlines():
+                parts = [p.strip() for p in line.split(",")]
+                try:
+                    mhz, mx, mask = float(parts[0]), float(parts[1]), int(parts[2], 16)
+                except (ValueError, IndexError):
+                    continue
+                self.max_mhz = mx
+                self.samples.append((mhz, mask))
+        reasons = set()
+        for _, mask in self.samples:
+            for bit, name in self.REASONS.items():
+                if mask & bit:
+                    reasons.add(name)
+        busy = [m for m, mask in self.samples if not mask & 0x1] or [m for m, _ in self.samples]
+        return {
+            "sm_mhz": statistics.median(busy) if busy else None,
+            "sm_max_mhz": self.max_mhz,
+            "reasons": sorted(reasons),
+            "samples": len(self.samples),
+            "source": "nvml" if self._nvml is not None else "nvidia-smi",
+        }
+
+    @classmethod
+    def rejected(cls, clocks: dict) -> bool:
+        if any(r in cls.REJECT for r in clocks.get("reasons", [])):
+            return True
+        mhz, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+        return bool(mhz and mx and mhz < 0.5 * mx and not clocks.get("reasons"))
+
+
+def external_events_supported() -> bool:
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        return True
+    except TypeError:
+        return False
+
+
+# --------------------------------------------------------- decode workload --
+
+class DecodeBench:
+    """Inputs, workspaces and the captured step graphs of the headline workload."""
+
+    def __init__(self, dev: torch.device):
+        import deterministic_invariant_gemm_gb300 as dig
+        self.dig = dig
+        self.dev = dev
+        seed = workloads.BASE_SEED + DECODE["index"]
+        self.split = dig.bigemm_default_split_k(K_DEC)
+        self.A = {M: workloads.normal_bf16((M, K_DEC), seed + M, DECODE["a_std"]).to(dev) for M in MS}
+        self.B = [workloads.normal_bf16((K_DEC, N_DEC), seed + 1000 + j, DECODE["b_std"]).to(dev)
+                  for j in range(POOL)]
+        self.C = {M: torch.empty((M, N_DEC), dtype=torch.float32, device=dev) for M in MS}
+        self.ws_bytes = {M: dig.bigemm_partial_workspace_bytes(M, N_DEC, K_DEC, self.split) for M in MS}
+        self.ws = {M: torch.empty(self.ws_bytes[M], dtype=torch.uint8, device=dev) for M in MS}
+        self.eff = dig.bigemm_effective_split_k(K_DEC, self.split)
+        self.period = POOL // len(MS)            # steps per rotation of the weight pool
+        self.launches_per_step = 2 * len(MS)
+        self.graphs = []
+        self.events = []                          # per graph: [(M, start, end)]
+
+    def product(self, M: int, B: torch.Tensor, ev=None):
+        dig = self.dig
+        if ev is not None:
+            ev[0].record()
+        dig.bigemm_run_partial(self.A[M], B, M, N_DEC, K_DEC, K_DEC, N_DEC, self.split,
+                               self.ws[M], self.ws_bytes[M])
+        if ev is not None:
+            ev[1].record()
+        dig.bigemm_splitk_reduce(self.ws[M], self.eff, M, N_DEC, self.C[M], N_DEC, 0)
+
+    def step(self, i: int, events=None):
+        for idx, M in enumerate(MS):
+            B = self.B[(i * len(MS) + idx) % POOL]
+            self.product(M, B, None if events is None else events[idx])
+
+    def capture(self, with_events: bool):
+        """One graph per step of the rotation period, so that every replay
+        streams a different set of four weight matrices."""
+        s = torch.cuda.Stream(device=self.dev)
+        s.wait_stream(torch.cuda.current_stream())
+        for i in range(self.period):
+            g = torch.cuda.CUDAGraph()
+            evs = None
+            if with_events:
+                evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                        torch.cuda.Event(enable_timing=True, external=True)) for _ in MS]
+            with torch.cuda.graph(g, stream=s):
+                self.step(i, evs)
+            self.graphs.append(g)
+            self.events.append(evs)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+
+    def replay(self, i: int):
+        self.graphs[i % self.period].replay()
+
+    def kernel_times_eager(self, steps: int):
+        """Fallback: time the partial kernel of every product of `steps` eager
+        steps with CUDA events on the launching (current) stream."""
+        out = []
+        for i in range(steps):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in MS]
+            self.step(i, evs)
+            torch.cuda.synchronize()
+            out.extend((M, a.elapsed_time(b)) for M, (a, b) in zip(MS, evs))
+        return out
+
+    def kernel_times_ms(self):
+        """Durations of the partial-kernel launches recorded by the last replay
+        of every graph: [(M, ms)]."""
+        out = []
+        for evs in self.events:
+            if evs is None:
+                continue
+            for M, (a, b) in zip(MS, evs):
+                out.append((M, a.elapsed_time(b)))
+        return out
+
+
+def time_region(fn, steps: int, world: int) -> float:
+    """Seconds for `steps` calls of fn(i), device-timed with CUDA events, with
+    a barrier and a device synchronise on both sides; max over ranks."""
+    import torch.distributed as dist
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        fn(i)
+    e1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    return max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+
+
+def run_e2e(bench: DecodeBench, steps: int, warmup: int) -> dict:
+    """The decode step through the public API with host buffers: every step
+    copies its A and B matrices from pinned host memory, runs the four
+    products, and reads the four results back."""
+    dig = bench.dig
+    hostA = {M: bench.A[M].cpu().pin_memory() for M in MS}
+    hostB = [bench.B[j].cpu().pin_memory() for j in range(len(MS))]
+    devA = {M: torch.empty_like(bench.A[M]) for M in MS}
+    devB = [torch.empty_like(bench.B[0]) for _ in MS]
+    hostC = {M: torch.empty((M, N_DEC), dtype=torch.float32).pin_memory() for M in MS}
+    h2d = sum(t.numel() * t.element_size() for t in hostA.values()) + \
+        sum(t.numel() * t.element_size() for t in hostB)
+    d2h = sum(t.numel() * t.element_size() for t in hostC.values())
+
+    def one(_i):
+        for idx, M in enumerate(MS):
+            devA[M].copy_(hostA[M], non_blocking=True)
+            devB[idx].copy_(hostB[idx], non_blocking=True)
+            dig.bigemm_run(devA[M], devB[idx], bench.C[M], M, N_DEC, K_DEC, K_DEC, N_DEC, N_DEC,
+                           bench.split, bench.ws[M], bench.ws_bytes[M])
+            hostC[M].copy_(bench.C[M], non_blocking=True)
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize()
+    secs = time_region(one, steps, 1)
+    return {"value": decode_flops_per_step() * steps / secs / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": secs * 1e3 / steps}
+
+
+# ----------------------------------------------------------- other shapes --
+
+def run_other_workloads(dev, peaks) -> dict:
+    """Large squares (tensor-core bound) and long K, each a few timed calls on
+    inputs larger than L2 (rotating copies where one copy fits)."""
+    import deterministic_invariant_gemm_gb300 as dig
+    out = {}
+    bf16_peak = peaks["bf16_tflops"]
+    cases = [("square_2048", 2048, 2048, 2048, 1, False, "uniform", 20),
+             ("square_4096", 4096, 4096, 4096, 1, False, "uniform", 10),
+             ("square_8192", 8192, 8192, 8192, 1, False, "uniform", 10),
+             ("large_16384_bf16out", 16384, 16384, 16384, 1, True, "normal", 5),
+             ("longk_256x256x65536_s16", 256, 256, 65536, 16, False, "normal", 20)]
+    for name, M, N, K, S, bf16, dist_name, iters in cases:
+        in_bytes = 2 * (M * K + K * N)
+        copies = max(1, min(8, math.ceil(2 * L2_BYTES / in_bytes)))
+        AB = [workloads.pair(M, N, K, 4321 + c, dist=dist_name) for c in range(copies)]
+        AB = [(a.to(dev), b.to(dev)) for a, b in AB]
+        C = torch.empty((M, N), dtype=torch.bfloat16 if bf16 else torch.float32, device=dev)
+        wsb = dig.bigemm_workspace_bytes(M, N, K, S)
+        ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+        fn = dig.bigemm_run_bf16out if bf16 else dig.bigemm_run
+
+        def call(i):
+            a, b = AB[i % copies]
+            fn(a, b, C, M, N, K, K, N, N, S, ws, wsb)
+
+        for i in range(3):
+            call(i)
+        secs = time_region(call, iters, 1)
+        tflops = 2.0 * M * N * K * iters / secs / 1e12
+        out[name] = {"tflops": round(tflops, 2), "frac_of_bf16_peak": round(tflops / bf16_peak, 4),
+                     "ms": round(secs * 1e3 / iters, 4), "split_k": S,
+                     "out": "bf16" if bf16 else "fp32", "input_copies": copies}
+        if name.startswith("longk"):
+            alg = 2.0 * (M * K + K * N) + 4.0 * M * N
+            out[name]["hbm_frac"] = round(alg / (secs / iters) / 1e9 / peaks["hbm_gbs"], 4)
+        del AB, C, ws
+        torch.cuda.empty_cache()
+    return out
+
+
+# -------------------------------------------------------------- CPU oracle --
+
+_ORACLE_INPUTS = {}
+
+
+def oracle_decode_step():
+    """The decode step computed by the CPU oracle: the four products against
+    four weight matrices (the same seeded inputs as the GPU step).  Returns
+    (seconds, threads); input generation is outside the timing."""
+    import oracle
+    if not _ORACLE_INPUTS:
+        seed = workloads.BASE_SEED + DECODE["index"]
+        _ORACLE_INPUTS["A"] = {M: workloads.normal_bf16((M, K_DEC), seed + M, DECODE["a_std"]) for M in MS}
+        _ORACLE_INPUTS["B"] = [workloads.normal_bf16((K_DEC, N_DEC), seed + 1000 + j, DECODE["b_std"])
+                               for j in range(len(MS))]
+        oracle.build()
+    As, Bs = _ORACLE_INPUTS["A"], _ORACLE_INPUTS["B"]
+    t0 = time.perf_counter()
+    for idx, M in enumerate(MS):
+        oracle.gemm_rows(As[M], Bs[idx], M, N_DEC, K_DEC)
+    return time.perf_counter() - t0, oracle.num_threads()
+
+
+def cpu_baseline(budget_s: float = 10.0) -> dict:
+    """The oracle, as it stands, timed on this host's cores on whole decode
+    steps, repeated until about `budget_s` seconds of CPU work."""
+    total, reps, threads = 0.0, 0, 1
+    while total < budget_s or reps == 0:
+        dt, threads = oracle_decode_step()
+        total += dt
+        reps += 1
+        if reps >= 200:
+            break
+    value = decode_flops_per_step() * reps / total / 1e12
+    return {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "%d whole decode steps (M=1,4,16,64 x N=K=4096, binary64 triple loop, "
+                      "OpenMP over rows), %.1f s" % (reps, total)}
+
+
+def run_reference(args, world: int, rank: int):
+    """--impl reference: the CPU oracle on the decode step, K timed steps."""
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_decode_step()
+    total, threads = 0.0, 1
+    for _ in range(args.steps):
+        dt, threads = oracle_decode_step()
+        total += dt
+    value = decode_flops_per_step() * args.steps / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": decode_config(8),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "%d whole decode steps on the host cores" % args.steps},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def decode_config(split: int) -> dict:
+    return {"workload": "decode-shaped BF16 GEMM: M in {1,4,16,64}, N=K=4096, A~N(0,1), "
+                        "B~N(0,0.02) bf16, FP32 out, split_k=%d from K only" % split,
+            "M": list(MS), "N": N_DEC, "K": K_DEC, "split_k": split,
+            "l2": "weights rotate through a pool of %d matrices (%d MiB > L2)"
+                  % (POOL, POOL * N_DEC * K_DEC * 2 >> 20),
+            "parallelism": "replicas"}
+
+
+# ------------------------------------------------------------------- main --
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other shapes, e2e and the CPU baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+
+    bench = DecodeBench(dev)
+    for i in range(args.warmup):          # eager warm-up (loads the module)
+        bench.step(i)
+    torch.cuda.synchronize()
+    with_events = external_events_supported()
+    bench.capture(with_events)
+    for i in range(args.warmup):
+        bench.replay(i)
+    torch.cuda.synchronize()
+
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    nvml_index = int(vis.split(",")[local]) if vis and vis.split(",")[local].isdigit() else local
+    sampler = ClockSampler(nvml_index)
+    remeasured = False
+    for attempt in range(2):
+        sampler.start()
+        secs = time_region(bench.replay, args.steps, world)
+        clocks = sampler.stop()
+        if not ClockSampler.rejected(clocks):
+            break
+        remeasured = True
+    kt = bench.kernel_times_ms()
+    kt_source = "external CUDA events around each partial launch in the last replay of each step graph"
+    if not kt:
+        kt = bench.kernel_times_eager(8)
+        kt_source = "CUDA events around eager partial launches (no external graph events in this torch)"
+
+    flops_step = decode_flops_per_step()
+    value = job_throughput(flops_step * args.steps, world, secs)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": decode_config(bench.split),
+        "gpu_launches": bench.launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if remeasured:
+        line["clocks"]["remeasured"] = True
+    if kt:
+        by_m = {}
+        for M, ms in kt:
+            by_m.setdefault(M, []).append(ms)
+        alg = sum(decode_alg_bytes(M) * len(v) for M, v in by_m.items())
+        dur = sum(sum(v) for v in by_m.values())
+        achieved = alg / (dur / 1e3) / 1e9
+        line["roofline"] = {
+            "kernel": "bigemm_tc_kernel<kOutSlices> (split-K partial)",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": None,
+            "per_M_us": {str(M): round(1e3 * sum(v) / len(v), 3) for M, v in sorted(by_m.items())},
+            "per_M_hbm_frac": {str(M): round(decode_alg_bytes(M) / (sum(v) / len(v) / 1e3) / 1e9
+                                             / peaks["hbm_gbs"], 4) for M, v in sorted(by_m.items())},
+            "launches_timed": len(kt),
+            "timing": kt_source,
+        }
+    if rank == 0 and world == 1 and not args.no_extras:
+        line["e2e"] = run_e2e(bench, max(20, args.steps // 20), 5)
+        line["workloads"] = run_other_workloads(dev, peaks)
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -248,6 +248,11 @@ def matmul(A, B, out_dtype=None, split_k: int = 1, out=None, workspace=None, str
     lda = A.stride(0) if M > 1 else max(K, 8 * ((K + 7) // 8))
     ldb = B.stride(0) if K > 1 else max(N, 8 * ((N + 7) // 8))
     ldc = out.stride(0) if M > 1 else max(N, 8 * ((N + 7) // 8))
+    if lda % 8 or ldb % 8 or ldc % (8 if out_dtype == torch.bfloat16 else 4):
+        raise ValueError(
+            "row strides must be multiples of 8 elements for A and B (16-byte rows for the "
+            "tensor memory accelerator) and of %d for C; got lda=%d ldb=%d ldc=%d -- store the "
+            "matrices with padded rows" % (8 if out_dtype == torch.bfloat16 else 4, lda, ldb, ldc))
     if atomic:
         if out_dtype != torch.float32:
             raise ValueError("the atomic contrast writes fp32")

@@ -110,7 +110,7 @@ def test_empty_products():
 
 
 def test_matmul_wrapper_and_launch_count(cuda_device):
-    M, N, K = 100, 300, 2048
+    M, N, K = 100, 320, 2048
     A, B = workloads.pair(M, N, K, 5)
     Cref, D = oracle_rows(A, B, M, N, K)
     Ad, Bd = A.cuda(), B.cuda()
@@ -121,6 +121,10 @@ def test_matmul_wrapper_and_launch_count(cuda_device):
     torch.cuda.synchronize()
     check_tolerance(to_f64(C), Cref, D, False, "matmul S=4")
     check_tolerance(to_f64(C1), Cref, D, False, "matmul S=1")
+    # a B whose row stride is not a multiple of 8 elements is refused up front
+    Bbad = workloads.normal_bf16((K, 300), 6).cuda()
+    with pytest.raises(ValueError):
+        dig.matmul(Ad, Bbad)
 
 
 # -------------------------------------------------- the reduction, bitwise --
