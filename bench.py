@@ -234,8 +234,8 @@ class DecodeBench:
         self.eff = dig.bigemm_effective_split_k(K_DEC, self.split)
         self.period = POOL // len(MS)            # steps per rotation of the weight pool
         self.launches_per_step = 2 * len(MS)
-        self.graphs = []
-        self.events = []                          # per graph: [(M, start, end)]
+        self.full = None
+        self.single = []
 
     def product(self, M: int, B: torch.Tensor, ev=None):
         dig = self.dig
@@ -252,49 +252,74 @@ class DecodeBench:
             B = self.B[(i * len(MS) + idx) % POOL]
             self.product(M, B, None if events is None else events[idx])
 
-    def capture(self, with_events: bool):
-        """One graph per step of the rotation period, so that every replay
-        streams a different set of four weight matrices."""
+    def _capture(self, fn):
         s = torch.cuda.Stream(device=self.dev)
         s.wait_stream(torch.cuda.current_stream())
-        for i in range(self.period):
-            g = torch.cuda.CUDAGraph()
-            evs = None
-            if with_events:
-                evs = [(torch.cuda.Event(enable_timing=True, external=True),
-                        torch.cuda.Event(enable_timing=True, external=True)) for _ in MS]
-            with torch.cuda.graph(g, stream=s):
-                self.step(i, evs)
-            self.graphs.append(g)
-            self.events.append(evs)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fn()
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
+        return g
 
-    def replay(self, i: int):
-        self.graphs[i % self.period].replay()
+    def capture(self):
+        """The timed graphs hold kernels only, so consecutive launches keep their
+        programmatic (early-launch) dependencies: one graph for a whole
+        rotation of the weight pool (`period` steps) and one per single step
+        for a remainder."""
+        self.full = self._capture(lambda: [self.step(i) for i in range(self.period)])
+        self.single = [self._capture(lambda i=i: self.step(i)) for i in range(self.period)]
 
-    def kernel_times_eager(self, steps: int):
-        """Fallback: time the partial kernel of every product of `steps` eager
-        steps with CUDA events on the launching (current) stream."""
-        out = []
-        for i in range(steps):
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in MS]
-            self.step(i, evs)
+    def run_steps(self, first: int, count: int):
+        """Replay `count` steps starting at step index `first`."""
+        i = first
+        while count >= self.period and i % self.period == 0:
+            self.full.replay()
+            i += self.period
+            count -= self.period
+        for _ in range(count):
+            self.single[i % self.period].replay()
+            i += 1
+
+    def partial_chain_us(self, reps: int = 50):
+        """Average duration of the split-K partial kernel per M, launched back to
+        back (16 launches rotating through the weight pool, one graph, CUDA
+        events around `reps` replays).  Returns {M: microseconds}."""
+        out = {}
+        for M in MS:
+            def chain(M=M):
+                for j in range(POOL):
+                    self.dig.bigemm_run_partial(self.A[M], self.B[j], M, N_DEC, K_DEC, K_DEC, N_DEC,
+                                                self.split, self.ws[M], self.ws_bytes[M])
+            g = self._capture(chain)
+            for _ in range(3):
+                g.replay()
             torch.cuda.synchronize()
-            out.extend((M, a.elapsed_time(b)) for M, (a, b) in zip(MS, evs))
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            out[M] = e0.elapsed_time(e1) * 1e3 / (reps * POOL)
         return out
 
-    def kernel_times_ms(self):
-        """Durations of the partial-kernel launches recorded by the last replay
-        of every graph: [(M, ms)]."""
-        out = []
-        for evs in self.events:
-            if evs is None:
-                continue
+    def partial_isolated_us(self, rounds: int = 25):
+        """Durations of partial launches separated by events inside the step
+        graph (each duration then includes its kernel's start-up).  {M: us}"""
+        if not external_events_supported():
+            return {}
+        evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in MS]
+        g = self._capture(lambda: self.step(0, evs))
+        acc = {M: [] for M in MS}
+        for _ in range(rounds):
+            g.replay()
+            torch.cuda.synchronize()
             for M, (a, b) in zip(MS, evs):
-                out.append((M, a.elapsed_time(b)))
-        return out
+                acc[M].append(a.elapsed_time(b) * 1e3)
+        return {M: sum(v) / len(v) for M, v in acc.items()}
 
 
 def time_region(fn, steps: int, world: int) -> float:
@@ -309,6 +334,23 @@ def time_region(fn, steps: int, world: int) -> float:
     e0.record()
     for i in range(steps):
         fn(i)
+    e1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    return max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+
+
+def time_region_steps(bench: DecodeBench, steps: int, world: int) -> float:
+    """time_region for the decode step graphs (whole rotations in one replay)."""
+    import torch.distributed as dist
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    bench.run_steps(0, steps)
     e1.record()
     torch.cuda.synchronize()
     if world > 1:
@@ -492,10 +534,8 @@ def main():
     for i in range(args.warmup):          # eager warm-up (loads the module)
         bench.step(i)
     torch.cuda.synchronize()
-    with_events = external_events_supported()
-    bench.capture(with_events)
-    for i in range(args.warmup):
-        bench.replay(i)
+    bench.capture()
+    bench.run_steps(0, args.warmup)
     torch.cuda.synchronize()
 
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
@@ -504,16 +544,13 @@ def main():
     remeasured = False
     for attempt in range(2):
         sampler.start()
-        secs = time_region(bench.replay, args.steps, world)
+        secs = time_region_steps(bench, args.steps, world)
         clocks = sampler.stop()
         if not ClockSampler.rejected(clocks):
             break
         remeasured = True
-    kt = bench.kernel_times_ms()
-    kt_source = "external CUDA events around each partial launch in the last replay of each step graph"
-    if not kt:
-        kt = bench.kernel_times_eager(8)
-        kt_source = "CUDA events around eager partial launches (no external graph events in this torch)"
+    chain = bench.partial_chain_us()
+    isolated = bench.partial_isolated_us()
 
     flops_step = decode_flops_per_step()
     value = job_throughput(flops_step * args.steps, world, secs)
@@ -527,24 +564,23 @@ def main():
     }
     if remeasured:
         line["clocks"]["remeasured"] = True
-    if kt:
-        by_m = {}
-        for M, ms in kt:
-            by_m.setdefault(M, []).append(ms)
-        alg = sum(decode_alg_bytes(M) * len(v) for M, v in by_m.items())
-        dur = sum(sum(v) for v in by_m.values())
-        achieved = alg / (dur / 1e3) / 1e9
-        line["roofline"] = {
-            "kernel": "bigemm_tc_kernel<kOutSlices> (split-K partial)",
-            "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-            "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "traffic": None,
-            "per_M_us": {str(M): round(1e3 * sum(v) / len(v), 3) for M, v in sorted(by_m.items())},
-            "per_M_hbm_frac": {str(M): round(decode_alg_bytes(M) / (sum(v) / len(v) / 1e3) / 1e9
-                                             / peaks["hbm_gbs"], 4) for M, v in sorted(by_m.items())},
-            "launches_timed": len(kt),
-            "timing": kt_source,
-        }
+    alg = sum(decode_alg_bytes(M) for M in MS)
+    dur_s = sum(chain[M] for M in MS) / 1e6
+    achieved = alg / dur_s / 1e9
+    line["roofline"] = {
+        "kernel": "bigemm_tc_kernel<kOutSlices> (split-K partial, split_k=%d)" % bench.split,
+        "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+        "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+        "traffic": None,
+        "bytes_per_launch": {str(M): decode_alg_bytes(M) for M in MS},
+        "us_per_launch": {str(M): round(chain[M], 3) for M in MS},
+        "hbm_frac_per_M": {str(M): round(decode_alg_bytes(M) / (chain[M] / 1e6) / 1e9 / peaks["hbm_gbs"], 4)
+                           for M in MS},
+        "timing": "CUDA events on the launching stream around graph replays of %d back-to-back "
+                  "partial launches per M (weights rotating through the pool); achieved = sum of "
+                  "algorithmic bytes over sum of per-launch times for M=1,4,16,64" % POOL,
+        "isolated_us_per_launch": {str(M): round(v, 3) for M, v in isolated.items()},
+    }
     if rank == 0 and world == 1 and not args.no_extras:
         line["e2e"] = run_e2e(bench, max(20, args.steps // 20), 5)
         line["workloads"] = run_other_workloads(dev, peaks)

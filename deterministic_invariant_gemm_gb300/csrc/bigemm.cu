@@ -139,17 +139,61 @@ size_t slice_bytes(int64_t M, int64_t N, int slices) {
     return static_cast<size_t>(b);
 }
 
-bool encode_bf16_2d(CUtensorMap* map, const void* ptr, int64_t inner, int64_t outer, int64_t ld,
-                    uint32_t box_inner, uint32_t box_outer) {
+// A row-major tensor of `rank` (2 or 3) dimensions, innermost first: dims[0]
+// contiguous elements, dims[1] rows `ld` elements apart, dims[2] slices
+// `slice` elements apart.  Boxes of box[0] x box[1] (x 1).
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t esize, const void* ptr,
+                  int rank, const int64_t* dims, int64_t ld, int64_t slice, const uint32_t* box,
+                  CUtensorMapSwizzle swizzle) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    cuuint64_t gdims[3] = {static_cast<cuuint64_t>(dims[0]), static_cast<cuuint64_t>(dims[1]),
+                           static_cast<cuuint64_t>(rank > 2 ? dims[2] : 1)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * esize,
+                             static_cast<cuuint64_t>(slice) * esize};
+    cuuint32_t gbox[3] = {box[0], box[1], 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), gdims, strides, gbox,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Operand maps: A [M, K] in boxes of 64 k x 128 rows, B [K, N] in boxes of 64
+// columns x 64 k-rows, both with the 128-byte swizzle the MMA descriptors use.
+bool encode_operands(CUtensorMap* tmA, CUtensorMap* tmB, const void* A, const void* B, int64_t M,
+                     int64_t N, int64_t K, int64_t lda, int64_t ldb) {
+    const int64_t da[2] = {K, M}, db[2] = {N, K};
+    const uint32_t ba[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(kBM)};
+    const uint32_t bb[2] = {kBChunkCols, static_cast<uint32_t>(kBK)};
+    return encode_tiled(tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, 2, da, lda, 0, ba,
+                        CU_TENSOR_MAP_SWIZZLE_128B) &&
+           encode_tiled(tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, 2, db, ldb, 0, bb,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Output maps for the epilogue's 32 x 32 TMA stores: fp32 C (128-byte
+// swizzle), bf16 C (64-byte swizzle), or the fp32 workspace as a 3-D tensor
+// [splits][M][ws_ld] (128-byte swizzle).
+bool encode_out_f32(CUtensorMap* m, void* C, int64_t M, int64_t N, int64_t ldc) {
+    const int64_t d[2] = {N, M};
+    const uint32_t box[2] = {32, 32};
+    return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, 2, d, ldc, 0, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool encode_out_bf16(CUtensorMap* m, void* C, int64_t M, int64_t N, int64_t ldc) {
+    const int64_t d[2] = {N, M};
+    const uint32_t box[2] = {32, 32};
+    return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, 2, d, ldc, 0, box,
+                        CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+bool encode_out_slices(CUtensorMap* m, void* ws, int64_t M, int64_t N, int splits) {
+    const int64_t ld = ws_ld_of(N);
+    const int64_t d[3] = {N, M, splits};
+    const uint32_t box[2] = {32, 32};
+    return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, 3, d, ld, M * ld, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <typename Kernel, typename... Args>
@@ -240,9 +284,9 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
         return e == cudaSuccess ? BIGEMM_OK : BIGEMM_ERR_CUDA;
     }
 
-    CUtensorMap tmA, tmB;
-    if (!encode_bf16_2d(&tmA, A, K, M, lda, kBK, kBM)) return BIGEMM_ERR_CUDA;
-    if (!encode_bf16_2d(&tmB, B, N, K, ldb, kBChunkCols, kBK)) return BIGEMM_ERR_CUDA;
+    CUtensorMap tmA, tmB, tmC;
+    std::memset(&tmC, 0, sizeof(tmC));
+    if (!encode_operands(&tmA, &tmB, A, B, M, N, K, lda, ldb)) return BIGEMM_ERR_CUDA;
 
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
@@ -267,13 +311,14 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
         if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
         p.out = C;
         p.ld_out = ldc;
-        e = launch_pdl(bigemm_tc_kernel<kOutAtomic>, g, blk, kSmemBytes, stream, tmA, tmB, p);
+        e = launch_pdl(bigemm_tc_kernel<kOutAtomic>, g, blk, kSmemBytes, stream, tmA, tmB, tmC, p);
         launches = 1;
     } else if (mode == kModePartial || splits > 1) {
         p.out = ws;
         p.ld_out = ws_ld_of(N);
         p.slice_stride = M * p.ld_out;
-        e = launch_pdl(bigemm_tc_kernel<kOutSlices>, g, blk, kSmemBytes, stream, tmA, tmB, p);
+        if (!encode_out_slices(&tmC, ws, M, N, splits)) return BIGEMM_ERR_CUDA;
+        e = launch_pdl(bigemm_tc_kernel<kOutSlices>, g, blk, kSmemBytes, stream, tmA, tmB, tmC, p);
         launches = 1;
         if (e == cudaSuccess && mode != kModePartial) {
             st = launch_reduce(*d, static_cast<const float*>(ws), splits, M, N, C, ldc,
@@ -284,10 +329,13 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     } else {
         p.out = C;
         p.ld_out = ldc;
-        if (mode == kModeBF16)
-            e = launch_pdl(bigemm_tc_kernel<kOutBF16>, g, blk, kSmemBytes, stream, tmA, tmB, p);
-        else
-            e = launch_pdl(bigemm_tc_kernel<kOutF32>, g, blk, kSmemBytes, stream, tmA, tmB, p);
+        if (mode == kModeBF16) {
+            if (!encode_out_bf16(&tmC, C, M, N, ldc)) return BIGEMM_ERR_CUDA;
+            e = launch_pdl(bigemm_tc_kernel<kOutBF16>, g, blk, kSmemBytes, stream, tmA, tmB, tmC, p);
+        } else {
+            if (!encode_out_f32(&tmC, C, M, N, ldc)) return BIGEMM_ERR_CUDA;
+            e = launch_pdl(bigemm_tc_kernel<kOutF32>, g, blk, kSmemBytes, stream, tmA, tmB, tmC, p);
+        }
         launches = 1;
     }
     if (e != cudaSuccess) return BIGEMM_ERR_CUDA;

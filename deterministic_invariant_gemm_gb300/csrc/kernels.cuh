@@ -21,9 +21,9 @@
 // CTA roles (192 threads, one CTA per SM):
 //   warp 0      TMA producer: fills a kStages-deep shared-memory ring.
 //   warp 1      allocates TMEM; one lane issues the MMAs and commits.
-//   warps 2..5  epilogue: TMEM -> registers -> global, one C row per thread;
-//               two TMEM accumulators let the epilogue of tile t overlap the
-//               mainloop of tile t + 1.
+//   warps 2..5  epilogue: TMEM -> registers -> swizzled shared-memory boxes
+//               -> TMA stores; two TMEM accumulators let the epilogue of tile
+//               t overlap the mainloop of tile t + 1.
 #pragma once
 
 #include <cuda.h>
@@ -51,8 +51,14 @@ constexpr uint32_t kBChunkBytes = kBK * kBChunkCols * 2;  // 8 KiB: 64 k-rows x 
 constexpr uint32_t kBBytes = kBK * kBN * 2;       // 32 KiB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr int kNumBarriers = 2 * kStages + 2 * kAccStages + 1;
-constexpr uint32_t kSmemBytes =
-    1024 /* alignment slack */ + kStages * kStageBytes + kNumBarriers * 8 + 16;
+// Epilogue staging: two 32-row x 128-byte boxes per epilogue warp, the source
+// of the TMA stores (fp32: 32 columns, 128-byte swizzle; bf16: 32 columns in
+// the first 64 bytes of each row, 64-byte swizzle).
+constexpr uint32_t kStageBufBytes = 32 * 128;
+constexpr uint32_t kStagingBytes = (kEpilogueThreads / 32) * 2 * kStageBufBytes;  // 32 KiB
+constexpr uint32_t kSmemBytes = 1024 /* alignment slack */ + kStages * kStageBytes +
+                                kStagingBytes + kNumBarriers * 8 + 16;
+static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103 CTA");
 
 constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, /*A MN-major*/ false, /*B MN-major*/ true);
 
@@ -85,13 +91,14 @@ struct GemmParams {
     int units;              // m_tiles * n_tiles * splits
 };
 
-// Unit u -> (tile row, tile column, K segment).  Segments of one tile are
-// adjacent; tiles follow the GROUP_M swizzle: groups of kGroupM tile rows,
-// column-major inside a group.
+// Unit u -> (tile row, tile column, K segment).  All tiles of segment 0 come
+// first, then segment 1, ...; inside a segment the tiles follow the GROUP_M
+// swizzle: groups of kGroupM tile rows, column-major inside a group.
 __device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& mt, int& nt,
                                             int& seg) {
-    const int tile = u / p.splits;
-    seg = u - tile * p.splits;
+    const int tiles = p.m_tiles * p.n_tiles;
+    seg = u / tiles;
+    const int tile = u - seg * tiles;
     const int per_group = kGroupM * p.n_tiles;
     const int g = tile / per_group;
     const int first_m = g * kGroupM;
@@ -121,56 +128,67 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
     return false;
 }
 
+// Thread `lane` holds row `lane` of a 32 x 32 fp32 block (32 registers).  The
+// staging writers put it into a shared-memory box in the layout the TMA store
+// expects: fp32 rows of 128 bytes whose 16-byte chunks are permuted by the
+// 128-byte swizzle (chunk j of row r at j ^ (r % 8)); bf16 rows of 64 bytes
+// with the 64-byte swizzle (chunk j of row r at j ^ ((r / 2) % 4)).  Both
+// permutations also spread a quarter-warp's 16-byte stores over all banks.
+__device__ __forceinline__ void stage_f32(uint32_t buf, int lane, const uint32_t (&r)[32]) {
+    const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        st_shared_v4(row + ((static_cast<uint32_t>(j) ^ (lane & 7)) << 4), r[4 * j], r[4 * j + 1],
+                     r[4 * j + 2], r[4 * j + 3]);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+    return *reinterpret_cast<uint32_t*>(&b2);
+}
+
+__device__ __forceinline__ void stage_bf16(uint32_t buf, int lane, const uint32_t (&r)[32]) {
+    const uint32_t row = buf + static_cast<uint32_t>(lane) * 64u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        st_shared_v4(row + ((static_cast<uint32_t>(j) ^ ((lane >> 1) & 3)) << 4),
+                     pack_bf16x2(r[8 * j], r[8 * j + 1]), pack_bf16x2(r[8 * j + 2], r[8 * j + 3]),
+                     pack_bf16x2(r[8 * j + 4], r[8 * j + 5]), pack_bf16x2(r[8 * j + 6], r[8 * j + 7]));
+}
+
+// A row's 32 values stored element by element, columns >= N skipped.
 template <int kOut>
-__device__ __forceinline__ void store_row_chunk(const GemmParams& p, int seg, int row, int col,
-                                                const uint32_t (&r)[32]) {
+__device__ __forceinline__ void store_row_masked(const GemmParams& p, int row, int col,
+                                                 const uint32_t (&r)[32]) {
     const int valid = min(32, p.N - col);
     if constexpr (kOut == kOutBF16) {
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.ld_out + col;
-        if (valid == 32) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst);
+        __nv_bfloat16* dst =
+            static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.ld_out + col;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                uint32_t w[4];
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[8 * v + 2 * h]),
-                                                              __uint_as_float(r[8 * v + 2 * h + 1]));
-                    w[h] = *reinterpret_cast<uint32_t*>(&b2);
-                }
-                d4[v] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-                if (c < valid) dst[c] = __float2bfloat16_rn(__uint_as_float(r[c]));
-        }
-    } else if constexpr (kOut == kOutAtomic) {
+        for (int c = 0; c < 32; ++c)
+            if (c < valid) dst[c] = __float2bfloat16_rn(__uint_as_float(r[c]));
+    } else {
         float* dst = static_cast<float*>(p.out) + static_cast<int64_t>(row) * p.ld_out + col;
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-            if (c < valid) atomicAdd(dst + c, __uint_as_float(r[c]));
-    } else {
-        float* dst = static_cast<float*>(p.out) + static_cast<int64_t>(row) * p.ld_out + col;
-        if constexpr (kOut == kOutSlices) dst += static_cast<int64_t>(seg) * p.slice_stride;
-        if (valid == 32) {
-            float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-                d4[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                    __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-        } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-                if (c < valid) dst[c] = __uint_as_float(r[c]);
-        }
+            if (c < valid) dst[c] = __uint_as_float(r[c]);
     }
+}
+
+// The atomic contrast: every thread adds its row's 32 values into C.
+__device__ __forceinline__ void atomic_add_row_chunk(const GemmParams& p, int row, int col,
+                                                     const uint32_t (&r)[32]) {
+    const int valid = min(32, p.N - col);
+    float* dst = static_cast<float*>(p.out) + static_cast<int64_t>(row) * p.ld_out + col;
+#pragma unroll
+    for (int c = 0; c < 32; ++c)
+        if (c < valid) atomicAdd(dst + c, __uint_as_float(r[c]));
 }
 
 template <int kOut>
 __global__ void __launch_bounds__(kNumThreads, 1)
     bigemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     // 128-byte-swizzled tiles must start on 1024-byte boundaries.
     const uint32_t raw = smem_addr(smem_raw);
@@ -178,7 +196,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     uint8_t* gbase = smem_raw + (base - raw);
     const uint32_t sA = base;                                // stage s: sA + s * kABytes
     const uint32_t sB = base + kStages * kABytes;            // stage s: sB + s * kBBytes
-    uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kStages * kStageBytes);
+    const uint32_t sOut = base + kStages * kStageBytes;      // epilogue staging boxes
+    uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kStages * kStageBytes + kStagingBytes);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBarriers);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -208,6 +227,21 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if constexpr (kOut != kOutAtomic) tma_prefetch_desc(&tmC);
+        // Warm L2 with the first weight tiles of this CTA's first unit while the
+        // previous kernel in the stream finishes.  An L2 prefetch writes no
+        // shared memory and L2 is the device's point of coherence, so it cannot
+        // expose data older than the dependency wait below.
+        if (static_cast<int>(blockIdx.x) < p.units) {
+            int mt, nt, seg;
+            unit_coords(p, blockIdx.x, mt, nt, seg);
+            const int kb0 = seg * p.kb_per_split;
+            const int kb1 = min(min(kb0 + p.kb_per_split, p.kb_total), kb0 + kStages);
+            for (int kb = kb0; kb < kb1; ++kb)
+#pragma unroll
+                for (int c = 0; c < kBN / static_cast<int>(kBChunkCols); ++c)
+                    tma_prefetch_l2_2d(&tmB, nt * kBN + c * static_cast<int>(kBChunkCols), kb * kBK);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -218,13 +252,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    // Everything above overlaps the previous kernel in the stream; global
-    // memory is touched only after it has finished.
+    // Everything above overlaps the previous kernel in the stream; from here on
+    // global memory is read and written only after it has completed.
     grid_dependency_wait();
 
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer --
+            // The next kernel in the stream may start its own prologue now; it
+            // waits for this grid to complete before touching memory.
+            grid_launch_dependents();
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
@@ -256,7 +293,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                 }
             }
-            grid_launch_dependents();
             // No copy may still be in flight when the CTA exits: wait (bounded)
             // for the last load issued into every stage.
             for (int s = 0; s < kStages; ++s)
@@ -318,8 +354,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
     } else {
         // ------------------------------------------------------ epilogue --
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int row_in_tile = q * 32 + lane;
+        // Warp w reads TMEM lanes 32 (w % 4) .. +31, i.e. tile rows q*32 .. q*32+31.
+        // Each 32 x 32 block goes TMEM -> registers -> a swizzled staging box ->
+        // one TMA store (coalesced, asynchronous; rows >= M and columns >= N
+        // fall outside the tensor map and are not written).  Two boxes per
+        // warp alternate, so a block is staged while the previous one is stored.
+        const int q = warp & 3;
+        const uint32_t my_boxes = sOut + static_cast<uint32_t>(warp - 2) * 2u * kStageBufBytes;
+        uint32_t nblk = 0;  // blocks this warp has handed to the TMA unit
         int t = 0;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
             int mt, nt, seg;
@@ -329,10 +371,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (!wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.status, kErrWaitEpilogue))
                 break;
             tc_fence_after();
-            const int m0 = mt * kBM, n0 = nt * kBN;
-            const int row = m0 + row_in_tile;
-            const bool warp_has_rows = (m0 + q * 32) < p.M;  // uniform per warp
-            if (warp_has_rows) {
+            const int m0 = mt * kBM + q * 32, n0 = nt * kBN;
+            if (m0 < p.M) {  // uniform per warp: a warp whose rows are all past M skips
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        static_cast<uint32_t>(acc * kBN);
 #pragma unroll 1
@@ -342,12 +382,42 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tbase + ch * 32, r);
                     tmem_ld_wait();
-                    if (row < p.M) store_row_chunk<kOut>(p, seg, row, col, r);
+                    // The TMA unit clips the innermost dimension at 16-byte granularity,
+                    // so a block ending in a partial 16-byte chunk of a C row is
+                    // written element by element (the workspace owns its padding).
+                    constexpr int kVec = (kOut == kOutBF16) ? 8 : 4;
+                    const bool ragged = kOut != kOutSlices && col + 32 > p.N && (p.N % kVec) != 0;
+                    if constexpr (kOut == kOutAtomic) {
+                        if (m0 + lane < p.M) atomic_add_row_chunk(p, m0 + lane, col, r);
+                    } else if (ragged) {
+                        if (m0 + lane < p.M) store_row_masked<kOut>(p, m0 + lane, col, r);
+                    } else {
+                        const uint32_t box = my_boxes + (nblk & 1u) * kStageBufBytes;
+                        if (nblk >= 2) {
+                            // the store issued from this box two blocks ago must
+                            // have finished reading it
+                            if (lane == 0) bulk_wait_group_read<1>();
+                            __syncwarp();
+                        }
+                        if constexpr (kOut == kOutBF16) stage_bf16(box, lane, r);
+                        else stage_f32(box, lane, r);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if constexpr (kOut == kOutSlices) tma_store_3d(&tmC, box, col, m0, seg);
+                            else tma_store_2d(&tmC, box, col, m0);
+                            bulk_commit_group();
+                        }
+                        ++nblk;
+                    }
                 }
             }
             tc_fence_before();
             mbar_arrive(tempty_bar(acc));
         }
+        // All of this warp's stores complete before the CTA exits.
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -368,6 +438,7 @@ __global__ void __launch_bounds__(256)
     splitk_reduce_kernel(const float* __restrict__ ws, void* __restrict__ C, int M, int N,
                          int64_t ldc, int64_t ws_ld, int S) {
     grid_dependency_wait();
+    grid_launch_dependents();
     const int64_t vec_per_row = ws_ld / 4;
     const int64_t total = static_cast<int64_t>(M) * vec_per_row;
     const int64_t slice = static_cast<int64_t>(M) * ws_ld;
@@ -415,7 +486,6 @@ __global__ void __launch_bounds__(256)
             }
         }
     }
-    grid_launch_dependents();
 }
 
 }  // namespace bigemm
