@@ -34,7 +34,7 @@ __all__ = [
     "bigemm_workspace_bytes", "bigemm_partial_workspace_bytes", "bigemm_run",
     "bigemm_run_bf16out", "bigemm_run_partial", "bigemm_splitk_reduce",
     "bigemm_run_atomic_splitk", "bigemm_device_status", "bigemm_last_launch_count",
-    "matmul", "EXPORTED_SYMBOLS",
+    "bigemm_run_splitk_static", "STATIC_SCRATCH_BYTES", "matmul", "EXPORTED_SYMBOLS",
 ]
 
 BLOCK_K = 64
@@ -44,14 +44,17 @@ TILE_N = 256
 STATUS_NAMES = {
     0: "BIGEMM_OK", 1: "BIGEMM_ERR_ARG", 2: "BIGEMM_ERR_ALIGN", 3: "BIGEMM_ERR_WORKSPACE",
     4: "BIGEMM_ERR_UNSUPPORTED", 5: "BIGEMM_ERR_CUDA", 6: "BIGEMM_ERR_TIMEOUT",
+    7: "BIGEMM_ERR_STATIC_LIMIT",
 }
+
+STATIC_SCRATCH_BYTES = 16 << 20
 
 EXPORTED_SYMBOLS = (
     "bigemm_version", "bigemm_status_string", "bigemm_max_split_k", "bigemm_default_split_k",
     "bigemm_effective_split_k", "bigemm_workspace_ld", "bigemm_workspace_bytes",
     "bigemm_partial_workspace_bytes", "bigemm_run", "bigemm_run_bf16out", "bigemm_run_partial",
     "bigemm_splitk_reduce", "bigemm_run_atomic_splitk", "bigemm_device_status",
-    "bigemm_last_launch_count",
+    "bigemm_last_launch_count", "bigemm_run_splitk_static",
 )
 
 
@@ -94,6 +97,7 @@ def load():
         "bigemm_splitk_reduce": ([vp, i32, i64, i64, vp, i64, i32, vp], i32),
         "bigemm_run_atomic_splitk": ([vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, vp], i32),
         "bigemm_device_status": ([i32], i32),
+        "bigemm_run_splitk_static": ([vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, vp], i32),
         "bigemm_last_launch_count": ([], i32),
     }
     for name, (args, res) in sig.items():
@@ -210,6 +214,19 @@ def bigemm_run_atomic_splitk(A, B, C, M, N, K, lda, ldb, ldc, split_k, stream=No
                                          split_k, _stream(stream))
     if check:
         _check(st, "bigemm_run_atomic_splitk")
+    return st
+
+
+def bigemm_run_splitk_static(A, B, C, M, N, K, lda, ldb, ldc, split_k, stream=None,
+                             check=True) -> int:
+    """bigemm_run without a workspace argument and without any allocation: the
+    split-K partials go to the library's built-in 16 MiB device array.  For
+    callers that may not allocate device memory per call; calls that can
+    overlap on the GPU share that array and must be ordered."""
+    st = load().bigemm_run_splitk_static(_ptr(A), _ptr(B), _ptr(C), M, N, K, lda, ldb, ldc,
+                                         split_k, _stream(stream))
+    if check:
+        _check(st, "bigemm_run_splitk_static")
     return st
 
 

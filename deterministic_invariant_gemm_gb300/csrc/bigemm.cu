@@ -344,6 +344,36 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
 }
 
 }  // namespace
+
+// Split-K scratch for bigemm_run_splitk_static, for callers that cannot
+// allocate: a fixed array in every loaded device image.  Host code sees only a
+// host-side stand-in under this name, so the device address is looked up per
+// device with cudaGetSymbolAddress and passed to the kernels.
+static __device__ __align__(256) unsigned char g_static_scratch[BIGEMM_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_static_mu;
+void* g_static_addr[kMaxDevices];
+
+// Device address of g_static_scratch on the current device, looked up on the
+// first call for that device.
+bigemm_status static_scratch_address(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BIGEMM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return BIGEMM_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (g_static_addr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress((void**)&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr)
+            return BIGEMM_ERR_CUDA;
+        g_static_addr[dev] = ptr;
+    }
+    *out = g_static_addr[dev];
+    return BIGEMM_OK;
+}
+
+}  // namespace
 }  // namespace bigemm
 
 using namespace bigemm;
@@ -361,6 +391,10 @@ const char* bigemm_status_string(bigemm_status s) {
         case BIGEMM_ERR_UNSUPPORTED: return "BIGEMM_ERR_UNSUPPORTED: current device is not sm_103";
         case BIGEMM_ERR_CUDA: return "BIGEMM_ERR_CUDA: a CUDA call failed";
         case BIGEMM_ERR_TIMEOUT: return "BIGEMM_ERR_TIMEOUT: a kernel's bounded wait expired";
+        case BIGEMM_ERR_STATIC_LIMIT:
+            return "BIGEMM_ERR_STATIC_LIMIT: the product needs more split-K scratch than the "
+                   "library's built-in 16 MiB array; pass a workspace to bigemm_run or use a "
+                   "smaller split_k";
     }
     return "BIGEMM_ERR_UNKNOWN";
 }
@@ -430,6 +464,22 @@ bigemm_status bigemm_run_atomic_splitk(const void* A, const void* B, float* C, i
                                        int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int split_k,
                                        bigemm_stream stream) {
     return run_impl(kModeAtomic, A, B, C, M, N, K, lda, ldb, ldc, split_k, nullptr, 0,
+                    static_cast<cudaStream_t>(stream));
+}
+
+bigemm_status bigemm_run_splitk_static(const void* A, const void* B, float* C, int64_t M, int64_t N,
+                                       int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                       int split_k, bigemm_stream stream) {
+    g_last_launches = 0;
+    const size_t need = bigemm_workspace_bytes(M, N, K, split_k);
+    if (need > BIGEMM_STATIC_SCRATCH_BYTES) return BIGEMM_ERR_STATIC_LIMIT;
+    void* scratch = nullptr;
+    if (need > 0) {
+        const bigemm_status st = static_scratch_address(&scratch);
+        if (st != BIGEMM_OK) return st;
+    }
+    return run_impl(kModeF32, A, B, C, M, N, K, lda, ldb, ldc, split_k, scratch,
+                    scratch ? static_cast<size_t>(BIGEMM_STATIC_SCRATCH_BYTES) : 0,
                     static_cast<cudaStream_t>(stream));
 }
 

@@ -52,6 +52,8 @@
  *                         bounded wait expired; the kernel stopped early,
  *                         released its tensor memory and returned (its output
  *                         is then undefined)
+ *   BIGEMM_ERR_STATIC_LIMIT bigemm_run_splitk_static only: the product needs
+ *                         more split-K scratch than the built-in array holds
  * Empty products are valid: M == 0 or N == 0 enqueue nothing, K == 0 writes
  * zeros to C.
  */
@@ -78,7 +80,8 @@ typedef enum {
     BIGEMM_ERR_WORKSPACE = 3,
     BIGEMM_ERR_UNSUPPORTED = 4,
     BIGEMM_ERR_CUDA = 5,
-    BIGEMM_ERR_TIMEOUT = 6
+    BIGEMM_ERR_TIMEOUT = 6,
+    BIGEMM_ERR_STATIC_LIMIT = 7
 } bigemm_status;
 
 /* A cudaStream_t passed through the C ABI. */
@@ -179,6 +182,40 @@ BIGEMM_API bigemm_status bigemm_run_atomic_splitk(const void *A, const void *B, 
                                        int64_t M, int64_t N, int64_t K,
                                        int64_t lda, int64_t ldb, int64_t ldc,
                                        int split_k, bigemm_stream stream);
+
+/* Size of the scratch array built into the library for
+ * bigemm_run_splitk_static: 16 MiB of device memory on every GPU that loads
+ * the library, held until the process exits. */
+#define BIGEMM_STATIC_SCRATCH_BYTES (16u << 20)
+
+/* Split-K product without a caller workspace and without any allocation.
+ * The pages have no counterpart to this call: it exists for callers that
+ * cannot allocate device memory or hand the library a scratch buffer -- for
+ * example a serving loop that forbids allocation after start-up (cudaMalloc
+ * may synchronise the whole device and stall unrelated streams), or a plugin
+ * inside a host framework that owns all device memory through its own
+ * allocator and does not expose it over a C interface.
+ *
+ * Arguments and result are those of bigemm_run (C fp32 [M, N]); the split-K
+ * partial sums go to a BIGEMM_STATIC_SCRATCH_BYTES array compiled into the
+ * library instead of a caller workspace, and the same two kernels run, so the
+ * bits equal bigemm_run's for the same split_k.  It calls no cudaMalloc,
+ * cudaFree or allocating library routine.
+ *   - Products whose bigemm_workspace_bytes(M, N, K, split_k) exceeds
+ *     BIGEMM_STATIC_SCRATCH_BYTES return BIGEMM_ERR_STATIC_LIMIT and enqueue
+ *     nothing; use bigemm_run with a workspace, or a smaller split_k.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and keeps it; make
+ *     that first call before any stream capture on the device.
+ *   - Every call on a device shares the one array, which keeps the last
+ *     call's contents.  Nothing in it needs to start at zero: each call's
+ *     partial kernel writes every element its reduction reads.  Calls that
+ *     can overlap on the GPU (other streams, no ordering event) race on it
+ *     and corrupt each other's results; order them. */
+BIGEMM_API bigemm_status bigemm_run_splitk_static(const void *A, const void *B, float *C,
+                                                  int64_t M, int64_t N, int64_t K,
+                                                  int64_t lda, int64_t ldb, int64_t ldc,
+                                                  int split_k, bigemm_stream stream);
 
 /* Reads (and, if reset != 0, clears) the device-side error word the kernels
  * set when a bounded wait expires.  Synchronises the current device.

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         s = dig.bigemm_status_string(code)
         assert s.startswith(dig.STATUS_NAMES[code])
     assert dig.bigemm_status_string(99) == "BIGEMM_ERR_UNKNOWN"
