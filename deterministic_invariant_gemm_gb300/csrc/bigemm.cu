@@ -139,6 +139,43 @@ size_t slice_bytes(int64_t M, int64_t N, int slices) {
     return static_cast<size_t>(b);
 }
 
+// A general strided view: rank dimensions, innermost first (dims[0] elements
+// contiguous), strides[i] = bytes between consecutive indices of dimension
+// i + 1, boxes of box[0..rank-1].
+bool encode_view(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr, int rank,
+                 const int64_t* dims, const int64_t* strides, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr || rank < 1 || rank > 5) return false;
+    cuuint64_t gdims[5], gstr[4];
+    cuuint32_t gbox[5], estr[5];
+    for (int i = 0; i < rank; ++i) {
+        gdims[i] = static_cast<cuuint64_t>(dims[i]);
+        gbox[i] = box[i];
+        estr[i] = 1;
+        if (i + 1 < rank) gstr[i] = static_cast<cuuint64_t>(strides[i]);
+    }
+    return fn(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), gdims, gstr, gbox, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Grouped output views for one TMA store per epilogue batch (N a multiple of
+// 32): {32 columns, M rows, N/32 column groups [, slices]} -- the staging
+// boxes of a batch sit group after group in shared memory.  Returns false if
+// N is not a multiple of 32 or the driver refuses the view; the caller then
+// uses the plain 2-D / 3-D maps with one store per 32 x 32 block.
+bool encode_out_grouped(CUtensorMap* m, CUtensorMapDataType dtype, uint32_t esize, void* ptr,
+                        int64_t M, int64_t N, int64_t ld, int splits, int64_t slice, int batch) {
+    if (N % 32 != 0) return false;
+    const CUtensorMapSwizzle sw = esize == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const int64_t dims[4] = {32, M, N / 32, splits};
+    const int64_t strides[3] = {ld * static_cast<int64_t>(esize), 32 * static_cast<int64_t>(esize),
+                                slice * static_cast<int64_t>(esize)};
+    const uint32_t box[4] = {32, 32, static_cast<uint32_t>(batch), 1};
+    return encode_view(m, dtype, ptr, splits > 0 ? 4 : 3, dims, strides, box, sw);
+}
+
 // A row-major tensor of `rank` (2 or 3) dimensions, innermost first: dims[0]
 // contiguous elements, dims[1] rows `ld` elements apart, dims[2] slices
 // `slice` elements apart.  Boxes of box[0] x box[1] (x 1).
@@ -299,6 +336,9 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     p.kb_total = static_cast<int>(ceil_div(K, kBK));
     p.kb_per_split = kb_per_split;
     p.units = static_cast<int>(units);
+    p.epi_boxes = epi_boxes_for(static_cast<int>(M));
+    p.epi_batch = epi_batch_for(static_cast<int>(M));
+    p.grouped = 0;
 
     const int grid = static_cast<int>(units < d->sm_count ? units : d->sm_count);
     const dim3 g(static_cast<unsigned>(grid)), blk(kNumThreads);
@@ -317,7 +357,11 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
         p.out = ws;
         p.ld_out = ws_ld_of(N);
         p.slice_stride = M * p.ld_out;
-        if (!encode_out_slices(&tmC, ws, M, N, splits)) return BIGEMM_ERR_CUDA;
+        if (encode_out_grouped(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, M, N, p.ld_out, splits,
+                               p.slice_stride, p.epi_batch))
+            p.grouped = 1;
+        else if (!encode_out_slices(&tmC, ws, M, N, splits))
+            return BIGEMM_ERR_CUDA;
         e = launch_pdl(bigemm_tc_kernel<kOutSlices>, g, blk, kSmemBytes, stream, tmA, tmB, tmC, p);
         launches = 1;
         if (e == cudaSuccess && mode != kModePartial) {
@@ -330,10 +374,18 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
         p.out = C;
         p.ld_out = ldc;
         if (mode == kModeBF16) {
-            if (!encode_out_bf16(&tmC, C, M, N, ldc)) return BIGEMM_ERR_CUDA;
+            if (encode_out_grouped(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, M, N, ldc, 0, 0,
+                                   p.epi_batch))
+                p.grouped = 1;
+            else if (!encode_out_bf16(&tmC, C, M, N, ldc))
+                return BIGEMM_ERR_CUDA;
             e = launch_pdl(bigemm_tc_kernel<kOutBF16>, g, blk, kSmemBytes, stream, tmA, tmB, tmC, p);
         } else {
-            if (!encode_out_f32(&tmC, C, M, N, ldc)) return BIGEMM_ERR_CUDA;
+            if (encode_out_grouped(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, M, N, ldc, 0, 0,
+                                   p.epi_batch))
+                p.grouped = 1;
+            else if (!encode_out_f32(&tmC, C, M, N, ldc))
+                return BIGEMM_ERR_CUDA;
             e = launch_pdl(bigemm_tc_kernel<kOutF32>, g, blk, kSmemBytes, stream, tmA, tmB, tmC, p);
         }
         launches = 1;

@@ -51,11 +51,13 @@ constexpr uint32_t kBChunkBytes = kBK * kBChunkCols * 2;  // 8 KiB: 64 k-rows x 
 constexpr uint32_t kBBytes = kBK * kBN * 2;       // 32 KiB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr int kNumBarriers = 2 * kStages + 2 * kAccStages + 1;
-// Epilogue staging: two 32-row x 128-byte boxes per epilogue warp, the source
-// of the TMA stores (fp32: 32 columns, 128-byte swizzle; bf16: 32 columns in
-// the first 64 bytes of each row, 64-byte swizzle).
+// Epilogue staging: eight 32-row x 128-byte boxes, the sources of the TMA
+// stores (fp32: 32 columns, 128-byte swizzle; bf16: 32 columns in the first 64
+// bytes of each row, 64-byte swizzle).  They are split evenly between the
+// epilogue warps that have rows (8, 4 or 2 boxes each, a function of M only).
+constexpr int kNumBoxes = 8;
 constexpr uint32_t kStageBufBytes = 32 * 128;
-constexpr uint32_t kStagingBytes = (kEpilogueThreads / 32) * 2 * kStageBufBytes;  // 32 KiB
+constexpr uint32_t kStagingBytes = kNumBoxes * kStageBufBytes;  // 32 KiB
 constexpr uint32_t kSmemBytes = 1024 /* alignment slack */ + kStages * kStageBytes +
                                 kStagingBytes + kNumBarriers * 8 + 16;
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103 CTA");
@@ -89,7 +91,19 @@ struct GemmParams {
     int kb_total;           // ceil(K / kBK)
     int kb_per_split;       // K blocks per segment
     int units;              // m_tiles * n_tiles * splits
+    // Epilogue layout, a function of M only (see the epilogue below).
+    int epi_boxes;          // staging boxes owned by each epilogue warp with rows (8, 4 or 2)
+    int epi_batch;          // 32-column blocks read from TMEM and stored together (4 or 2)
+    int grouped;            // 1: tmC views the output as {32 columns, rows, column groups
+                            //    [, slices]} with boxes of epi_batch groups, one store per batch
 };
+
+// The epilogue layout for M rows: the warps that have rows in a tile
+// (ceil(M / 32), at most 4) share the eight staging boxes evenly.
+__host__ __device__ constexpr int epi_boxes_for(int M) {
+    return (M + 31) / 32 <= 1 ? 8 : ((M + 31) / 32 == 2 ? 4 : 2);
+}
+__host__ __device__ constexpr int epi_batch_for(int M) { return epi_boxes_for(M) >= 4 ? 4 : 2; }
 
 // Unit u -> (tile row, tile column, K segment).  All tiles of segment 0 come
 // first, then segment 1, ...; inside a segment the tiles follow the GROUP_M
@@ -211,7 +225,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    if (threadIdx.x == 0) {
+    if (warp == 2 && lane == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
@@ -355,13 +369,24 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     } else {
         // ------------------------------------------------------ epilogue --
         // Warp w reads TMEM lanes 32 (w % 4) .. +31, i.e. tile rows q*32 .. q*32+31.
-        // Each 32 x 32 block goes TMEM -> registers -> a swizzled staging box ->
-        // one TMA store (coalesced, asynchronous; rows >= M and columns >= N
-        // fall outside the tensor map and are not written).  Two boxes per
-        // warp alternate, so a block is staged while the previous one is stored.
+        // Blocks of 32 x 32 go TMEM -> registers -> swizzled staging boxes -> TMA
+        // stores (coalesced, asynchronous; rows >= M and columns >= N fall outside
+        // the tensor map and are not written).  A batch of epi_batch blocks is
+        // read from TMEM with one load, staged, fenced once and stored with one
+        // TMA store (or one per block when the output is not viewed as column
+        // groups); each batch is one bulk group.  The warps that have rows split
+        // the eight boxes evenly -- a split that depends on M alone, so every
+        // warp owns its boxes for the whole launch and recycles them batch by
+        // batch.
         const int q = warp & 3;
-        const uint32_t my_boxes = sOut + static_cast<uint32_t>(warp - 2) * 2u * kStageBufBytes;
-        uint32_t nblk = 0;  // blocks this warp has handed to the TMA unit
+        const int per_warp = p.epi_boxes;
+        const int batch = p.epi_batch;
+        const int slots = per_warp / batch;  // batches in flight per warp (2 or 1)
+        // fp32 boxes are 32 rows x 128 bytes; bf16 boxes 32 rows x 64 bytes, packed
+        // at 2 KiB so that a batch of them is one contiguous grouped box.
+        constexpr uint32_t kBox = (kOut == kOutBF16) ? kStageBufBytes / 2 : kStageBufBytes;
+        const uint32_t my_boxes = sOut + static_cast<uint32_t>(q * per_warp) * kBox;
+        uint32_t nbat = 0;  // batches this warp has handed to the TMA unit
         int t = 0;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
             int mt, nt, seg;
@@ -372,48 +397,87 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 break;
             tc_fence_after();
             const int m0 = mt * kBM + q * 32, n0 = nt * kBN;
+            bool released = false;
             if (m0 < p.M) {  // uniform per warp: a warp whose rows are all past M skips
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        static_cast<uint32_t>(acc * kBN);
+                const int nchunks = min(kBN / 32, (p.N - n0 + 31) / 32);
 #pragma unroll 1
-                for (int ch = 0; ch < kBN / 32; ++ch) {
-                    const int col = n0 + ch * 32;
-                    if (col >= p.N) break;  // uniform
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tbase + ch * 32, r);
+                for (int c0 = 0; c0 < nchunks; c0 += batch) {
+                    const int nb = min(batch, nchunks - c0);
+                    uint32_t r[128];
+                    if (batch == 4) tmem_ld_32x32b_x128(tbase + c0 * 32, r);
+                    else tmem_ld_32x32b_x64(tbase + c0 * 32, r);
                     tmem_ld_wait();
-                    // The TMA unit clips the innermost dimension at 16-byte granularity,
-                    // so a block ending in a partial 16-byte chunk of a C row is
-                    // written element by element (the workspace owns its padding).
-                    constexpr int kVec = (kOut == kOutBF16) ? 8 : 4;
-                    const bool ragged = kOut != kOutSlices && col + 32 > p.N && (p.N % kVec) != 0;
+                    if (c0 + nb >= nchunks) {  // the accumulator is no longer needed
+                        tc_fence_before();
+                        mbar_arrive(tempty_bar(acc));
+                        released = true;
+                    }
                     if constexpr (kOut == kOutAtomic) {
-                        if (m0 + lane < p.M) atomic_add_row_chunk(p, m0 + lane, col, r);
-                    } else if (ragged) {
-                        if (m0 + lane < p.M) store_row_masked<kOut>(p, m0 + lane, col, r);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (i < nb && m0 + lane < p.M)
+                                atomic_add_row_chunk(p, m0 + lane, n0 + (c0 + i) * 32,
+                                                     *reinterpret_cast<const uint32_t(*)[32]>(r + 32 * i));
                     } else {
-                        const uint32_t box = my_boxes + (nblk & 1u) * kStageBufBytes;
-                        if (nblk >= 2) {
-                            // the store issued from this box two blocks ago must
-                            // have finished reading it
-                            if (lane == 0) bulk_wait_group_read<1>();
+                        // The slot this batch reuses must have been read by its
+                        // earlier store: at most slots - 1 batches may pend.
+                        const uint32_t box0 =
+                            my_boxes + (nbat % static_cast<uint32_t>(slots)) * batch * kBox;
+                        if (nbat >= static_cast<uint32_t>(slots)) {
+                            if (lane == 0) bulk_wait_group_read_dyn(slots - 1);
                             __syncwarp();
                         }
-                        if constexpr (kOut == kOutBF16) stage_bf16(box, lane, r);
-                        else stage_f32(box, lane, r);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            if constexpr (kOut == kOutSlices) tma_store_3d(&tmC, box, col, m0, seg);
-                            else tma_store_2d(&tmC, box, col, m0);
-                            bulk_commit_group();
+                        // The TMA unit clips the innermost dimension at 16-byte
+                        // granularity, so a block ending in a partial 16-byte chunk
+                        // of a C row is written element by element instead (the
+                        // workspace owns its padding).
+                        constexpr int kVec = (kOut == kOutBF16) ? 8 : 4;
+                        int staged = 0;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            if (i >= nb) break;
+                            const int col = n0 + (c0 + i) * 32;
+                            const uint32_t(&ri)[32] = *reinterpret_cast<const uint32_t(*)[32]>(r + 32 * i);
+                            const bool ragged =
+                                kOut != kOutSlices && col + 32 > p.N && (p.N % kVec) != 0;
+                            if (ragged) {
+                                if (m0 + lane < p.M) store_row_masked<kOut>(p, m0 + lane, col, ri);
+                            } else {
+                                const uint32_t box = box0 + static_cast<uint32_t>(i) * kBox;
+                                if constexpr (kOut == kOutBF16) stage_bf16(box, lane, ri);
+                                else stage_f32(box, lane, ri);
+                                ++staged;
+                            }
                         }
-                        ++nblk;
+                        if (staged > 0) {
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                const int g0 = (n0 + c0 * 32) / 32;
+                                if (p.grouped) {
+                                    if constexpr (kOut == kOutSlices) tma_store_4d(&tmC, box0, 0, m0, g0, seg);
+                                    else tma_store_3d(&tmC, box0, 0, m0, g0);
+                                } else {
+                                    for (int i = 0; i < staged; ++i) {
+                                        const uint32_t box = box0 + static_cast<uint32_t>(i) * kBox;
+                                        const int col = n0 + (c0 + i) * 32;
+                                        if constexpr (kOut == kOutSlices) tma_store_3d(&tmC, box, col, m0, seg);
+                                        else tma_store_2d(&tmC, box, col, m0);
+                                    }
+                                }
+                                bulk_commit_group();
+                            }
+                            ++nbat;
+                        }
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(tempty_bar(acc));
+            if (!released) {
+                tc_fence_before();
+                mbar_arrive(tempty_bar(acc));
+            }
         }
         // All of this warp's stores complete before the CTA exits.
         if (lane == 0) bulk_wait_group<0>();
