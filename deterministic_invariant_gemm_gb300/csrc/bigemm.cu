@@ -75,14 +75,14 @@ bigemm_status device_info(const DeviceInfo** out) {
         d.sm_count = sms;
         if (d.supported) {
             const int smem = static_cast<int>(kSmemBytes);
-            if (cudaFuncSetAttribute(bigemm_tc_kernel<kOutF32>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-                cudaFuncSetAttribute(bigemm_tc_kernel<kOutBF16>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-                cudaFuncSetAttribute(bigemm_tc_kernel<kOutSlices>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-                cudaFuncSetAttribute(bigemm_tc_kernel<kOutAtomic>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            const auto opt_in = [smem](const void* fn) {
+                return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+                       cudaSuccess;
+            };
+            if (!opt_in((const void*)bigemm_tc_kernel<kOutF32>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutBF16>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutSlices>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutAtomic>))
                 return BIGEMM_ERR_CUDA;
             void* sym = nullptr;
             if (cudaGetSymbolAddress(&sym, g_device_status) != cudaSuccess) return BIGEMM_ERR_CUDA;
@@ -196,16 +196,20 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t esize, c
 }
 
 // Operand maps: A [M, K] in boxes of 64 k x 128 rows, B [K, N] in boxes of 64
-// columns x 64 k-rows, both with the 128-byte swizzle the MMA descriptors use.
-bool encode_operands(CUtensorMap* tmA, CUtensorMap* tmB, const void* A, const void* B, int64_t M,
-                     int64_t N, int64_t K, int64_t lda, int64_t ldb) {
+// columns x 64 k-rows, both with the 128-byte swizzle the MMA descriptors use;
+// and B again in 256 x 256 boxes without swizzle, used only to warm L2.
+bool encode_operands(CUtensorMap* tmA, CUtensorMap* tmB, CUtensorMap* tmBp, const void* A,
+                     const void* B, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb) {
     const int64_t da[2] = {K, M}, db[2] = {N, K};
     const uint32_t ba[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(kBM)};
     const uint32_t bb[2] = {kBChunkCols, static_cast<uint32_t>(kBK)};
+    const uint32_t bp[2] = {static_cast<uint32_t>(kBN), static_cast<uint32_t>(kPrefetchRows)};
     return encode_tiled(tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, 2, da, lda, 0, ba,
                         CU_TENSOR_MAP_SWIZZLE_128B) &&
            encode_tiled(tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, 2, db, ldb, 0, bb,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
+                        CU_TENSOR_MAP_SWIZZLE_128B) &&
+           encode_tiled(tmBp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, 2, db, ldb, 0, bp,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // Output maps for the epilogue's 32 x 32 TMA stores: fp32 C (128-byte
@@ -249,23 +253,33 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaSt
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+template <int kOut>
+cudaError_t launch_gemm(dim3 g, dim3 blk, cudaStream_t stream, const CUtensorMap& tmA,
+                        const CUtensorMap& tmB, const CUtensorMap& tmBp, const CUtensorMap& tmC,
+                        const GemmParams& p) {
+    return launch_pdl(bigemm_tc_kernel<kOut>, g, blk, kSmemBytes, stream, tmA, tmB, tmBp, tmC, p);
+}
+
 enum Mode { kModeF32, kModeBF16, kModePartial, kModeAtomic };
 
 bigemm_status launch_reduce(const DeviceInfo& d, const float* ws, int splits, int64_t M, int64_t N,
                             void* C, int64_t ldc, bool bf16, cudaStream_t stream) {
     const int64_t ws_ld = ws_ld_of(N);
     const int64_t items = M * (ws_ld / 4);
-    int64_t blocks = ceil_div(items, 256);
-    const int64_t cap = static_cast<int64_t>(d.sm_count) * 8;
-    if (blocks > cap) blocks = cap;
+    // At most one block per SM, so the reduction never crowds out the next
+    // kernel's blocks while it waits for the partial kernel.
+    int64_t blocks = ceil_div(items, kReduceThreads);
+    if (blocks > d.sm_count) blocks = d.sm_count;
     if (blocks < 1) blocks = 1;
     cudaError_t e;
     if (bf16)
-        e = launch_pdl(splitk_reduce_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
-                       stream, ws, C, static_cast<int>(M), static_cast<int>(N), ldc, ws_ld, splits);
+        e = launch_pdl(splitk_reduce_kernel<true>, dim3(static_cast<unsigned>(blocks)),
+                       dim3(kReduceThreads), 0, stream, ws, C, static_cast<int>(M), static_cast<int>(N),
+                       ldc, ws_ld, splits);
     else
-        e = launch_pdl(splitk_reduce_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
-                       stream, ws, C, static_cast<int>(M), static_cast<int>(N), ldc, ws_ld, splits);
+        e = launch_pdl(splitk_reduce_kernel<false>, dim3(static_cast<unsigned>(blocks)),
+                       dim3(kReduceThreads), 0, stream, ws, C, static_cast<int>(M), static_cast<int>(N),
+                       ldc, ws_ld, splits);
     return e == cudaSuccess ? BIGEMM_OK : BIGEMM_ERR_CUDA;
 }
 
@@ -321,9 +335,9 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
         return e == cudaSuccess ? BIGEMM_OK : BIGEMM_ERR_CUDA;
     }
 
-    CUtensorMap tmA, tmB, tmC;
+    CUtensorMap tmA, tmB, tmBp, tmC;
     std::memset(&tmC, 0, sizeof(tmC));
-    if (!encode_operands(&tmA, &tmB, A, B, M, N, K, lda, ldb)) return BIGEMM_ERR_CUDA;
+    if (!encode_operands(&tmA, &tmB, &tmBp, A, B, M, N, K, lda, ldb)) return BIGEMM_ERR_CUDA;
 
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
@@ -339,6 +353,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     p.epi_boxes = epi_boxes_for(static_cast<int>(M));
     p.epi_batch = epi_batch_for(static_cast<int>(M));
     p.grouped = 0;
+    p.prefetch_rows = kStages * kBK;  // what the ring holds: the first four K blocks
 
     const int grid = static_cast<int>(units < d->sm_count ? units : d->sm_count);
     const dim3 g(static_cast<unsigned>(grid)), blk(kNumThreads);
@@ -351,7 +366,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
         if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
         p.out = C;
         p.ld_out = ldc;
-        e = launch_pdl(bigemm_tc_kernel<kOutAtomic>, g, blk, kSmemBytes, stream, tmA, tmB, tmC, p);
+        e = launch_gemm<kOutAtomic>(g, blk, stream, tmA, tmB, tmBp, tmC, p);
         launches = 1;
     } else if (mode == kModePartial || splits > 1) {
         p.out = ws;
@@ -362,7 +377,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
             p.grouped = 1;
         else if (!encode_out_slices(&tmC, ws, M, N, splits))
             return BIGEMM_ERR_CUDA;
-        e = launch_pdl(bigemm_tc_kernel<kOutSlices>, g, blk, kSmemBytes, stream, tmA, tmB, tmC, p);
+        e = launch_gemm<kOutSlices>(g, blk, stream, tmA, tmB, tmBp, tmC, p);
         launches = 1;
         if (e == cudaSuccess && mode != kModePartial) {
             st = launch_reduce(*d, static_cast<const float*>(ws), splits, M, N, C, ldc,
@@ -379,14 +394,14 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
                 p.grouped = 1;
             else if (!encode_out_bf16(&tmC, C, M, N, ldc))
                 return BIGEMM_ERR_CUDA;
-            e = launch_pdl(bigemm_tc_kernel<kOutBF16>, g, blk, kSmemBytes, stream, tmA, tmB, tmC, p);
+            e = launch_gemm<kOutBF16>(g, blk, stream, tmA, tmB, tmBp, tmC, p);
         } else {
             if (encode_out_grouped(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, M, N, ldc, 0, 0,
                                    p.epi_batch))
                 p.grouped = 1;
             else if (!encode_out_f32(&tmC, C, M, N, ldc))
                 return BIGEMM_ERR_CUDA;
-            e = launch_pdl(bigemm_tc_kernel<kOutF32>, g, blk, kSmemBytes, stream, tmA, tmB, tmC, p);
+            e = launch_gemm<kOutF32>(g, blk, stream, tmA, tmB, tmBp, tmC, p);
         }
         launches = 1;
     }

@@ -18,12 +18,13 @@
 // used for every M: short batches are padded by the TMA unit's zero fill, never
 // served by a different code path.
 //
-// CTA roles (192 threads, one CTA per SM):
+// CTA roles (320 threads, one CTA per SM):
 //   warp 0      TMA producer: fills a kStages-deep shared-memory ring.
 //   warp 1      allocates TMEM; one lane issues the MMAs and commits.
-//   warps 2..5  epilogue: TMEM -> registers -> swizzled shared-memory boxes
-//               -> TMA stores; two TMEM accumulators let the epilogue of tile
-//               t overlap the mainloop of tile t + 1.
+//   warps 2..9  epilogue, two warps per TMEM lane quarter, each taking half
+//               of the tile's columns: TMEM -> registers -> swizzled
+//               shared-memory boxes -> TMA stores; two TMEM accumulators let
+//               the epilogue of tile t overlap the mainloop of tile t + 1.
 #pragma once
 
 #include <cuda.h>
@@ -38,29 +39,44 @@ constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
 constexpr int kUmmaK = 16;
-constexpr int kStages = 4;
-constexpr int kAccStages = 2;
 constexpr int kGroupM = 8;
-constexpr int kTmemCols = kAccStages * kBN;  // 512: all of TMEM, one CTA per SM
-constexpr int kNumThreads = 192;
-constexpr int kEpilogueThreads = 128;
+constexpr int kNumThreads = 320;       // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kEpilogueThreads = 256;
 
 constexpr uint32_t kABytes = kBM * kBK * 2;       // 16 KiB: 128 rows x 128 B
 constexpr uint32_t kBChunkCols = 64;              // one 128-byte swizzle span of N
 constexpr uint32_t kBChunkBytes = kBK * kBChunkCols * 2;  // 8 KiB: 64 k-rows x 128 B
 constexpr uint32_t kBBytes = kBK * kBN * 2;       // 32 KiB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr int kNumBarriers = 2 * kStages + 2 * kAccStages + 1;
-// Epilogue staging: eight 32-row x 128-byte boxes, the sources of the TMA
-// stores (fp32: 32 columns, 128-byte swizzle; bf16: 32 columns in the first 64
-// bytes of each row, 64-byte swizzle).  They are split evenly between the
-// epilogue warps that have rows (8, 4 or 2 boxes each, a function of M only).
+constexpr uint32_t kStageBufBytes = 32 * 128;     // one epilogue staging box
+constexpr int kPrefetchRows = 256;                // K rows per L2-prefetch box of B
+
+// Pipeline depth, TMEM accumulators and epilogue staging.  One CTA per SM: a
+// 4-stage ring of 48 KiB stages, two 128 x 256 FP32 accumulators (all 512 TMEM
+// columns) so that the epilogue of one tile overlaps the mainloop of the next,
+// and eight staging boxes, the sources of the epilogue's TMA stores (fp32: 32
+// rows x 128 bytes, 128-byte swizzle; bf16: 32 rows x 64 bytes, 64-byte
+// swizzle).  The epilogue warps that have rows split the boxes evenly.
+constexpr int kStages = 4;
+constexpr int kAccStages = 2;
+constexpr int kTmemCols = kAccStages * kBN;
 constexpr int kNumBoxes = 8;
-constexpr uint32_t kStageBufBytes = 32 * 128;
-constexpr uint32_t kStagingBytes = kNumBoxes * kStageBufBytes;  // 32 KiB
-constexpr uint32_t kSmemBytes = 1024 /* alignment slack */ + kStages * kStageBytes +
-                                kStagingBytes + kNumBarriers * 8 + 16;
+constexpr int kMaxBatch = 4;  // 32-column blocks per TMEM load
+constexpr int kNumBarriers = 2 * kStages + 2 * kAccStages + 1;
+constexpr uint32_t kStagingBytes = kNumBoxes * kStageBufBytes;
+// The dynamic shared memory base is 1024-byte aligned (checked at run time).
+constexpr uint32_t kSmemBytes = kStages * kStageBytes + kStagingBytes + kNumBarriers * 8 + 16;
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103 CTA");
+
+// Epilogue layout for M rows: two warps per TMEM lane quarter with rows
+// (ceil(M / 32) quarters, at most 4) share the staging boxes (4, 2 or 1 each);
+// each reads `batch` 32-column blocks per TMEM load.
+__host__ __device__ constexpr int epi_boxes_for(int M) {
+    return kNumBoxes / (2 * ((M + 31) / 32 <= 1 ? 1 : ((M + 31) / 32 == 2 ? 2 : 4)));
+}
+__host__ __device__ constexpr int epi_batch_for(int M) {
+    return epi_boxes_for(M) < kMaxBatch ? epi_boxes_for(M) : kMaxBatch;
+}
 
 constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, /*A MN-major*/ false, /*B MN-major*/ true);
 
@@ -72,6 +88,7 @@ constexpr unsigned kErrWaitProducer = 1u;
 constexpr unsigned kErrWaitMma = 2u;
 constexpr unsigned kErrWaitEpilogue = 4u;
 constexpr unsigned kErrWaitDrain = 8u;
+constexpr unsigned kErrSmemAlign = 16u;
 
 enum OutKind : int {
     kOutF32 = 0,     // C fp32, plain stores
@@ -92,18 +109,12 @@ struct GemmParams {
     int kb_per_split;       // K blocks per segment
     int units;              // m_tiles * n_tiles * splits
     // Epilogue layout, a function of M only (see the epilogue below).
-    int epi_boxes;          // staging boxes owned by each epilogue warp with rows (8, 4 or 2)
-    int epi_batch;          // 32-column blocks read from TMEM and stored together (4 or 2)
+    int epi_boxes;          // staging boxes owned by each epilogue warp with rows
+    int epi_batch;          // 32-column blocks read from TMEM and stored together (1, 2 or 4)
     int grouped;            // 1: tmC views the output as {32 columns, rows, column groups
                             //    [, slices]} with boxes of epi_batch groups, one store per batch
+    int prefetch_rows;      // K rows of B warmed in L2 before the dependency wait
 };
-
-// The epilogue layout for M rows: the warps that have rows in a tile
-// (ceil(M / 32), at most 4) share the eight staging boxes evenly.
-__host__ __device__ constexpr int epi_boxes_for(int M) {
-    return (M + 31) / 32 <= 1 ? 8 : ((M + 31) / 32 == 2 ? 4 : 2);
-}
-__host__ __device__ constexpr int epi_batch_for(int M) { return epi_boxes_for(M) >= 4 ? 4 : 2; }
 
 // Unit u -> (tile row, tile column, K segment).  All tiles of segment 0 come
 // first, then segment 1, ...; inside a segment the tiles follow the GROUP_M
@@ -202,12 +213,18 @@ __device__ __forceinline__ void atomic_add_row_chunk(const GemmParams& p, int ro
 template <int kOut>
 __global__ void __launch_bounds__(kNumThreads, 1)
     bigemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    // 128-byte-swizzled tiles must start on 1024-byte boundaries.
-    const uint32_t raw = smem_addr(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t* gbase = smem_raw + (base - raw);
+                     const __grid_constant__ CUtensorMap tmBp, const __grid_constant__ CUtensorMap tmC,
+                     const GemmParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 128-byte-swizzled tiles must start on 1024-byte boundaries; the layout
+    // below assumes the base is.  Should it not be, stop before touching
+    // anything (no barrier, no TMEM yet) and report it.
+    const uint32_t base = smem_addr(smem_raw);
+    if (base & 1023u) {
+        if (threadIdx.x == 0) atomicOr(p.status, kErrSmemAlign);
+        return;
+    }
+    uint8_t* gbase = smem_raw;
     const uint32_t sA = base;                                // stage s: sA + s * kABytes
     const uint32_t sB = base + kStages * kABytes;            // stage s: sB + s * kBBytes
     const uint32_t sOut = base + kStages * kStageBytes;      // epilogue staging boxes
@@ -239,23 +256,22 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
-        if constexpr (kOut != kOutAtomic) tma_prefetch_desc(&tmC);
-        // Warm L2 with the first weight tiles of this CTA's first unit while the
-        // previous kernel in the stream finishes.  An L2 prefetch writes no
-        // shared memory and L2 is the device's point of coherence, so it cannot
-        // expose data older than the dependency wait below.
+        // Warm L2 with the weights of this CTA's first unit (its first
+        // p.prefetch_rows K rows) while the previous kernel in the stream
+        // finishes.  An L2 prefetch writes no shared memory and L2 is the
+        // device's point of coherence, so it cannot expose data older than the
+        // dependency wait below.
+        tma_prefetch_desc(&tmBp);
         if (static_cast<int>(blockIdx.x) < p.units) {
             int mt, nt, seg;
             unit_coords(p, blockIdx.x, mt, nt, seg);
-            const int kb0 = seg * p.kb_per_split;
-            const int kb1 = min(min(kb0 + p.kb_per_split, p.kb_total), kb0 + kStages);
-            for (int kb = kb0; kb < kb1; ++kb)
-#pragma unroll
-                for (int c = 0; c < kBN / static_cast<int>(kBChunkCols); ++c)
-                    tma_prefetch_l2_2d(&tmB, nt * kBN + c * static_cast<int>(kBChunkCols), kb * kBK);
+            const int k0 = seg * p.kb_per_split * kBK;
+            const int k1 = min(k0 + p.prefetch_rows, min(k0 + p.kb_per_split * kBK, p.kb_total * kBK));
+            for (int k = k0; k < k1; k += kPrefetchRows) tma_prefetch_l2_2d(&tmBp, nt * kBN, k);
         }
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        if constexpr (kOut != kOutAtomic) tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -266,6 +282,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
+    // The next kernel in the stream may be scheduled from now on (this CTA
+    // already holds its TMEM, so a dependent cannot take it first); it waits
+    // for this grid to complete before touching memory.
+    if (threadIdx.x == 0) grid_launch_dependents();
+
     // Everything above overlaps the previous kernel in the stream; from here on
     // global memory is read and written only after it has completed.
     grid_dependency_wait();
@@ -273,9 +294,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer --
-            // The next kernel in the stream may start its own prologue now; it
-            // waits for this grid to complete before touching memory.
-            grid_launch_dependents();
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
@@ -326,8 +344,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 unit_coords(p, u, mt, nt, seg);
                 const int kb0 = seg * p.kb_per_split;
                 const int kb1 = min(kb0 + p.kb_per_split, p.kb_total);
-                const int acc = t & 1;
-                const uint32_t acc_phase = (t >> 1) & 1;
+                const int acc = t % kAccStages;
+                const uint32_t acc_phase = static_cast<uint32_t>(t / kAccStages) & 1u;
                 if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status,
                                   kErrWaitMma)) {
                     ok = false;
@@ -368,7 +386,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
     } else {
         // ------------------------------------------------------ epilogue --
-        // Warp w reads TMEM lanes 32 (w % 4) .. +31, i.e. tile rows q*32 .. q*32+31.
+        // Warp w reads TMEM lanes 32 (w % 4) .. +31, i.e. tile rows q*32 .. q*32+31,
+        // and the columns of half h = (w - 2) / 4 of the tile (128 each).
         // Blocks of 32 x 32 go TMEM -> registers -> swizzled staging boxes -> TMA
         // stores (coalesced, asynchronous; rows >= M and columns >= N fall outside
         // the tensor map and are not written).  A batch of epi_batch blocks is
@@ -379,20 +398,22 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // warp owns its boxes for the whole launch and recycles them batch by
         // batch.
         const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
         const int per_warp = p.epi_boxes;
         const int batch = p.epi_batch;
         const int slots = per_warp / batch;  // batches in flight per warp (2 or 1)
         // fp32 boxes are 32 rows x 128 bytes; bf16 boxes 32 rows x 64 bytes, packed
         // at 2 KiB so that a batch of them is one contiguous grouped box.
+        // (Warps whose rows are always past M never use their box range.)
         constexpr uint32_t kBox = (kOut == kOutBF16) ? kStageBufBytes / 2 : kStageBufBytes;
-        const uint32_t my_boxes = sOut + static_cast<uint32_t>(q * per_warp) * kBox;
+        const uint32_t my_boxes = sOut + static_cast<uint32_t>((q * 2 + h) * per_warp) * kBox;
         uint32_t nbat = 0;  // batches this warp has handed to the TMA unit
         int t = 0;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
             int mt, nt, seg;
             unit_coords(p, u, mt, nt, seg);
-            const int acc = t & 1;
-            const uint32_t acc_phase = (t >> 1) & 1;
+            const int acc = t % kAccStages;
+            const uint32_t acc_phase = static_cast<uint32_t>(t / kAccStages) & 1u;
             if (!wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.status, kErrWaitEpilogue))
                 break;
             tc_fence_after();
@@ -401,13 +422,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (m0 < p.M) {  // uniform per warp: a warp whose rows are all past M skips
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        static_cast<uint32_t>(acc * kBN);
-                const int nchunks = min(kBN / 32, (p.N - n0 + 31) / 32);
+                // this warp's 32-column blocks: [h * 4, nchunks)
+                const int nchunks = min(h * 4 + 4, min(kBN / 32, (p.N - n0 + 31) / 32));
 #pragma unroll 1
-                for (int c0 = 0; c0 < nchunks; c0 += batch) {
+                for (int c0 = h * 4; c0 < nchunks; c0 += batch) {
                     const int nb = min(batch, nchunks - c0);
-                    uint32_t r[128];
+                    uint32_t r[kMaxBatch * 32];
                     if (batch == 4) tmem_ld_32x32b_x128(tbase + c0 * 32, r);
-                    else tmem_ld_32x32b_x64(tbase + c0 * 32, r);
+                    else if (batch == 2) tmem_ld_32x32b_x64(tbase + c0 * 32, r);
+                    else tmem_ld_32x32b_x32(tbase + c0 * 32, *reinterpret_cast<uint32_t(*)[32]>(r));
                     tmem_ld_wait();
                     if (c0 + nb >= nchunks) {  // the accumulator is no longer needed
                         tc_fence_before();
@@ -416,7 +439,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                     if constexpr (kOut == kOutAtomic) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
+                        for (int i = 0; i < kMaxBatch; ++i)
                             if (i < nb && m0 + lane < p.M)
                                 atomic_add_row_chunk(p, m0 + lane, n0 + (c0 + i) * 32,
                                                      *reinterpret_cast<const uint32_t(*)[32]>(r + 32 * i));
@@ -436,7 +459,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         constexpr int kVec = (kOut == kOutBF16) ? 8 : 4;
                         int staged = 0;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
+                        for (int i = 0; i < kMaxBatch; ++i) {
                             if (i >= nb) break;
                             const int col = n0 + (c0 + i) * 32;
                             const uint32_t(&ri)[32] = *reinterpret_cast<const uint32_t(*)[32]>(r + 32 * i);
@@ -497,12 +520,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 // rather than 0.0f keeps a lone -0.0 partial intact.  One thread handles four
 // adjacent columns of one row (16-byte loads, coalesced along N); the loads of
 // up to eight slices are issued before their additions.
+constexpr int kReduceThreads = 128;
+
 template <bool kBF16Out>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kReduceThreads)
     splitk_reduce_kernel(const float* __restrict__ ws, void* __restrict__ C, int M, int N,
                          int64_t ldc, int64_t ws_ld, int S) {
-    grid_dependency_wait();
+    // The next kernel in the stream may be scheduled at once: it waits for
+    // this grid to complete before touching memory, and this kernel holds no
+    // tensor memory a dependent could need.
     grid_launch_dependents();
+    grid_dependency_wait();
     const int64_t vec_per_row = ws_ld / 4;
     const int64_t total = static_cast<int64_t>(M) * vec_per_row;
     const int64_t slice = static_cast<int64_t>(M) * ws_ld;
