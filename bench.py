@@ -206,6 +206,40 @@ class ClockSampler:
         return bool(mhz and mx and mhz < 0.5 * mx and not clocks.get("reasons"))
 
 
+def nvml_index(local: int) -> int:
+    """NVML index of CUDA device `local` (CUDA_VISIBLE_DEVICES may remap it)."""
+    vis = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    if local < len(vis) and vis[local].isdigit():
+        return int(vis[local])
+    return local
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("kernels.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "deterministic_invariant_gemm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the decode partial kernel from the committed
+    ncu summary, or None when that capture was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "bigemm_partial_decode_M16_M64.md")
+    try:
+        text = open(path, encoding="utf-8").read()
+    except OSError:
+        return None
+    for line in text.splitlines():
+        if line.startswith("traffic_bytes_per_launch:"):
+            fields = dict(f.split("=", 1) for f in line.split(":", 1)[1].split())
+            if fields.pop("source_sha", None) != kernel_source_hash():
+                return None
+            return {int(k[1:]): int(v) for k, v in fields.items()}
+    return None
+
+
 def external_events_supported() -> bool:
     try:
         torch.cuda.Event(enable_timing=True, external=True)
@@ -389,6 +423,74 @@ def run_e2e(bench: DecodeBench, steps: int, warmup: int) -> dict:
             "ms_per_step": secs * 1e3 / steps}
 
 
+# ------------------------------------------------------ single workloads --
+
+# name -> (M, N, K, split_k, bf16 out, value distribution, roofline bound)
+SINGLE = {
+    "small": (64, 256, 512, 1, False, "normal", "latency"),
+    "square2048": (2048, 2048, 2048, 1, False, "uniform", "tensor"),
+    "square4096": (4096, 4096, 4096, 1, False, "uniform", "tensor"),
+    "square8192": (8192, 8192, 8192, 1, False, "uniform", "tensor"),
+    "large16384": (16384, 16384, 16384, 1, True, "normal", "tensor"),
+    "longk": (256, 256, 65536, 16, False, "normal", "hbm"),
+}
+
+
+def run_single(name, args, world, rank, dev, peaks, peak_src):
+    """One product per step through bigemm_run / bigemm_run_bf16out, inputs in
+    rotating copies that together exceed L2."""
+    import deterministic_invariant_gemm_gb300 as dig
+    M, N, K, S, bf16, dist_name, bound = SINGLE[name]
+    in_bytes = 2 * (M * K + K * N)
+    copies = max(1, min(8, math.ceil(2 * L2_BYTES / in_bytes)))
+    AB = [workloads.pair(M, N, K, 4321 + c, dist=dist_name) for c in range(copies)]
+    AB = [(a.to(dev), b.to(dev)) for a, b in AB]
+    C = torch.empty((M, N), dtype=torch.bfloat16 if bf16 else torch.float32, device=dev)
+    wsb = dig.bigemm_workspace_bytes(M, N, K, S)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+    fn = dig.bigemm_run_bf16out if bf16 else dig.bigemm_run
+    launches = 1 if dig.bigemm_effective_split_k(K, S) == 1 else 2
+
+    def call(i):
+        a, b = AB[i % copies]
+        fn(a, b, C, M, N, K, K, N, N, S, ws, wsb)
+
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(nvml_index(dev.index or 0))
+    sampler.start()
+    secs = time_region(call, args.steps, world)
+    clocks = sampler.stop()
+    flops = 2.0 * M * N * K
+    value = job_throughput(flops * args.steps, world, secs)
+    per = secs / args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": per * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "%s: M=%d N=%d K=%d split_k=%d, %s out, %s inputs" %
+                   (name, M, N, K, S, "bf16" if bf16 else "fp32", dist_name),
+                   "l2": "%d rotating input copies (%d MiB)" % (copies, copies * in_bytes >> 20),
+                   "parallelism": "replicas"},
+        "gpu_launches": launches * args.steps, "clocks": clocks,
+    }
+    if bound == "tensor":
+        peak = peaks["bf16_tflops"]
+        line["roofline"] = {"kernel": "bigemm_tc_kernel", "bound": "tensor",
+                            "achieved": round(flops / per / 1e12, 1), "peak": peak,
+                            "peak_source": peak_src, "unit": "TFLOP/s",
+                            "frac": round(flops / per / 1e12 / peak, 4), "traffic": None}
+    elif bound == "hbm":
+        alg = 2.0 * (M * K + K * N) + 4.0 * M * N
+        line["roofline"] = {"kernel": "bigemm_tc_kernel + splitk_reduce_kernel", "bound": "hbm",
+                            "achieved": round(alg / per / 1e9, 1), "peak": peaks["hbm_gbs"],
+                            "peak_source": peak_src, "unit": "GB/s",
+                            "frac": round(alg / per / 1e9 / peaks["hbm_gbs"], 4), "traffic": None}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------- other shapes --
 
 def run_other_workloads(dev, peaks) -> dict:
@@ -513,6 +615,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the other shapes, e2e and the CPU baseline")
+    ap.add_argument("--workload", default="decode", choices=("decode",) + tuple(SINGLE),
+                    help="decode (the headline step) or one of the other workload shapes")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -529,6 +633,12 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
+    if args.workload != "decode":
+        run_single(args.workload, args, world, rank, dev, peaks, peak_src)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
 
     bench = DecodeBench(dev)
     for i in range(args.warmup):          # eager warm-up (loads the module)
@@ -538,9 +648,7 @@ def main():
     bench.run_steps(0, args.warmup)
     torch.cuda.synchronize()
 
-    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-    nvml_index = int(vis.split(",")[local]) if vis and vis.split(",")[local].isdigit() else local
-    sampler = ClockSampler(nvml_index)
+    sampler = ClockSampler(nvml_index(local))
     remeasured = False
     for attempt in range(2):
         sampler.start()
@@ -581,6 +689,13 @@ def main():
                   "algorithmic bytes over sum of per-launch times for M=1,4,16,64" % POOL,
         "isolated_us_per_launch": {str(M): round(v, 3) for M, v in isolated.items()},
     }
+    traffic = profiled_traffic()
+    if traffic:
+        line["roofline"]["traffic"] = sum(traffic.values()) / len(traffic)
+        line["roofline"]["traffic_source"] = (
+            "dram__bytes_read.sum + dram__bytes_write.sum per launch, ncu capture of the current "
+            "kernel sources (profiles/bigemm_partial_decode_M16_M64.md), mean of M=%s"
+            % ",".join(str(m) for m in sorted(traffic)))
     if rank == 0 and world == 1 and not args.no_extras:
         line["e2e"] = run_e2e(bench, max(20, args.steps // 20), 5)
         line["workloads"] = run_other_workloads(dev, peaks)
