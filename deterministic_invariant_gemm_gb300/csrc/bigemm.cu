@@ -354,6 +354,10 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     p.epi_batch = epi_batch_for(static_cast<int>(M));
     p.grouped = 0;
     p.prefetch_rows = kStages * kBK;  // what the ring holds: the first four K blocks
+    // GROUP_M swizzle: 16 tile rows per group once there are four or more waves
+    // of tiles (the concurrent tiles then span about 16 x 9 tiles, whose A and
+    // B panels stay in L2), else 8.  It orders tiles only; no sum changes.
+    p.group_m = (m_tiles * n_tiles >= 4 * static_cast<int64_t>(d->sm_count)) ? 16 : 8;
 
     const int grid = static_cast<int>(units < d->sm_count ? units : d->sm_count);
     const dim3 g(static_cast<unsigned>(grid)), blk(kNumThreads);

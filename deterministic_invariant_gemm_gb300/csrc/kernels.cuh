@@ -9,7 +9,7 @@
 //   * "Split-K": with S > 1 segments the K blocks are dealt into S contiguous
 //     segments; each unit writes its FP32 partial to workspace slice s with plain
 //     stores, and splitk_reduce_kernel adds the slices in the order 0..S-1.
-//   * "GROUP_M - Swizzle L2 Cache": units are ordered in groups of kGroupM tile
+//   * "GROUP_M - Swizzle L2 Cache": units are ordered in groups of GROUP_M tile
 //     rows; a persistent grid of at most one CTA per SM takes units
 //     blockIdx.x, blockIdx.x + gridDim.x, ... -- a static schedule.
 // None of the three changes the order in which any single C element's terms
@@ -39,7 +39,6 @@ constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
 constexpr int kUmmaK = 16;
-constexpr int kGroupM = 8;
 constexpr int kNumThreads = 320;       // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
 constexpr int kEpilogueThreads = 256;
 
@@ -114,20 +113,22 @@ struct GemmParams {
     int grouped;            // 1: tmC views the output as {32 columns, rows, column groups
                             //    [, slices]} with boxes of epi_batch groups, one store per batch
     int prefetch_rows;      // K rows of B warmed in L2 before the dependency wait
+    int group_m;            // tile rows per GROUP_M swizzle group
 };
 
 // Unit u -> (tile row, tile column, K segment).  All tiles of segment 0 come
 // first, then segment 1, ...; inside a segment the tiles follow the GROUP_M
-// swizzle: groups of kGroupM tile rows, column-major inside a group.
+// swizzle: groups of p.group_m tile rows, column-major inside a group.  The
+// order decides only which CTA computes a tile, never how a sum is formed.
 __device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& mt, int& nt,
                                             int& seg) {
     const int tiles = p.m_tiles * p.n_tiles;
     seg = u / tiles;
     const int tile = u - seg * tiles;
-    const int per_group = kGroupM * p.n_tiles;
+    const int per_group = p.group_m * p.n_tiles;
     const int g = tile / per_group;
-    const int first_m = g * kGroupM;
-    const int gm = min(p.m_tiles - first_m, kGroupM);
+    const int first_m = g * p.group_m;
+    const int gm = min(p.m_tiles - first_m, p.group_m);
     const int r = tile - g * per_group;
     mt = first_m + r % gm;
     nt = r / gm;
@@ -282,11 +283,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    // The next kernel in the stream may be scheduled from now on (this CTA
-    // already holds its TMEM, so a dependent cannot take it first); it waits
-    // for this grid to complete before touching memory.
-    if (threadIdx.x == 0) grid_launch_dependents();
-
     // Everything above overlaps the previous kernel in the stream; from here on
     // global memory is read and written only after it has completed.
     grid_dependency_wait();
@@ -325,6 +321,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                 }
             }
+            // Every load of this CTA is issued: the next kernel in the stream may
+            // be scheduled from now on (it waits for this grid to complete before
+            // touching memory; this CTA already holds its TMEM, so a dependent
+            // cannot take it first).  Triggering here rather than at the start
+            // keeps the next kernel's blocks from starting while this one is
+            // still streaming.
+            grid_launch_dependents();
             // No copy may still be in flight when the CTA exits: wait (bounded)
             // for the last load issued into every stage.
             for (int s = 0; s < kStages; ++s)
