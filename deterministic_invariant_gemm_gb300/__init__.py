@@ -34,7 +34,8 @@ __all__ = [
     "bigemm_workspace_bytes", "bigemm_partial_workspace_bytes", "bigemm_run",
     "bigemm_run_bf16out", "bigemm_run_partial", "bigemm_splitk_reduce",
     "bigemm_run_atomic_splitk", "bigemm_device_status", "bigemm_last_launch_count",
-    "bigemm_run_splitk_static", "STATIC_SCRATCH_BYTES", "matmul", "EXPORTED_SYMBOLS",
+    "bigemm_run_splitk_static", "bigemm_linear", "STATIC_SCRATCH_BYTES", "matmul", "linear",
+    "EXPORTED_SYMBOLS",
 ]
 
 BLOCK_K = 64
@@ -54,7 +55,7 @@ EXPORTED_SYMBOLS = (
     "bigemm_effective_split_k", "bigemm_workspace_ld", "bigemm_workspace_bytes",
     "bigemm_partial_workspace_bytes", "bigemm_run", "bigemm_run_bf16out", "bigemm_run_partial",
     "bigemm_splitk_reduce", "bigemm_run_atomic_splitk", "bigemm_device_status",
-    "bigemm_last_launch_count", "bigemm_run_splitk_static",
+    "bigemm_last_launch_count", "bigemm_run_splitk_static", "bigemm_linear",
 )
 
 
@@ -98,6 +99,7 @@ def load():
         "bigemm_run_atomic_splitk": ([vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, vp], i32),
         "bigemm_device_status": ([i32], i32),
         "bigemm_run_splitk_static": ([vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, vp], i32),
+        "bigemm_linear": ([vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, i32, vp, sz, vp], i32),
         "bigemm_last_launch_count": ([], i32),
     }
     for name, (args, res) in sig.items():
@@ -178,6 +180,16 @@ def bigemm_run(A, B, C, M, N, K, lda, ldb, ldc, split_k, workspace=None, workspa
                            _ptr(workspace), workspace_bytes, _stream(stream))
     if check:
         _check(st, "bigemm_run")
+    return st
+
+
+def bigemm_linear(A, W, bias, C, M, N, K, lda, ldw, ldc, split_k, c_is_bf16, workspace=None,
+                  workspace_bytes=0, stream=None, check=True) -> int:
+    st = load().bigemm_linear(_ptr(A), _ptr(W), _ptr(bias), _ptr(C), M, N, K, lda, ldw, ldc,
+                              split_k, int(bool(c_is_bf16)), _ptr(workspace), workspace_bytes,
+                              _stream(stream))
+    if check:
+        _check(st, "bigemm_linear")
     return st
 
 
@@ -285,4 +297,41 @@ def matmul(A, B, out_dtype=None, split_k: int = 1, out=None, workspace=None, str
         bigemm_run_bf16out(A, B, out, M, N, K, lda, ldb, ldc, split_k, workspace, wbytes, stream)
     else:
         raise TypeError("out_dtype must be float32 or bfloat16")
+    return out
+
+
+def linear(x, weight, bias=None, out_dtype=None, split_k: int = 1, out=None, workspace=None,
+           stream=None):
+    """y = x @ weight.T + bias for bf16 CUDA tensors x [M, K], weight [N, K] and
+    bias [N] (or None), through bigemm_linear.  ``out_dtype`` float32 (default)
+    or bfloat16; ``split_k`` as in :func:`matmul`."""
+    import torch
+    if x.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise TypeError("x and weight must be bfloat16")
+    if bias is not None and (bias.dtype != torch.bfloat16 or bias.dim() != 1 or bias.stride(0) != 1):
+        raise TypeError("bias must be a contiguous bfloat16 vector")
+    if x.dim() != 2 or weight.dim() != 2 or x.shape[1] != weight.shape[1]:
+        raise ValueError("shapes do not compose: %s x %s^T" % (tuple(x.shape), tuple(weight.shape)))
+    if x.stride(1) != 1 or weight.stride(1) != 1:
+        raise ValueError("x and weight need unit column stride (row-major)")
+    out_dtype = torch.float32 if out_dtype is None else out_dtype
+    M, K = x.shape
+    N = weight.shape[0]
+    if bias is not None and bias.shape[0] != N:
+        raise ValueError("bias has %d entries, weight has %d rows" % (bias.shape[0], N))
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    lda = x.stride(0) if M > 1 else max(K, 8 * ((K + 7) // 8))
+    ldw = weight.stride(0) if N > 1 else max(K, 8 * ((K + 7) // 8))
+    ldc = out.stride(0) if M > 1 else max(N, 8 * ((N + 7) // 8))
+    bf16 = out_dtype == torch.bfloat16
+    if lda % 8 or ldw % 8 or ldc % (8 if bf16 else 4):
+        raise ValueError("row strides must be multiples of 8 elements for x and weight and of %d "
+                         "for the output; got %d, %d, %d" % (8 if bf16 else 4, lda, ldw, ldc))
+    need = bigemm_workspace_bytes(M, N, K, split_k)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    bigemm_linear(x, weight, bias, out, M, N, K, lda, ldw, ldc, split_k, bf16, workspace, wbytes,
+                  stream)
     return out

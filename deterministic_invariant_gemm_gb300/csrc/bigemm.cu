@@ -79,10 +79,13 @@ bigemm_status device_info(const DeviceInfo** out) {
                 return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
                        cudaSuccess;
             };
-            if (!opt_in((const void*)bigemm_tc_kernel<kOutF32>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutBF16>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutSlices>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutAtomic>))
+            if (!opt_in((const void*)bigemm_tc_kernel<kOutF32, false>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutBF16, false>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutSlices, false>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutAtomic, false>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutF32, true>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutBF16, true>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutSlices, true>))
                 return BIGEMM_ERR_CUDA;
             void* sym = nullptr;
             if (cudaGetSymbolAddress(&sym, g_device_status) != cudaSuccess) return BIGEMM_ERR_CUDA;
@@ -195,15 +198,20 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t esize, c
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Operand maps: A [M, K] in boxes of 64 k x 128 rows, B [K, N] in boxes of 64
-// columns x 64 k-rows, both with the 128-byte swizzle the MMA descriptors use;
-// and B again in 256 x 256 boxes without swizzle, used only to warm L2.
+// Operand maps: A [M, K] in boxes of 64 k x 128 rows; B [K, N] in boxes of 64
+// columns x 64 k-rows, or a weight matrix W [N, K] (wt) in boxes of 64 k x 256
+// rows; all with the 128-byte swizzle the MMA descriptors use.  The second
+// operand again in 256 x 256 boxes without swizzle, used only to warm L2.
 bool encode_operands(CUtensorMap* tmA, CUtensorMap* tmB, CUtensorMap* tmBp, const void* A,
-                     const void* B, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb) {
-    const int64_t da[2] = {K, M}, db[2] = {N, K};
+                     const void* B, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                     bool wt) {
+    const int64_t da[2] = {K, M};
+    const int64_t db[2] = {wt ? K : N, wt ? N : K};
     const uint32_t ba[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(kBM)};
-    const uint32_t bb[2] = {kBChunkCols, static_cast<uint32_t>(kBK)};
-    const uint32_t bp[2] = {static_cast<uint32_t>(kBN), static_cast<uint32_t>(kPrefetchRows)};
+    const uint32_t bb[2] = {wt ? static_cast<uint32_t>(kBK) : kBChunkCols,
+                            wt ? static_cast<uint32_t>(kBN) : static_cast<uint32_t>(kBK)};
+    const uint32_t bp[2] = {wt ? static_cast<uint32_t>(kPrefetchRows) : static_cast<uint32_t>(kBN),
+                            wt ? static_cast<uint32_t>(kBN) : static_cast<uint32_t>(kPrefetchRows)};
     return encode_tiled(tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, 2, da, lda, 0, ba,
                         CU_TENSOR_MAP_SWIZZLE_128B) &&
            encode_tiled(tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, 2, db, ldb, 0, bb,
@@ -254,16 +262,28 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaSt
 }
 
 template <int kOut>
-cudaError_t launch_gemm(dim3 g, dim3 blk, cudaStream_t stream, const CUtensorMap& tmA,
+cudaError_t launch_gemm(bool wt, dim3 g, dim3 blk, cudaStream_t stream, const CUtensorMap& tmA,
                         const CUtensorMap& tmB, const CUtensorMap& tmBp, const CUtensorMap& tmC,
                         const GemmParams& p) {
-    return launch_pdl(bigemm_tc_kernel<kOut>, g, blk, kSmemBytes, stream, tmA, tmB, tmBp, tmC, p);
+    if constexpr (kOut == kOutAtomic) {
+        if (wt) return cudaErrorInvalidValue;  // the contrast exists for B [K, N] only
+        return launch_pdl(bigemm_tc_kernel<kOut, false>, g, blk, kSmemBytes, stream, tmA, tmB, tmBp,
+                          tmC, p);
+    } else {
+        if (wt)
+            return launch_pdl(bigemm_tc_kernel<kOut, true>, g, blk, kSmemBytes, stream, tmA, tmB, tmBp,
+                              tmC, p);
+        return launch_pdl(bigemm_tc_kernel<kOut, false>, g, blk, kSmemBytes, stream, tmA, tmB, tmBp,
+                          tmC, p);
+    }
 }
 
 enum Mode { kModeF32, kModeBF16, kModePartial, kModeAtomic };
 
 bigemm_status launch_reduce(const DeviceInfo& d, const float* ws, int splits, int64_t M, int64_t N,
-                            void* C, int64_t ldc, bool bf16, cudaStream_t stream) {
+                            void* C, int64_t ldc, bool bf16, cudaStream_t stream,
+                            const void* bias = nullptr) {
+    const __nv_bfloat16* b = static_cast<const __nv_bfloat16*>(bias);
     const int64_t ws_ld = ws_ld_of(N);
     const int64_t items = M * (ws_ld / 4);
     // At most one block per SM, so the reduction never crowds out the next
@@ -275,17 +295,21 @@ bigemm_status launch_reduce(const DeviceInfo& d, const float* ws, int splits, in
     if (bf16)
         e = launch_pdl(splitk_reduce_kernel<true>, dim3(static_cast<unsigned>(blocks)),
                        dim3(kReduceThreads), 0, stream, ws, C, static_cast<int>(M), static_cast<int>(N),
-                       ldc, ws_ld, splits);
+                       ldc, ws_ld, splits, b);
     else
         e = launch_pdl(splitk_reduce_kernel<false>, dim3(static_cast<unsigned>(blocks)),
                        dim3(kReduceThreads), 0, stream, ws, C, static_cast<int>(M), static_cast<int>(N),
-                       ldc, ws_ld, splits);
+                       ldc, ws_ld, splits, b);
     return e == cudaSuccess ? BIGEMM_OK : BIGEMM_ERR_CUDA;
 }
 
+// wt: the second operand is a weight matrix W [N, K] (ldb is its row stride);
+// otherwise B [K, N].  bias: bf16 [N] added to every row (linear layers), or
+// nullptr.
 bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t M, int64_t N,
                        int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int split_k, void* ws,
-                       size_t ws_bytes, cudaStream_t stream) {
+                       size_t ws_bytes, cudaStream_t stream, bool wt = false,
+                       const void* bias = nullptr) {
     g_last_launches = 0;
     // ---- sizes and the split
     if (M < 0 || N < 0 || K < 0) return BIGEMM_ERR_ARG;
@@ -296,7 +320,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     const bool want_c = (mode != kModePartial);
     // ---- pointers and strides (checked even for empty products)
     if (K > 0 && (A == nullptr || B == nullptr)) return BIGEMM_ERR_ARG;
-    if (K > 0 && (lda < K || ldb < N)) return BIGEMM_ERR_ARG;
+    if (K > 0 && (lda < K || ldb < (wt ? K : N))) return BIGEMM_ERR_ARG;
     if (want_c && (C == nullptr || ldc < N)) return BIGEMM_ERR_ARG;
     if (K > 0 && (!aligned16(A) || !aligned16(B) || lda % 8 != 0 || ldb % 8 != 0))
         return BIGEMM_ERR_ALIGN;
@@ -304,6 +328,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
         if (!aligned16(C)) return BIGEMM_ERR_ALIGN;
         if (ldc % (mode == kModeBF16 ? 8 : 4) != 0) return BIGEMM_ERR_ALIGN;
     }
+    if (bias != nullptr && !aligned16(bias)) return BIGEMM_ERR_ALIGN;
     // ---- workspace
     const bool need_ws = (mode == kModePartial) || ((mode == kModeF32 || mode == kModeBF16) && splits > 1);
     if (need_ws) {
@@ -322,7 +347,12 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     bigemm_status st = device_info(&d);
     if (st != BIGEMM_OK) return st;
 
-    // ---- K == 0: the empty sum is +0.0 everywhere
+    // ---- K == 0: the empty sum is +0.0 everywhere (plus the bias, if any)
+    if (K == 0 && bias != nullptr) {
+        st = launch_reduce(*d, nullptr, 0, M, N, C, ldc, mode == kModeBF16, stream, bias);
+        if (st == BIGEMM_OK) g_last_launches = 1;
+        return st;
+    }
     if (K == 0) {
         cudaError_t e;
         if (mode == kModePartial) {
@@ -337,7 +367,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
 
     CUtensorMap tmA, tmB, tmBp, tmC;
     std::memset(&tmC, 0, sizeof(tmC));
-    if (!encode_operands(&tmA, &tmB, &tmBp, A, B, M, N, K, lda, ldb)) return BIGEMM_ERR_CUDA;
+    if (!encode_operands(&tmA, &tmB, &tmBp, A, B, M, N, K, lda, ldb, wt)) return BIGEMM_ERR_CUDA;
 
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
@@ -358,6 +388,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     // of tiles (the concurrent tiles then span about 16 x 9 tiles, whose A and
     // B panels stay in L2), else 8.  It orders tiles only; no sum changes.
     p.group_m = (m_tiles * n_tiles >= 4 * static_cast<int64_t>(d->sm_count)) ? 16 : 8;
+    p.bias = (splits == 1) ? static_cast<const __nv_bfloat16*>(bias) : nullptr;
 
     const int grid = static_cast<int>(units < d->sm_count ? units : d->sm_count);
     const dim3 g(static_cast<unsigned>(grid)), blk(kNumThreads);
@@ -370,7 +401,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
         if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
         p.out = C;
         p.ld_out = ldc;
-        e = launch_gemm<kOutAtomic>(g, blk, stream, tmA, tmB, tmBp, tmC, p);
+        e = launch_gemm<kOutAtomic>(wt, g, blk, stream, tmA, tmB, tmBp, tmC, p);
         launches = 1;
     } else if (mode == kModePartial || splits > 1) {
         p.out = ws;
@@ -381,11 +412,11 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
             p.grouped = 1;
         else if (!encode_out_slices(&tmC, ws, M, N, splits))
             return BIGEMM_ERR_CUDA;
-        e = launch_gemm<kOutSlices>(g, blk, stream, tmA, tmB, tmBp, tmC, p);
+        e = launch_gemm<kOutSlices>(wt, g, blk, stream, tmA, tmB, tmBp, tmC, p);
         launches = 1;
         if (e == cudaSuccess && mode != kModePartial) {
             st = launch_reduce(*d, static_cast<const float*>(ws), splits, M, N, C, ldc,
-                               mode == kModeBF16, stream);
+                               mode == kModeBF16, stream, bias);
             if (st != BIGEMM_OK) return st;
             launches = 2;
         }
@@ -398,14 +429,14 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
                 p.grouped = 1;
             else if (!encode_out_bf16(&tmC, C, M, N, ldc))
                 return BIGEMM_ERR_CUDA;
-            e = launch_gemm<kOutBF16>(g, blk, stream, tmA, tmB, tmBp, tmC, p);
+            e = launch_gemm<kOutBF16>(wt, g, blk, stream, tmA, tmB, tmBp, tmC, p);
         } else {
             if (encode_out_grouped(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, M, N, ldc, 0, 0,
                                    p.epi_batch))
                 p.grouped = 1;
             else if (!encode_out_f32(&tmC, C, M, N, ldc))
                 return BIGEMM_ERR_CUDA;
-            e = launch_gemm<kOutF32>(g, blk, stream, tmA, tmB, tmBp, tmC, p);
+            e = launch_gemm<kOutF32>(wt, g, blk, stream, tmA, tmB, tmBp, tmC, p);
         }
         launches = 1;
     }
@@ -529,6 +560,14 @@ bigemm_status bigemm_splitk_reduce(const float* workspace, int splits, int64_t M
                        static_cast<cudaStream_t>(stream));
     if (st == BIGEMM_OK) g_last_launches = 1;
     return st;
+}
+
+bigemm_status bigemm_linear(const void* A, const void* W, const void* bias, void* C, int64_t M,
+                            int64_t N, int64_t K, int64_t lda, int64_t ldw, int64_t ldc, int split_k,
+                            int c_is_bf16, void* workspace, size_t workspace_bytes,
+                            bigemm_stream stream) {
+    return run_impl(c_is_bf16 ? kModeBF16 : kModeF32, A, W, C, M, N, K, lda, ldw, ldc, split_k,
+                    workspace, workspace_bytes, static_cast<cudaStream_t>(stream), /*wt=*/true, bias);
 }
 
 bigemm_status bigemm_run_atomic_splitk(const void* A, const void* B, float* C, int64_t M, int64_t N,

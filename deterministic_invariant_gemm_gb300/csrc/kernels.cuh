@@ -77,7 +77,10 @@ __host__ __device__ constexpr int epi_batch_for(int M) {
     return epi_boxes_for(M) < kMaxBatch ? epi_boxes_for(M) : kMaxBatch;
 }
 
-constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, /*A MN-major*/ false, /*B MN-major*/ true);
+// B [K, N] row-major is read N-major; the weight layout W [N, K] of a linear
+// layer is read K-major, like A.
+constexpr uint32_t kIdescBN = idesc_bf16_f32(kBM, kBN, /*A MN-major*/ false, /*B MN-major*/ true);
+constexpr uint32_t kIdescWt = idesc_bf16_f32(kBM, kBN, /*A MN-major*/ false, /*B MN-major*/ false);
 
 // A wait that gives up: 2 s of global time, checked every 256 polls.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
@@ -114,6 +117,8 @@ struct GemmParams {
                             //    [, slices]} with boxes of epi_batch groups, one store per batch
     int prefetch_rows;      // K rows of B warmed in L2 before the dependency wait
     int group_m;            // tile rows per GROUP_M swizzle group
+    const __nv_bfloat16* bias;  // [N] added to every row by the direct (unsplit)
+                                // epilogue, or nullptr
 };
 
 // Unit u -> (tile row, tile column, K segment).  All tiles of segment 0 come
@@ -201,6 +206,35 @@ __device__ __forceinline__ void store_row_masked(const GemmParams& p, int row, i
     }
 }
 
+// Adds bias[col .. col+31] (bf16, every lane the same values) to a thread's
+// 32 FP32 accumulators, one FP32 addition each, rounded to nearest even.
+// Columns >= N are left alone.
+__device__ __forceinline__ void add_bias_block(const __nv_bfloat16* bias, int col, int N,
+                                               uint32_t* r) {
+    if (col + 32 <= N) {
+        const uint4* b4 = reinterpret_cast<const uint4*>(bias + col);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const uint4 w = __ldg(b4 + v);
+            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                // a bf16 value is the upper half of the FP32 with the same value
+                const float lo = __uint_as_float(wv[h] << 16);
+                const float hi = __uint_as_float(wv[h] & 0xFFFF0000u);
+                r[8 * v + 2 * h] = __float_as_uint(__fadd_rn(__uint_as_float(r[8 * v + 2 * h]), lo));
+                r[8 * v + 2 * h + 1] =
+                    __float_as_uint(__fadd_rn(__uint_as_float(r[8 * v + 2 * h + 1]), hi));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (col + j < N)
+                r[j] = __float_as_uint(__fadd_rn(__uint_as_float(r[j]), __bfloat162float(bias[col + j])));
+    }
+}
+
 // The atomic contrast: every thread adds its row's 32 values into C.
 __device__ __forceinline__ void atomic_add_row_chunk(const GemmParams& p, int row, int col,
                                                      const uint32_t (&r)[32]) {
@@ -211,7 +245,9 @@ __device__ __forceinline__ void atomic_add_row_chunk(const GemmParams& p, int ro
         if (c < valid) atomicAdd(dst + c, __uint_as_float(r[c]));
 }
 
-template <int kOut>
+// kWt: the second operand is the weight matrix W [N, K] (K-major); otherwise
+// B [K, N] (N-major).  Both products run the same K = 16 instruction sequence.
+template <int kOut, bool kWt>
 __global__ void __launch_bounds__(kNumThreads, 1)
     bigemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmBp, const __grid_constant__ CUtensorMap tmC,
@@ -268,7 +304,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             unit_coords(p, blockIdx.x, mt, nt, seg);
             const int k0 = seg * p.kb_per_split * kBK;
             const int k1 = min(k0 + p.prefetch_rows, min(k0 + p.kb_per_split * kBK, p.kb_total * kBK));
-            for (int k = k0; k < k1; k += kPrefetchRows) tma_prefetch_l2_2d(&tmBp, nt * kBN, k);
+            for (int k = k0; k < k1; k += kPrefetchRows) {
+                if constexpr (kWt) tma_prefetch_l2_2d(&tmBp, k, nt * kBN);
+                else tma_prefetch_l2_2d(&tmBp, nt * kBN, k);
+            }
         }
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
@@ -309,10 +348,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const uint32_t fb = full_bar(stage);
                     mbar_arrive_expect_tx(fb, kStageBytes);
                     tma_load_2d(sA + stage * kABytes, &tmA, fb, kb * kBK, m0);
+                    if constexpr (kWt) {
+                        // one box: 256 weight rows x 64 k (128 bytes each)
+                        tma_load_2d(sB + stage * kBBytes, &tmB, fb, kb * kBK, n0);
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < kBN / static_cast<int>(kBChunkCols); ++c)
-                        tma_load_2d(sB + stage * kBBytes + c * kBChunkBytes, &tmB, fb,
-                                    n0 + c * static_cast<int>(kBChunkCols), kb * kBK);
+                        for (int c = 0; c < kBN / static_cast<int>(kBChunkCols); ++c)
+                            tma_load_2d(sB + stage * kBBytes + c * kBChunkBytes, &tmB, fb,
+                                        n0 + c * static_cast<int>(kBChunkCols), kb * kBK);
+                    }
                     issued_mask |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) {
@@ -368,11 +412,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
                         // A: K-major, 128-byte rows; advance 16 elements = 32 bytes.
                         const uint64_t ad = smem_desc_sw128(a0 + kk * kUmmaK * 2, 16, 1024);
-                        // B: N-major; 16 k-rows of 128 bytes = 2048 bytes per step.
-                        // LBO = distance between 64-column chunks, SBO = 8 k-rows.
-                        const uint64_t bd =
-                            smem_desc_sw128(b0 + kk * kUmmaK * 128, kBChunkBytes, 1024);
-                        mma_bf16(d_tmem, ad, bd, kIdesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                        uint64_t bd;
+                        if constexpr (kWt) {
+                            // W: K-major like A, 256 rows of 128 bytes.
+                            bd = smem_desc_sw128(b0 + kk * kUmmaK * 2, 16, 1024);
+                        } else {
+                            // B: N-major; 16 k-rows of 128 bytes = 2048 bytes per step.
+                            // LBO = distance between 64-column chunks, SBO = 8 k-rows.
+                            bd = smem_desc_sw128(b0 + kk * kUmmaK * 128, kBChunkBytes, 1024);
+                        }
+                        mma_bf16(d_tmem, ad, bd, kWt ? kIdescWt : kIdescBN,
+                                 (kb > kb0 || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(empty_bar(stage));
                     if (++stage == kStages) {
@@ -439,6 +489,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         tc_fence_before();
                         mbar_arrive(tempty_bar(acc));
                         released = true;
+                    }
+                    if constexpr (kOut == kOutF32 || kOut == kOutBF16) {
+                        if (p.bias != nullptr) {  // uniform
+#pragma unroll
+                            for (int i = 0; i < kMaxBatch; ++i)
+                                if (i < nb) add_bias_block(p.bias, n0 + (c0 + i) * 32, p.N, r + 32 * i);
+                        }
                     }
                     if constexpr (kOut == kOutAtomic) {
 #pragma unroll
@@ -519,7 +576,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 }
 
 // Split-K reduction: for every element, acc = w_0, then acc = acc + w_s for
-// s = 1 .. S-1 in that order (FP32, round to nearest even); starting from w_0
+// s = 1 .. S-1 in that order (FP32, round to nearest even), then acc + bias[n]
+// when a bias is given; starting from w_0
 // rather than 0.0f keeps a lone -0.0 partial intact.  One thread handles four
 // adjacent columns of one row (16-byte loads, coalesced along N); the loads of
 // up to eight slices are issued before their additions.
@@ -528,7 +586,7 @@ constexpr int kReduceThreads = 128;
 template <bool kBF16Out>
 __global__ void __launch_bounds__(kReduceThreads)
     splitk_reduce_kernel(const float* __restrict__ ws, void* __restrict__ C, int M, int N,
-                         int64_t ldc, int64_t ws_ld, int S) {
+                         int64_t ldc, int64_t ws_ld, int S, const __nv_bfloat16* __restrict__ bias) {
     // The next kernel in the stream may be scheduled at once: it waits for
     // this grid to complete before touching memory, and this kernel holds no
     // tensor memory a dependent could need.
@@ -542,7 +600,8 @@ __global__ void __launch_bounds__(kReduceThreads)
         const int64_t m = v / vec_per_row;
         const int col = static_cast<int>(v - m * vec_per_row) * 4;
         const float* src = ws + m * ws_ld + col;
-        float4 acc = __ldcs(reinterpret_cast<const float4*>(src));
+        // S == 0: no slices (an empty K); the sum is +0.0 and only a bias remains
+        float4 acc = S > 0 ? __ldcs(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int s0 = 1; s0 < S; s0 += 8) {
             float4 w[8];
 #pragma unroll
@@ -560,6 +619,10 @@ __global__ void __launch_bounds__(kReduceThreads)
         }
         const int valid = min(4, N - col);
         if (valid <= 0) continue;
+        if (bias != nullptr) {  // a linear layer's bias, added after the split sum
+            float* a = &acc.x;
+            for (int c = 0; c < valid; ++c) a[c] = __fadd_rn(a[c], __bfloat162float(bias[col + c]));
+        }
         if constexpr (kBF16Out) {
             __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(C) + m * ldc + col;
             if (valid == 4) {

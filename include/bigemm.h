@@ -173,6 +173,30 @@ BIGEMM_API bigemm_status bigemm_splitk_reduce(const float *workspace, int splits
                                    void *C, int64_t ldc, int c_is_bf16,
                                    bigemm_stream stream);
 
+/* Batch-invariant linear layer: C = A * W^T + bias, i.e.
+ *     C_ij = sum_{k=0}^{K-1} A_ik * W_jk + bias_j
+ * with the weight matrix in the layout linear layers keep it: W bf16 [N, K]
+ * row-major (ldw >= K, a multiple of 8).  This is the call the Tencent
+ * article's serving path routes a linear layer to when batch invariance is
+ * on ("vLLM における GEMM の Batch Invariance サポート": linear_batch_invariant(x,
+ * weight, bias)).  A bf16 [M, K] (lda), C [M, N] fp32 (c_is_bf16 = 0, ldc % 4
+ * == 0) or bf16 (c_is_bf16 = 1, ldc % 8 == 0); bias bf16 [N], 16-byte
+ * aligned, or NULL.
+ * The reduction order is that of bigemm_run for the same K and split_k -- K
+ * blocks of 64 in ascending order, S contiguous segments summed in the order
+ * 0..S-1 -- and the bias is added last, one FP32 addition per element (in the
+ * epilogue when S = 1, in the reduction kernel when S > 1).  Row i of C is
+ * bit-for-bit a function of (row i of A, W, bias, K, split_k, output type).
+ * The weight is read K-major, so the bits may differ from bigemm_run with B =
+ * W^T; each entry point is batch-invariant on its own.  Workspace and errors
+ * as in bigemm_run. */
+BIGEMM_API bigemm_status bigemm_linear(const void *A, const void *W, const void *bias, void *C,
+                                       int64_t M, int64_t N, int64_t K,
+                                       int64_t lda, int64_t ldw, int64_t ldc,
+                                       int split_k, int c_is_bf16,
+                                       void *workspace, size_t workspace_bytes,
+                                       bigemm_stream stream);
+
 /* Measured contrast only -- NOT deterministic.  Same arguments as bigemm_run
  * without a workspace: C (fp32) is zeroed on the stream, then every K
  * segment's partial is added into C with atomic adds ("Split-K": atomic_add;

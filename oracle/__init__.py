@@ -16,6 +16,9 @@ passage of the pages it follows in ``oracle.c``'s header:
 * :func:`ulp` -- ULP(x) = 2^(E - M) (same section).
 * :func:`splitk_reduce_f32` -- the split-K workspace reduction in serial order
   (same article, "Split-K").
+* :func:`linear_rows` -- a linear layer, C = A W^T + b (same article, "vLLM に
+  おける GEMM の Batch Invariance サポート": linear_batch_invariant(x, weight,
+  bias)).
 
 Pins (tests/test_oracle.py) tie each function to something other than itself:
 identity and permutation products, small-integer products checked against
@@ -172,6 +175,22 @@ def gemm_rows(A, B, M: int, N: int, K: int, lda: int | None = None,
                                   _ptr(C), _ptr(D))
     if rc != 0:
         raise ValueError("oracle_gemm_rows: bad arguments")
+    return C, D
+
+
+def linear_rows(A, W, bias, M: int, N: int, K: int, rows=None):
+    """(C, D) of a linear layer for the selected rows of A:
+    C_ij = sum_k A_ik W_jk + b_j (binary64; the K terms k-ascending, then b_j),
+    D_ij = sum_k |A_ik W_jk| + |b_j|, the scale of all the terms summed.
+    W: bf16 patterns [N, K]; bias: bf16 patterns [N] or None.  W^T is formed
+    by moving the 16-bit patterns (exact) and the product is gemm_rows'."""
+    w = _bits16(W).reshape(N, K)
+    wt = np.ascontiguousarray(w.T)
+    C, D = gemm_rows(A, wt, M, N, K, rows=rows)
+    if bias is not None:
+        b = decode(FMT_BF16, _bits16(bias).reshape(N))
+        C = C + b[None, :]
+        D = D + np.abs(b)[None, :]
     return C, D
 
 

@@ -14,8 +14,9 @@ import pytest
 import torch
 
 import deterministic_invariant_gemm_gb300 as dig
+import oracle
 import workloads
-from gemm_check import bits_equal
+from gemm_check import bits_equal, check_tolerance, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -25,6 +26,17 @@ def _device(cuda_device):
     dig.load()
     yield
     assert dig.bigemm_device_status(reset=True) == 0
+
+
+def assert_correct(C, A, B, bf16_out=False, rows=None):
+    """Bitwise agreement alone would also accept a consistently wrong result:
+    the reference output of each invariance check is held to the oracle too
+    (on a row sample for large products)."""
+    M, K = A.shape
+    N = B.shape[1]
+    Cref, D = oracle.gemm_rows(A.cpu(), B.cpu(), M, N, K, rows=rows)
+    got = C if rows is None else C[torch.tensor(rows, device=C.device)]
+    check_tolerance(to_f64(got), Cref, D, bf16_out, "invariance reference")
 
 
 def gemm(A, B, split_k=1, bf16_out=False, atomic=False, ws=None):
@@ -43,6 +55,7 @@ def test_small_rows_invariant_at_m_1_7_64(split_k, bf16_out):
     A, B = workloads.pair(M, N, K, workloads.BASE_SEED + w["index"])
     A, B = A.cuda(), B.cuda()
     full = gemm(A, B, split_k, bf16_out)
+    assert_correct(full, A, B, bf16_out)
     for i in range(M):
         one = gemm(A[i:i + 1].contiguous(), B, split_k, bf16_out)
         assert bits_equal(one, full[i:i + 1]), "row %d differs at M=1" % i
@@ -61,6 +74,7 @@ def test_decode_rows_invariant_across_batch_sizes():
                           b_std=w["b_std"])
     A, B = A.cuda(), B.cuda()
     ref = gemm(A, B, split_k=0)
+    assert_correct(ref, A, B)
     for M in w["Ms"]:
         for off in (0, 64 - M, (64 - M) // 2):
             out = gemm(A[off:off + M].contiguous(), B, split_k=0)
@@ -80,6 +94,7 @@ def test_row_position_inside_tiles():
     filler = workloads.normal_bf16((383, K), 45)
     row, B, filler = row.cuda(), B.cuda(), filler.cuda()
     ref = gemm(row, B)
+    assert_correct(ref, row, B)
     for pos in (0, 1, 31, 32, 63, 64, 95, 96, 127, 128, 255, 256, 383):
         batch = torch.cat([filler[:pos], row, filler[pos:]])
         out = gemm(batch, B)
@@ -94,6 +109,7 @@ def test_mixed_batch_permuted_and_padded(size, bf16_out):
     A, B = workloads.pair(M, N, K, workloads.BASE_SEED + 3)
     A, B = A.cuda(), B.cuda()
     C = gemm(A, B, 1, bf16_out)
+    assert_correct(C, A, B, bf16_out, rows=[0, 1, size // 2, size - 1])
     g = torch.Generator().manual_seed(size)
     perm = torch.randperm(M, generator=g).cuda()
     r = int(torch.randint(1, 128, (1,), generator=g))
@@ -113,6 +129,7 @@ def test_longk_workspace_path_bit_stable_over_10_runs(S):
     A, B = workloads.pair(M, N, K, workloads.BASE_SEED + w["index"])
     A, B = A.cuda(), B.cuda()
     first = gemm(A, B, S)
+    assert_correct(first, A, B)
     for _ in range(9):
         assert bits_equal(gemm(A, B, S), first)
 
@@ -132,6 +149,7 @@ def test_split_changes_bits_only_through_split_k():
     A, B = A.cuda(), B.cuda()
     outs = {S: gemm(A, B, S) for S in (1, 2, 4, 8, 16)}
     for S, o in outs.items():
+        assert_correct(o, A, B)
         assert bits_equal(gemm(A, B, S), o)
     assert any(not bits_equal(outs[1], outs[S]) for S in (2, 4, 8, 16))
 

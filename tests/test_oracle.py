@@ -315,3 +315,51 @@ def test_serial_f32_reduction_integers_and_shape():
     assert out.shape == (3, 5)
     assert np.array_equal(out, W.astype(np.int64).sum(axis=0).astype(np.float32))
     assert np.array_equal(oracle.splitk_reduce_f32(W[:1]), W[0])
+
+
+# --------------------------------------------------------------------------
+# The linear layer C = A W^T + b
+# --------------------------------------------------------------------------
+
+def test_linear_zero_input_gives_the_bias():
+    M, N, K = 5, 33, 70
+    A = torch.zeros(M, K, dtype=torch.bfloat16)
+    W = workloads.normal_bf16((N, K), 3)
+    b = workloads.normal_bf16((N,), 4)
+    C, D = oracle.linear_rows(A, W, b, M, N, K)
+    bd = b.to(torch.float64).numpy()
+    assert np.array_equal(C, np.broadcast_to(bd, (M, N)))
+    assert np.array_equal(D, np.broadcast_to(np.abs(bd), (M, N)))
+
+
+def test_linear_identity_weight_adds_bias_exactly():
+    M, K = 9, 48
+    A = workloads.normal_bf16((M, K), 5)
+    W = torch.eye(K, dtype=torch.bfloat16)            # N = K
+    b = workloads.normal_bf16((K,), 6)
+    C, _ = oracle.linear_rows(A, W, b, M, K, K)
+    # bf16 + bf16 is exact in binary64
+    assert np.array_equal(C, A.to(torch.float64).numpy() + b.to(torch.float64).numpy()[None, :])
+    C0, _ = oracle.linear_rows(A, W, None, M, K, K)
+    assert np.array_equal(C0, A.to(torch.float64).numpy())
+
+
+@pytest.mark.parametrize("seed", [11, 12, 13])
+def test_linear_brute_force_rational(seed):
+    rnd = random.Random(seed)
+    M, N, K = rnd.randint(1, 4), rnd.randint(1, 5), rnd.randint(1, 6)
+    A = workloads.normal_bf16((M, K), 600 + seed)
+    W = workloads.normal_bf16((N, K), 700 + seed)
+    b = workloads.normal_bf16((N,), 800 + seed)
+    C, D = oracle.linear_rows(A, W, b, M, N, K)
+    a = A.to(torch.float64).numpy()
+    w = W.to(torch.float64).numpy()
+    bb = b.to(torch.float64).numpy()
+    u = Fraction(2.0 ** -53)
+    for i in range(M):
+        for j in range(N):
+            terms = [Fraction(float(a[i, k])) * Fraction(float(w[j, k])) for k in range(K)]
+            exact = sum(terms, Fraction(0)) + Fraction(float(bb[j]))
+            scale = sum((abs(t) for t in terms), Fraction(0)) + abs(Fraction(float(bb[j])))
+            assert abs(Fraction(C[i, j]) - exact) <= (K + 1) * u * scale
+            assert abs(Fraction(D[i, j]) - scale) <= (K + 1) * u * scale
