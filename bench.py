@@ -251,17 +251,23 @@ def external_events_supported() -> bool:
 # --------------------------------------------------------- decode workload --
 
 class DecodeBench:
-    """Inputs, workspaces and the captured step graphs of the headline workload."""
+    """Inputs, workspaces and the captured step graphs of the headline workload.
+    linear=True: the same step as a stack of linear layers, weights stored
+    [N, K] with a bias, through bigemm_linear."""
 
-    def __init__(self, dev: torch.device):
+    def __init__(self, dev: torch.device, linear: bool = False):
         import deterministic_invariant_gemm_gb300 as dig
         self.dig = dig
         self.dev = dev
+        self.linear = linear
         seed = workloads.BASE_SEED + DECODE["index"]
         self.split = dig.bigemm_default_split_k(K_DEC)
         self.A = {M: workloads.normal_bf16((M, K_DEC), seed + M, DECODE["a_std"]).to(dev) for M in MS}
-        self.B = [workloads.normal_bf16((K_DEC, N_DEC), seed + 1000 + j, DECODE["b_std"]).to(dev)
+        shape = (N_DEC, K_DEC) if linear else (K_DEC, N_DEC)
+        self.B = [workloads.normal_bf16(shape, seed + 1000 + j, DECODE["b_std"]).to(dev)
                   for j in range(POOL)]
+        self.bias = [workloads.normal_bf16((N_DEC,), seed + 2000 + j, 0.02).to(dev)
+                     for j in range(POOL)] if linear else None
         self.C = {M: torch.empty((M, N_DEC), dtype=torch.float32, device=dev) for M in MS}
         self.ws_bytes = {M: dig.bigemm_partial_workspace_bytes(M, N_DEC, K_DEC, self.split) for M in MS}
         self.ws = {M: torch.empty(self.ws_bytes[M], dtype=torch.uint8, device=dev) for M in MS}
@@ -271,8 +277,13 @@ class DecodeBench:
         self.full = None
         self.single = []
 
-    def product(self, M: int, B: torch.Tensor, ev=None):
+    def product(self, M: int, B: torch.Tensor, ev=None, j: int = 0):
         dig = self.dig
+        if self.linear:
+            need = dig.bigemm_workspace_bytes(M, N_DEC, K_DEC, self.split)
+            dig.bigemm_linear(self.A[M], B, self.bias[j], self.C[M], M, N_DEC, K_DEC, K_DEC, K_DEC,
+                              N_DEC, self.split, 0, self.ws[M], need)
+            return
         if ev is not None:
             ev[0].record()
         dig.bigemm_run_partial(self.A[M], B, M, N_DEC, K_DEC, K_DEC, N_DEC, self.split,
@@ -283,8 +294,8 @@ class DecodeBench:
 
     def step(self, i: int, events=None):
         for idx, M in enumerate(MS):
-            B = self.B[(i * len(MS) + idx) % POOL]
-            self.product(M, B, None if events is None else events[idx])
+            j = (i * len(MS) + idx) % POOL
+            self.product(M, self.B[j], None if events is None else events[idx], j)
 
     def _capture(self, fn):
         s = torch.cuda.Stream(device=self.dev)
@@ -421,6 +432,26 @@ def run_e2e(bench: DecodeBench, steps: int, warmup: int) -> dict:
     return {"value": decode_flops_per_step() * steps / secs / 1e12, "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": secs * 1e3 / steps}
+
+
+def run_decode_linear(dev, args) -> dict:
+    """The headline step as linear layers (bigemm_linear, weights [N, K] plus a
+    bias), timed the same way."""
+    lb = DecodeBench(dev, linear=True)
+    for i in range(5):
+        lb.step(i)
+    torch.cuda.synchronize()
+    lb.capture()
+    lb.run_steps(0, 8)
+    torch.cuda.synchronize()
+    steps = max(200, args.steps // 4)
+    secs = time_region_steps(lb, steps, 1)
+    out = {"tflops": round(decode_flops_per_step() * steps / secs / 1e12, 2),
+           "us_per_step": round(secs * 1e6 / steps, 2), "split_k": lb.split,
+           "weights": "[N, K] + bias (bigemm_linear)"}
+    del lb
+    torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------ single workloads --
@@ -699,6 +730,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_extras:
         line["e2e"] = run_e2e(bench, max(20, args.steps // 20), 5)
         line["workloads"] = run_other_workloads(dev, peaks)
+        line["workloads"]["decode_linear"] = run_decode_linear(dev, args)
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
         print(json.dumps(line), flush=True)
