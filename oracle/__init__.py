@@ -16,6 +16,9 @@ passage of the pages it follows in ``oracle.c``'s header:
 * :func:`ulp` -- ULP(x) = 2^(E - M) (same section).
 * :func:`splitk_reduce_f32` -- the split-K workspace reduction in serial order
   (same article, "Split-K").
+* :func:`decode8` / :func:`linear8_rows` -- 8-bit float (E5M2, E4M3) codecs and
+  an 8-bit linear layer (the FP8 matmul of the cuTile article's benchmark,
+  techplay.jp "TileGymで行列積ベンチマーク").
 * :func:`linear_rows` -- a linear layer, C = A W^T + b (same article, "vLLM に
   おける GEMM の Batch Invariance サポート": linear_batch_invariant(x, weight,
   bias)).
@@ -41,6 +44,8 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 
 FMT_FP16 = 0
 FMT_BF16 = 1
+FMT_E5M2 = 2
+FMT_E4M3 = 3
 
 _lib = None
 
@@ -88,6 +93,9 @@ def _load():
     lib.oracle_ulp.restype = dbl
     lib.oracle_gemm_rows.argtypes = [vp, vp, i64, i64, i64, i64, i64, vp, i64, vp, vp]
     lib.oracle_gemm_rows.restype = ctypes.c_int
+    lib.oracle_linear8_rows.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, i64, i64, i64, i64, i64,
+                                        vp, i64, vp, vp]
+    lib.oracle_linear8_rows.restype = ctypes.c_int
     lib.oracle_splitk_reduce_f32.argtypes = [vp, i64, i64, vp]
     lib.oracle_splitk_reduce_f32.restype = ctypes.c_int
     lib.oracle_decode_array.argtypes = [ctypes.c_int, vp, i64, vp]
@@ -187,6 +195,60 @@ def linear_rows(A, W, bias, M: int, N: int, K: int, rows=None):
     w = _bits16(W).reshape(N, K)
     wt = np.ascontiguousarray(w.T)
     C, D = gemm_rows(A, wt, M, N, K, rows=rows)
+    if bias is not None:
+        b = decode(FMT_BF16, _bits16(bias).reshape(N))
+        C = C + b[None, :]
+        D = D + np.abs(b)[None, :]
+    return C, D
+
+
+def _bits8(x) -> np.ndarray:
+    """Accept a numpy uint8/int8 array or a torch 8-bit float / uint8 tensor (CPU)."""
+    if hasattr(x, "detach"):
+        import torch
+        t = x.detach()
+        if t.device.type != "cpu":
+            raise ValueError("oracle: inputs must live in host memory")
+        if t.element_size() != 1:
+            raise TypeError("oracle: expected 8-bit patterns")
+        x = t.contiguous().view(torch.uint8).numpy()
+    a = np.ascontiguousarray(x)
+    if a.dtype == np.int8:
+        a = a.view(np.uint8)
+    if a.dtype != np.uint8:
+        raise TypeError("oracle: expected 8-bit patterns, got %s" % a.dtype)
+    return a
+
+
+def decode8(fmt: int, bits) -> np.ndarray:
+    """Values of 8-bit float patterns (FMT_E5M2 / FMT_E4M3)."""
+    b = _bits8(np.asarray(bits, dtype=np.uint8) if not hasattr(bits, "detach") else bits)
+    lib = _load()
+    return np.array([lib.oracle_decode(fmt, int(v)) for v in b.reshape(-1)],
+                    dtype=np.float64).reshape(b.shape)
+
+
+def linear8_rows(A, W, fmt_a: int, fmt_b: int, M: int, N: int, K: int, scale: float = 1.0,
+                 bias=None, rows=None):
+    """(C, D) of an 8-bit float linear layer for the selected rows of A:
+    C_ij = scale * sum_k A_ik W_jk + b_j   (binary64, k ascending, then the
+    scale, then the bias), D_ij = |scale| * sum_k |A_ik W_jk| + |b_j|.
+    A: [M, K] bytes, W: [N, K] bytes (weight layout), bias: bf16 [N] or None."""
+    a = _bits8(A).reshape(M, K)
+    w = _bits8(W).reshape(N, K)
+    if rows is None:
+        r, nrows = None, M
+    else:
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = r.size
+    C = np.empty((nrows, N), dtype=np.float64)
+    D = np.empty((nrows, N), dtype=np.float64)
+    rc = _load().oracle_linear8_rows(_ptr(a), _ptr(w), fmt_a, fmt_b, M, N, K, K, K,
+                                     None if r is None else _ptr(r), nrows, _ptr(C), _ptr(D))
+    if rc != 0:
+        raise ValueError("oracle_linear8_rows: bad arguments")
+    C = C * scale
+    D = D * abs(scale)
     if bias is not None:
         b = decode(FMT_BF16, _bits16(bias).reshape(N))
         C = C + b[None, :]

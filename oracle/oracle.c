@@ -20,8 +20,12 @@
  *                         It also returns D_ij = sum_k |A_ik * B_kj|, the scale
  *                         the error criterion |C - C_ref| <= 1e-5 * D uses.
  *   oracle_decode         value of an IEEE-754 binary16 / bfloat16 bit pattern,
- *                         written from the field definitions (sign, biased
- *                         exponent, fraction; subnormals; inf/nan).
+ *                         or of the 8-bit floats E5M2 / E4M3 (the FP8 formats
+ *                         of the cuTile article's FP8 benchmark), written from
+ *                         the field definitions (sign, biased exponent,
+ *                         fraction; subnormals; inf/nan).
+ *   oracle_linear8_rows   C_ij = sum_k A_ik W_jk for 8-bit float operands, W in
+ *                         the weight layout [N][K], binary64, k ascending.
  *   oracle_encode_rne     round a binary64 value to the nearest binary16 /
  *                         bfloat16, ties to even (the rounding rule the same
  *                         article's "背景" section applies to 2048 + 1 in FP16).
@@ -53,10 +57,16 @@
 
 #define ORACLE_FMT_FP16 0
 #define ORACLE_FMT_BF16 1
+#define ORACLE_FMT_E5M2 2   /* 8-bit float, IEEE-style: 5 exponent, 2 fraction bits */
+#define ORACLE_FMT_E4M3 3   /* 8-bit float, 4 exponent, 3 fraction bits, no infinity:
+                               the all-ones exponent is an ordinary binade except
+                               fraction 111, the only NaN (the "FN" variant) */
 
 static void fmt_fields(int fmt, int *ebits, int *fbits) {
-    if (fmt == ORACLE_FMT_FP16) { *ebits = 5; *fbits = 10; }
-    else                        { *ebits = 8; *fbits = 7; }
+    if (fmt == ORACLE_FMT_FP16)      { *ebits = 5; *fbits = 10; }
+    else if (fmt == ORACLE_FMT_E5M2) { *ebits = 5; *fbits = 2; }
+    else if (fmt == ORACLE_FMT_E4M3) { *ebits = 4; *fbits = 3; }
+    else                             { *ebits = 8; *fbits = 7; }
 }
 
 /* Decode one bit pattern of the given format to its exact binary64 value. */
@@ -71,7 +81,10 @@ double oracle_decode(int fmt, uint32_t bits) {
     const int bias = (1 << (ebits - 1)) - 1;
     const uint32_t emax_field = (1u << ebits) - 1u;
     double mag;
-    if (e == emax_field) {
+    if (fmt == ORACLE_FMT_E4M3 && e == emax_field) {
+        /* no infinity: 1.f * 2^(15 - 7), except the single NaN pattern */
+        mag = (f == 7u) ? NAN : ldexp((double)((1u << fbits) | f), (int)e - bias - fbits);
+    } else if (e == emax_field) {
         mag = (f == 0) ? INFINITY : NAN;
     } else if (e == 0) {
         /* subnormal: 0.f * 2^(1 - bias) */
@@ -213,6 +226,49 @@ int oracle_splitk_reduce_f32(const float *W, int64_t S, int64_t count, float *ou
         float acc = W[e];
         for (int64_t s = 1; s < S; ++s) acc = acc + W[s * count + e];
         out[e] = acc;
+    }
+    return 0;
+}
+
+/*
+ * A linear layer with 8-bit float operands: C_ij = sum_{k} A_ik * W_jk, in
+ * binary64 with k ascending (each 8-bit x 8-bit product is exact), and the
+ * scale D_ij = sum_k |A_ik * W_jk|.  A: [M][lda] bytes of format fmt_a, W:
+ * [N][ldw] bytes (the weight layout, row j = output column j) of format fmt_b.
+ * rows / nrows / C / D as in oracle_gemm_rows.  Returns 0 or -1.
+ */
+int oracle_linear8_rows(const uint8_t *A, const uint8_t *W, int fmt_a, int fmt_b,
+                        int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldw,
+                        const int64_t *rows, int64_t nrows, double *C, double *D) {
+    if (M < 0 || N < 0 || K < 0 || nrows < 0) return -1;
+    if (nrows > 0 && N > 0 && (C == NULL || D == NULL)) return -1;
+    if (K > 0 && (lda < K || ldw < K)) return -1;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t i = rows ? rows[r] : r;
+        if (i < 0 || i >= M) return -1;
+    }
+    double va[256], vb[256];
+    for (uint32_t h = 0; h < 256u; ++h) {
+        va[h] = oracle_decode(fmt_a, h);
+        vb[h] = oracle_decode(fmt_b, h);
+    }
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t i = rows ? rows[r] : r;
+        const uint8_t *arow = A + i * lda;
+        for (int64_t j = 0; j < N; ++j) {
+            const uint8_t *wrow = W + j * ldw;
+            double c = 0.0, d = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double p = va[arow[k]] * vb[wrow[k]];   /* exact */
+                c = c + p;
+                d = d + fabs(p);
+            }
+            C[r * N + j] = c;
+            D[r * N + j] = d;
+        }
     }
     return 0;
 }

@@ -363,3 +363,60 @@ def test_linear_brute_force_rational(seed):
             scale = sum((abs(t) for t in terms), Fraction(0)) + abs(Fraction(float(bb[j])))
             assert abs(Fraction(C[i, j]) - exact) <= (K + 1) * u * scale
             assert abs(Fraction(D[i, j]) - scale) <= (K + 1) * u * scale
+
+
+# --------------------------------------------------------------------------
+# 8-bit floats and the 8-bit linear layer
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt,tdtype", [(oracle.FMT_E4M3, torch.float8_e4m3fn),
+                                        (oracle.FMT_E5M2, torch.float8_e5m2)])
+def test_fp8_decode_exhaustive_against_torch(fmt, tdtype):
+    pats = np.arange(256, dtype=np.uint8)
+    ours = oracle.decode8(fmt, pats)
+    ref = torch.from_numpy(pats.copy()).view(tdtype).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))
+    if fmt == oracle.FMT_E4M3:
+        assert np.nanmax(ours) == 448.0 and nan.sum() == 2          # no infinity
+    else:
+        assert np.isinf(ours).sum() == 2 and np.nanmax(ours[~np.isinf(ours)]) == 57344.0
+
+
+def _fp8(t: torch.Tensor, fmt):
+    return t.to(torch.float8_e4m3fn if fmt == oracle.FMT_E4M3 else torch.float8_e5m2)
+
+
+@pytest.mark.parametrize("fa,fb", [(oracle.FMT_E4M3, oracle.FMT_E4M3),
+                                   (oracle.FMT_E5M2, oracle.FMT_E4M3)])
+def test_linear8_small_integers_exact(fa, fb):
+    M, N, K = 6, 9, 300
+    g = torch.Generator().manual_seed(1)
+    ai = torch.randint(-8, 9, (M, K), generator=g)
+    wi = torch.randint(-8, 9, (N, K), generator=g)
+    A, W = _fp8(ai.float(), fa), _fp8(wi.float(), fb)      # |v| <= 8 is exact in both formats
+    C, D = oracle.linear8_rows(A, W, fa, fb, M, N, K)
+    assert np.array_equal(C, (ai.numpy() @ wi.numpy().T).astype(np.float64))
+    assert np.array_equal(D, (np.abs(ai.numpy()) @ np.abs(wi.numpy()).T).astype(np.float64))
+
+
+def test_linear8_scale_bias_and_rational_brute_force():
+    M, N, K = 3, 4, 5
+    g = torch.Generator().manual_seed(2)
+    A = _fp8(torch.randn(M, K, generator=g) * 3, oracle.FMT_E4M3)
+    W = _fp8(torch.randn(N, K, generator=g), oracle.FMT_E5M2)
+    b = workloads.normal_bf16((N,), 3)
+    scale = 0.375
+    C, D = oracle.linear8_rows(A, W, oracle.FMT_E4M3, oracle.FMT_E5M2, M, N, K, scale, b)
+    a = A.to(torch.float64).numpy()
+    w = W.to(torch.float64).numpy()
+    bb = b.to(torch.float64).numpy()
+    u = Fraction(2.0 ** -53)
+    for i in range(M):
+        for j in range(N):
+            terms = [Fraction(float(a[i, k])) * Fraction(float(w[j, k])) for k in range(K)]
+            exact = Fraction(scale) * sum(terms, Fraction(0)) + Fraction(float(bb[j]))
+            scl = Fraction(scale) * sum((abs(t) for t in terms), Fraction(0)) + abs(Fraction(float(bb[j])))
+            assert abs(Fraction(C[i, j]) - exact) <= (K + 2) * u * scl
