@@ -561,6 +561,33 @@ def run_other_workloads(dev, peaks) -> dict:
             out[name]["hbm_frac"] = round(alg / (secs / iters) / 1e9 / peaks["hbm_gbs"], 4)
         del AB, C, ws
         torch.cuda.empty_cache()
+    # linear layers, weights [N, K]: BF16 and 8-bit floats (E4M3).  The FP8
+    # peak is the measured BF16 peak times the nominal FP8 / BF16 ratio (2).
+    fp8_peak = 2.0 * bf16_peak
+    for name, n, fp8 in (("linear_bf16_8192", 8192, False), ("linear_fp8_e4m3_8192", 8192, True),
+                         ("linear_fp8_e4m3_16384", 16384, True)):
+        g = workloads.generator(99)
+        x = torch.randn(n, n, generator=g)
+        w = torch.randn(n, n, generator=g)
+        if fp8:
+            x, w = x.to(torch.float8_e4m3fn).to(dev), w.to(torch.float8_e4m3fn).to(dev)
+        else:
+            x, w = x.to(torch.bfloat16).to(dev), w.to(torch.bfloat16).to(dev)
+        C = torch.empty((n, n), dtype=torch.bfloat16, device=dev)
+        call = (lambda i: dig.linear_fp8(x, w, 1.0, out_dtype=torch.bfloat16, out=C)) if fp8 else \
+            (lambda i: dig.linear(x, w, out_dtype=torch.bfloat16, out=C))
+        for i in range(3):
+            call(i)
+        iters = 10 if n <= 8192 else 4
+        secs = time_region(call, iters, 1)
+        tflops = 2.0 * n ** 3 * iters / secs / 1e12
+        peak = fp8_peak if fp8 else bf16_peak
+        out[name] = {"tflops": round(tflops, 2), "frac_of_peak": round(tflops / peak, 4),
+                     "peak": peak, "peak_note": "measured bf16 x 2 (nominal fp8/bf16 ratio)"
+                     if fp8 else "measured bf16", "ms": round(secs * 1e3 / iters, 4),
+                     "out": "bf16", "inputs": "fp8 e4m3" if fp8 else "bf16"}
+        del x, w, C
+        torch.cuda.empty_cache()
     return out
 
 

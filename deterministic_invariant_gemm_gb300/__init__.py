@@ -34,8 +34,9 @@ __all__ = [
     "bigemm_workspace_bytes", "bigemm_partial_workspace_bytes", "bigemm_run",
     "bigemm_run_bf16out", "bigemm_run_partial", "bigemm_splitk_reduce",
     "bigemm_run_atomic_splitk", "bigemm_device_status", "bigemm_last_launch_count",
-    "bigemm_run_splitk_static", "bigemm_linear", "STATIC_SCRATCH_BYTES", "matmul", "linear",
-    "EXPORTED_SYMBOLS",
+    "bigemm_run_splitk_static", "bigemm_linear", "bigemm_fp8_effective_split_k",
+    "bigemm_fp8_workspace_bytes", "bigemm_linear_fp8", "FP8_E4M3", "FP8_E5M2",
+    "STATIC_SCRATCH_BYTES", "matmul", "linear", "linear_fp8", "EXPORTED_SYMBOLS",
 ]
 
 BLOCK_K = 64
@@ -56,7 +57,11 @@ EXPORTED_SYMBOLS = (
     "bigemm_partial_workspace_bytes", "bigemm_run", "bigemm_run_bf16out", "bigemm_run_partial",
     "bigemm_splitk_reduce", "bigemm_run_atomic_splitk", "bigemm_device_status",
     "bigemm_last_launch_count", "bigemm_run_splitk_static", "bigemm_linear",
+    "bigemm_fp8_effective_split_k", "bigemm_fp8_workspace_bytes", "bigemm_linear_fp8",
 )
+
+FP8_E4M3 = 0
+FP8_E5M2 = 1
 
 
 class BigemmError(RuntimeError):
@@ -100,6 +105,10 @@ def load():
         "bigemm_device_status": ([i32], i32),
         "bigemm_run_splitk_static": ([vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, vp], i32),
         "bigemm_linear": ([vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, i32, vp, sz, vp], i32),
+        "bigemm_fp8_effective_split_k": ([i64, i32], i32),
+        "bigemm_fp8_workspace_bytes": ([i64, i64, i64, i32], sz),
+        "bigemm_linear_fp8": ([vp, vp, i32, i32, ctypes.c_float, vp, vp, i64, i64, i64, i64, i64,
+                               i64, i32, i32, vp, sz, vp], i32),
         "bigemm_last_launch_count": ([], i32),
     }
     for name, (args, res) in sig.items():
@@ -190,6 +199,24 @@ def bigemm_linear(A, W, bias, C, M, N, K, lda, ldw, ldc, split_k, c_is_bf16, wor
                               _stream(stream))
     if check:
         _check(st, "bigemm_linear")
+    return st
+
+
+def bigemm_fp8_effective_split_k(K: int, split_k: int) -> int:
+    return int(load().bigemm_fp8_effective_split_k(K, split_k))
+
+
+def bigemm_fp8_workspace_bytes(M: int, N: int, K: int, split_k: int) -> int:
+    return int(load().bigemm_fp8_workspace_bytes(M, N, K, split_k))
+
+
+def bigemm_linear_fp8(A, W, fmt_a, fmt_w, scale, bias, C, M, N, K, lda, ldw, ldc, split_k,
+                      c_is_bf16, workspace=None, workspace_bytes=0, stream=None, check=True) -> int:
+    st = load().bigemm_linear_fp8(_ptr(A), _ptr(W), fmt_a, fmt_w, float(scale), _ptr(bias), _ptr(C),
+                                  M, N, K, lda, ldw, ldc, split_k, int(bool(c_is_bf16)),
+                                  _ptr(workspace), workspace_bytes, _stream(stream))
+    if check:
+        _check(st, "bigemm_linear_fp8")
     return st
 
 
@@ -334,4 +361,41 @@ def linear(x, weight, bias=None, out_dtype=None, split_k: int = 1, out=None, wor
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     bigemm_linear(x, weight, bias, out, M, N, K, lda, ldw, ldc, split_k, bf16, workspace, wbytes,
                   stream)
+    return out
+
+
+def linear_fp8(x, weight, scale=1.0, bias=None, out_dtype=None, split_k: int = 1, out=None,
+               workspace=None, stream=None):
+    """y = scale * (x @ weight.T) + bias for 8-bit float CUDA tensors x [M, K] and
+    weight [N, K] (torch.float8_e4m3fn or torch.float8_e5m2, each), through
+    bigemm_linear_fp8.  bias: bf16 [N] or None; output float32 (default) or
+    bfloat16."""
+    import torch
+    fmts = {torch.float8_e4m3fn: FP8_E4M3, torch.float8_e5m2: FP8_E5M2}
+    if x.dtype not in fmts or weight.dtype not in fmts:
+        raise TypeError("x and weight must be float8_e4m3fn or float8_e5m2")
+    if bias is not None and (bias.dtype != torch.bfloat16 or bias.dim() != 1 or bias.stride(0) != 1):
+        raise TypeError("bias must be a contiguous bfloat16 vector")
+    if x.dim() != 2 or weight.dim() != 2 or x.shape[1] != weight.shape[1]:
+        raise ValueError("shapes do not compose: %s x %s^T" % (tuple(x.shape), tuple(weight.shape)))
+    if x.stride(1) != 1 or weight.stride(1) != 1:
+        raise ValueError("x and weight need unit column stride (row-major)")
+    out_dtype = torch.float32 if out_dtype is None else out_dtype
+    M, K = x.shape
+    N = weight.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    lda = x.stride(0) if M > 1 else max(K, 16 * ((K + 15) // 16))
+    ldw = weight.stride(0) if N > 1 else max(K, 16 * ((K + 15) // 16))
+    ldc = out.stride(0) if M > 1 else max(N, 8 * ((N + 7) // 8))
+    bf16 = out_dtype == torch.bfloat16
+    if lda % 16 or ldw % 16 or ldc % (8 if bf16 else 4):
+        raise ValueError("row strides must be multiples of 16 bytes for x and weight and of %d "
+                         "elements for the output; got %d, %d, %d" % (8 if bf16 else 4, lda, ldw, ldc))
+    need = bigemm_fp8_workspace_bytes(M, N, K, split_k)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    bigemm_linear_fp8(x, weight, fmts[x.dtype], fmts[weight.dtype], scale, bias, out, M, N, K, lda,
+                      ldw, ldc, split_k, bf16, workspace, wbytes, stream)
     return out

@@ -79,13 +79,16 @@ bigemm_status device_info(const DeviceInfo** out) {
                 return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
                        cudaSuccess;
             };
-            if (!opt_in((const void*)bigemm_tc_kernel<kOutF32, false>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutBF16, false>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutSlices, false>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutAtomic, false>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutF32, true>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutBF16, true>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutSlices, true>))
+            if (!opt_in((const void*)bigemm_tc_kernel<kOutF32, false, false>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutBF16, false, false>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutSlices, false, false>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutAtomic, false, false>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutF32, true, false>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutBF16, true, false>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutSlices, true, false>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutF32, true, true>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutBF16, true, true>) ||
+                !opt_in((const void*)bigemm_tc_kernel<kOutSlices, true, true>))
                 return BIGEMM_ERR_CUDA;
             void* sym = nullptr;
             if (cudaGetSymbolAddress(&sym, g_device_status) != cudaSuccess) return BIGEMM_ERR_CUDA;
@@ -102,9 +105,11 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int max_split(int64_t K) {
+// kb_elems: elements per K block -- 64 for BF16, 128 for 8-bit floats (both
+// 128 bytes per row).
+int max_split(int64_t K, int kb_elems = kBK) {
     if (K <= 0) return 1;
-    const int64_t kb = ceil_div(K, kBK);
+    const int64_t kb = ceil_div(K, kb_elems);
     return kb > INT_MAX ? INT_MAX : static_cast<int>(kb);
 }
 
@@ -117,15 +122,15 @@ int default_split(int64_t K) {
 }
 
 // Effective split and blocks per segment; 0 when split_k is invalid.
-int effective_split(int64_t K, int split_k, int* blocks_per_split) {
+int effective_split(int64_t K, int split_k, int* blocks_per_split, int kb_elems = kBK) {
     if (K < 0) return 0;
     if (split_k == 0) split_k = default_split(K);
-    if (split_k < 1 || split_k > max_split(K)) return 0;
+    if (split_k < 1 || split_k > max_split(K, kb_elems)) return 0;
     if (K == 0) {
         if (blocks_per_split) *blocks_per_split = 0;
         return 1;
     }
-    const int64_t kb = ceil_div(K, kBK);
+    const int64_t kb = ceil_div(K, kb_elems);
     const int64_t L = ceil_div(kb, split_k);
     if (blocks_per_split) *blocks_per_split = static_cast<int>(L);
     return static_cast<int>(ceil_div(kb, L));
@@ -204,20 +209,20 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t esize, c
 // operand again in 256 x 256 boxes without swizzle, used only to warm L2.
 bool encode_operands(CUtensorMap* tmA, CUtensorMap* tmB, CUtensorMap* tmBp, const void* A,
                      const void* B, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
-                     bool wt) {
+                     bool wt, bool fp8) {
+    // 8-bit operands: a K block of 128 elements is still 128 bytes per row
+    const uint32_t kb = fp8 ? 128u : static_cast<uint32_t>(kBK);
+    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint32_t es = fp8 ? 1u : 2u;
     const int64_t da[2] = {K, M};
     const int64_t db[2] = {wt ? K : N, wt ? N : K};
-    const uint32_t ba[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(kBM)};
-    const uint32_t bb[2] = {wt ? static_cast<uint32_t>(kBK) : kBChunkCols,
-                            wt ? static_cast<uint32_t>(kBN) : static_cast<uint32_t>(kBK)};
+    const uint32_t ba[2] = {kb, static_cast<uint32_t>(kBM)};
+    const uint32_t bb[2] = {wt ? kb : kBChunkCols, wt ? static_cast<uint32_t>(kBN) : kb};
     const uint32_t bp[2] = {wt ? static_cast<uint32_t>(kPrefetchRows) : static_cast<uint32_t>(kBN),
                             wt ? static_cast<uint32_t>(kBN) : static_cast<uint32_t>(kPrefetchRows)};
-    return encode_tiled(tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, 2, da, lda, 0, ba,
-                        CU_TENSOR_MAP_SWIZZLE_128B) &&
-           encode_tiled(tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, 2, db, ldb, 0, bb,
-                        CU_TENSOR_MAP_SWIZZLE_128B) &&
-           encode_tiled(tmBp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, 2, db, ldb, 0, bp,
-                        CU_TENSOR_MAP_SWIZZLE_NONE);
+    return encode_tiled(tmA, dt, es, A, 2, da, lda, 0, ba, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           encode_tiled(tmB, dt, es, B, 2, db, ldb, 0, bb, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           encode_tiled(tmBp, dt, es, B, 2, db, ldb, 0, bp, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // Output maps for the epilogue's 32 x 32 TMA stores: fp32 C (128-byte
@@ -262,19 +267,24 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaSt
 }
 
 template <int kOut>
-cudaError_t launch_gemm(bool wt, dim3 g, dim3 blk, cudaStream_t stream, const CUtensorMap& tmA,
-                        const CUtensorMap& tmB, const CUtensorMap& tmBp, const CUtensorMap& tmC,
-                        const GemmParams& p) {
+cudaError_t launch_gemm(bool wt, bool fp8, dim3 g, dim3 blk, cudaStream_t stream,
+                        const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBp,
+                        const CUtensorMap& tmC, const GemmParams& p) {
     if constexpr (kOut == kOutAtomic) {
-        if (wt) return cudaErrorInvalidValue;  // the contrast exists for B [K, N] only
-        return launch_pdl(bigemm_tc_kernel<kOut, false>, g, blk, kSmemBytes, stream, tmA, tmB, tmBp,
-                          tmC, p);
+        if (wt || fp8) return cudaErrorInvalidValue;  // the contrast exists for bf16 B [K, N] only
+        return launch_pdl(bigemm_tc_kernel<kOut, false, false>, g, blk, kSmemBytes, stream, tmA, tmB,
+                          tmBp, tmC, p);
     } else {
+        if (fp8) {
+            if (!wt) return cudaErrorInvalidValue;
+            return launch_pdl(bigemm_tc_kernel<kOut, true, true>, g, blk, kSmemBytes, stream, tmA, tmB,
+                              tmBp, tmC, p);
+        }
         if (wt)
-            return launch_pdl(bigemm_tc_kernel<kOut, true>, g, blk, kSmemBytes, stream, tmA, tmB, tmBp,
-                              tmC, p);
-        return launch_pdl(bigemm_tc_kernel<kOut, false>, g, blk, kSmemBytes, stream, tmA, tmB, tmBp,
-                          tmC, p);
+            return launch_pdl(bigemm_tc_kernel<kOut, true, false>, g, blk, kSmemBytes, stream, tmA, tmB,
+                              tmBp, tmC, p);
+        return launch_pdl(bigemm_tc_kernel<kOut, false, false>, g, blk, kSmemBytes, stream, tmA, tmB,
+                          tmBp, tmC, p);
     }
 }
 
@@ -282,7 +292,7 @@ enum Mode { kModeF32, kModeBF16, kModePartial, kModeAtomic };
 
 bigemm_status launch_reduce(const DeviceInfo& d, const float* ws, int splits, int64_t M, int64_t N,
                             void* C, int64_t ldc, bool bf16, cudaStream_t stream,
-                            const void* bias = nullptr) {
+                            const void* bias = nullptr, float scale = 1.0f) {
     const __nv_bfloat16* b = static_cast<const __nv_bfloat16*>(bias);
     const int64_t ws_ld = ws_ld_of(N);
     const int64_t items = M * (ws_ld / 4);
@@ -295,11 +305,11 @@ bigemm_status launch_reduce(const DeviceInfo& d, const float* ws, int splits, in
     if (bf16)
         e = launch_pdl(splitk_reduce_kernel<true>, dim3(static_cast<unsigned>(blocks)),
                        dim3(kReduceThreads), 0, stream, ws, C, static_cast<int>(M), static_cast<int>(N),
-                       ldc, ws_ld, splits, b);
+                       ldc, ws_ld, splits, b, scale);
     else
         e = launch_pdl(splitk_reduce_kernel<false>, dim3(static_cast<unsigned>(blocks)),
                        dim3(kReduceThreads), 0, stream, ws, C, static_cast<int>(M), static_cast<int>(N),
-                       ldc, ws_ld, splits, b);
+                       ldc, ws_ld, splits, b, scale);
     return e == cudaSuccess ? BIGEMM_OK : BIGEMM_ERR_CUDA;
 }
 
@@ -309,20 +319,25 @@ bigemm_status launch_reduce(const DeviceInfo& d, const float* ws, int splits, in
 bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t M, int64_t N,
                        int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int split_k, void* ws,
                        size_t ws_bytes, cudaStream_t stream, bool wt = false,
-                       const void* bias = nullptr) {
+                       const void* bias = nullptr, int fp8_fmt_a = -1, int fp8_fmt_b = -1,
+                       float scale = 1.0f) {
+    // fp8_fmt_a / fp8_fmt_b >= 0: 8-bit float operands (0 = E4M3, 1 = E5M2), W layout
+    const bool fp8 = fp8_fmt_a >= 0;
+    const int kb_elems = fp8 ? 128 : kBK;
+    const int ld_align = fp8 ? 16 : 8;  // elements per 16 bytes
     g_last_launches = 0;
     // ---- sizes and the split
     if (M < 0 || N < 0 || K < 0) return BIGEMM_ERR_ARG;
     if (M > INT_MAX || N > INT_MAX || K > INT_MAX) return BIGEMM_ERR_ARG;
     int kb_per_split = 0;
-    const int splits = effective_split(K, split_k, &kb_per_split);
+    const int splits = effective_split(K, split_k, &kb_per_split, kb_elems);
     if (splits == 0) return BIGEMM_ERR_ARG;
     const bool want_c = (mode != kModePartial);
     // ---- pointers and strides (checked even for empty products)
     if (K > 0 && (A == nullptr || B == nullptr)) return BIGEMM_ERR_ARG;
     if (K > 0 && (lda < K || ldb < (wt ? K : N))) return BIGEMM_ERR_ARG;
     if (want_c && (C == nullptr || ldc < N)) return BIGEMM_ERR_ARG;
-    if (K > 0 && (!aligned16(A) || !aligned16(B) || lda % 8 != 0 || ldb % 8 != 0))
+    if (K > 0 && (!aligned16(A) || !aligned16(B) || lda % ld_align != 0 || ldb % ld_align != 0))
         return BIGEMM_ERR_ALIGN;
     if (want_c) {
         if (!aligned16(C)) return BIGEMM_ERR_ALIGN;
@@ -349,7 +364,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
 
     // ---- K == 0: the empty sum is +0.0 everywhere (plus the bias, if any)
     if (K == 0 && bias != nullptr) {
-        st = launch_reduce(*d, nullptr, 0, M, N, C, ldc, mode == kModeBF16, stream, bias);
+        st = launch_reduce(*d, nullptr, 0, M, N, C, ldc, mode == kModeBF16, stream, bias, scale);
         if (st == BIGEMM_OK) g_last_launches = 1;
         return st;
     }
@@ -367,7 +382,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
 
     CUtensorMap tmA, tmB, tmBp, tmC;
     std::memset(&tmC, 0, sizeof(tmC));
-    if (!encode_operands(&tmA, &tmB, &tmBp, A, B, M, N, K, lda, ldb, wt)) return BIGEMM_ERR_CUDA;
+    if (!encode_operands(&tmA, &tmB, &tmBp, A, B, M, N, K, lda, ldb, wt, fp8)) return BIGEMM_ERR_CUDA;
 
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
@@ -377,18 +392,22 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     p.m_tiles = static_cast<int>(m_tiles);
     p.n_tiles = static_cast<int>(n_tiles);
     p.splits = splits;
-    p.kb_total = static_cast<int>(ceil_div(K, kBK));
+    p.kb_total = static_cast<int>(ceil_div(K, kb_elems));
     p.kb_per_split = kb_per_split;
     p.units = static_cast<int>(units);
     p.epi_boxes = epi_boxes_for(static_cast<int>(M));
     p.epi_batch = epi_batch_for(static_cast<int>(M));
     p.grouped = 0;
-    p.prefetch_rows = kStages * kBK;  // what the ring holds: the first four K blocks
+    p.prefetch_rows = kStages * kb_elems;  // what the ring holds: the first four K blocks
     // GROUP_M swizzle: 16 tile rows per group once there are four or more waves
     // of tiles (the concurrent tiles then span about 16 x 9 tiles, whose A and
     // B panels stay in L2), else 8.  It orders tiles only; no sum changes.
     p.group_m = (m_tiles * n_tiles >= 4 * static_cast<int64_t>(d->sm_count)) ? 16 : 8;
     p.bias = (splits == 1) ? static_cast<const __nv_bfloat16*>(bias) : nullptr;
+    p.scale = (splits == 1) ? scale : 1.0f;
+    p.idesc_fp8 = fp8 ? idesc_fp8_f32(kBM, kBN, static_cast<uint32_t>(fp8_fmt_a),
+                                      static_cast<uint32_t>(fp8_fmt_b))
+                      : 0u;
 
     const int grid = static_cast<int>(units < d->sm_count ? units : d->sm_count);
     const dim3 g(static_cast<unsigned>(grid)), blk(kNumThreads);
@@ -401,7 +420,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
         if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
         p.out = C;
         p.ld_out = ldc;
-        e = launch_gemm<kOutAtomic>(wt, g, blk, stream, tmA, tmB, tmBp, tmC, p);
+        e = launch_gemm<kOutAtomic>(wt, fp8, g, blk, stream, tmA, tmB, tmBp, tmC, p);
         launches = 1;
     } else if (mode == kModePartial || splits > 1) {
         p.out = ws;
@@ -412,11 +431,11 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
             p.grouped = 1;
         else if (!encode_out_slices(&tmC, ws, M, N, splits))
             return BIGEMM_ERR_CUDA;
-        e = launch_gemm<kOutSlices>(wt, g, blk, stream, tmA, tmB, tmBp, tmC, p);
+        e = launch_gemm<kOutSlices>(wt, fp8, g, blk, stream, tmA, tmB, tmBp, tmC, p);
         launches = 1;
         if (e == cudaSuccess && mode != kModePartial) {
             st = launch_reduce(*d, static_cast<const float*>(ws), splits, M, N, C, ldc,
-                               mode == kModeBF16, stream, bias);
+                               mode == kModeBF16, stream, bias, scale);
             if (st != BIGEMM_OK) return st;
             launches = 2;
         }
@@ -429,14 +448,14 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
                 p.grouped = 1;
             else if (!encode_out_bf16(&tmC, C, M, N, ldc))
                 return BIGEMM_ERR_CUDA;
-            e = launch_gemm<kOutBF16>(wt, g, blk, stream, tmA, tmB, tmBp, tmC, p);
+            e = launch_gemm<kOutBF16>(wt, fp8, g, blk, stream, tmA, tmB, tmBp, tmC, p);
         } else {
             if (encode_out_grouped(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, M, N, ldc, 0, 0,
                                    p.epi_batch))
                 p.grouped = 1;
             else if (!encode_out_f32(&tmC, C, M, N, ldc))
                 return BIGEMM_ERR_CUDA;
-            e = launch_gemm<kOutF32>(wt, g, blk, stream, tmA, tmB, tmBp, tmC, p);
+            e = launch_gemm<kOutF32>(wt, fp8, g, blk, stream, tmA, tmB, tmBp, tmC, p);
         }
         launches = 1;
     }
@@ -568,6 +587,30 @@ bigemm_status bigemm_linear(const void* A, const void* W, const void* bias, void
                             bigemm_stream stream) {
     return run_impl(c_is_bf16 ? kModeBF16 : kModeF32, A, W, C, M, N, K, lda, ldw, ldc, split_k,
                     workspace, workspace_bytes, static_cast<cudaStream_t>(stream), /*wt=*/true, bias);
+}
+
+int bigemm_fp8_effective_split_k(int64_t K, int split_k) {
+    return effective_split(K, split_k, nullptr, 128);
+}
+
+size_t bigemm_fp8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {
+    if (M < 0 || N < 0) return 0;
+    const int s = effective_split(K, split_k, nullptr, 128);
+    if (s <= 1) return 0;
+    return slice_bytes(M, N, s);
+}
+
+bigemm_status bigemm_linear_fp8(const void* A, const void* W, int fmt_a, int fmt_w, float scale,
+                                const void* bias, void* C, int64_t M, int64_t N, int64_t K,
+                                int64_t lda, int64_t ldw, int64_t ldc, int split_k, int c_is_bf16,
+                                void* workspace, size_t workspace_bytes, bigemm_stream stream) {
+    g_last_launches = 0;
+    if ((fmt_a != BIGEMM_FP8_E4M3 && fmt_a != BIGEMM_FP8_E5M2) ||
+        (fmt_w != BIGEMM_FP8_E4M3 && fmt_w != BIGEMM_FP8_E5M2) || !(scale == scale))
+        return BIGEMM_ERR_ARG;
+    return run_impl(c_is_bf16 ? kModeBF16 : kModeF32, A, W, C, M, N, K, lda, ldw, ldc, split_k,
+                    workspace, workspace_bytes, static_cast<cudaStream_t>(stream), /*wt=*/true, bias,
+                    fmt_a, fmt_w, scale);
 }
 
 bigemm_status bigemm_run_atomic_splitk(const void* A, const void* B, float* C, int64_t M, int64_t N,

@@ -119,6 +119,8 @@ struct GemmParams {
     int group_m;            // tile rows per GROUP_M swizzle group
     const __nv_bfloat16* bias;  // [N] added to every row by the direct (unsplit)
                                 // epilogue, or nullptr
+    float scale;            // the direct epilogue multiplies the sum by this (1: none)
+    uint32_t idesc_fp8;     // instruction descriptor of the 8-bit float product
 };
 
 // Unit u -> (tile row, tile column, K segment).  All tiles of segment 0 come
@@ -247,11 +249,16 @@ __device__ __forceinline__ void atomic_add_row_chunk(const GemmParams& p, int ro
 
 // kWt: the second operand is the weight matrix W [N, K] (K-major); otherwise
 // B [K, N] (N-major).  Both products run the same K = 16 instruction sequence.
-template <int kOut, bool kWt>
+// kFp8: 8-bit float operands (both K-major, kWt): a K block is 128 elements,
+// still 128 bytes per row, consumed by four tcgen05.mma.kind::f8f6f4 of K = 32;
+// the shared-memory layout and descriptors are byte for byte those of BF16.
+template <int kOut, bool kWt, bool kFp8>
 __global__ void __launch_bounds__(kNumThreads, 1)
     bigemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmBp, const __grid_constant__ CUtensorMap tmC,
                      const GemmParams p) {
+    static_assert(!kFp8 || kWt, "8-bit operands are read K-major only");
+    constexpr int kKB = kFp8 ? 128 : kBK;  // elements per K block (128 bytes per row)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 128-byte-swizzled tiles must start on 1024-byte boundaries; the layout
     // below assumes the base is.  Should it not be, stop before touching
@@ -302,8 +309,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (static_cast<int>(blockIdx.x) < p.units) {
             int mt, nt, seg;
             unit_coords(p, blockIdx.x, mt, nt, seg);
-            const int k0 = seg * p.kb_per_split * kBK;
-            const int k1 = min(k0 + p.prefetch_rows, min(k0 + p.kb_per_split * kBK, p.kb_total * kBK));
+            const int k0 = seg * p.kb_per_split * kKB;
+            const int k1 = min(k0 + p.prefetch_rows, min(k0 + p.kb_per_split * kKB, p.kb_total * kKB));
             for (int k = k0; k < k1; k += kPrefetchRows) {
                 if constexpr (kWt) tma_prefetch_l2_2d(&tmBp, k, nt * kBN);
                 else tma_prefetch_l2_2d(&tmBp, nt * kBN, k);
@@ -347,10 +354,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                     const uint32_t fb = full_bar(stage);
                     mbar_arrive_expect_tx(fb, kStageBytes);
-                    tma_load_2d(sA + stage * kABytes, &tmA, fb, kb * kBK, m0);
+                    tma_load_2d(sA + stage * kABytes, &tmA, fb, kb * kKB, m0);
                     if constexpr (kWt) {
                         // one box: 256 weight rows x 64 k (128 bytes each)
-                        tma_load_2d(sB + stage * kBBytes, &tmB, fb, kb * kBK, n0);
+                        tma_load_2d(sB + stage * kBBytes, &tmB, fb, kb * kKB, n0);
                     } else {
 #pragma unroll
                         for (int c = 0; c < kBN / static_cast<int>(kBChunkCols); ++c)
@@ -421,8 +428,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             // LBO = distance between 64-column chunks, SBO = 8 k-rows.
                             bd = smem_desc_sw128(b0 + kk * kUmmaK * 128, kBChunkBytes, 1024);
                         }
-                        mma_bf16(d_tmem, ad, bd, kWt ? kIdescWt : kIdescBN,
-                                 (kb > kb0 || kk > 0) ? 1u : 0u);
+                        if constexpr (kFp8)
+                            mma_fp8(d_tmem, ad, bd, p.idesc_fp8, (kb > kb0 || kk > 0) ? 1u : 0u);
+                        else
+                            mma_bf16(d_tmem, ad, bd, kWt ? kIdescWt : kIdescBN,
+                                     (kb > kb0 || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(empty_bar(stage));
                     if (++stage == kStages) {
@@ -491,6 +501,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         released = true;
                     }
                     if constexpr (kOut == kOutF32 || kOut == kOutBF16) {
+                        if (p.scale != 1.0f) {  // uniform: one FP32 multiply per element
+#pragma unroll
+                            for (int i = 0; i < kMaxBatch * 32; ++i)
+                                if (i < nb * 32)
+                                    r[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), p.scale));
+                        }
                         if (p.bias != nullptr) {  // uniform
 #pragma unroll
                             for (int i = 0; i < kMaxBatch; ++i)
@@ -576,8 +592,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 }
 
 // Split-K reduction: for every element, acc = w_0, then acc = acc + w_s for
-// s = 1 .. S-1 in that order (FP32, round to nearest even), then acc + bias[n]
-// when a bias is given; starting from w_0
+// s = 1 .. S-1 in that order (FP32, round to nearest even), then acc * scale
+// and acc + bias[n] when given; starting from w_0
 // rather than 0.0f keeps a lone -0.0 partial intact.  One thread handles four
 // adjacent columns of one row (16-byte loads, coalesced along N); the loads of
 // up to eight slices are issued before their additions.
@@ -586,7 +602,8 @@ constexpr int kReduceThreads = 128;
 template <bool kBF16Out>
 __global__ void __launch_bounds__(kReduceThreads)
     splitk_reduce_kernel(const float* __restrict__ ws, void* __restrict__ C, int M, int N,
-                         int64_t ldc, int64_t ws_ld, int S, const __nv_bfloat16* __restrict__ bias) {
+                         int64_t ldc, int64_t ws_ld, int S, const __nv_bfloat16* __restrict__ bias,
+                         float scale) {
     // The next kernel in the stream may be scheduled at once: it waits for
     // this grid to complete before touching memory, and this kernel holds no
     // tensor memory a dependent could need.
@@ -619,6 +636,12 @@ __global__ void __launch_bounds__(kReduceThreads)
         }
         const int valid = min(4, N - col);
         if (valid <= 0) continue;
+        if (scale != 1.0f) {  // an 8-bit product's output scale, after the split sum
+            acc.x = __fmul_rn(acc.x, scale);
+            acc.y = __fmul_rn(acc.y, scale);
+            acc.z = __fmul_rn(acc.z, scale);
+            acc.w = __fmul_rn(acc.w, scale);
+        }
         if (bias != nullptr) {  // a linear layer's bias, added after the split sum
             float* a = &acc.x;
             for (int c = 0; c < valid; ++c) a[c] = __fadd_rn(a[c], __bfloat162float(bias[col + c]));

@@ -184,6 +184,18 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem] with 8-bit float inputs (the formats are in
+// the instruction descriptor), FP32 accumulate; one thread issues.
+__device__ __forceinline__ void mma_fp8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -257,6 +269,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     d |= static_cast<uint64_t>(1) << 46;
     d |= static_cast<uint64_t>(2) << 61;
     return d;
+}
+
+// Instruction descriptor for tcgen05.mma.kind::f8f6f4 with FP32 accumulation:
+// the same fields as below, A / B formats in bits 7-9 / 10-12 with E4M3 = 0 and
+// E5M2 = 1.
+__host__ __device__ constexpr uint32_t idesc_fp8_f32(int m, int n, uint32_t a_fmt, uint32_t b_fmt) {
+    return (1u << 4) | ((a_fmt & 7u) << 7) | ((b_fmt & 7u) << 10) |
+           (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 // Instruction descriptor for tcgen05.mma.kind::f16:

@@ -197,6 +197,42 @@ BIGEMM_API bigemm_status bigemm_linear(const void *A, const void *W, const void 
                                        void *workspace, size_t workspace_bytes,
                                        bigemm_stream stream);
 
+/* 8-bit float formats of bigemm_linear_fp8 (the values of the instruction
+ * descriptor's format fields). */
+#define BIGEMM_FP8_E4M3 0   /* 4 exponent, 3 fraction bits, no infinity ("fn") */
+#define BIGEMM_FP8_E5M2 1   /* 5 exponent, 2 fraction bits, IEEE-style */
+
+/* Number of non-empty K segments of an 8-bit float product: as
+ * bigemm_effective_split_k, but a K block is 128 elements (128 bytes per row,
+ * like 64 BF16 elements).  0 for an invalid split_k. */
+BIGEMM_API int bigemm_fp8_effective_split_k(int64_t K, int split_k);
+
+/* Workspace bytes bigemm_linear_fp8 needs (0 when its effective split is 1). */
+BIGEMM_API size_t bigemm_fp8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
+
+/* Batch-invariant linear layer with 8-bit float operands:
+ *     C_ij = scale * (sum_{k=0}^{K-1} A_ik * W_jk) + bias_j
+ * A: [M, K] bytes in format fmt_a (lda a multiple of 16), W: [N, K] bytes in
+ * format fmt_w (ldw a multiple of 16), BIGEMM_FP8_E4M3 or BIGEMM_FP8_E5M2
+ * (either may be mixed); scale: one FP32 factor, e.g. the product of per-tensor
+ * quantisation scales; bias: bf16 [N] or NULL; C fp32 or bf16 as in
+ * bigemm_linear.  The products are exact and accumulate in FP32 on the tensor
+ * cores (tcgen05.mma.kind::f8f6f4, K = 32 per instruction), K blocks of 128
+ * in ascending order, split-K segments summed in the order 0..S-1; then one
+ * FP32 multiply by scale and one FP32 addition of the bias.  Row i of C is
+ * bit-for-bit a function of (row i of A, W, formats, scale, bias, K, split_k,
+ * output type) -- the pages' batch invariance carried to the FP8 products
+ * they benchmark (cuTile article, "TileGymで行列積ベンチマーク"; Tencent
+ * article, "vLLM における…": FP8 goes to other kernels there).  The workspace
+ * holds bigemm_fp8_effective_split_k slices (bigemm_fp8_workspace_bytes). */
+BIGEMM_API bigemm_status bigemm_linear_fp8(const void *A, const void *W, int fmt_a, int fmt_w,
+                                           float scale, const void *bias, void *C,
+                                           int64_t M, int64_t N, int64_t K,
+                                           int64_t lda, int64_t ldw, int64_t ldc,
+                                           int split_k, int c_is_bf16,
+                                           void *workspace, size_t workspace_bytes,
+                                           bigemm_stream stream);
+
 /* Measured contrast only -- NOT deterministic.  Same arguments as bigemm_run
  * without a workspace: C (fp32) is zeroed on the stream, then every K
  * segment's partial is added into C with atomic adds ("Split-K": atomic_add;
