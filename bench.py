@@ -464,6 +464,11 @@ SINGLE = {
     "square8192": (8192, 8192, 8192, 1, False, "uniform", "tensor"),
     "large16384": (16384, 16384, 16384, 1, True, "normal", "tensor"),
     "longk": (256, 256, 65536, 16, False, "normal", "hbm"),
+    # linear layers, weights [N, K], bf16 out: bf16 and 8-bit float (E4M3) operands
+    "linear8192": (8192, 8192, 8192, 1, True, "linear", "tensor"),
+    "linearfp8_8192": (8192, 8192, 8192, 1, True, "linear_fp8", "tensor_fp8"),
+    # split-K at a size whose tiles fill the GPU: segments summed in the CTA
+    "fold8192": (8192, 8192, 8192, 16, False, "uniform", "tensor"),
 }
 
 
@@ -472,19 +477,35 @@ def run_single(name, args, world, rank, dev, peaks, peak_src):
     rotating copies that together exceed L2."""
     import deterministic_invariant_gemm_gb300 as dig
     M, N, K, S, bf16, dist_name, bound = SINGLE[name]
-    in_bytes = 2 * (M * K + K * N)
+    esize = 1 if dist_name == "linear_fp8" else 2
+    in_bytes = esize * (M * K + K * N)
     copies = max(1, min(8, math.ceil(2 * L2_BYTES / in_bytes)))
-    AB = [workloads.pair(M, N, K, 4321 + c, dist=dist_name) for c in range(copies)]
-    AB = [(a.to(dev), b.to(dev)) for a, b in AB]
     C = torch.empty((M, N), dtype=torch.bfloat16 if bf16 else torch.float32, device=dev)
-    wsb = dig.bigemm_workspace_bytes(M, N, K, S)
-    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
-    fn = dig.bigemm_run_bf16out if bf16 else dig.bigemm_run
-    launches = 1 if dig.bigemm_effective_split_k(K, S) == 1 else 2
+    if dist_name in ("linear", "linear_fp8"):
+        g = workloads.generator(99)
+        AB = [(torch.randn(M, K, generator=g), torch.randn(N, K, generator=g)) for _ in range(copies)]
+        td = torch.float8_e4m3fn if dist_name == "linear_fp8" else torch.bfloat16
+        AB = [(a.to(td).to(dev), w.to(td).to(dev)) for a, w in AB]
+        launches = 1
 
-    def call(i):
-        a, b = AB[i % copies]
-        fn(a, b, C, M, N, K, K, N, N, S, ws, wsb)
+        def call(i):
+            a, w = AB[i % copies]
+            if dist_name == "linear_fp8":
+                dig.linear_fp8(a, w, 1.0, out_dtype=C.dtype, out=C)
+            else:
+                dig.linear(a, w, out_dtype=C.dtype, out=C)
+    else:
+        AB = [workloads.pair(M, N, K, 4321 + c, dist=dist_name) for c in range(copies)]
+        AB = [(a.to(dev), b.to(dev)) for a, b in AB]
+        wsb = dig.bigemm_workspace_bytes(M, N, K, S)
+        ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+        fn = dig.bigemm_run_bf16out if bf16 else dig.bigemm_run
+        launches = 1 if (dig.bigemm_effective_split_k(K, S) == 1 or
+                         dig.bigemm_split_is_folded(M, N, K, S)) else 2
+
+        def call(i):
+            a, b = AB[i % copies]
+            fn(a, b, C, M, N, K, K, N, N, S, ws, wsb)
 
     for i in range(args.warmup):
         call(i)
@@ -499,15 +520,17 @@ def run_single(name, args, world, rank, dev, peaks, peak_src):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": per * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if dist_name == "linear_fp8" else "bf16", "data": "synthetic",
         "config": {"workload": "%s: M=%d N=%d K=%d split_k=%d, %s out, %s inputs" %
                    (name, M, N, K, S, "bf16" if bf16 else "fp32", dist_name),
                    "l2": "%d rotating input copies (%d MiB)" % (copies, copies * in_bytes >> 20),
                    "parallelism": "replicas"},
         "gpu_launches": launches * args.steps, "clocks": clocks,
     }
-    if bound == "tensor":
-        peak = peaks["bf16_tflops"]
+    if bound in ("tensor", "tensor_fp8"):
+        # an 8-bit product takes the measured bf16 peak times the nominal ratio 2
+        peak = peaks["bf16_tflops"] * (2.0 if bound == "tensor_fp8" else 1.0)
         line["roofline"] = {"kernel": "bigemm_tc_kernel", "bound": "tensor",
                             "achieved": round(flops / per / 1e12, 1), "peak": peak,
                             "peak_source": peak_src, "unit": "TFLOP/s",
@@ -534,7 +557,11 @@ def run_other_workloads(dev, peaks) -> dict:
              ("square_4096", 4096, 4096, 4096, 1, False, "uniform", 10),
              ("square_8192", 8192, 8192, 8192, 1, False, "uniform", 10),
              ("large_16384_bf16out", 16384, 16384, 16384, 1, True, "normal", 5),
-             ("longk_256x256x65536_s16", 256, 256, 65536, 16, False, "normal", 20)]
+             ("longk_256x256x65536_s16", 256, 256, 65536, 16, False, "normal", 20),
+             # split products large enough to fold their segments in the CTA
+             ("square_4096_split8_folded", 4096, 4096, 4096, 8, False, "uniform", 10),
+             ("square_8192_split16_folded", 8192, 8192, 8192, 16, False, "uniform", 10),
+             ("prefill_1024x4096x4096_split8_folded", 1024, 4096, 4096, 8, False, "normal", 20)]
     for name, M, N, K, S, bf16, dist_name, iters in cases:
         in_bytes = 2 * (M * K + K * N)
         copies = max(1, min(8, math.ceil(2 * L2_BYTES / in_bytes)))
@@ -555,7 +582,8 @@ def run_other_workloads(dev, peaks) -> dict:
         tflops = 2.0 * M * N * K * iters / secs / 1e12
         out[name] = {"tflops": round(tflops, 2), "frac_of_bf16_peak": round(tflops / bf16_peak, 4),
                      "ms": round(secs * 1e3 / iters, 4), "split_k": S,
-                     "out": "bf16" if bf16 else "fp32", "input_copies": copies}
+                     "out": "bf16" if bf16 else "fp32", "input_copies": copies,
+                     "launches": dig.bigemm_last_launch_count()}
         if name.startswith("longk"):
             alg = 2.0 * (M * K + K * N) + 4.0 * M * N
             out[name]["hbm_frac"] = round(alg / (secs / iters) / 1e9 / peaks["hbm_gbs"], 4)

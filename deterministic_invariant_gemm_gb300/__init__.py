@@ -35,7 +35,8 @@ __all__ = [
     "bigemm_run_bf16out", "bigemm_run_partial", "bigemm_splitk_reduce",
     "bigemm_run_atomic_splitk", "bigemm_device_status", "bigemm_last_launch_count",
     "bigemm_run_splitk_static", "bigemm_linear", "bigemm_fp8_effective_split_k",
-    "bigemm_fp8_workspace_bytes", "bigemm_linear_fp8", "FP8_E4M3", "FP8_E5M2",
+    "bigemm_fp8_workspace_bytes", "bigemm_linear_fp8", "bigemm_split_is_folded", "FP8_E4M3",
+    "FP8_E5M2", "FOLD_MIN_ROWS", "FOLD_MIN_TILES",
     "STATIC_SCRATCH_BYTES", "matmul", "linear", "linear_fp8", "EXPORTED_SYMBOLS",
 ]
 
@@ -51,6 +52,11 @@ STATUS_NAMES = {
 
 STATIC_SCRATCH_BYTES = 16 << 20
 
+# a split product with at least this many rows and output tiles sums its
+# segments inside the CTA (no workspace); see bigemm_split_is_folded
+FOLD_MIN_ROWS = 97
+FOLD_MIN_TILES = 128
+
 EXPORTED_SYMBOLS = (
     "bigemm_version", "bigemm_status_string", "bigemm_max_split_k", "bigemm_default_split_k",
     "bigemm_effective_split_k", "bigemm_workspace_ld", "bigemm_workspace_bytes",
@@ -58,6 +64,7 @@ EXPORTED_SYMBOLS = (
     "bigemm_splitk_reduce", "bigemm_run_atomic_splitk", "bigemm_device_status",
     "bigemm_last_launch_count", "bigemm_run_splitk_static", "bigemm_linear",
     "bigemm_fp8_effective_split_k", "bigemm_fp8_workspace_bytes", "bigemm_linear_fp8",
+    "bigemm_split_is_folded",
 )
 
 FP8_E4M3 = 0
@@ -96,6 +103,7 @@ def load():
         "bigemm_effective_split_k": ([i64, i32], i32),
         "bigemm_workspace_ld": ([i64], i64),
         "bigemm_workspace_bytes": ([i64, i64, i64, i32], sz),
+        "bigemm_split_is_folded": ([i64, i64, i64, i32], i32),
         "bigemm_partial_workspace_bytes": ([i64, i64, i64, i32], sz),
         "bigemm_run": ([vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, vp, sz, vp], i32),
         "bigemm_run_bf16out": ([vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, vp, sz, vp], i32),
@@ -177,6 +185,10 @@ def bigemm_workspace_ld(N: int) -> int:
 
 def bigemm_workspace_bytes(M: int, N: int, K: int, split_k: int) -> int:
     return int(load().bigemm_workspace_bytes(M, N, K, split_k))
+
+
+def bigemm_split_is_folded(M: int, N: int, K: int, split_k: int) -> bool:
+    return bool(load().bigemm_split_is_folded(M, N, K, split_k))
 
 
 def bigemm_partial_workspace_bytes(M: int, N: int, K: int, split_k: int) -> int:

@@ -75,21 +75,36 @@ bigemm_status device_info(const DeviceInfo** out) {
         d.sm_count = sms;
         if (d.supported) {
             const int smem = static_cast<int>(kSmemBytes);
+            // Besides the shared-memory opt-in: every GEMM kernel must have been
+            // compiled with kLaunchRegs registers per thread, because its
+            // warpgroups re-divide exactly that allocation (setmaxnreg); with
+            // fewer, the epilogue's register increase could never be granted.
             const auto opt_in = [smem](const void* fn) {
+                cudaFuncAttributes fa;
+                if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return BIGEMM_ERR_CUDA;
+                if (fa.numRegs < kLaunchRegs || fa.maxThreadsPerBlock < kNumThreads)
+                    return BIGEMM_ERR_UNSUPPORTED;
                 return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
-                       cudaSuccess;
+                               cudaSuccess
+                           ? BIGEMM_OK
+                           : BIGEMM_ERR_CUDA;
             };
-            if (!opt_in((const void*)bigemm_tc_kernel<kOutF32, false, false>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutBF16, false, false>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutSlices, false, false>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutAtomic, false, false>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutF32, true, false>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutBF16, true, false>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutSlices, true, false>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutF32, true, true>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutBF16, true, true>) ||
-                !opt_in((const void*)bigemm_tc_kernel<kOutSlices, true, true>))
-                return BIGEMM_ERR_CUDA;
+            const void* const kernels[] = {
+                (const void*)bigemm_tc_kernel<kOutF32, false, false>,
+                (const void*)bigemm_tc_kernel<kOutBF16, false, false>,
+                (const void*)bigemm_tc_kernel<kOutSlices, false, false>,
+                (const void*)bigemm_tc_kernel<kOutAtomic, false, false>,
+                (const void*)bigemm_tc_kernel<kOutF32, true, false>,
+                (const void*)bigemm_tc_kernel<kOutBF16, true, false>,
+                (const void*)bigemm_tc_kernel<kOutSlices, true, false>,
+                (const void*)bigemm_tc_kernel<kOutF32, true, true>,
+                (const void*)bigemm_tc_kernel<kOutBF16, true, true>,
+                (const void*)bigemm_tc_kernel<kOutSlices, true, true>,
+            };
+            for (const void* fn : kernels) {
+                const bigemm_status st = opt_in(fn);
+                if (st != BIGEMM_OK) return st;
+            }
             void* sym = nullptr;
             if (cudaGetSymbolAddress(&sym, g_device_status) != cudaSuccess) return BIGEMM_ERR_CUDA;
             d.status = static_cast<unsigned*>(sym);
@@ -102,6 +117,18 @@ bigemm_status device_info(const DeviceInfo** out) {
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// A split product that fills the GPU with whole tiles sums its K segments in
+// the CTA that owns the tile (GemmParams::fold): no workspace, no second
+// kernel, and the same additions in the same order as the reduction kernel.
+// A rule on the shape alone; the folded epilogue assumes one 32-column block
+// per store batch, which every M >= BIGEMM_FOLD_MIN_ROWS has.
+static_assert(epi_batch_for(BIGEMM_FOLD_MIN_ROWS) == 1 && epi_boxes_for(BIGEMM_FOLD_MIN_ROWS) == 1,
+              "folded epilogue layout");
+bool folds(int64_t M, int64_t N, int splits) {
+    if (splits <= 1 || M < BIGEMM_FOLD_MIN_ROWS || N <= 0) return false;
+    return ceil_div(M, kBM) * ceil_div(N, kBN) >= BIGEMM_FOLD_MIN_TILES;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -345,7 +372,9 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     }
     if (bias != nullptr && !aligned16(bias)) return BIGEMM_ERR_ALIGN;
     // ---- workspace
-    const bool need_ws = (mode == kModePartial) || ((mode == kModeF32 || mode == kModeBF16) && splits > 1);
+    const bool direct = (mode == kModeF32 || mode == kModeBF16);
+    const bool fold = direct && folds(M, N, splits);
+    const bool need_ws = (mode == kModePartial) || (direct && splits > 1 && !fold);
     if (need_ws) {
         const size_t need = slice_bytes(M, N, splits);
         if (need == SIZE_MAX) return BIGEMM_ERR_ARG;
@@ -355,7 +384,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     if (M == 0 || N == 0) return BIGEMM_OK;
     const int64_t m_tiles = ceil_div(M, kBM);
     const int64_t n_tiles = ceil_div(N, kBN);
-    const int64_t units = m_tiles * n_tiles * splits;
+    const int64_t units = m_tiles * n_tiles * (fold ? 1 : splits);
     if (units > INT_MAX) return BIGEMM_ERR_ARG;
 
     const DeviceInfo* d = nullptr;
@@ -403,8 +432,12 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     // of tiles (the concurrent tiles then span about 16 x 9 tiles, whose A and
     // B panels stay in L2), else 8.  It orders tiles only; no sum changes.
     p.group_m = (m_tiles * n_tiles >= 4 * static_cast<int64_t>(d->sm_count)) ? 16 : 8;
-    p.bias = (splits == 1) ? static_cast<const __nv_bfloat16*>(bias) : nullptr;
-    p.scale = (splits == 1) ? scale : 1.0f;
+    p.fold = fold ? 1 : 0;
+    // the scale and the bias follow the full sum: in this kernel's epilogue
+    // unless a reduction kernel forms that sum
+    const bool sum_here = (splits == 1) || fold;
+    p.bias = sum_here ? static_cast<const __nv_bfloat16*>(bias) : nullptr;
+    p.scale = sum_here ? scale : 1.0f;
     p.idesc_fp8 = fp8 ? idesc_fp8_f32(kBM, kBN, static_cast<uint32_t>(fp8_fmt_a),
                                       static_cast<uint32_t>(fp8_fmt_b))
                       : 0u;
@@ -422,7 +455,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
         p.ld_out = ldc;
         e = launch_gemm<kOutAtomic>(wt, fp8, g, blk, stream, tmA, tmB, tmBp, tmC, p);
         launches = 1;
-    } else if (mode == kModePartial || splits > 1) {
+    } else if (mode == kModePartial || (splits > 1 && !fold)) {
         p.out = ws;
         p.ld_out = ws_ld_of(N);
         p.slice_stride = M * p.ld_out;
@@ -528,10 +561,15 @@ int bigemm_effective_split_k(int64_t K, int split_k) { return effective_split(K,
 
 int64_t bigemm_workspace_ld(int64_t N) { return N < 0 ? 0 : ws_ld_of(N); }
 
+int bigemm_split_is_folded(int64_t M, int64_t N, int64_t K, int split_k) {
+    if (M < 0 || N < 0) return 0;
+    return folds(M, N, effective_split(K, split_k, nullptr)) ? 1 : 0;
+}
+
 size_t bigemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {
     if (M < 0 || N < 0) return 0;
     const int s = effective_split(K, split_k, nullptr);
-    if (s <= 1) return 0;
+    if (s <= 1 || folds(M, N, s)) return 0;
     return slice_bytes(M, N, s);
 }
 
@@ -596,7 +634,7 @@ int bigemm_fp8_effective_split_k(int64_t K, int split_k) {
 size_t bigemm_fp8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {
     if (M < 0 || N < 0) return 0;
     const int s = effective_split(K, split_k, nullptr, 128);
-    if (s <= 1) return 0;
+    if (s <= 1 || folds(M, N, s)) return 0;
     return slice_bytes(M, N, s);
 }
 

@@ -18,13 +18,17 @@
 // used for every M: short batches are padded by the TMA unit's zero fill, never
 // served by a different code path.
 //
-// CTA roles (320 threads, one CTA per SM):
-//   warp 0      TMA producer: fills a kStages-deep shared-memory ring.
-//   warp 1      allocates TMEM; one lane issues the MMAs and commits.
-//   warps 2..9  epilogue, two warps per TMEM lane quarter, each taking half
-//               of the tile's columns: TMEM -> registers -> swizzled
-//               shared-memory boxes -> TMA stores; two TMEM accumulators let
-//               the epilogue of tile t overlap the mainloop of tile t + 1.
+// CTA roles (384 threads = three warpgroups, one CTA per SM):
+//   warp 0       TMA producer: fills a kStages-deep shared-memory ring.
+//   warp 1       allocates TMEM; one lane issues the MMAs and commits.
+//   warps 2, 3   set-up only (barrier initialisation).
+//   warps 4..11  epilogue, two warps per TMEM lane quarter, each taking half
+//                of the tile's columns: TMEM -> registers -> swizzled
+//                shared-memory boxes -> TMA stores; two TMEM accumulators let
+//                the epilogue of tile t overlap the mainloop of tile t + 1.
+// The first warpgroup gives most of its registers to the two epilogue
+// warpgroups, which hold up to a 32 x 256 FP32 block per warp (a folded
+// tile's running sum).
 #pragma once
 
 #include <cuda.h>
@@ -39,8 +43,22 @@ constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
 constexpr int kUmmaK = 16;
-constexpr int kNumThreads = 320;       // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kNumThreads = 384;       // warp 0 TMA, warp 1 MMA, warps 4..11 epilogue
 constexpr int kEpilogueThreads = 256;
+constexpr int kEpilogueWarp0 = 4;      // first epilogue warp: the second warpgroup
+
+// Register split.  The block is launched with kLaunchRegs registers per thread
+// (65536 over 384 threads, in steps of 8: what ptxas assigns to a 384-thread,
+// one-block-per-SM kernel; the host checks it before the first launch).  The
+// producer / MMA warpgroup drops to kFrontRegs and the two epilogue
+// warpgroups take the rest -- never more than the launch provided, or the
+// increase would wait for registers that never come free.
+constexpr int kLaunchRegs = 168;
+constexpr int kFrontRegs = 56;
+constexpr int kEpilogueRegs = 224;
+static_assert(128 * kFrontRegs + 256 * kEpilogueRegs <= kNumThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
+static_assert(kNumThreads * kLaunchRegs <= 65536, "one block per SM");
 
 constexpr uint32_t kABytes = kBM * kBK * 2;       // 16 KiB: 128 rows x 128 B
 constexpr uint32_t kBChunkCols = 64;              // one 128-byte swizzle span of N
@@ -121,6 +139,8 @@ struct GemmParams {
                                 // epilogue, or nullptr
     float scale;            // the direct epilogue multiplies the sum by this (1: none)
     uint32_t idesc_fp8;     // instruction descriptor of the 8-bit float product
+    int fold;               // 1: a unit is a whole tile whose `splits` K segments are
+                            //    summed in the CTA (splits > 1, direct output)
 };
 
 // Unit u -> (tile row, tile column, K segment).  All tiles of segment 0 come
@@ -247,6 +267,84 @@ __device__ __forceinline__ void atomic_add_row_chunk(const GemmParams& p, int ro
         if (c < valid) atomicAdd(dst + c, __uint_as_float(r[c]));
 }
 
+// The epilogue's last step for nb (<= kNbMax) 32-column blocks of one warp's
+// 32 rows, held in r: the output scale and the bias (direct outputs), then
+// either the atomic additions of the contrast or swizzled staging boxes and
+// their TMA stores.  Blocks ending in a partial 16-byte chunk of a C row are
+// written element by element instead (the TMA unit clips the innermost
+// dimension at 16-byte granularity; the workspace owns its padding).  `nbat`
+// counts the batches this warp has handed to the TMA unit; the slot a batch
+// reuses must have been read by its earlier store, so at most slots - 1 may
+// pend.
+template <int kOut, int kNbMax>
+__device__ __forceinline__ void emit_blocks(const GemmParams& p, const CUtensorMap* tmC, uint32_t* r,
+                                            int nb, int c0, int n0, int m0, int seg, int lane,
+                                            uint32_t my_boxes, int batch, int slots, uint32_t& nbat) {
+    constexpr uint32_t kBox = (kOut == kOutBF16) ? kStageBufBytes / 2 : kStageBufBytes;
+    if constexpr (kOut == kOutF32 || kOut == kOutBF16) {
+        if (p.scale != 1.0f) {  // uniform: one FP32 multiply per element
+#pragma unroll
+            for (int i = 0; i < kNbMax * 32; ++i)
+                if (i < nb * 32) r[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), p.scale));
+        }
+        if (p.bias != nullptr) {  // uniform
+#pragma unroll
+            for (int i = 0; i < kNbMax; ++i)
+                if (i < nb) add_bias_block(p.bias, n0 + (c0 + i) * 32, p.N, r + 32 * i);
+        }
+    }
+    if constexpr (kOut == kOutAtomic) {
+#pragma unroll
+        for (int i = 0; i < kNbMax; ++i)
+            if (i < nb && m0 + lane < p.M)
+                atomic_add_row_chunk(p, m0 + lane, n0 + (c0 + i) * 32,
+                                     *reinterpret_cast<const uint32_t(*)[32]>(r + 32 * i));
+    } else {
+        const uint32_t box0 = my_boxes + (nbat % static_cast<uint32_t>(slots)) * batch * kBox;
+        if (nbat >= static_cast<uint32_t>(slots)) {
+            if (lane == 0) bulk_wait_group_read_dyn(slots - 1);
+            __syncwarp();
+        }
+        constexpr int kVec = (kOut == kOutBF16) ? 8 : 4;
+        int staged = 0;
+#pragma unroll
+        for (int i = 0; i < kNbMax; ++i) {
+            if (i >= nb) break;
+            const int col = n0 + (c0 + i) * 32;
+            const uint32_t(&ri)[32] = *reinterpret_cast<const uint32_t(*)[32]>(r + 32 * i);
+            const bool ragged = kOut != kOutSlices && col + 32 > p.N && (p.N % kVec) != 0;
+            if (ragged) {
+                if (m0 + lane < p.M) store_row_masked<kOut>(p, m0 + lane, col, ri);
+            } else {
+                const uint32_t box = box0 + static_cast<uint32_t>(i) * kBox;
+                if constexpr (kOut == kOutBF16) stage_bf16(box, lane, ri);
+                else stage_f32(box, lane, ri);
+                ++staged;
+            }
+        }
+        if (staged > 0) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const int g0 = (n0 + c0 * 32) / 32;
+                if (p.grouped) {
+                    if constexpr (kOut == kOutSlices) tma_store_4d(tmC, box0, 0, m0, g0, seg);
+                    else tma_store_3d(tmC, box0, 0, m0, g0);
+                } else {
+                    for (int i = 0; i < staged; ++i) {
+                        const uint32_t box = box0 + static_cast<uint32_t>(i) * kBox;
+                        const int col = n0 + (c0 + i) * 32;
+                        if constexpr (kOut == kOutSlices) tma_store_3d(tmC, box, col, m0, seg);
+                        else tma_store_2d(tmC, box, col, m0);
+                    }
+                }
+                bulk_commit_group();
+            }
+            ++nbat;
+        }
+    }
+}
+
 // kWt: the second operand is the weight matrix W [N, K] (K-major); otherwise
 // B [K, N] (N-major).  Both products run the same K = 16 instruction sequence.
 // kFp8: 8-bit float operands (both K-major, kWt): a K block is 128 elements,
@@ -310,7 +408,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             int mt, nt, seg;
             unit_coords(p, blockIdx.x, mt, nt, seg);
             const int k0 = seg * p.kb_per_split * kKB;
-            const int k1 = min(k0 + p.prefetch_rows, min(k0 + p.kb_per_split * kKB, p.kb_total * kKB));
+            const int seg_rows = (p.fold ? p.kb_total : p.kb_per_split) * kKB;
+            const int k1 = min(k0 + p.prefetch_rows, min(k0 + seg_rows, p.kb_total * kKB));
             for (int k = k0; k < k1; k += kPrefetchRows) {
                 if constexpr (kWt) tma_prefetch_l2_2d(&tmBp, k, nt * kBN);
                 else tma_prefetch_l2_2d(&tmBp, nt * kBN, k);
@@ -333,7 +432,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // global memory is read and written only after it has completed.
     grid_dependency_wait();
 
-    if (warp == 0) {
+    if (warp < kEpilogueWarp0) {
+      regs_release_to<kFrontRegs>();
+      if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer --
             int stage = 0;
@@ -343,8 +444,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
                 int mt, nt, seg;
                 unit_coords(p, u, mt, nt, seg);
-                const int kb0 = seg * p.kb_per_split;
-                const int kb1 = min(kb0 + p.kb_per_split, p.kb_total);
+                // a folded unit streams all of K; its segments follow one another
+                const int kb0 = p.fold ? 0 : seg * p.kb_per_split;
+                const int kb1 = p.fold ? p.kb_total : min(kb0 + p.kb_per_split, p.kb_total);
                 const int m0 = mt * kBM, n0 = nt * kBN;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.status,
@@ -391,66 +493,74 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // ------------------------------------------------- MMA issuer --
             int stage = 0;
             uint32_t phase = 0;
-            int t = 0;
+            int t = 0;  // accumulators filled so far (one per segment)
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x, ++t) {
-                int mt, nt, seg;
-                unit_coords(p, u, mt, nt, seg);
-                const int kb0 = seg * p.kb_per_split;
-                const int kb1 = min(kb0 + p.kb_per_split, p.kb_total);
-                const int acc = t % kAccStages;
-                const uint32_t acc_phase = static_cast<uint32_t>(t / kAccStages) & 1u;
-                if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status,
-                                  kErrWaitMma)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_bounded(full_bar(stage), phase, abort_flag, p.status, kErrWaitMma)) {
+            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+                int mt, nt, seg0;
+                unit_coords(p, u, mt, nt, seg0);
+                // A folded unit fills one accumulator per K segment, in order; the
+                // epilogue adds them.  Otherwise the unit is the single segment seg0.
+                const int nseg = p.fold ? p.splits : 1;
+                for (int sg = 0; ok && sg < nseg; ++sg, ++t) {
+                    const int seg = p.fold ? sg : seg0;
+                    const int kb0 = seg * p.kb_per_split;
+                    const int kb1 = min(kb0 + p.kb_per_split, p.kb_total);
+                    const int acc = t % kAccStages;
+                    const uint32_t acc_phase = static_cast<uint32_t>(t / kAccStages) & 1u;
+                    if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status,
+                                      kErrWaitMma)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = sA + stage * kABytes;
-                    const uint32_t b0 = sB + stage * kBBytes;
-#pragma unroll
-                    for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-                        // A: K-major, 128-byte rows; advance 16 elements = 32 bytes.
-                        const uint64_t ad = smem_desc_sw128(a0 + kk * kUmmaK * 2, 16, 1024);
-                        uint64_t bd;
-                        if constexpr (kWt) {
-                            // W: K-major like A, 256 rows of 128 bytes.
-                            bd = smem_desc_sw128(b0 + kk * kUmmaK * 2, 16, 1024);
-                        } else {
-                            // B: N-major; 16 k-rows of 128 bytes = 2048 bytes per step.
-                            // LBO = distance between 64-column chunks, SBO = 8 k-rows.
-                            bd = smem_desc_sw128(b0 + kk * kUmmaK * 128, kBChunkBytes, 1024);
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!wait_bounded(full_bar(stage), phase, abort_flag, p.status, kErrWaitMma)) {
+                            ok = false;
+                            break;
                         }
-                        if constexpr (kFp8)
-                            mma_fp8(d_tmem, ad, bd, p.idesc_fp8, (kb > kb0 || kk > 0) ? 1u : 0u);
-                        else
-                            mma_bf16(d_tmem, ad, bd, kWt ? kIdescWt : kIdescBN,
-                                     (kb > kb0 || kk > 0) ? 1u : 0u);
+                        tc_fence_after();
+                        const uint32_t a0 = sA + stage * kABytes;
+                        const uint32_t b0 = sB + stage * kBBytes;
+    #pragma unroll
+                        for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                            // A: K-major, 128-byte rows; advance 16 elements = 32 bytes.
+                            const uint64_t ad = smem_desc_sw128(a0 + kk * kUmmaK * 2, 16, 1024);
+                            uint64_t bd;
+                            if constexpr (kWt) {
+                                // W: K-major like A, 256 rows of 128 bytes.
+                                bd = smem_desc_sw128(b0 + kk * kUmmaK * 2, 16, 1024);
+                            } else {
+                                // B: N-major; 16 k-rows of 128 bytes = 2048 bytes per step.
+                                // LBO = distance between 64-column chunks, SBO = 8 k-rows.
+                                bd = smem_desc_sw128(b0 + kk * kUmmaK * 128, kBChunkBytes, 1024);
+                            }
+                            if constexpr (kFp8)
+                                mma_fp8(d_tmem, ad, bd, p.idesc_fp8, (kb > kb0 || kk > 0) ? 1u : 0u);
+                            else
+                                mma_bf16(d_tmem, ad, bd, kWt ? kIdescWt : kIdescBN,
+                                         (kb > kb0 || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit(empty_bar(stage));
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
-                    mma_commit(empty_bar(stage));
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    if (!ok) break;
+                    mma_commit(tfull_bar(acc));
                 }
-                if (!ok) break;
-                mma_commit(tfull_bar(acc));
             }
             // Every MMA this thread issued completes before TMEM is released.
             mma_commit(drain_bar);
             wait_bounded(drain_bar, 0, abort_flag, p.status, kErrWaitDrain, /*honour_abort=*/false);
         }
+      }
     } else {
+        regs_grow_to<kEpilogueRegs>();
         // ------------------------------------------------------ epilogue --
         // Warp w reads TMEM lanes 32 (w % 4) .. +31, i.e. tile rows q*32 .. q*32+31,
-        // and the columns of half h = (w - 2) / 4 of the tile (128 each).
+        // and the columns of half h = (w - 4) / 4 of the tile (128 each).
         // Blocks of 32 x 32 go TMEM -> registers -> swizzled staging boxes -> TMA
         // stores (coalesced, asynchronous; rows >= M and columns >= N fall outside
         // the tensor map and are not written).  A batch of epi_batch blocks is
@@ -461,7 +571,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // warp owns its boxes for the whole launch and recycles them batch by
         // batch.
         const int q = warp & 3;
-        const int h = (warp - 2) >> 2;
+        const int h = (warp - kEpilogueWarp0) >> 2;
         const int per_warp = p.epi_boxes;
         const int batch = p.epi_batch;
         const int slots = per_warp / batch;  // batches in flight per warp (2 or 1)
@@ -471,111 +581,110 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         constexpr uint32_t kBox = (kOut == kOutBF16) ? kStageBufBytes / 2 : kStageBufBytes;
         const uint32_t my_boxes = sOut + static_cast<uint32_t>((q * 2 + h) * per_warp) * kBox;
         uint32_t nbat = 0;  // batches this warp has handed to the TMA unit
-        int t = 0;
-        for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
-            int mt, nt, seg;
-            unit_coords(p, u, mt, nt, seg);
-            const int acc = t % kAccStages;
-            const uint32_t acc_phase = static_cast<uint32_t>(t / kAccStages) & 1u;
-            if (!wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.status, kErrWaitEpilogue))
-                break;
-            tc_fence_after();
-            const int m0 = mt * kBM + q * 32, n0 = nt * kBN;
-            bool released = false;
-            if (m0 < p.M) {  // uniform per warp: a warp whose rows are all past M skips
-                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                       static_cast<uint32_t>(acc * kBN);
-                // this warp's 32-column blocks: [h * 4, nchunks)
-                const int nchunks = min(h * 4 + 4, min(kBN / 32, (p.N - n0 + 31) / 32));
+        int t = 0;          // accumulators drained so far (one per segment)
+        bool folded = false;
+        if constexpr (kOut == kOutF32 || kOut == kOutBF16) {
+            if (p.fold) {
+                // ---- folded tiles: sum = w_0, then sum = sum + w_s for s = 1 ..
+                // splits-1 (FP32, round to nearest even) -- the additions
+                // splitk_reduce_kernel makes, in the same order, on the same
+                // partials, so the bits agree with the workspace path.  The
+                // host folds only when every warp with rows stores one block per
+                // batch (p.epi_batch == 1).  The sum lives in 128 registers.
+                folded = true;
+                for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+                    int mt, nt, seg;
+                    unit_coords(p, u, mt, nt, seg);
+                    const int m0 = mt * kBM + q * 32, n0 = nt * kBN;
+                    const int nchunks = min(h * 4 + 4, min(kBN / 32, (p.N - n0 + 31) / 32));
+                    uint32_t sum[128];
+                    bool ok = true;
 #pragma unroll 1
-                for (int c0 = h * 4; c0 < nchunks; c0 += batch) {
-                    const int nb = min(batch, nchunks - c0);
-                    uint32_t r[kMaxBatch * 32];
-                    if (batch == 4) tmem_ld_32x32b_x128(tbase + c0 * 32, r);
-                    else if (batch == 2) tmem_ld_32x32b_x64(tbase + c0 * 32, r);
-                    else tmem_ld_32x32b_x32(tbase + c0 * 32, *reinterpret_cast<uint32_t(*)[32]>(r));
-                    tmem_ld_wait();
-                    if (c0 + nb >= nchunks) {  // the accumulator is no longer needed
-                        tc_fence_before();
-                        mbar_arrive(tempty_bar(acc));
-                        released = true;
-                    }
-                    if constexpr (kOut == kOutF32 || kOut == kOutBF16) {
-                        if (p.scale != 1.0f) {  // uniform: one FP32 multiply per element
-#pragma unroll
-                            for (int i = 0; i < kMaxBatch * 32; ++i)
-                                if (i < nb * 32)
-                                    r[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), p.scale));
+                    for (int sg = 0; sg < p.splits; ++sg, ++t) {
+                        const int acc = t % kAccStages;
+                        const uint32_t acc_phase = static_cast<uint32_t>(t / kAccStages) & 1u;
+                        if (!wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.status,
+                                          kErrWaitEpilogue)) {
+                            ok = false;
+                            break;
                         }
-                        if (p.bias != nullptr) {  // uniform
+                        tc_fence_after();
+                        if (m0 < p.M) {
+                            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                                   static_cast<uint32_t>(acc * kBN);
+                            if (sg == 0) {  // sum = w_0 itself (a -0.0 stays -0.0)
 #pragma unroll
-                            for (int i = 0; i < kMaxBatch; ++i)
-                                if (i < nb) add_bias_block(p.bias, n0 + (c0 + i) * 32, p.N, r + 32 * i);
-                        }
-                    }
-                    if constexpr (kOut == kOutAtomic) {
-#pragma unroll
-                        for (int i = 0; i < kMaxBatch; ++i)
-                            if (i < nb && m0 + lane < p.M)
-                                atomic_add_row_chunk(p, m0 + lane, n0 + (c0 + i) * 32,
-                                                     *reinterpret_cast<const uint32_t(*)[32]>(r + 32 * i));
-                    } else {
-                        // The slot this batch reuses must have been read by its
-                        // earlier store: at most slots - 1 batches may pend.
-                        const uint32_t box0 =
-                            my_boxes + (nbat % static_cast<uint32_t>(slots)) * batch * kBox;
-                        if (nbat >= static_cast<uint32_t>(slots)) {
-                            if (lane == 0) bulk_wait_group_read_dyn(slots - 1);
-                            __syncwarp();
-                        }
-                        // The TMA unit clips the innermost dimension at 16-byte
-                        // granularity, so a block ending in a partial 16-byte chunk
-                        // of a C row is written element by element instead (the
-                        // workspace owns its padding).
-                        constexpr int kVec = (kOut == kOutBF16) ? 8 : 4;
-                        int staged = 0;
-#pragma unroll
-                        for (int i = 0; i < kMaxBatch; ++i) {
-                            if (i >= nb) break;
-                            const int col = n0 + (c0 + i) * 32;
-                            const uint32_t(&ri)[32] = *reinterpret_cast<const uint32_t(*)[32]>(r + 32 * i);
-                            const bool ragged =
-                                kOut != kOutSlices && col + 32 > p.N && (p.N % kVec) != 0;
-                            if (ragged) {
-                                if (m0 + lane < p.M) store_row_masked<kOut>(p, m0 + lane, col, ri);
+                                for (int i = 0; i < 4; ++i)
+                                    if (h * 4 + i < nchunks)
+                                        tmem_ld_32x32b_x32(tbase + (h * 4 + i) * 32,
+                                                           *reinterpret_cast<uint32_t(*)[32]>(sum + 32 * i));
+                                tmem_ld_wait();
                             } else {
-                                const uint32_t box = box0 + static_cast<uint32_t>(i) * kBox;
-                                if constexpr (kOut == kOutBF16) stage_bf16(box, lane, ri);
-                                else stage_f32(box, lane, ri);
-                                ++staged;
-                            }
-                        }
-                        if (staged > 0) {
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0) {
-                                const int g0 = (n0 + c0 * 32) / 32;
-                                if (p.grouped) {
-                                    if constexpr (kOut == kOutSlices) tma_store_4d(&tmC, box0, 0, m0, g0, seg);
-                                    else tma_store_3d(&tmC, box0, 0, m0, g0);
-                                } else {
-                                    for (int i = 0; i < staged; ++i) {
-                                        const uint32_t box = box0 + static_cast<uint32_t>(i) * kBox;
-                                        const int col = n0 + (c0 + i) * 32;
-                                        if constexpr (kOut == kOutSlices) tma_store_3d(&tmC, box, col, m0, seg);
-                                        else tma_store_2d(&tmC, box, col, m0);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    if (h * 4 + i < nchunks) {
+                                        uint32_t w[32];
+                                        tmem_ld_32x32b_x32(tbase + (h * 4 + i) * 32, w);
+                                        tmem_ld_wait();
+#pragma unroll
+                                        for (int j = 0; j < 32; ++j)
+                                            sum[32 * i + j] = __float_as_uint(__fadd_rn(
+                                                __uint_as_float(sum[32 * i + j]), __uint_as_float(w[j])));
                                     }
                                 }
-                                bulk_commit_group();
                             }
-                            ++nbat;
                         }
+                        tc_fence_before();
+                        mbar_arrive(tempty_bar(acc));
+                    }
+                    if (!ok) break;
+                    if (m0 < p.M) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (h * 4 + i < nchunks)
+                                emit_blocks<kOut, 1>(p, &tmC, sum + 32 * i, 1, h * 4 + i, n0, m0, seg,
+                                                     lane, my_boxes, 1, slots, nbat);
                     }
                 }
             }
-            if (!released) {
-                tc_fence_before();
-                mbar_arrive(tempty_bar(acc));
+        }
+        if (!folded) {
+            for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
+                int mt, nt, seg;
+                unit_coords(p, u, mt, nt, seg);
+                const int m0 = mt * kBM + q * 32, n0 = nt * kBN;
+                // this warp's 32-column blocks: [h * 4, nchunks)
+                const int nchunks = min(h * 4 + 4, min(kBN / 32, (p.N - n0 + 31) / 32));
+                const int acc = t % kAccStages;
+                const uint32_t acc_phase = static_cast<uint32_t>(t / kAccStages) & 1u;
+                if (!wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.status, kErrWaitEpilogue))
+                    break;
+                tc_fence_after();
+                bool released = false;
+                if (m0 < p.M) {  // uniform per warp: a warp whose rows are all past M skips
+                    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                           static_cast<uint32_t>(acc * kBN);
+#pragma unroll 1
+                    for (int c0 = h * 4; c0 < nchunks; c0 += batch) {
+                        const int nb = min(batch, nchunks - c0);
+                        uint32_t r[kMaxBatch * 32];
+                        if (batch == 4) tmem_ld_32x32b_x128(tbase + c0 * 32, r);
+                        else if (batch == 2) tmem_ld_32x32b_x64(tbase + c0 * 32, r);
+                        else tmem_ld_32x32b_x32(tbase + c0 * 32, *reinterpret_cast<uint32_t(*)[32]>(r));
+                        tmem_ld_wait();
+                        if (c0 + nb >= nchunks) {  // the accumulator is no longer needed
+                            tc_fence_before();
+                            mbar_arrive(tempty_bar(acc));
+                            released = true;
+                        }
+                        emit_blocks<kOut, kMaxBatch>(p, &tmC, r, nb, c0, n0, m0, seg, lane, my_boxes,
+                                                     batch, slots, nbat);
+                    }
+                }
+                if (!released) {
+                    tc_fence_before();
+                    mbar_arrive(tempty_bar(acc));
+                }
             }
         }
         // All of this warp's stores complete before the CTA exits.

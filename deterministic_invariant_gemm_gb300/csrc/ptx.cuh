@@ -219,6 +219,14 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         : "r"(taddr));
 }
 
+// The same for 8 consecutive columns (r[0..7]).
+__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t* r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
 // The same for 64 / 128 consecutive columns (r[0..63] / r[0..127]).
 __device__ __forceinline__ void tmem_ld_32x32b_x64(uint32_t taddr, uint32_t* r) {
     asm volatile(
@@ -249,6 +257,21 @@ __device__ __forceinline__ void grid_dependency_wait() {
 // Allows the next programmatically-launched kernel to start its prologue.
 __device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Per-warpgroup register budget (all four warps of a warpgroup execute the
+// same one).  `dec` returns registers to the block's pool; `inc` takes them
+// and blocks until the pool holds enough, so the budgets of all warpgroups
+// must add up to no more than the block was launched with.
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_release_to() {
+    static_assert(kRegs >= 24 && kRegs <= 256 && kRegs % 8 == 0, "setmaxnreg range");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_grow_to() {
+    static_assert(kRegs >= 24 && kRegs <= 256 && kRegs % 8 == 0, "setmaxnreg range");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 
 // ----------------------------------------------------- UMMA descriptors --

@@ -16,7 +16,11 @@
  *     each segment's FP32 partial goes to its own workspace slice, and a
  *     separate kernel adds the slices in the fixed order s = 0, 1, ..., S-1
  *     ("Split-K": workspace [split_k, M, N], partial GEMM kernel, reduction
- *     kernel) -- no atomics;
+ *     kernel) -- no atomics.  A product large enough to fill the GPU with
+ *     whole tiles (bigemm_split_is_folded) instead has the CTA that owns a
+ *     tile compute its S segment partials one after another and add them in
+ *     the same order with the same FP32 additions: the same bits, with no
+ *     workspace and no second kernel;
  *   - the M and N tile sizes and the order in which tiles run (a GROUP_M
  *     swizzle, "GROUP_M - Swizzle L2 Cache") change no sum.
  * So row i of C is bit-for-bit a function of (row i of A, B, K, split_k,
@@ -97,6 +101,12 @@ typedef void *bigemm_stream;
 #define BIGEMM_TILE_M 128
 #define BIGEMM_TILE_N 256
 
+/* A split product is folded (its segments summed inside the CTA, no
+ * workspace) when it has at least BIGEMM_FOLD_MIN_ROWS rows and at least
+ * BIGEMM_FOLD_MIN_TILES output tiles; see bigemm_split_is_folded. */
+#define BIGEMM_FOLD_MIN_ROWS 97
+#define BIGEMM_FOLD_MIN_TILES 128
+
 /* Library version, (major << 16) | minor. */
 BIGEMM_API int bigemm_version(void);
 
@@ -125,9 +135,21 @@ BIGEMM_API int bigemm_effective_split_k(int64_t K, int split_k);
  * multiple of 4, so that every row starts 16-byte aligned. */
 BIGEMM_API int64_t bigemm_workspace_ld(int64_t N);
 
-/* Workspace bytes bigemm_run / bigemm_run_bf16out need for (M, N, K,
- * split_k): effective_split * M * bigemm_workspace_ld(N) * 4 when the
- * effective split is > 1, else 0.  Returns 0 for invalid arguments too. */
+/* 1 when a product of this shape with effective split S > 1 sums its
+ * segments inside the CTA rather than through the workspace: M >=
+ * BIGEMM_FOLD_MIN_ROWS and ceil(M / 128) * ceil(N / 256) >=
+ * BIGEMM_FOLD_MIN_TILES, so that whole tiles alone occupy most SMs.  The
+ * choice is one of speed only: both ways form every sum the same way (the
+ * same segment partials, added in the order 0..S-1, each addition one FP32
+ * addition rounded to nearest even), so row i of C has the same bits either
+ * way.  A shape test only, for any K and split_k (8-bit products too); 0 for
+ * invalid arguments or an effective split of 1. */
+BIGEMM_API int bigemm_split_is_folded(int64_t M, int64_t N, int64_t K, int split_k);
+
+/* Workspace bytes bigemm_run / bigemm_run_bf16out / bigemm_linear need for
+ * (M, N, K, split_k): effective_split * M * bigemm_workspace_ld(N) * 4 when
+ * the effective split is > 1 and the product is not folded
+ * (bigemm_split_is_folded), else 0.  Returns 0 for invalid arguments too. */
 BIGEMM_API size_t bigemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
 
 /* Workspace bytes bigemm_run_partial needs: effective_split * M *
@@ -207,7 +229,8 @@ BIGEMM_API bigemm_status bigemm_linear(const void *A, const void *W, const void 
  * like 64 BF16 elements).  0 for an invalid split_k. */
 BIGEMM_API int bigemm_fp8_effective_split_k(int64_t K, int split_k);
 
-/* Workspace bytes bigemm_linear_fp8 needs (0 when its effective split is 1). */
+/* Workspace bytes bigemm_linear_fp8 needs: as bigemm_workspace_bytes with
+ * the 8-bit effective split (0 when it is 1 or the product is folded). */
 BIGEMM_API size_t bigemm_fp8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
 
 /* Batch-invariant linear layer with 8-bit float operands:

@@ -84,6 +84,36 @@ def test_workspace_sizes(lib):
     assert dig.bigemm_workspace_bytes(-1, 5, 640, 2) == 0
 
 
+def test_fold_rule_is_a_function_of_the_shape(lib):
+    """A split product folds (no workspace) exactly when it has at least
+    FOLD_MIN_ROWS rows and FOLD_MIN_TILES tiles of 128 x 256; K and split_k
+    matter only through whether the effective split exceeds 1."""
+    def tiles(M, N):
+        return -(-M // 128) * -(-N // 256)
+
+    for M in (1, 16, 96, 97, 128, 511, 512, 1024, 1025, 4096, 8192):
+        for N in (256, 4096, 4100, 6144, 32768, 65536):
+            for K, S in ((4096, 8), (4096, 1), (4096, 0), (65536, 16), (640, 7), (64, 4)):
+                s = dig.bigemm_effective_split_k(K, S)
+                want = s > 1 and M >= dig.FOLD_MIN_ROWS and tiles(M, N) >= dig.FOLD_MIN_TILES
+                assert dig.bigemm_split_is_folded(M, N, K, S) == want, (M, N, K, S)
+                ws = dig.bigemm_workspace_bytes(M, N, K, S)
+                assert ws == (0 if (s <= 1 or want) else s * M * dig.bigemm_workspace_ld(N) * 4)
+                s8 = dig.bigemm_fp8_effective_split_k(K, S)
+                want8 = s8 > 1 and M >= dig.FOLD_MIN_ROWS and tiles(M, N) >= dig.FOLD_MIN_TILES
+                ws8 = dig.bigemm_fp8_workspace_bytes(M, N, K, S)
+                assert ws8 == (0 if (s8 <= 1 or want8) else s8 * M * dig.bigemm_workspace_ld(N) * 4)
+                # the explicit partial kernel always writes slices (0 bytes for
+                # an invalid split, e.g. 4 segments of one K block)
+                assert dig.bigemm_partial_workspace_bytes(M, N, K, S) == \
+                    s * M * dig.bigemm_workspace_ld(N) * 4
+    # the decode shapes never fold; a prefill of 1024 rows at N = 4096 does
+    assert not dig.bigemm_split_is_folded(64, 4096, 4096, 8)
+    assert dig.bigemm_split_is_folded(1024, 4096, 4096, 8)
+    assert not dig.bigemm_split_is_folded(1024, 4096, 4096, 1)
+    assert not dig.bigemm_split_is_folded(-1, 4096, 4096, 8)
+
+
 A16 = 1 << 20      # fake, 16-byte aligned addresses: never dereferenced
 B16 = 2 << 20
 C16 = 3 << 20

@@ -74,7 +74,8 @@ def test_static_scratch_matches_workspace_entry_point(cuda_device, order):
 
 
 def test_static_scratch_rejects_products_past_its_size(cuda_device):
-    M, N, K, S = 1024, 4096, 4096, 8            # needs 128 MiB of split-K scratch
+    M, N, K, S = 512, 4096, 4096, 8             # needs 64 MiB of split-K scratch
+    assert not dig.bigemm_split_is_folded(M, N, K, S)   # 64 tiles: the workspace path
     assert dig.bigemm_workspace_bytes(M, N, K, S) > dig.STATIC_SCRATCH_BYTES
     a = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
     b = torch.zeros((K, N), dtype=torch.bfloat16, device="cuda")
