@@ -226,7 +226,7 @@ def kernel_source_hash() -> str:
 def profiled_traffic():
     """DRAM bytes per launch of the decode partial kernel from the committed
     ncu summary, or None when that capture was taken on other kernel sources."""
-    path = os.path.join(ROOT, "profiles", "bigemm_partial_decode_M16_M64.md")
+    path = os.path.join(ROOT, "profiles", "bigemm_partial_decode_N4096_K4096.md")
     try:
         text = open(path, encoding="utf-8").read()
     except OSError:
@@ -780,7 +780,7 @@ def main():
         line["roofline"]["traffic"] = sum(traffic.values()) / len(traffic)
         line["roofline"]["traffic_source"] = (
             "dram__bytes_read.sum + dram__bytes_write.sum per launch, ncu capture of the current "
-            "kernel sources (profiles/bigemm_partial_decode_M16_M64.md), mean of M=%s"
+            "kernel sources (profiles/bigemm_partial_decode_N4096_K4096.md), mean of M=%s"
             % ",".join(str(m) for m in sorted(traffic)))
     if rank == 0 and world == 1 and not args.no_extras:
         line["e2e"] = run_e2e(bench, max(20, args.steps // 20), 5)
