@@ -434,6 +434,58 @@ def run_e2e(bench: DecodeBench, steps: int, warmup: int) -> dict:
             "ms_per_step": secs * 1e3 / steps}
 
 
+def run_split_paths(dev) -> dict:
+    """A split product that clusters on this device, timed through bigemm_run
+    (one kernel: the cluster adds the segment partials in shared memory) and
+    through the explicit two-kernel path (partial kernel + reduction kernel);
+    both give the same bits.  Graphs of launches over a rotating weight pool
+    larger than L2, CUDA events around 50 replays."""
+    import deterministic_invariant_gemm_gb300 as dig
+    out = {}
+    for M, N, K, S in ((64, 3840, 4096, 8), (16, 2048, 4096, 8), (16, 4096, 4096, 4)):
+        pool = (2 * L2_BYTES) // (2 * K * N) + 1
+        A = workloads.normal_bf16((M, K), 1).to(dev)
+        Bs = [workloads.normal_bf16((K, N), 10 + j, 0.02).to(dev) for j in range(pool)]
+        C = torch.empty((M, N), device=dev)
+        need = dig.bigemm_partial_workspace_bytes(M, N, K, S)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        s_eff = dig.bigemm_effective_split_k(K, S)
+
+        def one_call():
+            for B in Bs:
+                dig.bigemm_run(A, B, C, M, N, K, K, N, N, S, ws, need)
+
+        def two_kernels():
+            for B in Bs:
+                dig.bigemm_run_partial(A, B, M, N, K, K, N, S, ws, need)
+                dig.bigemm_splitk_reduce(ws, s_eff, M, N, C, N, 0)
+
+        res = {"path": {0: "unsplit", 1: "workspace", 2: "folded", 3: "cluster"}.get(
+            dig.bigemm_split_path(M, N, K, S), "?"), "weights": pool}
+        for name, fn in (("bigemm_run_us", one_call), ("two_kernel_us", two_kernels)):
+            s = torch.cuda.Stream(device=dev)
+            s.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                fn()
+            torch.cuda.current_stream().wait_stream(s)
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(50):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            res[name] = round(e0.elapsed_time(e1) * 1e3 / (50 * pool), 3)
+        out["M%d_N%d_K%d_S%d" % (M, N, K, S)] = res
+        del Bs
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_decode_linear(dev, args) -> dict:
     """The headline step as linear layers (bigemm_linear, weights [N, K] plus a
     bias), timed the same way."""
@@ -786,6 +838,7 @@ def main():
         line["e2e"] = run_e2e(bench, max(20, args.steps // 20), 5)
         line["workloads"] = run_other_workloads(dev, peaks)
         line["workloads"]["decode_linear"] = run_decode_linear(dev, args)
+        line["workloads"]["split_paths"] = run_split_paths(dev)
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -35,7 +35,8 @@ __all__ = [
     "bigemm_run_bf16out", "bigemm_run_partial", "bigemm_splitk_reduce",
     "bigemm_run_atomic_splitk", "bigemm_device_status", "bigemm_last_launch_count",
     "bigemm_run_splitk_static", "bigemm_linear", "bigemm_fp8_effective_split_k",
-    "bigemm_fp8_workspace_bytes", "bigemm_linear_fp8", "bigemm_split_is_folded", "FP8_E4M3",
+    "bigemm_fp8_workspace_bytes", "bigemm_linear_fp8", "bigemm_split_is_folded", "bigemm_split_path",
+    "bigemm_cluster_capacity", "PATH_UNSPLIT", "PATH_WORKSPACE", "PATH_FOLDED", "PATH_CLUSTER", "FP8_E4M3",
     "FP8_E5M2", "FOLD_MIN_ROWS", "FOLD_MIN_TILES",
     "STATIC_SCRATCH_BYTES", "matmul", "linear", "linear_fp8", "EXPORTED_SYMBOLS",
 ]
@@ -64,7 +65,7 @@ EXPORTED_SYMBOLS = (
     "bigemm_splitk_reduce", "bigemm_run_atomic_splitk", "bigemm_device_status",
     "bigemm_last_launch_count", "bigemm_run_splitk_static", "bigemm_linear",
     "bigemm_fp8_effective_split_k", "bigemm_fp8_workspace_bytes", "bigemm_linear_fp8",
-    "bigemm_split_is_folded",
+    "bigemm_split_is_folded", "bigemm_split_path", "bigemm_cluster_capacity",
 )
 
 FP8_E4M3 = 0
@@ -104,6 +105,8 @@ def load():
         "bigemm_workspace_ld": ([i64], i64),
         "bigemm_workspace_bytes": ([i64, i64, i64, i32], sz),
         "bigemm_split_is_folded": ([i64, i64, i64, i32], i32),
+        "bigemm_split_path": ([i64, i64, i64, i32, i32], i32),
+        "bigemm_cluster_capacity": ([i32], i32),
         "bigemm_partial_workspace_bytes": ([i64, i64, i64, i32], sz),
         "bigemm_run": ([vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, vp, sz, vp], i32),
         "bigemm_run_bf16out": ([vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, vp, sz, vp], i32),
@@ -189,6 +192,19 @@ def bigemm_workspace_bytes(M: int, N: int, K: int, split_k: int) -> int:
 
 def bigemm_split_is_folded(M: int, N: int, K: int, split_k: int) -> bool:
     return bool(load().bigemm_split_is_folded(M, N, K, split_k))
+
+
+PATH_UNSPLIT, PATH_WORKSPACE, PATH_FOLDED, PATH_CLUSTER = 0, 1, 2, 3
+
+
+def bigemm_cluster_capacity(splits: int) -> int:
+    return int(load().bigemm_cluster_capacity(splits))
+
+
+def bigemm_split_path(M: int, N: int, K: int, split_k: int, fp8: bool = False) -> int:
+    """How a direct-output product of this shape runs on the current device:
+    PATH_UNSPLIT, PATH_WORKSPACE, PATH_FOLDED or PATH_CLUSTER (-1: invalid)."""
+    return int(load().bigemm_split_path(M, N, K, split_k, 1 if fp8 else 0))
 
 
 def bigemm_partial_workspace_bytes(M: int, N: int, K: int, split_k: int) -> int:

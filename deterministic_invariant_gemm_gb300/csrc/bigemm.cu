@@ -51,6 +51,8 @@ struct DeviceInfo {
     bool supported = false;
     int sm_count = 0;
     unsigned* status = nullptr;
+    // clusters of S GEMM CTAs that can be resident at once, S = 0..8 (0: none)
+    int max_clusters[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
 };
 
 constexpr int kMaxDevices = 64;
@@ -108,6 +110,29 @@ bigemm_status device_info(const DeviceInfo** out) {
             void* sym = nullptr;
             if (cudaGetSymbolAddress(&sym, g_device_status) != cudaSuccess) return BIGEMM_ERR_CUDA;
             d.status = static_cast<unsigned*>(sym);
+            // How many clusters of S one-CTA-per-SM GEMM blocks fit at once (all
+            // instantiations have the same block size, registers and shared
+            // memory).  A failed query leaves 0: that split never clusters.
+            for (int S = 2; S <= 8; ++S) {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(static_cast<unsigned>(S));
+                cfg.blockDim = dim3(kNumThreads);
+                cfg.dynamicSmemBytes = kSmemBytes;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                int n = 0;
+                if (cudaOccupancyMaxActiveClusters(
+                        &n, (const void*)bigemm_tc_kernel<kOutF32, false, false>, &cfg) != cudaSuccess) {
+                    (void)cudaGetLastError();
+                    n = 0;
+                }
+                d.max_clusters[S] = n;
+            }
         }
         d.ready = true;
     }
@@ -277,26 +302,41 @@ bool encode_out_slices(CUtensorMap* m, void* ws, int64_t M, int64_t N, int split
                         CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// A launch with programmatic stream serialisation, and with thread-block
+// clusters of `cluster_x` CTAs along x when cluster_x > 1.
 template <typename Kernel, typename... Args>
-cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                       Args... args) {
+cudaError_t launch_pdl_cluster(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                               unsigned cluster_x, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (cluster_x > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = cluster_x;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    return launch_pdl_cluster(kernel, grid, block, smem, stream, 1u, args...);
 }
 
 template <int kOut>
 cudaError_t launch_gemm(bool wt, bool fp8, dim3 g, dim3 blk, cudaStream_t stream,
                         const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBp,
-                        const CUtensorMap& tmC, const GemmParams& p) {
+                        const CUtensorMap& tmC, const GemmParams& p, unsigned cluster_x = 1) {
     if constexpr (kOut == kOutAtomic) {
         if (wt || fp8) return cudaErrorInvalidValue;  // the contrast exists for bf16 B [K, N] only
         return launch_pdl(bigemm_tc_kernel<kOut, false, false>, g, blk, kSmemBytes, stream, tmA, tmB,
@@ -304,14 +344,14 @@ cudaError_t launch_gemm(bool wt, bool fp8, dim3 g, dim3 blk, cudaStream_t stream
     } else {
         if (fp8) {
             if (!wt) return cudaErrorInvalidValue;
-            return launch_pdl(bigemm_tc_kernel<kOut, true, true>, g, blk, kSmemBytes, stream, tmA, tmB,
-                              tmBp, tmC, p);
+            return launch_pdl_cluster(bigemm_tc_kernel<kOut, true, true>, g, blk, kSmemBytes, stream,
+                                      cluster_x, tmA, tmB, tmBp, tmC, p);
         }
         if (wt)
-            return launch_pdl(bigemm_tc_kernel<kOut, true, false>, g, blk, kSmemBytes, stream, tmA, tmB,
-                              tmBp, tmC, p);
-        return launch_pdl(bigemm_tc_kernel<kOut, false, false>, g, blk, kSmemBytes, stream, tmA, tmB,
-                          tmBp, tmC, p);
+            return launch_pdl_cluster(bigemm_tc_kernel<kOut, true, false>, g, blk, kSmemBytes, stream,
+                                      cluster_x, tmA, tmB, tmBp, tmC, p);
+        return launch_pdl_cluster(bigemm_tc_kernel<kOut, false, false>, g, blk, kSmemBytes, stream,
+                                  cluster_x, tmA, tmB, tmBp, tmC, p);
     }
 }
 
@@ -390,6 +430,12 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     const DeviceInfo* d = nullptr;
     bigemm_status st = device_info(&d);
     if (st != BIGEMM_OK) return st;
+    // A split product that is not folded sums its segments inside clusters of
+    // `splits` CTAs when all of its clusters can be resident at once (one
+    // wave); otherwise through the workspace and the reduction kernel.  Same
+    // bits either way; the workspace is required in both cases.
+    const bool cluster = direct && !fold && splits >= 2 && splits <= 8 && K > 0 &&
+                         m_tiles * n_tiles <= d->max_clusters[splits];
 
     // ---- K == 0: the empty sum is +0.0 everywhere (plus the bias, if any)
     if (K == 0 && bias != nullptr) {
@@ -433,16 +479,19 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     // B panels stay in L2), else 8.  It orders tiles only; no sum changes.
     p.group_m = (m_tiles * n_tiles >= 4 * static_cast<int64_t>(d->sm_count)) ? 16 : 8;
     p.fold = fold ? 1 : 0;
-    // the scale and the bias follow the full sum: in this kernel's epilogue
-    // unless a reduction kernel forms that sum
-    const bool sum_here = (splits == 1) || fold;
+    p.cluster = cluster ? 1 : 0;
+    // the scale and the bias follow the full sum: in this kernel unless a
+    // reduction kernel forms that sum
+    const bool sum_here = (splits == 1) || fold || cluster;
     p.bias = sum_here ? static_cast<const __nv_bfloat16*>(bias) : nullptr;
     p.scale = sum_here ? scale : 1.0f;
     p.idesc_fp8 = fp8 ? idesc_fp8_f32(kBM, kBN, static_cast<uint32_t>(fp8_fmt_a),
                                       static_cast<uint32_t>(fp8_fmt_b))
                       : 0u;
 
-    const int grid = static_cast<int>(units < d->sm_count ? units : d->sm_count);
+    // persistent (at most one CTA per SM), except with clusters: one unit per CTA
+    const int grid = cluster ? static_cast<int>(units)
+                             : static_cast<int>(units < d->sm_count ? units : d->sm_count);
     const dim3 g(static_cast<unsigned>(grid)), blk(kNumThreads);
     cudaError_t e = cudaSuccess;
     int launches = 0;
@@ -455,7 +504,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
         p.ld_out = ldc;
         e = launch_gemm<kOutAtomic>(wt, fp8, g, blk, stream, tmA, tmB, tmBp, tmC, p);
         launches = 1;
-    } else if (mode == kModePartial || (splits > 1 && !fold)) {
+    } else if (mode == kModePartial || (splits > 1 && !fold && !cluster)) {
         p.out = ws;
         p.ld_out = ws_ld_of(N);
         p.slice_stride = M * p.ld_out;
@@ -481,14 +530,16 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
                 p.grouped = 1;
             else if (!encode_out_bf16(&tmC, C, M, N, ldc))
                 return BIGEMM_ERR_CUDA;
-            e = launch_gemm<kOutBF16>(wt, fp8, g, blk, stream, tmA, tmB, tmBp, tmC, p);
+            e = launch_gemm<kOutBF16>(wt, fp8, g, blk, stream, tmA, tmB, tmBp, tmC, p,
+                                      cluster ? static_cast<unsigned>(splits) : 1u);
         } else {
             if (encode_out_grouped(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, M, N, ldc, 0, 0,
                                    p.epi_batch))
                 p.grouped = 1;
             else if (!encode_out_f32(&tmC, C, M, N, ldc))
                 return BIGEMM_ERR_CUDA;
-            e = launch_gemm<kOutF32>(wt, fp8, g, blk, stream, tmA, tmB, tmBp, tmC, p);
+            e = launch_gemm<kOutF32>(wt, fp8, g, blk, stream, tmA, tmB, tmBp, tmC, p,
+                                     cluster ? static_cast<unsigned>(splits) : 1u);
         }
         launches = 1;
     }
@@ -564,6 +615,25 @@ int64_t bigemm_workspace_ld(int64_t N) { return N < 0 ? 0 : ws_ld_of(N); }
 int bigemm_split_is_folded(int64_t M, int64_t N, int64_t K, int split_k) {
     if (M < 0 || N < 0) return 0;
     return folds(M, N, effective_split(K, split_k, nullptr)) ? 1 : 0;
+}
+
+int bigemm_cluster_capacity(int splits) {
+    if (splits < 2 || splits > 8) return 0;
+    const DeviceInfo* d = nullptr;
+    if (device_info(&d) != BIGEMM_OK) return -1;
+    return d->max_clusters[splits];
+}
+
+int bigemm_split_path(int64_t M, int64_t N, int64_t K, int split_k, int fp8) {
+    if (M < 0 || N < 0 || K < 0) return -1;
+    const int s = effective_split(K, split_k, nullptr, fp8 ? 128 : kBK);
+    if (s == 0) return -1;
+    if (s == 1 || K == 0) return BIGEMM_PATH_UNSPLIT;
+    if (folds(M, N, s)) return BIGEMM_PATH_FOLDED;
+    const DeviceInfo* d = nullptr;
+    if (device_info(&d) != BIGEMM_OK) return -1;
+    if (s <= 8 && ceil_div(M, kBM) * ceil_div(N, kBN) <= d->max_clusters[s]) return BIGEMM_PATH_CLUSTER;
+    return BIGEMM_PATH_WORKSPACE;
 }
 
 size_t bigemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {

@@ -141,17 +141,28 @@ struct GemmParams {
     uint32_t idesc_fp8;     // instruction descriptor of the 8-bit float product
     int fold;               // 1: a unit is a whole tile whose `splits` K segments are
                             //    summed in the CTA (splits > 1, direct output)
+    int cluster;            // 1: clusters of `splits` CTAs, one per K segment of a tile,
+                            //    sum their partials through distributed shared memory
+                            //    (splits in 2..8, direct output, one unit per CTA)
 };
 
 // Unit u -> (tile row, tile column, K segment).  All tiles of segment 0 come
 // first, then segment 1, ...; inside a segment the tiles follow the GROUP_M
-// swizzle: groups of p.group_m tile rows, column-major inside a group.  The
-// order decides only which CTA computes a tile, never how a sum is formed.
+// swizzle: groups of p.group_m tile rows, column-major inside a group.  With
+// clusters the segments of one tile are consecutive instead (a cluster is
+// consecutive CTAs).  The order decides only which CTA computes a tile, never
+// how a sum is formed.
 __device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& mt, int& nt,
                                             int& seg) {
     const int tiles = p.m_tiles * p.n_tiles;
-    seg = u / tiles;
-    const int tile = u - seg * tiles;
+    int tile;
+    if (p.cluster) {
+        tile = u / p.splits;
+        seg = u - tile * p.splits;
+    } else {
+        seg = u / tiles;
+        tile = u - seg * tiles;
+    }
     const int per_group = p.group_m * p.n_tiles;
     const int g = tile / per_group;
     const int first_m = g * p.group_m;
@@ -341,6 +352,83 @@ __device__ __forceinline__ void emit_blocks(const GemmParams& p, const CUtensorM
                 bulk_commit_group();
             }
             ++nbat;
+        }
+    }
+}
+
+// The in-cluster split-K sum of one tile.  CTA rank s of the cluster holds
+// the FP32 partial of K segment s (layout: row r at r * 1 KiB, 16-byte chunk c
+// at c ^ (r % 8)).  The tile's valid rows x 64 chunks are dealt to the ranks
+// in equal contiguous shares; for each chunk: acc = w_0, then acc = acc + w_s
+// for s = 1 .. splits-1 (FP32, round to nearest even), then acc * scale and
+// acc + bias -- splitk_reduce_kernel's arithmetic in its order, so the bits
+// equal the workspace path's.  `e` is the thread's index among the 256
+// epilogue threads.
+template <int kOut>
+__device__ __forceinline__ void cluster_reduce(const GemmParams& p, uint32_t part_base, int e) {
+    int mt, nt, seg;
+    unit_coords(p, blockIdx.x, mt, nt, seg);
+    const int m0 = mt * kBM, n0 = nt * kBN;
+    const int rows = min(kBM, p.M - m0);
+    const int items = rows * (kBN / 4);
+    const int S = p.splits;
+    const int per = (items + S - 1) / S;
+    const int lo = static_cast<int>(cluster_ctarank()) * per;
+    const int hi = min(items, lo + per);
+    uint32_t src[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) src[s] = s < S ? map_shared_rank(part_base, static_cast<uint32_t>(s)) : 0u;
+    for (int v = lo + e; v < hi; v += kEpilogueThreads) {
+        const int row = v >> 6, c = v & 63;
+        const int col = n0 + c * 4;
+        if (col >= p.N) continue;
+        const uint32_t off = static_cast<uint32_t>(row) * 1024u +
+                             ((static_cast<uint32_t>(c) ^ (static_cast<uint32_t>(row) & 7u)) << 4);
+        float4 w[8];
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            if (s < S) w[s] = ld_shared_cluster_f32x4(src[s] + off);
+        float4 acc = w[0];
+#pragma unroll
+        for (int s = 1; s < 8; ++s) {
+            if (s < S) {
+                acc.x = __fadd_rn(acc.x, w[s].x);
+                acc.y = __fadd_rn(acc.y, w[s].y);
+                acc.z = __fadd_rn(acc.z, w[s].z);
+                acc.w = __fadd_rn(acc.w, w[s].w);
+            }
+        }
+        const int valid = min(4, p.N - col);
+        if (p.scale != 1.0f) {
+            acc.x = __fmul_rn(acc.x, p.scale);
+            acc.y = __fmul_rn(acc.y, p.scale);
+            acc.z = __fmul_rn(acc.z, p.scale);
+            acc.w = __fmul_rn(acc.w, p.scale);
+        }
+        if (p.bias != nullptr) {
+            float* a = &acc.x;
+            for (int k = 0; k < valid; ++k) a[k] = __fadd_rn(a[k], __bfloat162float(p.bias[col + k]));
+        }
+        const int64_t grow = m0 + row;
+        if constexpr (kOut == kOutBF16) {
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + grow * p.ld_out + col;
+            if (valid == 4) {
+                __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y);
+                __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z, acc.w);
+                *reinterpret_cast<uint2*>(dst) =
+                    make_uint2(*reinterpret_cast<uint32_t*>(&lo2), *reinterpret_cast<uint32_t*>(&hi2));
+            } else {
+                const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+                for (int k = 0; k < valid; ++k) dst[k] = __float2bfloat16_rn(a[k]);
+            }
+        } else {
+            float* dst = static_cast<float*>(p.out) + grow * p.ld_out + col;
+            if (valid == 4) {
+                *reinterpret_cast<float4*>(dst) = acc;
+            } else {
+                const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+                for (int k = 0; k < valid; ++k) dst[k] = a[k];
+            }
         }
     }
 }
@@ -556,6 +644,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             wait_bounded(drain_bar, 0, abort_flag, p.status, kErrWaitDrain, /*honour_abort=*/false);
         }
       }
+      // The cluster's two barriers (see the epilogue): every thread of every
+      // CTA passes both, on every path.
+      if constexpr (kOut == kOutF32 || kOut == kOutBF16) {
+          if (p.cluster) {
+              cluster_arrive_release();
+              cluster_wait_acquire();
+              cluster_arrive_release();
+              cluster_wait_acquire();
+          }
+      }
     } else {
         regs_grow_to<kEpilogueRegs>();
         // ------------------------------------------------------ epilogue --
@@ -584,7 +682,51 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         int t = 0;          // accumulators drained so far (one per segment)
         bool folded = false;
         if constexpr (kOut == kOutF32 || kOut == kOutBF16) {
-            if (p.fold) {
+            if (p.cluster) {
+                // ---- one K segment of a clustered tile: the FP32 partial goes
+                // to this CTA's shared memory (the pipeline stages, idle once
+                // the last MMA has completed), row r of the tile at r * 1 KiB,
+                // its 16-byte chunk c at c ^ (r % 8).
+                folded = true;
+                if (static_cast<int>(blockIdx.x) < p.units) {
+                    int mt, nt, seg;
+                    unit_coords(p, blockIdx.x, mt, nt, seg);
+                    if (wait_bounded(tfull_bar(0), 0, abort_flag, p.status, kErrWaitEpilogue)) {
+                        tc_fence_after();
+                        // the tensor core's reads of the stages are complete
+                        fence_proxy_async_smem();
+                        if (mt * kBM + q * 32 < p.M) {
+                            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+                            const uint32_t row = static_cast<uint32_t>(q * 32 + lane);
+                            const uint32_t prow = sA + row * 1024u;
+#pragma unroll 1
+                            for (int i = 0; i < 4; ++i) {
+                                uint32_t r[32];
+                                tmem_ld_32x32b_x32(tbase + (h * 4 + i) * 32, r);
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    const uint32_t c = static_cast<uint32_t>(h * 32 + i * 8 + j);
+                                    st_shared_v4(prow + ((c ^ (row & 7u)) << 4), r[4 * j], r[4 * j + 1],
+                                                 r[4 * j + 2], r[4 * j + 3]);
+                                }
+                            }
+                        }
+                        tc_fence_before();
+                        mbar_arrive(tempty_bar(0));
+                    }
+                }
+                // The first barrier publishes the partials to the cluster; the
+                // second keeps each CTA's shared memory alive until the others
+                // have read it.  Every thread of every CTA of the cluster
+                // passes both, on every path (the first warpgroup included).
+                cluster_arrive_release();
+                cluster_wait_acquire();
+                if (static_cast<int>(blockIdx.x) < p.units)
+                    cluster_reduce<kOut>(p, sA, static_cast<int>(threadIdx.x) - kEpilogueWarp0 * 32);
+                cluster_arrive_release();
+                cluster_wait_acquire();
+            } else if (p.fold) {
                 // ---- folded tiles: sum = w_0, then sum = sum + w_s for s = 1 ..
                 // splits-1 (FP32, round to nearest even) -- the additions
                 // splitk_reduce_kernel makes, in the same order, on the same

@@ -19,8 +19,11 @@
  *     kernel) -- no atomics.  A product large enough to fill the GPU with
  *     whole tiles (bigemm_split_is_folded) instead has the CTA that owns a
  *     tile compute its S segment partials one after another and add them in
- *     the same order with the same FP32 additions: the same bits, with no
- *     workspace and no second kernel;
+ *     the same order with the same FP32 additions; a smaller one (S <= 8)
+ *     may have the S CTAs of a thread-block cluster compute one segment each
+ *     and add the partials through distributed shared memory, again in that
+ *     order with those additions (bigemm_split_path).  The same bits every
+ *     way, with no workspace traffic and no second kernel;
  *   - the M and N tile sizes and the order in which tiles run (a GROUP_M
  *     swizzle, "GROUP_M - Swizzle L2 Cache") change no sum.
  * So row i of C is bit-for-bit a function of (row i of A, B, K, split_k,
@@ -146,10 +149,37 @@ BIGEMM_API int64_t bigemm_workspace_ld(int64_t N);
  * invalid arguments or an effective split of 1. */
 BIGEMM_API int bigemm_split_is_folded(int64_t M, int64_t N, int64_t K, int split_k);
 
+/* How bigemm_run, bigemm_run_bf16out, bigemm_linear (fp8 = 0) or
+ * bigemm_linear_fp8 (fp8 = 1) execute a product of this shape on the current
+ * device -- a matter of speed only, every way forms each sum identically:
+ *   BIGEMM_PATH_UNSPLIT    effective split 1 (or K = 0): one kernel;
+ *   BIGEMM_PATH_WORKSPACE  partial kernel into the workspace, then
+ *                          splitk_reduce_kernel (two kernels);
+ *   BIGEMM_PATH_FOLDED     segments summed inside the CTA (one kernel);
+ *   BIGEMM_PATH_CLUSTER    effective split S in 2..8 and every tile's cluster
+ *                          of S CTAs resident at once: each CTA computes one
+ *                          segment and the cluster adds the partials through
+ *                          distributed shared memory in the order 0..S-1
+ *                          (one kernel).
+ * -1 for invalid arguments or when the device cannot be queried. */
+/* Number of clusters of `splits` GEMM CTAs (one CTA per SM) the current
+ * device can hold at once, as the CUDA occupancy calculator reports it; a
+ * product clusters when its tiles are no more than this.  0 for splits
+ * outside 2..8, -1 when the device cannot be queried. */
+BIGEMM_API int bigemm_cluster_capacity(int splits);
+
+#define BIGEMM_PATH_UNSPLIT 0
+#define BIGEMM_PATH_WORKSPACE 1
+#define BIGEMM_PATH_FOLDED 2
+#define BIGEMM_PATH_CLUSTER 3
+BIGEMM_API int bigemm_split_path(int64_t M, int64_t N, int64_t K, int split_k, int fp8);
+
 /* Workspace bytes bigemm_run / bigemm_run_bf16out / bigemm_linear need for
  * (M, N, K, split_k): effective_split * M * bigemm_workspace_ld(N) * 4 when
  * the effective split is > 1 and the product is not folded
- * (bigemm_split_is_folded), else 0.  Returns 0 for invalid arguments too. */
+ * (bigemm_split_is_folded), else 0.  A function of the shape alone: the
+ * workspace is required even when the product then runs on the cluster path,
+ * which leaves it untouched.  Returns 0 for invalid arguments too. */
 BIGEMM_API size_t bigemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
 
 /* Workspace bytes bigemm_run_partial needs: effective_split * M *

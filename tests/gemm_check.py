@@ -138,3 +138,11 @@ def bits_equal(x: torch.Tensor, y: torch.Tensor) -> bool:
 
 def log2_ceil(x: int) -> int:
     return int(math.ceil(math.log2(x)))
+
+
+def expected_launches(M: int, N: int, K: int, split_k: int, fp8: bool = False) -> int:
+    """Kernels bigemm_run (or a linear entry point) launches for this shape on
+    the current device: 2 on the workspace path (partial + reduction), else 1."""
+    path = dig.bigemm_split_path(M, N, K, split_k, fp8)
+    assert path >= 0
+    return 2 if path == dig.PATH_WORKSPACE else 1

@@ -15,7 +15,7 @@ import torch
 import deterministic_invariant_gemm_gb300 as dig
 import oracle
 import workloads
-from gemm_check import (bits_equal, canary_intact, check_tolerance, device_matrix,
+from gemm_check import (bits_equal, canary_intact, check_tolerance, device_matrix, expected_launches,
                         oracle_rows, round_up, run_gemm, sample_rows, to_f64)
 
 pytestmark = pytest.mark.gpu
@@ -115,7 +115,7 @@ def test_matmul_wrapper_and_launch_count(cuda_device):
     Cref, D = oracle_rows(A, B, M, N, K)
     Ad, Bd = A.cuda(), B.cuda()
     C = dig.matmul(Ad, Bd, split_k=4)
-    assert dig.bigemm_last_launch_count() == 2          # partial + reduction
+    assert dig.bigemm_last_launch_count() == expected_launches(M, N, K, 4)
     C1 = dig.matmul(Ad, Bd, split_k=1)
     assert dig.bigemm_last_launch_count() == 1
     torch.cuda.synchronize()

@@ -39,7 +39,9 @@ def _device_pair(M, N, K, seed):
 def test_static_scratch_matches_workspace_entry_point(cuda_device, order):
     # Two calls in a row with different shapes and splits; the second finds
     # the first call's partials in the shared array.
-    cases = [(16, 4096, 4096, 8, 21), (64, 1000, 3000, 5, 22)]
+    # splits above 8 always take the workspace path (partial + reduction), so
+    # the array is really used
+    cases = [(16, 4096, 8192, 16, 21), (64, 1000, 3000, 12, 22)]
     for M, N, K, S, seed in cases:
         assert 0 < dig.bigemm_workspace_bytes(M, N, K, S) <= dig.STATIC_SCRATCH_BYTES
         A, B, Ad, Bd, lda, ldb = _device_pair(M, N, K, seed)
