@@ -22,6 +22,10 @@ passage of the pages it follows in ``oracle.c``'s header:
 * :func:`linear_rows` -- a linear layer, C = A W^T + b (same article, "vLLM に
   おける GEMM の Batch Invariance サポート": linear_batch_invariant(x, weight,
   bias)).
+* :func:`ozaki_rho`, :func:`ozaki_split`, :func:`ozaki_pairs`,
+  :func:`ozaki_gemm` -- the Ozaki scheme's binary64 product from bfloat16
+  slices (cuTile article, "倍精度行列積エミュレーション": the Veltkamp split of
+  eqs. (1)-(5), the slice-pair products of eqs. (10)-(11), Fast Mode's d).
 
 Pins (tests/test_oracle.py) tie each function to something other than itself:
 identity and permutation products, small-integer products checked against
@@ -104,6 +108,16 @@ def _load():
     lib.oracle_encode_rne_array.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
+    lib.oracle_ozaki_rho.argtypes = [i64]
+    lib.oracle_ozaki_rho.restype = ctypes.c_int
+    lib.oracle_ozaki_pairs.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.oracle_ozaki_pairs.restype = i64
+    lib.oracle_ozaki_split.argtypes = [vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       vp, vp, vp]
+    lib.oracle_ozaki_split.restype = ctypes.c_int
+    lib.oracle_ozaki_gemm.argtypes = [vp, vp, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, vp, i64, vp]
+    lib.oracle_ozaki_gemm.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -271,3 +285,68 @@ def splitk_reduce_f32(W: np.ndarray) -> np.ndarray:
 def bf16_round(x) -> np.ndarray:
     """Round binary64 values to bfloat16 (ties to even); returns binary64 values."""
     return decode(FMT_BF16, encode_rne(FMT_BF16, x))
+
+
+# --------------------------------------------------------------- Ozaki --
+
+OZ_M1, OZ_M2, OZ_M3 = 53, 8, 24      # binary64, bfloat16, binary32 significand bits
+
+
+def ozaki_rho(k: int) -> int:
+    """rho = max(ceil(m1 - (m3 - log2 k) / 2), m1 - m2) for inner length k."""
+    return int(_load().oracle_ozaki_rho(int(k)))
+
+
+def ozaki_default_slices(rho: int) -> int:
+    """Slices whose bits reach 2^-53 below a vector's maximum: with beta =
+    m1 - rho bits in the first slice and beta + 1 in each later one,
+    s (beta + 1) - 1 >= m1."""
+    beta = OZ_M1 - rho
+    return -(-(OZ_M1 + 1) // (beta + 1))
+
+
+def ozaki_pairs(slices: int, d: int) -> int:
+    """Slice pairs (p, q) kept by Fast Mode: 0 <= p, q < slices, p + q < d."""
+    return int(_load().oracle_ozaki_pairs(int(slices), int(d)))
+
+
+def _f64(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def ozaki_split(X, axis: int, rho: int, slices: int):
+    """Split the rows (axis 0) or columns (axis 1) of X into bfloat16 slices.
+    Returns (S [slices, rows, cols] float64 slice values, c1 int32 per vector,
+    R [rows, cols] the residual after the last slice)."""
+    x = _f64(X)
+    rows, cols = x.shape
+    S = np.empty((slices, rows, cols), dtype=np.float64)
+    c1 = np.empty(rows if axis == 0 else cols, dtype=np.int32)
+    R = np.empty((rows, cols), dtype=np.float64)
+    st = _load().oracle_ozaki_split(_ptr(x), rows, cols, cols, axis, rho, slices, _ptr(S), _ptr(c1),
+                                    _ptr(R))
+    if st != 0:
+        raise ValueError("oracle_ozaki_split failed")
+    return S, c1, R
+
+
+def ozaki_gemm(A, B, rho: int | None = None, slices: int | None = None, d: int | None = None):
+    """C = A B (binary64) by the Ozaki scheme; returns (C, inexact) where
+    inexact counts slice-pair sums that a binary32 accumulation could round
+    (0 when rho fits K)."""
+    a, b = _f64(A), _f64(B)
+    M, K = a.shape
+    K2, N = b.shape
+    assert K == K2
+    rho = ozaki_rho(max(K, 1)) if rho is None else rho
+    slices = ozaki_default_slices(rho) if slices is None else slices
+    d = slices if d is None else d
+    C = np.empty((M, N), dtype=np.float64)
+    bad = np.zeros(1, dtype=np.int64)
+    st = _load().oracle_ozaki_gemm(_ptr(a), _ptr(b), M, N, K, K, N, rho, slices, d, _ptr(C), N,
+                                   _ptr(bad))
+    if st != 0:
+        raise ValueError("oracle_ozaki_gemm failed")
+    return C, int(bad[0])

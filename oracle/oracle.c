@@ -36,6 +36,13 @@
  *                         "Split-K" section: out = w_0, then out = out + w_s for
  *                         s = 1 .. S-1, every addition rounded to binary32
  *                         (round to nearest even), in that serial order.
+ *   oracle_ozaki_rho, oracle_ozaki_split, oracle_ozaki_pairs,
+ *   oracle_ozaki_gemm     the Ozaki scheme of the cuTile article (section
+ *                         "倍精度行列積エミュレーション"): a binary64 matrix product
+ *                         from bfloat16 slices -- the Veltkamp split, eqs.
+ *                         (1)-(5); slice-pair products, eqs. (10)-(11); the
+ *                         binary64 outer accumulation; Fast Mode's skip of the
+ *                         pairs with p + q >= d.
  *
  * Build: a C99 compiler with -O2 -ffp-contract=off (no fused multiply-add, no
  * fast-math); OpenMP is optional and only splits the rows between threads --
@@ -271,6 +278,206 @@ int oracle_linear8_rows(const uint8_t *A, const uint8_t *W, int fmt_a, int fmt_b
         }
     }
     return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Ozaki scheme (cuTile article, "倍精度行列積エミュレーション": "Ozaki Scheme   */
+/* について", "分解(Split)", "行列積の計算", "Fast Mode（GEMMの削減）",            */
+/* "Fused Split Kernel（分割の融合）").                                        */
+/*                                                                          */
+/* Type1 = binary64 (m1 = 53 significand bits), Type2 = bfloat16 (m2 = 8),  */
+/* Type3 = binary32 (m3 = 24), all counting the hidden bit.                 */
+/* ------------------------------------------------------------------------ */
+
+#define OZ_M1 53
+#define OZ_M2 8
+#define OZ_M3 24
+
+/* The precision parameter rho = max(gamma, xi) of "分解(Split)":
+ * gamma = ceil(m1 - (m3 - log2 k) / 2) and xi = m1 - m2, k the inner-product
+ * length.  gamma = ceil(41 + log2(k) / 2) = 41 + t, t the least integer with
+ * 4^t >= k -- evaluated in integers, with no logarithm to round.
+ * Returns -1 for k < 1. */
+int oracle_ozaki_rho(int64_t k) {
+    if (k < 1) return -1;
+    int t = 0;
+    int64_t p = 1;
+    while (p < k) {
+        p *= 4;
+        ++t;
+    }
+    const int gamma = (OZ_M1 - OZ_M3 / 2) + t;
+    const int xi = OZ_M1 - OZ_M2;
+    return gamma > xi ? gamma : xi;
+}
+
+/* Number of slice pairs (p, q), 0 <= p, q < slices, that Fast Mode keeps:
+ * those with p + q < d. */
+int64_t oracle_ozaki_pairs(int slices, int d) {
+    int64_t n = 0;
+    for (int p = 0; p < slices; ++p)
+        for (int q = 0; q < slices; ++q)
+            if (p + q < d) ++n;
+    return n;
+}
+
+/* c = ceil(log2 m) for m > 0, exactly: m = f * 2^e with f in [0.5, 1). */
+static int oz_ceil_log2(double m) {
+    int e = 0;
+    const double f = frexp(m, &e);
+    return f == 0.5 ? e - 1 : e;
+}
+
+/*
+ * The split of one vector x (n values at stride inc) into `slices` bfloat16
+ * slices, eqs. (1)-(5):
+ *   c^(1)   = ceil(log2 max_i |x_i|)                                     (1)
+ *   sigma   = 0.75 * 2^(rho + c^(p))                                     (2)
+ *   v_i     = fl((x_i^(p) + sigma) - sigma)                              (3)
+ *   x^(p+1) = fl(x^(p) - v)                                              (4)
+ *   xbar^(p)= cvt_bf16(fl(2^(-c^(p)) * v))                               (5)
+ * The fused split computes every slice's exponent from the first maximum;
+ * the one it uses here is the bound eq. (3) gives on the residual:
+ * |x^(p+1)| <= ulp(sigma) / 2 = 2^(c^(p) - (m1 - rho) - 1), so
+ *   c^(p+1) = c^(p) - (m1 - rho) - 1.
+ * Every v is then a multiple of 2^(rho + c^(p) - m1) no larger than
+ * 2^(c^(p)), so xbar^(p) has at most m1 - rho <= m2 significant bits and the
+ * conversion to bfloat16 is exact; it is checked here (a failed check
+ * returns -1).  out[p * p_stride + i * out_inc] = value of xbar^(p)_i,
+ * *c1 = c^(1) (0 for an all-zero vector, whose slices are all zero), and
+ * res[i * out_inc] = x^(slices+1)_i when res is not NULL.
+ */
+static int oz_split_vector(const double *x, int64_t n, int64_t inc, int rho, int slices,
+                           double *out, int64_t p_stride, int64_t out_inc, int *c1, double *res) {
+    double m = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        const double a = fabs(x[i * inc]);
+        if (a > m) m = a;
+    }
+    if (m == 0.0) {
+        *c1 = 0;
+        for (int p = 0; p < slices; ++p)
+            for (int64_t i = 0; i < n; ++i) out[p * p_stride + i * out_inc] = 0.0;
+        if (res)
+            for (int64_t i = 0; i < n; ++i) res[i * out_inc] = 0.0;
+        return 0;
+    }
+    const int beta = OZ_M1 - rho;
+    *c1 = oz_ceil_log2(m);
+    for (int64_t i = 0; i < n; ++i) {
+        double r = x[i * inc];                         /* x^(1) */
+        int c = *c1;
+        for (int p = 0; p < slices; ++p) {
+            const double sigma = ldexp(0.75, rho + c);  /* (2) */
+            const double t = r + sigma;
+            const double v = t - sigma;                 /* (3) */
+            r = r - v;                                  /* (4) */
+            const double xb = ldexp(v, -c);             /* (5), before the conversion */
+            if (g_bf16_value[oracle_encode_rne(ORACLE_FMT_BF16, xb)] != xb) return -1;
+            out[p * p_stride + i * out_inc] = xb;
+            c = c - beta - 1;
+        }
+        if (res) res[i * out_inc] = r;
+    }
+    return 0;
+}
+
+/*
+ * Split every row (axis 0, the vectors of A in A B) or every column (axis 1,
+ * the vectors of B) of X [rows][cols] (leading dimension ld) into `slices`
+ * bfloat16 slices.  S: [slices][rows][cols] dense, the slice values; c1: one
+ * c^(1) per vector (rows entries for axis 0, cols for axis 1); R: the final
+ * residual [rows][cols] dense, or NULL.  Returns 0, or -1 on a bad argument
+ * or an inexact conversion.
+ */
+int oracle_ozaki_split(const double *X, int64_t rows, int64_t cols, int64_t ld, int axis,
+                       int rho, int slices, double *S, int *c1, double *R) {
+    if (rows < 0 || cols < 0 || ld < cols || slices < 1 || rho < OZ_M1 - OZ_M2 || rho >= OZ_M1)
+        return -1;
+    if (axis != 0 && axis != 1) return -1;
+    bf16_table_init();
+    const int64_t plane = rows * cols;
+    int bad = 0;
+    if (axis == 0) {
+        for (int64_t i = 0; i < rows; ++i)
+            if (oz_split_vector(X + i * ld, cols, 1, rho, slices, S + i * cols, plane, 1, c1 + i,
+                                R ? R + i * cols : NULL))
+                bad = 1;
+    } else {
+        for (int64_t j = 0; j < cols; ++j)
+            if (oz_split_vector(X + j, rows, ld, rho, slices, S + j, plane, cols, c1 + j,
+                                R ? R + j : NULL))
+                bad = 1;
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * C = A B in the Ozaki scheme.  A: [M][lda], B: [K][ldb] binary64; C: [M][ldc].
+ * A is split by rows and B by columns (each row of A and column of B is one
+ * vector x, y of eq. (10)); then, for p = 0 .. slices-1 and, inside, q = 0 ..
+ * slices-1, skipping the pairs with p + q >= d (Fast Mode):
+ *   P = xbar^(p)T ybar^(q) = sum_k a_p[i][k] b_q[k][j]        (11), in binary64
+ *   C[i][j] = C[i][j] + 2^(c_a^(p)[i] + c_b^(q)[j]) * P        (10), binary64
+ * with C starting at +0.0.  P is exact: every term is a multiple of
+ * 2^(2 (rho - m1)); *inexact (when not NULL) counts the (pair, i, j) whose
+ * sum of |terms| exceeds 2^m3 such units, where a binary32 accumulation in
+ * some order could round -- rho is chosen so that this count is 0
+ * ("行列積の計算": no rounding error in the Type3 accumulation).  The scaling
+ * by a power of two is exact (inputs within the normal range), so each pair
+ * costs one binary64 rounding, in the addition.  Returns 0 or -1.
+ */
+int oracle_ozaki_gemm(const double *A, const double *B, int64_t M, int64_t N, int64_t K,
+                      int64_t lda, int64_t ldb, int rho, int slices, int d, double *C, int64_t ldc,
+                      int64_t *inexact) {
+    if (M < 0 || N < 0 || K < 0 || slices < 1 || d < 0) return -1;
+    if ((K > 0 && (lda < K || ldb < N)) || ldc < N) return -1;
+    if (rho < OZ_M1 - OZ_M2 || rho >= OZ_M1) return -1;
+    const int beta = OZ_M1 - rho;
+    double *Sa = (double *)malloc(sizeof(double) * (size_t)(slices * M * (K > 0 ? K : 1)));
+    double *Sb = (double *)malloc(sizeof(double) * (size_t)(slices * (K > 0 ? K : 1) * N));
+    int *ca = (int *)malloc(sizeof(int) * (size_t)(M > 0 ? M : 1));
+    int *cb = (int *)malloc(sizeof(int) * (size_t)(N > 0 ? N : 1));
+    int st = (Sa && Sb && ca && cb) ? 0 : -1;
+    if (st == 0 && K > 0) st = oracle_ozaki_split(A, M, K, lda, 0, rho, slices, Sa, ca, NULL);
+    if (st == 0 && K > 0) st = oracle_ozaki_split(B, K, N, ldb, 1, rho, slices, Sb, cb, NULL);
+    int64_t bad = 0;
+    if (st == 0) {
+        const double unit_bound = ldexp(1.0, OZ_M3 + 2 * (rho - OZ_M1));
+        for (int64_t i = 0; i < M; ++i)
+            for (int64_t j = 0; j < N; ++j) C[i * ldc + j] = 0.0;
+        if (K > 0) {
+            for (int p = 0; p < slices; ++p) {
+                for (int q = 0; q < slices; ++q) {
+                    if (p + q >= d) continue;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+#endif
+                    for (int64_t i = 0; i < M; ++i) {
+                        const double *ap = Sa + ((int64_t)p * M + i) * K;
+                        for (int64_t j = 0; j < N; ++j) {
+                            const double *bq = Sb + (int64_t)q * K * N + j;
+                            double P = 0.0, D = 0.0;
+                            for (int64_t k = 0; k < K; ++k) {
+                                const double t = ap[k] * bq[k * N];
+                                P = P + t;
+                                D = D + fabs(t);
+                            }
+                            if (D > unit_bound) ++bad;
+                            const int e = (ca[i] - p * (beta + 1)) + (cb[j] - q * (beta + 1));
+                            C[i * ldc + j] = C[i * ldc + j] + ldexp(P, e);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    if (inexact) *inexact = bad;
+    free(Sa);
+    free(Sb);
+    free(ca);
+    free(cb);
+    return st;
 }
 
 /* Batch helpers for the Python side: decode / encode whole arrays. */

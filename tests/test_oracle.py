@@ -420,3 +420,183 @@ def test_linear8_scale_bias_and_rational_brute_force():
             exact = Fraction(scale) * sum(terms, Fraction(0)) + Fraction(float(bb[j]))
             scl = Fraction(scale) * sum((abs(t) for t in terms), Fraction(0)) + abs(Fraction(float(bb[j])))
             assert abs(Fraction(C[i, j]) - exact) <= (K + 2) * u * scl
+
+
+# ------------------------------------------------------------ Ozaki scheme --
+# cuTile article, "倍精度行列積エミュレーション": eqs. (1)-(5) split each vector
+# into bfloat16 slices, eqs. (10)-(11) multiply slice pairs, Fast Mode skips the
+# pairs with p + q >= d.
+
+def test_ozaki_pair_counts_match_the_pages_table():
+    path = os.path.join(os.path.dirname(__file__), "golden", "ozaki_fast_mode_pairs.txt")
+    n = 0
+    for line in open(path, encoding="utf-8"):
+        if line.startswith("#") or not line.strip():
+            continue
+        s, d, want = (int(v) for v in line.split())
+        assert oracle.ozaki_pairs(s, d) == want, (s, d)
+        n += 1
+    assert n == 6
+
+
+def test_ozaki_rho_gives_the_widest_exact_slices():
+    """beta = m1 - rho is the widest bfloat16 slice for which K products of two
+    slices add up exactly in binary32 in any order: K * (2^beta)^2 <= 2^24,
+    and either beta = 8 (all of bfloat16) or one more bit would break it."""
+    for K in list(range(1, 70)) + [127, 128, 129, 255, 256, 257, 1000, 1024, 1025, 3000, 4096,
+                                   4097, 8192, 16384, 65536, 1 << 20]:
+        beta = 53 - oracle.ozaki_rho(K)
+        assert 1 <= beta <= 8, K
+        assert K * 4 ** beta <= 1 << 24, K
+        assert beta == 8 or K * 4 ** (beta + 1) > 1 << 24, K
+
+
+def _exact_sum(terms):
+    return sum((Fraction(t) for t in terms), Fraction(0))
+
+
+@pytest.mark.parametrize("axis", [0, 1])
+def test_ozaki_split_reconstructs_exactly(axis):
+    """Eq. (9) plus the residual: x = sum_p 2^(c^(p)) xbar^(p) + x^(s+1),
+    exactly, for vectors with values across many binades, zeros included."""
+    rng = np.random.default_rng(5 + axis)
+    X = rng.standard_normal((12, 40)) * np.exp2(rng.integers(-30, 30, (12, 40)))
+    X[3, :] = 0.0
+    X[:, 7] = 0.0
+    X[5, 9] = -0.0
+    rho = oracle.ozaki_rho(40)
+    beta = 53 - rho
+    for slices in (1, 3, 9):
+        S, c1, R = oracle.ozaki_split(X, axis, rho, slices)
+        rows, cols = X.shape
+        for i in range(rows):
+            for j in range(cols):
+                v = i if axis == 0 else j
+                total = _exact_sum([Fraction(S[p, i, j]) * Fraction(2) ** (int(c1[v]) - p * (beta + 1))
+                                    for p in range(slices)] + [R[i, j]])
+                assert total == Fraction(X[i, j]), (slices, i, j)
+
+
+def test_ozaki_slices_are_narrow_bfloat16_values():
+    """Each slice value is an integer multiple of 2^(rho - 53) of magnitude at
+    most 1: a bfloat16 value with at most beta = 53 - rho significant bits."""
+    rng = np.random.default_rng(11)
+    X = rng.standard_normal((20, 300)) * np.exp2(rng.integers(-8, 8, (20, 300)))
+    for K in (300, 5000):
+        rho = oracle.ozaki_rho(K)
+        beta = 53 - rho
+        S, c1, R = oracle.ozaki_split(X, 0, rho, 6)
+        n = S * 2.0 ** (53 - rho)
+        assert np.array_equal(n, np.round(n))
+        assert np.abs(n).max() <= 2 ** beta
+        assert np.abs(S).max() <= 1.0
+        # exactly representable in bfloat16: the oracle's own codec round trip
+        assert np.array_equal(oracle.decode(oracle.FMT_BF16, oracle.encode_rne(oracle.FMT_BF16, S)), S)
+
+
+def test_ozaki_first_slice_is_x_rounded_to_its_grid():
+    """Eq. (3) on the first slice is round-to-nearest-even of x to a multiple of
+    2^(c^(1) + rho - 53), the unit of sigma's last place (the Veltkamp split):
+    compared with numpy's half-to-even rounding."""
+    rng = np.random.default_rng(2)
+    X = rng.standard_normal((9, 64))
+    X[0, :4] = [0.5, -0.75, 1.0, 0.0]
+    # maxima that are exact powers of two: ceil(log2 m) = log2 m
+    X[6] = rng.uniform(-1.0, 1.0, 64)
+    X[6, 5] = 1.0
+    X[7] = rng.uniform(-0.25, 0.25, 64) * 2.0 ** -30
+    X[7, 9] = -(2.0 ** -30)
+    X[8] = rng.uniform(-1.0, 1.0, 64) * 2.0 ** 40
+    X[8, 0] = 2.0 ** 40
+    rho = oracle.ozaki_rho(64)
+    S, c1, R = oracle.ozaki_split(X, 0, rho, 1)
+    assert list(c1[6:]) == [0, -30, 40]
+    for i in range(9):
+        u = 2.0 ** (int(c1[i]) + rho - 53)
+        v = np.round(X[i] / u) * u
+        assert np.array_equal(S[0, i] * 2.0 ** int(c1[i]), v)
+        m = np.abs(X[i]).max()
+        assert 2.0 ** (int(c1[i]) - 1) < m <= 2.0 ** int(c1[i])     # eq. (1)
+
+
+def test_ozaki_zero_vectors_split_to_zero():
+    X = np.zeros((3, 5))
+    S, c1, R = oracle.ozaki_split(X, 1, 45, 4)
+    assert not S.any() and not c1.any() and not R.any()
+
+
+@pytest.mark.parametrize("M,N,K", [(9, 7, 31), (16, 40, 300)])
+def test_ozaki_gemm_small_integers_exact(M, N, K):
+    """Integer inputs up to 1000 in magnitude: every bit lands in a slice, every
+    slice-pair sum and every binary64 partial sum is an exact integer, so C is
+    the exact product."""
+    rng = np.random.default_rng(M + K)
+    A = rng.integers(-1000, 1001, (M, K)).astype(np.float64)
+    B = rng.integers(-1000, 1001, (K, N)).astype(np.float64)
+    C, inexact = oracle.ozaki_gemm(A, B)
+    assert inexact == 0
+    assert np.array_equal(C, (A.astype(np.int64) @ B.astype(np.int64)).astype(np.float64))
+
+
+def test_ozaki_single_pair_is_the_product_of_leading_slices():
+    """d = 1 keeps the pair (0, 0) alone: C = 2^(c_a + c_b) * (xbar_a^(1) . ybar_b^(1)),
+    eq. (10) with one term, computed here from the oracle's slices with numpy."""
+    rng = np.random.default_rng(4)
+    A = rng.standard_normal((10, 64))
+    B = rng.standard_normal((64, 12))
+    rho = oracle.ozaki_rho(64)
+    C, inexact = oracle.ozaki_gemm(A, B, rho=rho, slices=5, d=1)
+    Sa, ca, _ = oracle.ozaki_split(A, 0, rho, 5)
+    Sb, cb, _ = oracle.ozaki_split(B, 1, rho, 5)
+    P = Sa[0] @ Sb[0]                       # integer multiples of one unit, < 2^24 of them: exact
+    want = P * np.exp2(ca[:, None] + cb[None, :])
+    assert inexact == 0 and np.array_equal(C, want)
+
+
+def test_ozaki_gemm_accuracy_against_exact_products():
+    """Random normal and wide-range inputs, against exact rational products.
+    With the default slices and d the error is binary64's: at most 8 units of
+    2^-53 of sum_k |a_ik b_kj| (the outer additions) plus what the slices
+    leave out, K * 2^(c_a + c_b) * 2^-(s (beta + 1) - 3) -- each vector keeps
+    s (beta + 1) - 1 >= 53 bits below its own maximum 2^c (eq. (1) scales by
+    the vector's maximum, not the element's).  Fast Mode with a smaller d is
+    never more accurate."""
+    rng = np.random.default_rng(9)
+    M, N, K = 8, 9, 200
+    for A, B in (
+        (rng.standard_normal((M, K)), rng.standard_normal((K, N))),
+        (rng.standard_normal((M, K)) * np.exp2(rng.integers(-20, 20, (M, K))),
+         rng.standard_normal((K, N)) * np.exp2(rng.integers(-20, 20, (K, N)))),
+    ):
+        exact = [[sum((Fraction(A[i, k]) * Fraction(B[k, j]) for k in range(K)), Fraction(0))
+                  for j in range(N)] for i in range(M)]
+        scale = np.abs(A) @ np.abs(B)
+        errs = {}
+        rho = oracle.ozaki_rho(K)
+        beta = 53 - rho
+        s = oracle.ozaki_default_slices(rho)
+        _, ca, _ = oracle.ozaki_split(A, 0, rho, 1)
+        _, cb, _ = oracle.ozaki_split(B, 1, rho, 1)
+        left_out = K * np.exp2(ca[:, None] + cb[None, :] - (s * (beta + 1) - 3))
+        bound = 8 * 2.0 ** -53 * scale + left_out
+        for d in (s, s - 2, 3):
+            C, inexact = oracle.ozaki_gemm(A, B, rho=rho, slices=s, d=d)
+            assert inexact == 0
+            err = np.array([[abs(float(Fraction(C[i, j]) - exact[i][j])) for j in range(N)]
+                            for i in range(M)])
+            if d == s:
+                assert (err <= bound).all(), (err / bound).max()
+            errs[d] = (err / scale).max()
+        assert errs[s] <= errs[s - 2] <= errs[3], errs
+
+
+def test_ozaki_inexact_count_flags_too_wide_slices():
+    """With rho below the value K needs (full 8-bit slices at K = 4096), the
+    slice-pair sums can exceed 2^24 units, and the oracle counts them; with
+    rho(K) it counts none."""
+    rng = np.random.default_rng(3)
+    A = rng.uniform(0.5, 1.0, (4, 4096))
+    B = rng.uniform(0.5, 1.0, (4096, 4))
+    _, bad_wide = oracle.ozaki_gemm(A, B, rho=45, slices=7, d=7)
+    _, bad_rho = oracle.ozaki_gemm(A, B)
+    assert bad_wide > 0 and bad_rho == 0
