@@ -36,7 +36,9 @@ __all__ = [
     "bigemm_run_atomic_splitk", "bigemm_device_status", "bigemm_last_launch_count",
     "bigemm_run_splitk_static", "bigemm_linear", "bigemm_fp8_effective_split_k",
     "bigemm_fp8_workspace_bytes", "bigemm_linear_fp8", "bigemm_split_is_folded", "bigemm_split_path",
-    "bigemm_cluster_capacity", "PATH_UNSPLIT", "PATH_WORKSPACE", "PATH_FOLDED", "PATH_CLUSTER", "FP8_E4M3",
+    "bigemm_cluster_capacity", "bigemm_ozaki_rho", "bigemm_ozaki_default_slices",
+    "bigemm_ozaki_pairs", "bigemm_ozaki_workspace_bytes", "bigemm_ozaki_split", "bigemm_ozaki_dgemm",
+    "ozaki_matmul", "PATH_UNSPLIT", "PATH_WORKSPACE", "PATH_FOLDED", "PATH_CLUSTER", "FP8_E4M3",
     "FP8_E5M2", "FOLD_MIN_ROWS", "FOLD_MIN_TILES",
     "STATIC_SCRATCH_BYTES", "matmul", "linear", "linear_fp8", "EXPORTED_SYMBOLS",
 ]
@@ -66,6 +68,8 @@ EXPORTED_SYMBOLS = (
     "bigemm_last_launch_count", "bigemm_run_splitk_static", "bigemm_linear",
     "bigemm_fp8_effective_split_k", "bigemm_fp8_workspace_bytes", "bigemm_linear_fp8",
     "bigemm_split_is_folded", "bigemm_split_path", "bigemm_cluster_capacity",
+    "bigemm_ozaki_rho", "bigemm_ozaki_default_slices", "bigemm_ozaki_pairs",
+    "bigemm_ozaki_workspace_bytes", "bigemm_ozaki_split", "bigemm_ozaki_dgemm",
 )
 
 FP8_E4M3 = 0
@@ -107,6 +111,12 @@ def load():
         "bigemm_split_is_folded": ([i64, i64, i64, i32], i32),
         "bigemm_split_path": ([i64, i64, i64, i32, i32], i32),
         "bigemm_cluster_capacity": ([i32], i32),
+        "bigemm_ozaki_rho": ([i64], i32),
+        "bigemm_ozaki_default_slices": ([i64], i32),
+        "bigemm_ozaki_pairs": ([i32, i32], i64),
+        "bigemm_ozaki_workspace_bytes": ([i64, i64, i64, i32], sz),
+        "bigemm_ozaki_split": ([vp, i64, i64, i64, i32, i32, i32, vp, i64, i64, vp, vp], i32),
+        "bigemm_ozaki_dgemm": ([vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, i32, vp, sz, vp], i32),
         "bigemm_partial_workspace_bytes": ([i64, i64, i64, i32], sz),
         "bigemm_run": ([vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, vp, sz, vp], i32),
         "bigemm_run_bf16out": ([vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, vp, sz, vp], i32),
@@ -426,4 +436,68 @@ def linear_fp8(x, weight, scale=1.0, bias=None, out_dtype=None, split_k: int = 1
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     bigemm_linear_fp8(x, weight, fmts[x.dtype], fmts[weight.dtype], scale, bias, out, M, N, K, lda,
                       ldw, ldc, split_k, bf16, workspace, wbytes, stream)
+    return out
+
+
+# ---------------------------------------------------------------- Ozaki --
+
+def bigemm_ozaki_rho(K: int) -> int:
+    return int(load().bigemm_ozaki_rho(K))
+
+
+def bigemm_ozaki_default_slices(K: int) -> int:
+    return int(load().bigemm_ozaki_default_slices(K))
+
+
+def bigemm_ozaki_pairs(slices: int, d: int) -> int:
+    return int(load().bigemm_ozaki_pairs(slices, d))
+
+
+def bigemm_ozaki_workspace_bytes(M: int, N: int, K: int, slices: int = 0) -> int:
+    return int(load().bigemm_ozaki_workspace_bytes(M, N, K, slices))
+
+
+def bigemm_ozaki_split(X, rows, cols, ld, axis, rho, slices, out, out_ld, out_rows, exps,
+                       stream=None, check=True) -> int:
+    st = load().bigemm_ozaki_split(_ptr(X), rows, cols, ld, axis, rho, slices, _ptr(out), out_ld,
+                                   out_rows, _ptr(exps), _stream(stream))
+    if check:
+        _check(st, "bigemm_ozaki_split")
+    return st
+
+
+def bigemm_ozaki_dgemm(A, B, C, M, N, K, lda, ldb, ldc, slices=0, d=0, workspace=None,
+                       workspace_bytes=0, stream=None, check=True) -> int:
+    st = load().bigemm_ozaki_dgemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, lda, ldb, ldc, slices, d,
+                                   _ptr(workspace), workspace_bytes, _stream(stream))
+    if check:
+        _check(st, "bigemm_ozaki_dgemm")
+    return st
+
+
+def ozaki_matmul(A, B, slices: int = 0, d: int = 0, out=None, workspace=None, stream=None):
+    """C = A @ B for float64 CUDA tensors A [M, K] and B [K, N] (row-major), by
+    the Ozaki scheme on the bf16 tensor cores (bigemm_ozaki_dgemm).  slices /
+    d: 0 for the defaults (binary64 accuracy).  Returns C float64 [M, N]."""
+    import torch
+    if A.dtype != torch.float64 or B.dtype != torch.float64:
+        raise TypeError("A and B must be float64")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError("shapes do not compose: %s x %s" % (tuple(A.shape), tuple(B.shape)))
+    if A.stride(1) != 1 or B.stride(1) != 1:
+        raise ValueError("A and B need unit column stride (row-major)")
+    M, K = A.shape
+    N = B.shape[1]
+    if out is None:
+        out = torch.empty((M, N + (N & 1)), dtype=torch.float64, device=A.device)[:, :N]
+    ldc = out.stride(0) if M > 1 else N + (N & 1)
+    if ldc % 2:
+        raise ValueError("the output's row stride must be even (16-byte vector stores)")
+    need = bigemm_ozaki_workspace_bytes(M, N, K, slices)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=A.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    lda = A.stride(0) if M > 1 else max(K, 1)
+    ldb = B.stride(0) if K > 1 else max(N, 1)
+    bigemm_ozaki_dgemm(A, B, out, M, N, K, lda, ldb, ldc, slices, d, workspace, wbytes, stream)
     return out

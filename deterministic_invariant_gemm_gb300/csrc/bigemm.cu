@@ -14,6 +14,7 @@
 
 #include "../../include/bigemm.h"
 #include "kernels.cuh"
+#include "ozaki.cuh"
 
 namespace bigemm {
 
@@ -102,6 +103,7 @@ bigemm_status device_info(const DeviceInfo** out) {
                 (const void*)bigemm_tc_kernel<kOutF32, true, true>,
                 (const void*)bigemm_tc_kernel<kOutBF16, true, true>,
                 (const void*)bigemm_tc_kernel<kOutSlices, true, true>,
+                (const void*)bigemm_tc_kernel<kOutOzaki, false, false>,
             };
             for (const void* fn : kernels) {
                 const bigemm_status st = opt_in(fn);
@@ -337,7 +339,11 @@ template <int kOut>
 cudaError_t launch_gemm(bool wt, bool fp8, dim3 g, dim3 blk, cudaStream_t stream,
                         const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBp,
                         const CUtensorMap& tmC, const GemmParams& p, unsigned cluster_x = 1) {
-    if constexpr (kOut == kOutAtomic) {
+    if constexpr (kOut == kOutOzaki) {
+        if (wt || fp8) return cudaErrorInvalidValue;  // bfloat16 slices of B [K, N] only
+        return launch_pdl(bigemm_tc_kernel<kOut, false, false>, g, blk, kSmemBytes, stream, tmA, tmB,
+                          tmBp, tmC, p);
+    } else if constexpr (kOut == kOutAtomic) {
         if (wt || fp8) return cudaErrorInvalidValue;  // the contrast exists for bf16 B [K, N] only
         return launch_pdl(bigemm_tc_kernel<kOut, false, false>, g, blk, kSmemBytes, stream, tmA, tmB,
                           tmBp, tmC, p);
@@ -548,6 +554,85 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     return BIGEMM_OK;
 }
 
+// ---------------------------------------------------------------- Ozaki --
+// The Ozaki scheme's binary64 product (cuTile article, "倍精度行列積エミュレー
+// ション"): rho = max(ceil(53 - (24 - log2 K) / 2), 53 - 8), in integers:
+// ceil(41 + log2(K) / 2) = 41 + t with t the least integer such that 4^t >= K.
+constexpr int64_t kOzakiMaxK = int64_t(1) << 22;   // rho <= 52: at least one bit per slice
+constexpr int kOzakiMaxSlices = 32;
+
+int ozaki_rho(int64_t K) {
+    int t = 0;
+    for (int64_t q = 1; q < K; q *= 4) ++t;
+    const int gamma = 41 + t;
+    return gamma > 45 ? gamma : 45;
+}
+
+// Slices whose bits reach 2^-53 below each vector's maximum: beta bits in the
+// first slice and beta + 1 in each later one, s (beta + 1) - 1 >= 53.
+int ozaki_default_slices(int rho) {
+    const int beta = 53 - rho;
+    return (54 + beta) / (beta + 1);
+}
+
+int64_t ozaki_pair_count(int slices, int d) {
+    int64_t n = 0;
+    for (int a = 0; a < slices; ++a)
+        for (int b = 0; b < slices; ++b)
+            if (a + b < d) ++n;
+    return n;
+}
+
+int64_t round_up(int64_t x, int64_t m) { return ceil_div(x, m) * m; }
+
+// Workspace of bigemm_ozaki_dgemm, in this order, each part 256-byte aligned:
+// A slices [s][M][lda_s] bf16, B slices [s][kpad][ldb_s] bf16, c^(1) of the
+// rows of A [M] int32, c^(1) of the columns of B [N] int32.
+struct OzakiLayout {
+    int64_t lda_s, ldb_s, kpad;
+    size_t off_b, off_ca, off_cb, total;
+};
+
+OzakiLayout ozaki_layout(int64_t M, int64_t N, int64_t K, int slices) {
+    OzakiLayout L;
+    L.lda_s = round_up(K > 0 ? K : 1, 8);
+    L.ldb_s = round_up(N > 0 ? N : 1, 8);
+    L.kpad = round_up(K > 0 ? K : 1, kBK);
+    const auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t a = up(static_cast<size_t>(slices) * M * L.lda_s * 2);
+    const size_t b = up(static_cast<size_t>(slices) * L.kpad * L.ldb_s * 2);
+    const size_t ca = up(static_cast<size_t>(M) * 4);
+    const size_t cb = up(static_cast<size_t>(N) * 4);
+    L.off_b = a;
+    L.off_ca = a + b;
+    L.off_cb = a + b + ca;
+    L.total = a + b + ca + cb;
+    return L;
+}
+
+bool aligned_to(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+cudaError_t launch_ozaki_split(const DeviceInfo& d, const double* X, int64_t rows, int64_t cols,
+                               int64_t ld, int axis, int rho, int slices, __nv_bfloat16* out,
+                               int64_t out_ld, int64_t out_rows, int* exps, cudaStream_t stream) {
+    if (axis == 0) {
+        int64_t blocks = ceil_div(rows, kOzakiRowWarps);
+        if (blocks > 8 * static_cast<int64_t>(d.sm_count)) blocks = 8 * static_cast<int64_t>(d.sm_count);
+        ozaki_split_rows_kernel<<<static_cast<unsigned>(blocks), kOzakiRowWarps * 32, 0, stream>>>(
+            X, rows, cols, ld, rho, slices, out, out_ld, rows * out_ld, exps);
+        return cudaGetLastError();
+    }
+    ozaki_col_exps_kernel<<<static_cast<unsigned>(ceil_div(cols, 32)), 256, 0, stream>>>(X, rows, cols,
+                                                                                        ld, exps);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    int64_t blocks = ceil_div(out_rows * cols, 256);
+    if (blocks > 16 * static_cast<int64_t>(d.sm_count)) blocks = 16 * static_cast<int64_t>(d.sm_count);
+    ozaki_split_cols_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        X, rows, cols, ld, out_rows, rho, slices, out, out_ld, out_rows * out_ld, exps);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 // Split-K scratch for bigemm_run_splitk_static, for callers that cannot
@@ -742,6 +827,140 @@ bigemm_status bigemm_run_splitk_static(const void* A, const void* B, float* C, i
     return run_impl(kModeF32, A, B, C, M, N, K, lda, ldb, ldc, split_k, scratch,
                     scratch ? static_cast<size_t>(BIGEMM_STATIC_SCRATCH_BYTES) : 0,
                     static_cast<cudaStream_t>(stream));
+}
+
+int bigemm_ozaki_rho(int64_t K) { return (K < 1 || K > kOzakiMaxK) ? -1 : ozaki_rho(K); }
+
+int bigemm_ozaki_default_slices(int64_t K) {
+    return (K < 1 || K > kOzakiMaxK) ? -1 : ozaki_default_slices(ozaki_rho(K));
+}
+
+int64_t bigemm_ozaki_pairs(int slices, int d) {
+    return (slices < 1 || d < 0) ? -1 : ozaki_pair_count(slices, d);
+}
+
+size_t bigemm_ozaki_workspace_bytes(int64_t M, int64_t N, int64_t K, int slices) {
+    if (M < 0 || N < 0 || K < 0 || K > kOzakiMaxK) return 0;
+    if (slices == 0) slices = K > 0 ? ozaki_default_slices(ozaki_rho(K)) : 1;
+    if (slices < 1 || slices > kOzakiMaxSlices) return 0;
+    return ozaki_layout(M, N, K, slices).total;
+}
+
+bigemm_status bigemm_ozaki_split(const double* X, int64_t rows, int64_t cols, int64_t ld, int axis,
+                                 int rho, int slices, void* out, int64_t out_ld, int64_t out_rows,
+                                 int* exps, bigemm_stream stream) {
+    g_last_launches = 0;
+    if (rows < 0 || cols < 0 || (axis != 0 && axis != 1)) return BIGEMM_ERR_ARG;
+    if (rho < 45 || rho > 52 || slices < 1 || slices > kOzakiMaxSlices) return BIGEMM_ERR_ARG;
+    if (rows == 0 || cols == 0) return BIGEMM_OK;
+    if (X == nullptr || out == nullptr || exps == nullptr || ld < cols || out_ld < cols) return BIGEMM_ERR_ARG;
+    if (axis == 1 && out_rows < rows) return BIGEMM_ERR_ARG;
+    if (!aligned_to(X, 8) || !aligned_to(out, 2) || !aligned_to(exps, 4)) return BIGEMM_ERR_ALIGN;
+    const DeviceInfo* d = nullptr;
+    bigemm_status st = device_info(&d);
+    if (st != BIGEMM_OK) return st;
+    const cudaError_t e = launch_ozaki_split(*d, X, rows, cols, ld, axis, rho, slices,
+                                             static_cast<__nv_bfloat16*>(out), out_ld,
+                                             axis == 1 ? out_rows : rows, exps,
+                                             static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
+    g_last_launches = axis == 0 ? 1 : 2;
+    return BIGEMM_OK;
+}
+
+bigemm_status bigemm_ozaki_dgemm(const double* A, const double* B, double* C, int64_t M, int64_t N,
+                                 int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int slices, int d,
+                                 void* workspace, size_t workspace_bytes, bigemm_stream stream) {
+    g_last_launches = 0;
+    const cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    if (M < 0 || N < 0 || K < 0 || K > kOzakiMaxK || M > INT_MAX || N > INT_MAX) return BIGEMM_ERR_ARG;
+    const int rho = K > 0 ? ozaki_rho(K) : 52;
+    if (slices == 0) slices = ozaki_default_slices(rho);
+    if (slices < 1 || slices > kOzakiMaxSlices || d < 0) return BIGEMM_ERR_ARG;
+    if (d == 0) d = slices;
+    if (K > 0 && (A == nullptr || B == nullptr || lda < K || ldb < N)) return BIGEMM_ERR_ARG;
+    if (C == nullptr || ldc < N) return BIGEMM_ERR_ARG;
+    if (K > 0 && (!aligned_to(A, 8) || !aligned_to(B, 8))) return BIGEMM_ERR_ALIGN;
+    if (!aligned16(C) || ldc % 2 != 0) return BIGEMM_ERR_ALIGN;
+    const OzakiLayout L = ozaki_layout(M, N, K, slices);
+    if (K > 0 && (workspace == nullptr || !aligned_to(workspace, 256) || workspace_bytes < L.total))
+        return BIGEMM_ERR_WORKSPACE;
+    if (static_cast<int64_t>(slices) * M > INT_MAX || static_cast<int64_t>(slices) * L.kpad > INT_MAX)
+        return BIGEMM_ERR_ARG;
+    if (M == 0 || N == 0) return BIGEMM_OK;
+    const DeviceInfo* dev = nullptr;
+    bigemm_status st = device_info(&dev);
+    if (st != BIGEMM_OK) return st;
+    if (K == 0) {  // the empty sum
+        const cudaError_t e = cudaMemset2DAsync(C, static_cast<size_t>(ldc) * 8, 0,
+                                                static_cast<size_t>(N) * 8, static_cast<size_t>(M), strm);
+        return e == cudaSuccess ? BIGEMM_OK : BIGEMM_ERR_CUDA;
+    }
+    const int64_t pairs = ozaki_pair_count(slices, d);
+    if (pairs == 0) {  // every pair skipped: the sum of no terms
+        const cudaError_t e = cudaMemset2DAsync(C, static_cast<size_t>(ldc) * 8, 0,
+                                                static_cast<size_t>(N) * 8, static_cast<size_t>(M), strm);
+        return e == cudaSuccess ? BIGEMM_OK : BIGEMM_ERR_CUDA;
+    }
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    __nv_bfloat16* As = reinterpret_cast<__nv_bfloat16*>(ws);
+    __nv_bfloat16* Bs = reinterpret_cast<__nv_bfloat16*>(ws + L.off_b);
+    int* ca = reinterpret_cast<int*>(ws + L.off_ca);
+    int* cb = reinterpret_cast<int*>(ws + L.off_cb);
+    // 1-3: split A by rows and B by columns (plain launches: they read the
+    // caller's A and B, so they wait for everything before them)
+    if (launch_ozaki_split(*dev, A, M, K, lda, 0, rho, slices, As, L.lda_s, M, ca, strm) != cudaSuccess ||
+        launch_ozaki_split(*dev, B, K, N, ldb, 1, rho, slices, Bs, L.ldb_s, L.kpad, cb, strm) != cudaSuccess)
+        return BIGEMM_ERR_CUDA;
+    // 4: every slice pair's product on the tensor cores, summed in binary64
+    CUtensorMap tmA, tmB, tmBp;
+    {
+        const int64_t da[2] = {K, slices * M};
+        const int64_t db[2] = {N, slices * L.kpad};
+        const uint32_t ba[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(kBM)};
+        const uint32_t bb[2] = {kBChunkCols, static_cast<uint32_t>(kBK)};
+        const uint32_t bp[2] = {static_cast<uint32_t>(kBN), static_cast<uint32_t>(kPrefetchRows)};
+        if (!encode_tiled(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, As, 2, da, L.lda_s, 0, ba,
+                          CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tiled(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Bs, 2, db, L.ldb_s, 0, bb,
+                          CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tiled(&tmBp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Bs, 2, db, L.ldb_s, 0, bp,
+                          CU_TENSOR_MAP_SWIZZLE_NONE))
+            return BIGEMM_ERR_CUDA;
+    }
+    const int64_t m_tiles = ceil_div(M, kBM), n_tiles = ceil_div(N, kBN);
+    if (m_tiles * n_tiles > INT_MAX) return BIGEMM_ERR_ARG;
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.out = C;
+    p.ld_out = ldc;
+    p.status = dev->status;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.m_tiles = static_cast<int>(m_tiles);
+    p.n_tiles = static_cast<int>(n_tiles);
+    p.splits = 1;
+    p.kb_total = static_cast<int>(ceil_div(K, kBK));
+    p.kb_per_split = p.kb_total;
+    p.units = static_cast<int>(m_tiles * n_tiles);
+    p.epi_boxes = epi_boxes_for(static_cast<int>(M));
+    p.epi_batch = epi_batch_for(static_cast<int>(M));
+    p.prefetch_rows = kStages * kBK;
+    p.group_m = (m_tiles * n_tiles >= 4 * static_cast<int64_t>(dev->sm_count)) ? 16 : 8;
+    p.scale = 1.0f;
+    p.oz_ca = ca;
+    p.oz_cb = cb;
+    p.oz_slices = slices;
+    p.oz_d = d;
+    p.oz_beta = 53 - rho;
+    p.oz_pairs = static_cast<int>(pairs);
+    p.oz_kpad = static_cast<int>(L.kpad);
+    const int grid = static_cast<int>(p.units < dev->sm_count ? p.units : dev->sm_count);
+    if (launch_gemm<kOutOzaki>(false, false, dim3(static_cast<unsigned>(grid)), dim3(kNumThreads), strm,
+                               tmA, tmB, tmBp, tmA, p) != cudaSuccess)
+        return BIGEMM_ERR_CUDA;
+    g_last_launches = 4;
+    return BIGEMM_OK;
 }
 
 bigemm_status bigemm_device_status(int reset) {

@@ -115,6 +115,7 @@ enum OutKind : int {
     kOutBF16 = 1,    // C bf16 (round to nearest even), plain stores
     kOutSlices = 2,  // fp32 split-K partial to workspace slice `seg`
     kOutAtomic = 3,  // fp32 atomic add into C (nondeterministic contrast)
+    kOutOzaki = 4,   // binary64 C += 2^e * (slice-pair product), Ozaki scheme
 };
 
 struct GemmParams {
@@ -144,7 +145,23 @@ struct GemmParams {
     int cluster;            // 1: clusters of `splits` CTAs, one per K segment of a tile,
                             //    sum their partials through distributed shared memory
                             //    (splits in 2..8, direct output, one unit per CTA)
+    // Ozaki scheme (kOutOzaki): A is `oz_slices` bfloat16 slices of M rows each
+    // (slice p at rows p * M), B the same number of slices of oz_kpad rows;
+    // a unit is a tile, run once for every slice pair (p, q) with p + q < oz_d.
+    const int* oz_ca;       // c^(1) of every row of A
+    const int* oz_cb;       // c^(1) of every column of B
+    int oz_slices, oz_d, oz_beta, oz_pairs, oz_kpad;
 };
+
+// The slice pairs of the Ozaki scheme in the order of the binary64
+// accumulation: p outer, q inner, skipping p + q >= d (Fast Mode).
+__device__ __forceinline__ void ozaki_next_pair(const GemmParams& p, int& a, int& b) {
+    ++b;
+    if (b >= p.oz_slices || a + b >= p.oz_d) {
+        ++a;
+        b = 0;
+    }
+}
 
 // Unit u -> (tile row, tile column, K segment).  All tiles of segment 0 come
 // first, then segment 1, ...; inside a segment the tiles follow the GROUP_M
@@ -433,6 +450,37 @@ __device__ __forceinline__ void cluster_reduce(const GemmParams& p, uint32_t par
     }
 }
 
+// One step of the Ozaki scheme's binary64 sum for 32 columns of one row:
+// c[j] = c[j] + 2^(e_pair + cb[j]) * P[j], P[j] the FP32 slice-pair product
+// (an exact integer multiple of its unit, so the scaling by a power of two
+// is exact and one rounding remains: a fused multiply-add with the power of
+// two is that addition).  first: the sum starts here from +0.0 and C is not
+// read.  valid < 32 at the right edge of C.
+__device__ __forceinline__ double ozaki_term(double c, uint32_t pbits, int e) {
+    const double P = static_cast<double>(__uint_as_float(pbits));
+    if (e >= -1022 && e <= 1023)
+        return __fma_rn(P, __longlong_as_double(static_cast<long long>(e + 1023) << 52), c);
+    return __dadd_rn(c, ldexp(P, e));
+}
+
+__device__ __forceinline__ void ozaki_accumulate_block(double* crow, const int* cb, int valid,
+                                                       int e_pair, const uint32_t (&r)[32],
+                                                       bool first) {
+    if (valid == 32) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            double2 c = first ? make_double2(0.0, 0.0) : *reinterpret_cast<const double2*>(crow + j);
+            c.x = ozaki_term(c.x, r[j], e_pair + __ldg(cb + j));
+            c.y = ozaki_term(c.y, r[j + 1], e_pair + __ldg(cb + j + 1));
+            *reinterpret_cast<double2*>(crow + j) = c;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < valid) crow[j] = ozaki_term(first ? 0.0 : crow[j], r[j], e_pair + __ldg(cb + j));
+    }
+}
+
 // kWt: the second operand is the weight matrix W [N, K] (K-major); otherwise
 // B [K, N] (N-major).  Both products run the same K = 16 instruction sequence.
 // kFp8: 8-bit float operands (both K-major, kWt): a K block is 128 elements,
@@ -505,7 +553,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        if constexpr (kOut != kOutAtomic) tma_prefetch_desc(&tmC);
+        if constexpr (kOut != kOutAtomic && kOut != kOutOzaki) tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -529,6 +577,42 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
+            if constexpr (kOut == kOutOzaki) {
+                // an Ozaki unit streams A and B once per slice pair (pa, pb):
+                // rows pa * M + m0 of the A slices, rows pb * oz_kpad + k of the
+                // B slices
+                for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+                    int mt, nt, seg;
+                    unit_coords(p, u, mt, nt, seg);
+                    const int n0 = nt * kBN;
+                    int pa = 0, pb = 0;
+                    for (int pair = 0; ok && pair < p.oz_pairs; ++pair) {
+                        const int a_row = mt * kBM + pa * p.M;
+                        const int b_row = pb * p.oz_kpad;
+                        for (int kb = 0; kb < p.kb_total; ++kb) {
+                            if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.status,
+                                              kErrWaitProducer)) {
+                                ok = false;
+                                break;
+                            }
+                            const uint32_t fb = full_bar(stage);
+                            mbar_arrive_expect_tx(fb, kStageBytes);
+                            tma_load_2d(sA + stage * kABytes, &tmA, fb, kb * kBK, a_row);
+#pragma unroll
+                            for (int c = 0; c < kBN / static_cast<int>(kBChunkCols); ++c)
+                                tma_load_2d(sB + stage * kBBytes + c * kBChunkBytes, &tmB, fb,
+                                            n0 + c * static_cast<int>(kBChunkCols), b_row + kb * kBK);
+                            issued_mask |= 1u << stage;
+                            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                            if (++stage == kStages) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
+                        }
+                        ozaki_next_pair(p, pa, pb);
+                    }
+                }
+            } else {
             for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
                 int mt, nt, seg;
                 unit_coords(p, u, mt, nt, seg);
@@ -562,6 +646,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                 }
             }
+            }
             // Every load of this CTA is issued: the next kernel in the stream may
             // be scheduled from now on (it waits for this grid to complete before
             // touching memory; this CTA already holds its TMEM, so a dependent
@@ -587,8 +672,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 int mt, nt, seg0;
                 unit_coords(p, u, mt, nt, seg0);
                 // A folded unit fills one accumulator per K segment, in order; the
-                // epilogue adds them.  Otherwise the unit is the single segment seg0.
-                const int nseg = p.fold ? p.splits : 1;
+                // epilogue adds them.  An Ozaki unit fills one per slice pair, each
+                // over all of K.  Otherwise the unit is the single segment seg0.
+                const int nseg = (kOut == kOutOzaki) ? p.oz_pairs : (p.fold ? p.splits : 1);
                 for (int sg = 0; ok && sg < nseg; ++sg, ++t) {
                     const int seg = p.fold ? sg : seg0;
                     const int kb0 = seg * p.kb_per_split;
@@ -681,6 +767,60 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         uint32_t nbat = 0;  // batches this warp has handed to the TMA unit
         int t = 0;          // accumulators drained so far (one per segment)
         bool folded = false;
+        if constexpr (kOut == kOutOzaki) {
+            // ---- Ozaki scheme: for every slice pair (pa, pb) of the tile, in the
+            // order of the binary64 sum, C[row][col] += 2^e * P with P the FP32
+            // slice-pair product (exact) and e = c_a^(pa)[row] + c_b^(pb)[col];
+            // the first pair starts the sum at +0.0.  Each thread owns its row
+            // and its half of the tile's columns, so it alone reads and writes
+            // those elements of C, pair after pair.
+            folded = true;
+            double* C = static_cast<double*>(p.out);
+            const int step = p.oz_beta + 1;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+                int mt, nt, seg;
+                unit_coords(p, u, mt, nt, seg);
+                const int m0 = mt * kBM + q * 32, n0 = nt * kBN;
+                const int row = m0 + lane;
+                const bool row_ok = row < p.M;
+                const int ca = row_ok ? p.oz_ca[row] : 0;
+                int pa = 0, pb = 0;
+                for (int pair = 0; pair < p.oz_pairs; ++pair, ++t) {
+                    const int acc = t % kAccStages;
+                    const uint32_t acc_phase = static_cast<uint32_t>(t / kAccStages) & 1u;
+                    if (!wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.status, kErrWaitEpilogue)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (m0 < p.M) {
+                        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                               static_cast<uint32_t>(acc * kBN);
+                        const int e_pair = (ca - pa * step) - pb * step;
+#pragma unroll 1
+                        for (int i = 0; i < 4; ++i) {
+                            uint32_t r[32];
+                            tmem_ld_32x32b_x32(tbase + (h * 4 + i) * 32, r);
+                            tmem_ld_wait();
+                            if (i == 3) {  // the accumulator is no longer needed
+                                tc_fence_before();
+                                mbar_arrive(tempty_bar(acc));
+                            }
+                            const int col0 = n0 + (h * 4 + i) * 32;
+                            if (row_ok && col0 < p.N)
+                                ozaki_accumulate_block(C + static_cast<int64_t>(row) * p.ld_out + col0,
+                                                       p.oz_cb + col0, min(32, p.N - col0), e_pair, r,
+                                                       pair == 0);
+                        }
+                    } else {
+                        tc_fence_before();
+                        mbar_arrive(tempty_bar(acc));
+                    }
+                    ozaki_next_pair(p, pa, pb);
+                }
+            }
+        }
         if constexpr (kOut == kOutF32 || kOut == kOutBF16) {
             if (p.cluster) {
                 // ---- one K segment of a clustered tile: the FP32 partial goes

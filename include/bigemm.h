@@ -286,6 +286,76 @@ BIGEMM_API bigemm_status bigemm_linear_fp8(const void *A, const void *W, int fmt
                                            void *workspace, size_t workspace_bytes,
                                            bigemm_stream stream);
 
+/* ------------------------------------------------------------------------
+ * Binary64 matrix product by the Ozaki scheme on the bfloat16 tensor cores
+ * (cuTile article, "倍精度行列積エミュレーション": "Ozaki Schemeについて",
+ * "分解(Split)", "行列積の計算", "Fast Mode（GEMMの削減）", "Fused Split
+ * Kernel（分割の融合）").  The pages give no API; these calls are this
+ * library's.
+ *
+ * Every row of A and every column of B (a vector x) is split into `slices`
+ * bfloat16 slices by the Veltkamp split, eqs. (1)-(5):
+ *   c^(1) = ceil(log2 max_i |x_i|),  sigma = 0.75 * 2^(rho + c^(p)),
+ *   v = fl((x^(p) + sigma) - sigma),  x^(p+1) = x^(p) - v,  xbar^(p) = 2^(-c^(p)) v,
+ * with c^(p+1) = c^(p) - (53 - rho) - 1 (the residual's bound, so that every
+ * exponent follows from the first maximum, as in the fused split) and
+ *   rho = max(ceil(53 - (24 - log2 K) / 2), 53 - 8),
+ * the value that makes every slice-pair product over all of K exact in FP32
+ * (eq. (11)).  Each vector is scaled by its own maximum -- per row of A, per
+ * column of B -- so row i of C depends on row i of A and on B only: the
+ * product is batch-invariant like the rest of the library.  Then
+ *   C_ij = sum over (p, q) with p + q < d, p outer and q inner, of
+ *          2^(c_a^(p)_i + c_b^(q)_j) * (xbar_a^(p)_i . ybar_b^(q)_j)      eq. (10)
+ * each term one binary64 addition in that fixed order, the products on the
+ * tensor cores (exact).  Inputs must be finite, with every scaled term a
+ * normal binary64 (|values| roughly within 2^-900 .. 2^900).
+ * ---------------------------------------------------------------------- */
+
+/* rho for inner length K (1 <= K <= 2^22), or -1. */
+BIGEMM_API int bigemm_ozaki_rho(int64_t K);
+
+/* The default number of slices for inner length K: the least s with
+ * s * (54 - rho) - 1 >= 53, enough to carry every vector to binary64
+ * precision below its maximum; -1 for K outside 1 .. 2^22. */
+BIGEMM_API int bigemm_ozaki_default_slices(int64_t K);
+
+/* Slice pairs (p, q), 0 <= p, q < slices, with p + q < d: the number of
+ * tensor-core products bigemm_ozaki_dgemm runs per output tile.  -1 for
+ * invalid arguments. */
+BIGEMM_API int64_t bigemm_ozaki_pairs(int slices, int d);
+
+/* Workspace bytes of bigemm_ozaki_dgemm (slices = 0: the default): the
+ * slices of A [s][M][round_up(K, 8)] and of B [s][round_up(K, 64)]
+ * [round_up(N, 8)] in bf16, then c^(1) of every row of A and every column
+ * of B (int32), each part 256-byte aligned.  0 for invalid arguments. */
+BIGEMM_API size_t bigemm_ozaki_workspace_bytes(int64_t M, int64_t N, int64_t K, int slices);
+
+/* The split alone.  X: binary64 [rows][ld].  axis 0: every row is a vector,
+ * slice p of row r goes to out[p * rows * out_ld + r * out_ld + k]; axis 1:
+ * every column, slice p of element (r, j) to out[p * out_rows * out_ld +
+ * r * out_ld + j], rows rows .. out_rows-1 of every slice written as zeros
+ * (out_rows >= rows).  out: bf16; exps: c^(1) per vector (int32).  rho in
+ * 45 .. 52, slices in 1 .. 32. */
+BIGEMM_API bigemm_status bigemm_ozaki_split(const double *X, int64_t rows, int64_t cols, int64_t ld,
+                                            int axis, int rho, int slices, void *out, int64_t out_ld,
+                                            int64_t out_rows, int *exps, bigemm_stream stream);
+
+/* C = A * B in binary64.  A [M][lda], B [K][ldb] binary64 (8-byte aligned),
+ * C [M][ldc] binary64 (16-byte aligned, ldc even).  slices: 0 = the default
+ * (bigemm_ozaki_default_slices), else 1 .. 32; d: 0 = slices (the deterministic
+ * binary64 bound: every skipped pair is below 2^-54 of its vectors' maxima),
+ * smaller for Fast Mode's trade of accuracy for speed.  K <= 2^22.  Four
+ * launches: the row split of A, the column maxima and column split of B, and
+ * one tensor-core kernel that runs every kept slice pair of each output tile
+ * and keeps the binary64 sum in C.  Workspace: bigemm_ozaki_workspace_bytes,
+ * 256-byte aligned. */
+BIGEMM_API bigemm_status bigemm_ozaki_dgemm(const double *A, const double *B, double *C,
+                                            int64_t M, int64_t N, int64_t K,
+                                            int64_t lda, int64_t ldb, int64_t ldc,
+                                            int slices, int d,
+                                            void *workspace, size_t workspace_bytes,
+                                            bigemm_stream stream);
+
 /* Measured contrast only -- NOT deterministic.  Same arguments as bigemm_run
  * without a workspace: C (fp32) is zeroed on the stream, then every K
  * segment's partial is added into C with atomic adds ("Split-K": atomic_add;

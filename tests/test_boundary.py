@@ -174,3 +174,23 @@ def test_product_path_has_no_oracle_or_fallback():
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "liboracle" not in text, f
+
+
+def test_ozaki_host_helpers_agree_with_the_oracle(lib):
+    """rho, the default slice count and the Fast Mode pair count are host
+    arithmetic; the oracle's versions are pinned against the pages."""
+    import oracle
+    for K in (1, 2, 63, 64, 128, 129, 1000, 4096, 8192, 16384, 1 << 20, 1 << 22):
+        rho = dig.bigemm_ozaki_rho(K)
+        assert rho == oracle.ozaki_rho(K)
+        assert dig.bigemm_ozaki_default_slices(K) == oracle.ozaki_default_slices(rho)
+    assert dig.bigemm_ozaki_rho(0) == -1 and dig.bigemm_ozaki_rho((1 << 22) + 1) == -1
+    for s in range(1, 12):
+        for d in range(0, 2 * s + 1):
+            assert dig.bigemm_ozaki_pairs(s, d) == oracle.ozaki_pairs(s, d)
+    # workspace: slices of A and B in bf16, then the two exponent vectors, 256-byte parts
+    M, N, K, s = 100, 70, 300, 0
+    s = dig.bigemm_ozaki_default_slices(K)
+    up = lambda x: (x + 255) // 256 * 256
+    want = up(s * M * 304 * 2) + up(s * 320 * 72 * 2) + up(M * 4) + up(N * 4)
+    assert dig.bigemm_ozaki_workspace_bytes(M, N, K, 0) == want

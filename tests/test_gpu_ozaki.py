@@ -1,0 +1,173 @@
+"""GPU: the Ozaki scheme's binary64 product on the bfloat16 tensor cores
+(bigemm_ozaki_split, bigemm_ozaki_dgemm) against the binary64 oracle
+(oracle.ozaki_split, oracle.ozaki_gemm) -- cuTile article, "倍精度行列積
+エミュレーション".  The split is the Veltkamp split of eqs. (1)-(5); the
+slice-pair products are exact in FP32 (eq. (11)); the binary64 sum of eq. (10)
+runs in the same pair order on both sides, so the GPU's C must equal the
+oracle's exactly, not just within a tolerance."""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import deterministic_invariant_gemm_gb300 as dig
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device(cuda_device):
+    dig.load()
+    yield
+    assert dig.bigemm_device_status(reset=True) == 0
+
+
+def wide(shape, seed, spread=20):
+    """Normal values scaled over 2^-spread .. 2^spread, a few exact zeros."""
+    g = workloads.generator(seed)
+    x = torch.randn(shape, generator=g, dtype=torch.float64)
+    e = torch.randint(-spread, spread + 1, shape, generator=g).double()
+    x = x * torch.exp2(e)
+    x.view(-1)[:: 97] = 0.0
+    return x
+
+
+def gpu_split(X, axis, rho, slices, out_rows=None):
+    rows, cols = X.shape
+    out_ld = cols + (-cols) % 8
+    out_rows = rows if out_rows is None else out_rows
+    plane_rows = rows if axis == 0 else out_rows
+    out = torch.full((slices, plane_rows, out_ld), -1.0, dtype=torch.bfloat16, device="cuda")
+    exps = torch.empty(rows if axis == 0 else cols, dtype=torch.int32, device="cuda")
+    Xd = X.cuda()
+    dig.bigemm_ozaki_split(Xd, rows, cols, cols, axis, rho, slices, out, out_ld, out_rows, exps)
+    torch.cuda.synchronize()
+    return out, exps
+
+
+@pytest.mark.parametrize("axis", [0, 1])
+@pytest.mark.parametrize("rows,cols,K", [(37, 300, 300), (300, 37, 4096), (5, 8, 1 << 20)])
+def test_split_matches_the_oracle_bit_for_bit(axis, rows, cols, K):
+    X = wide((rows, cols), rows * cols + axis)
+    X[0, 0] = -0.0
+    X[1, :] = 0.0                               # an all-zero row
+    X[2, 3] = 2.0 ** -1060                      # a subnormal
+    X[3, 1] = 2.0 ** 30                         # a power-of-two maximum
+    rho = dig.bigemm_ozaki_rho(K)
+    assert rho == oracle.ozaki_rho(K)
+    slices = dig.bigemm_ozaki_default_slices(K)
+    S, c1, _ = oracle.ozaki_split(X, axis, rho, slices)
+    out_rows = rows + 5 if axis == 1 else None
+    got, exps = gpu_split(X, axis, rho, slices, out_rows)
+    assert np.array_equal(exps.cpu().numpy(), c1)
+    want = oracle.encode_rne(oracle.FMT_BF16, S)            # exact: every slice is a bf16 value
+    assert np.array_equal(oracle.decode(oracle.FMT_BF16, want), S)
+    have = got[:, :rows, :cols].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    # +0.0 and -0.0 slices are both zero terms: compare values, then bits of the nonzeros
+    assert np.array_equal(oracle.decode(oracle.FMT_BF16, have), S)
+    if axis == 1:
+        assert (got[:, rows:, :cols].float() == 0).all()    # the padding rows are zeros
+
+
+def run_dgemm(A, B, slices=0, d=0, ldc_pad=0):
+    M, K = A.shape
+    N = B.shape[1]
+    ldc = N + (N & 1) + ldc_pad
+    C = torch.full((M + 2, ldc), float("nan"), dtype=torch.float64, device="cuda")
+    need = dig.bigemm_ozaki_workspace_bytes(M, N, K, slices)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    dig.bigemm_ozaki_dgemm(A.cuda(), B.cuda(), C, M, N, K, K, N, ldc, slices, d, ws, need)
+    torch.cuda.synchronize()
+    assert torch.isnan(C[:M, N:]).all() and torch.isnan(C[M:]).all()   # nothing written outside C
+    return C[:M, :N].cpu().numpy()
+
+
+@pytest.mark.parametrize("M,N,K,slices,d", [
+    (64, 256, 512, 0, 0),
+    (100, 70, 300, 0, 0),        # ragged: one partial tile, N not a multiple of 32
+    (257, 300, 1000, 0, 0),      # three tile rows, two tile columns
+    (130, 512, 4096, 0, 0),      # rho = 47: six-bit slices
+    (64, 256, 512, 4, 3),        # Fast Mode: 6 pairs of 16
+    (64, 256, 512, 7, 1),        # the leading pair alone
+    (33, 96, 70, 3, 5),          # d beyond 2 (slices - 1): every pair
+])
+def test_dgemm_equals_the_oracle_exactly(M, N, K, slices, d):
+    A = wide((M, K), M + K, 12)
+    B = wide((K, N), N + K, 12)
+    C = run_dgemm(A, B, slices, d)
+    rho = oracle.ozaki_rho(K)
+    s = slices or oracle.ozaki_default_slices(rho)
+    Cref, inexact = oracle.ozaki_gemm(A, B, rho=rho, slices=s, d=d or s)
+    assert inexact == 0
+    assert np.array_equal(C, Cref)
+
+
+def test_dgemm_accuracy_against_exact_products():
+    """1024^3 normal inputs: rows computed by the oracle match exactly, and
+    the error against exact rational products on a sample is binary64's."""
+    M = N = K = 1024
+    g = workloads.generator(77)
+    A = torch.randn(M, K, generator=g, dtype=torch.float64)
+    B = torch.randn(K, N, generator=g, dtype=torch.float64)
+    C = run_dgemm(A, B)
+    rows = [0, 511, 1023]
+    Cref, _ = oracle.ozaki_gemm(A[rows], B)                 # rows split alone: the same slices
+    assert np.array_equal(C[rows], Cref)
+    a, b = A.numpy(), B.numpy()
+    scale = np.abs(a) @ np.abs(b)
+    for i, j in ((0, 0), (511, 700), (1023, 1023), (17, 999)):
+        exact = sum((Fraction(a[i, k]) * Fraction(b[k, j]) for k in range(K)), Fraction(0))
+        err = abs(float(Fraction(C[i, j]) - exact))
+        assert err <= 8 * 2.0 ** -53 * scale[i, j], (i, j, err / scale[i, j])
+    # and against numpy's own binary64 product, elementwise on the whole matrix
+    assert np.max(np.abs(C - a @ b) / scale) < 1e-14
+
+
+def test_dgemm_rows_are_batch_invariant():
+    """Each row of A is split by its own maximum, so row i of C is the same at
+    M = 1, inside a window and inside the full batch, bit for bit."""
+    M, N, K = 300, 384, 777
+    A = wide((M, K), 5, 8)
+    B = wide((K, N), 6, 8)
+    full = run_dgemm(A, B)
+    for lo, hi in ((0, 1), (128, 129), (299, 300), (37, 170)):
+        part = run_dgemm(A[lo:hi].clone(), B)
+        assert np.array_equal(part.view(np.int64), full[lo:hi].view(np.int64)), (lo, hi)
+
+
+def test_dgemm_bit_stable_over_10_runs():
+    A = wide((256, 512), 8, 4)
+    B = wide((512, 256), 9, 4)
+    first = run_dgemm(A, B)
+    for _ in range(9):
+        assert np.array_equal(run_dgemm(A, B).view(np.int64), first.view(np.int64))
+
+
+def test_dgemm_small_integers_exact():
+    g = workloads.generator(3)
+    A = torch.randint(-1000, 1001, (96, 200), generator=g).double()
+    B = torch.randint(-1000, 1001, (200, 130), generator=g).double()
+    C = run_dgemm(A, B)
+    assert np.array_equal(C, (A.long() @ B.long()).double().numpy())
+
+
+def test_dgemm_wrapper_and_edge_cases():
+    A = torch.randn(40, 50, dtype=torch.float64, device="cuda")
+    B = torch.randn(50, 33, dtype=torch.float64, device="cuda")
+    C = dig.ozaki_matmul(A, B)
+    assert dig.bigemm_last_launch_count() == 4
+    torch.cuda.synchronize()
+    assert torch.allclose(C, A @ B, rtol=0, atol=1e-13)
+    # K = 0: the empty sum
+    Z = dig.ozaki_matmul(torch.zeros(4, 0, dtype=torch.float64, device="cuda"),
+                         torch.zeros(0, 6, dtype=torch.float64, device="cuda"))
+    assert torch.equal(Z.cpu(), torch.zeros(4, 6, dtype=torch.float64))
+    # argument checks: odd ldc, missing workspace, bad slice count
+    c = torch.empty(40, 33, dtype=torch.float64, device="cuda")
+    assert dig.bigemm_ozaki_dgemm(A, B, c, 40, 33, 50, 50, 33, 33, 0, 0, None, 0, check=False) == 2
+    c2 = torch.empty(40, 34, dtype=torch.float64, device="cuda")
+    assert dig.bigemm_ozaki_dgemm(A, B, c2, 40, 33, 50, 50, 33, 34, 0, 0, None, 0, check=False) == 3
+    assert dig.bigemm_ozaki_dgemm(A, B, c2, 40, 33, 50, 50, 33, 34, 33, 0, None, 0, check=False) == 1
