@@ -486,6 +486,69 @@ def run_split_paths(dev) -> dict:
     return out
 
 
+def run_ozaki(dev, peaks) -> dict:
+    """The Ozaki scheme's binary64 product (bigemm_ozaki_dgemm) on N(0, 1)
+    float64 squares: time per call, the split's share, FP64-equivalent
+    TFLOP/s (2 M N K per call), the tensor-core rate of the slice-pair
+    products against the measured BF16 peak, and the error against cuBLAS's
+    own binary64 product.  At 8192 also a Fast Mode sweep of d."""
+    import deterministic_invariant_gemm_gb300 as dig
+    out = {}
+    bf16_peak = peaks["bf16_tflops"]
+    for n, iters in ((4096, 5), (8192, 3)):
+        g = workloads.generator(1000 + n)
+        A = torch.randn(n, n, generator=g, dtype=torch.float64).to(dev)
+        B = torch.randn(n, n, generator=g, dtype=torch.float64).to(dev)
+        C = torch.empty(n, n, dtype=torch.float64, device=dev)
+        s = dig.bigemm_ozaki_default_slices(n)
+        rho = dig.bigemm_ozaki_rho(n)
+        need = dig.bigemm_ozaki_workspace_bytes(n, n, n, 0)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        ref = A @ B                                  # cuBLAS binary64
+        scale = A.abs() @ B.abs()
+        cases = [s] if n != 8192 else [s, s - 1, s - 2, s - 3]
+        res = {"slices": s, "rho": rho}
+        for d in cases:
+            def call(i, d=d):
+                dig.bigemm_ozaki_dgemm(A, B, C, n, n, n, n, n, n, s, d, ws, need)
+            for i in range(2):
+                call(i)
+            secs = time_region(call, iters, 1)
+            per = secs / iters
+            pairs = dig.bigemm_ozaki_pairs(s, d)
+            err = float(((C - ref).abs() / scale).max())
+            res["d%d" % d] = {"pairs": pairs, "ms": round(per * 1e3, 3),
+                              "fp64_equiv_tflops": round(2.0 * n ** 3 / per / 1e12, 2),
+                              "max_err_vs_cublas_fp64_over_absAabsB": err}
+        # the split alone (rows of A, columns of B), to separate it from the products
+        rows_out = ws[: s * n * n * 2].view(torch.bfloat16)
+        exps = torch.empty(2 * n, dtype=torch.int32, device=dev)
+
+        def split(i):
+            dig.bigemm_ozaki_split(A, n, n, n, 0, rho, s, rows_out, n, n, exps)
+            dig.bigemm_ozaki_split(B, n, n, n, 1, rho, s, rows_out, n, n, exps[n:])
+        for i in range(2):
+            split(i)
+        t_split = time_region(split, iters, 1) / iters
+        full = res["d%d" % s]
+        t_gemm = full["ms"] / 1e3 - t_split
+        tensor = full["pairs"] * 2.0 * n ** 3 / t_gemm / 1e12
+        res["split_ms"] = round(t_split * 1e3, 3)
+        res["products_tensor_tflops"] = round(tensor, 1)
+        res["products_frac_of_bf16_peak"] = round(tensor / bf16_peak, 4)
+        # cuBLAS binary64 for context (this GPU's FP64 rate is low)
+        def dgemm(i):
+            torch.matmul(A, B, out=ref)
+        dgemm(0)
+        t64 = time_region(dgemm, 1, 1)
+        res["cublas_fp64_ms"] = round(t64 * 1e3, 2)
+        res["cublas_fp64_tflops"] = round(2.0 * n ** 3 / t64 / 1e12, 2)
+        out["ozaki_%d" % n] = res
+        del A, B, C, ws, ref, scale
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_decode_linear(dev, args) -> dict:
     """The headline step as linear layers (bigemm_linear, weights [N, K] plus a
     bias), timed the same way."""
@@ -521,6 +584,9 @@ SINGLE = {
     "linearfp8_8192": (8192, 8192, 8192, 1, True, "linear_fp8", "tensor_fp8"),
     # split-K at a size whose tiles fill the GPU: segments summed in the CTA
     "fold8192": (8192, 8192, 8192, 16, False, "uniform", "tensor"),
+    # binary64 product by the Ozaki scheme (bf16 slices on the tensor cores)
+    "ozaki8192": (8192, 8192, 8192, 1, False, "ozaki", "tensor"),
+    "ozaki4096": (4096, 4096, 4096, 1, False, "ozaki", "tensor"),
 }
 
 
@@ -529,11 +595,24 @@ def run_single(name, args, world, rank, dev, peaks, peak_src):
     rotating copies that together exceed L2."""
     import deterministic_invariant_gemm_gb300 as dig
     M, N, K, S, bf16, dist_name, bound = SINGLE[name]
-    esize = 1 if dist_name == "linear_fp8" else 2
+    esize = {"linear_fp8": 1, "ozaki": 8}.get(dist_name, 2)
     in_bytes = esize * (M * K + K * N)
     copies = max(1, min(8, math.ceil(2 * L2_BYTES / in_bytes)))
     C = torch.empty((M, N), dtype=torch.bfloat16 if bf16 else torch.float32, device=dev)
-    if dist_name in ("linear", "linear_fp8"):
+    if dist_name == "ozaki":
+        g = workloads.generator(98)
+        AB = [(torch.randn(M, K, generator=g, dtype=torch.float64).to(dev),
+               torch.randn(K, N, generator=g, dtype=torch.float64).to(dev))]
+        copies = 1
+        C = torch.empty((M, N), dtype=torch.float64, device=dev)
+        need = dig.bigemm_ozaki_workspace_bytes(M, N, K, 0)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        launches = 4
+
+        def call(i):
+            a, b = AB[0]
+            dig.bigemm_ozaki_dgemm(a, b, C, M, N, K, K, N, N, 0, 0, ws, need)
+    elif dist_name in ("linear", "linear_fp8"):
         g = workloads.generator(99)
         AB = [(torch.randn(M, K, generator=g), torch.randn(N, K, generator=g)) for _ in range(copies)]
         td = torch.float8_e4m3fn if dist_name == "linear_fp8" else torch.bfloat16
@@ -573,14 +652,25 @@ def run_single(name, args, world, rank, dev, peaks, peak_src):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": per * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3" if dist_name == "linear_fp8" else "bf16", "data": "synthetic",
+        "dtype": {"linear_fp8": "e4m3", "ozaki": "f64"}.get(dist_name, "bf16"), "data": "synthetic",
         "config": {"workload": "%s: M=%d N=%d K=%d split_k=%d, %s out, %s inputs" %
                    (name, M, N, K, S, "bf16" if bf16 else "fp32", dist_name),
                    "l2": "%d rotating input copies (%d MiB)" % (copies, copies * in_bytes >> 20),
                    "parallelism": "replicas"},
         "gpu_launches": launches * args.steps, "clocks": clocks,
     }
-    if bound in ("tensor", "tensor_fp8"):
+    if dist_name == "ozaki":
+        # value: binary64-equivalent 2 M N K per call; the tensor cores run one
+        # bf16 product per kept slice pair (split kernels included in the time)
+        s_ = dig.bigemm_ozaki_default_slices(K)
+        tens = dig.bigemm_ozaki_pairs(s_, s_) * flops
+        peak = peaks["bf16_tflops"]
+        line["config"]["slices"] = s_
+        line["roofline"] = {"kernel": "ozaki split kernels + bigemm_tc_kernel<kOutOzaki>",
+                            "bound": "tensor", "achieved": round(tens / per / 1e12, 1), "peak": peak,
+                            "peak_source": peak_src, "unit": "TFLOP/s",
+                            "frac": round(tens / per / 1e12 / peak, 4), "traffic": None}
+    elif bound in ("tensor", "tensor_fp8"):
         # an 8-bit product takes the measured bf16 peak times the nominal ratio 2
         peak = peaks["bf16_tflops"] * (2.0 if bound == "tensor_fp8" else 1.0)
         line["roofline"] = {"kernel": "bigemm_tc_kernel", "bound": "tensor",
@@ -839,6 +929,7 @@ def main():
         line["workloads"] = run_other_workloads(dev, peaks)
         line["workloads"]["decode_linear"] = run_decode_linear(dev, args)
         line["workloads"]["split_paths"] = run_split_paths(dev)
+        line["workloads"].update(run_ozaki(dev, peaks))
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
         print(json.dumps(line), flush=True)

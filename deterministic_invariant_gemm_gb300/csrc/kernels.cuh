@@ -467,13 +467,49 @@ __device__ __forceinline__ void ozaki_accumulate_block(double* crow, const int* 
                                                        int e_pair, const uint32_t (&r)[32],
                                                        bool first) {
     if (valid == 32) {
+        // all loads first (C and the column exponents), then the arithmetic,
+        // then the stores: 32 independent memory operations in flight
+        int e[32];
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-            double2 c = first ? make_double2(0.0, 0.0) : *reinterpret_cast<const double2*>(crow + j);
-            c.x = ozaki_term(c.x, r[j], e_pair + __ldg(cb + j));
-            c.y = ozaki_term(c.y, r[j + 1], e_pair + __ldg(cb + j + 1));
-            *reinterpret_cast<double2*>(crow + j) = c;
+        for (int j = 0; j < 32; j += 4) {
+            const int4 v = __ldg(reinterpret_cast<const int4*>(cb + j));
+            e[j] = e_pair + v.x;
+            e[j + 1] = e_pair + v.y;
+            e[j + 2] = e_pair + v.z;
+            e[j + 3] = e_pair + v.w;
         }
+        double2 c[16];
+        if (first) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) c[j] = make_double2(0.0, 0.0);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) c[j] = *reinterpret_cast<const double2*>(crow + 2 * j);
+        }
+        int lo = e[0], hi = e[0];
+#pragma unroll
+        for (int j = 1; j < 32; ++j) {
+            lo = min(lo, e[j]);
+            hi = max(hi, e[j]);
+        }
+        if (lo >= -1022 && hi <= 1023) {  // every 2^e a normal binary64: the fused path
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                c[j].x = __fma_rn(static_cast<double>(__uint_as_float(r[2 * j])),
+                                  __longlong_as_double(static_cast<long long>(e[2 * j] + 1023) << 52), c[j].x);
+                c[j].y = __fma_rn(static_cast<double>(__uint_as_float(r[2 * j + 1])),
+                                  __longlong_as_double(static_cast<long long>(e[2 * j + 1] + 1023) << 52),
+                                  c[j].y);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                c[j].x = ozaki_term(c[j].x, r[2 * j], e[2 * j]);
+                c[j].y = ozaki_term(c[j].y, r[2 * j + 1], e[2 * j + 1]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) *reinterpret_cast<double2*>(crow + 2 * j) = c[j];
     } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
@@ -578,15 +614,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
             if constexpr (kOut == kOutOzaki) {
-                // an Ozaki unit streams A and B once per slice pair (pa, pb):
-                // rows pa * M + m0 of the A slices, rows pb * oz_kpad + k of the
-                // B slices
-                for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-                    int mt, nt, seg;
-                    unit_coords(p, u, mt, nt, seg);
-                    const int n0 = nt * kBN;
-                    int pa = 0, pb = 0;
-                    for (int pair = 0; ok && pair < p.oz_pairs; ++pair) {
+                // Slice pairs outermost, then this CTA's tiles: all CTAs work on
+                // the same pair (pa, pb) at a time and share its A and B panels
+                // in L2.  Per tile: rows pa * M + m0 of the A slices, rows
+                // pb * oz_kpad + k of the B slices.
+                int pa = 0, pb = 0;
+                for (int pair = 0; ok && pair < p.oz_pairs; ++pair) {
+                    for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+                        int mt, nt, seg;
+                        unit_coords(p, u, mt, nt, seg);
+                        const int n0 = nt * kBN;
                         const int a_row = mt * kBM + pa * p.M;
                         const int b_row = pb * p.oz_kpad;
                         for (int kb = 0; kb < p.kb_total; ++kb) {
@@ -609,8 +646,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                 phase ^= 1u;
                             }
                         }
-                        ozaki_next_pair(p, pa, pb);
                     }
+                    ozaki_next_pair(p, pa, pb);
                 }
             } else {
             for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
@@ -778,15 +815,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             double* C = static_cast<double*>(p.out);
             const int step = p.oz_beta + 1;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-                int mt, nt, seg;
-                unit_coords(p, u, mt, nt, seg);
-                const int m0 = mt * kBM + q * 32, n0 = nt * kBN;
-                const int row = m0 + lane;
-                const bool row_ok = row < p.M;
-                const int ca = row_ok ? p.oz_ca[row] : 0;
-                int pa = 0, pb = 0;
-                for (int pair = 0; pair < p.oz_pairs; ++pair, ++t) {
+            // the producer's order: slice pairs outermost, then this CTA's tiles
+            int pa = 0, pb = 0;
+            for (int pair = 0; ok && pair < p.oz_pairs; ++pair) {
+                for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
+                    int mt, nt, seg;
+                    unit_coords(p, u, mt, nt, seg);
+                    const int m0 = mt * kBM + q * 32, n0 = nt * kBN;
+                    const int row = m0 + lane;
+                    const bool row_ok = row < p.M;
                     const int acc = t % kAccStages;
                     const uint32_t acc_phase = static_cast<uint32_t>(t / kAccStages) & 1u;
                     if (!wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.status, kErrWaitEpilogue)) {
@@ -797,7 +834,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     if (m0 < p.M) {
                         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                                static_cast<uint32_t>(acc * kBN);
-                        const int e_pair = (ca - pa * step) - pb * step;
+                        const int e_pair = row_ok ? (p.oz_ca[row] - pa * step) - pb * step : 0;
 #pragma unroll 1
                         for (int i = 0; i < 4; ++i) {
                             uint32_t r[32];
@@ -817,8 +854,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         tc_fence_before();
                         mbar_arrive(tempty_bar(acc));
                     }
-                    ozaki_next_pair(p, pa, pb);
                 }
+                ozaki_next_pair(p, pa, pb);
             }
         }
         if constexpr (kOut == kOutF32 || kOut == kOutBF16) {
