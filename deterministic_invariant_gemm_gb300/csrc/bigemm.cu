@@ -626,9 +626,13 @@ cudaError_t launch_ozaki_split(const DeviceInfo& d, const double* X, int64_t row
                                                                                         ld, exps);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    int64_t blocks = ceil_div(out_rows * cols, 256);
-    if (blocks > 16 * static_cast<int64_t>(d.sm_count)) blocks = 16 * static_cast<int64_t>(d.sm_count);
-    ozaki_split_cols_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+    // columns across threads, rows across blockIdx.y: about 16 blocks per SM
+    const int64_t bx = ceil_div(cols, 256);
+    int64_t by = ceil_div(16 * static_cast<int64_t>(d.sm_count), bx);
+    if (by > out_rows) by = out_rows;
+    if (by > 65535) by = 65535;
+    if (by < 1) by = 1;
+    ozaki_split_cols_kernel<<<dim3(static_cast<unsigned>(bx), static_cast<unsigned>(by)), 256, 0, stream>>>(
         X, rows, cols, ld, out_rows, rho, slices, out, out_ld, out_rows * out_ld, exps);
     return cudaGetLastError();
 }

@@ -463,6 +463,17 @@ __device__ __forceinline__ double ozaki_term(double c, uint32_t pbits, int e) {
     return __dadd_rn(c, ldexp(P, e));
 }
 
+// 2^e * P for the bit pattern of a binary32 P that is zero or normal, with
+// e + exponent(P) inside the normal binary64 range: sign kept, exponent
+// moved by e and rebiased, the 23 fraction bits widened to 52.
+__device__ __forceinline__ double ozaki_scaled(uint32_t pbits, int e) {
+    const uint32_t mag = pbits & 0x7FFFFFFFu;
+    const uint64_t bits = (static_cast<uint64_t>(pbits >> 31) << 63) |
+                          (static_cast<uint64_t>(static_cast<int>(mag >> 23) - 127 + e + 1023) << 52) |
+                          (static_cast<uint64_t>(mag & 0x7FFFFFu) << 29);
+    return mag != 0u ? __longlong_as_double(static_cast<long long>(bits)) : 0.0;
+}
+
 __device__ __forceinline__ void ozaki_accumulate_block(double* crow, const int* cb, int valid,
                                                        int e_pair, const uint32_t (&r)[32],
                                                        bool first) {
@@ -492,14 +503,15 @@ __device__ __forceinline__ void ozaki_accumulate_block(double* crow, const int* 
             lo = min(lo, e[j]);
             hi = max(hi, e[j]);
         }
-        if (lo >= -1022 && hi <= 1023) {  // every 2^e a normal binary64: the fused path
+        if (lo >= -1006 && hi <= 1001) {
+            // P is a nonzero multiple of 2^-16 below 2^24, or zero, so 2^e P is a
+            // normal binary64 for e in this range: build it from P's bits
+            // (exponent rebiased, fraction widened) -- exact, integer work only
+            // -- and spend one binary64 addition per element.
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                c[j].x = __fma_rn(static_cast<double>(__uint_as_float(r[2 * j])),
-                                  __longlong_as_double(static_cast<long long>(e[2 * j] + 1023) << 52), c[j].x);
-                c[j].y = __fma_rn(static_cast<double>(__uint_as_float(r[2 * j + 1])),
-                                  __longlong_as_double(static_cast<long long>(e[2 * j + 1] + 1023) << 52),
-                                  c[j].y);
+                c[j].x = __dadd_rn(c[j].x, ozaki_scaled(r[2 * j], e[2 * j]));
+                c[j].y = __dadd_rn(c[j].y, ozaki_scaled(r[2 * j + 1], e[2 * j + 1]));
             }
         } else {
 #pragma unroll

@@ -129,17 +129,18 @@ __global__ void __launch_bounds__(256)
 
 // The column split: element (r, j) of X [rows][cols] goes to
 // out[p * plane + r * out_ld + j]; rows rows .. out_rows-1 of every slice
-// (the padding up to a whole K block) are written as zeros.
+// (the padding up to a whole K block) are written as zeros.  Threads run
+// along a row (coalesced), blocks along y step through the rows.
 __global__ void __launch_bounds__(256)
     ozaki_split_cols_kernel(const double* __restrict__ X, int64_t rows, int64_t cols, int64_t ld,
                             int64_t out_rows, int rho, int slices, __nv_bfloat16* __restrict__ out,
                             int64_t out_ld, int64_t plane, const int* __restrict__ exps) {
-    const int64_t total = out_rows * cols;
-    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
-         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = e / cols, j = e - r * cols;
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (j >= cols) return;
+    const int c1 = exps[j];
+    for (int64_t r = blockIdx.y; r < out_rows; r += gridDim.y) {
         const double x = r < rows ? X[r * ld + j] : 0.0;
-        ozaki_split_value(x, exps[j], rho, slices, out + r * out_ld + j, plane);
+        ozaki_split_value(x, c1, rho, slices, out + r * out_ld + j, plane);
     }
 }
 
