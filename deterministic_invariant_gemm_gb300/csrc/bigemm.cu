@@ -393,7 +393,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
                        int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int split_k, void* ws,
                        size_t ws_bytes, cudaStream_t stream, bool wt = false,
                        const void* bias = nullptr, int fp8_fmt_a = -1, int fp8_fmt_b = -1,
-                       float scale = 1.0f) {
+                       float scale = 1.0f, bool selftest_stall = false) {
     // fp8_fmt_a / fp8_fmt_b >= 0: 8-bit float operands (0 = E4M3, 1 = E5M2), W layout
     const bool fp8 = fp8_fmt_a >= 0;
     const int kb_elems = fp8 ? 128 : kBK;
@@ -486,6 +486,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     p.group_m = (m_tiles * n_tiles >= 4 * static_cast<int64_t>(d->sm_count)) ? 16 : 8;
     p.fold = fold ? 1 : 0;
     p.cluster = cluster ? 1 : 0;
+    p.selftest_stall = selftest_stall ? 1 : 0;
     // the scale and the bias follow the full sum: in this kernel unless a
     // reduction kernel forms that sum
     const bool sum_here = (splits == 1) || fold || cluster;
@@ -831,6 +832,19 @@ bigemm_status bigemm_run_splitk_static(const void* A, const void* B, float* C, i
     return run_impl(kModeF32, A, B, C, M, N, K, lda, ldb, ldc, split_k, scratch,
                     scratch ? static_cast<size_t>(BIGEMM_STATIC_SCRATCH_BYTES) : 0,
                     static_cast<cudaStream_t>(stream));
+}
+
+bigemm_status bigemm_selftest_timeout(bigemm_stream stream) {
+    g_last_launches = 0;
+    void* scratch = nullptr;
+    const bigemm_status st = static_scratch_address(&scratch);
+    if (st != BIGEMM_OK) return st;
+    // a 16 x 256 x 512 split-K partial product whose operands and workspace
+    // sit in the built-in array; nothing is ever loaded or stored
+    unsigned char* base = static_cast<unsigned char*>(scratch);
+    return run_impl(kModePartial, base, base + (64 << 10), nullptr, 16, 256, 512, 512, 256, 0, 1,
+                    base + (1 << 20), 16 * 256 * 4, static_cast<cudaStream_t>(stream), false, nullptr,
+                    -1, -1, 1.0f, /*selftest_stall=*/true);
 }
 
 int bigemm_ozaki_rho(int64_t K) { return (K < 1 || K > kOzakiMaxK) ? -1 : ozaki_rho(K); }

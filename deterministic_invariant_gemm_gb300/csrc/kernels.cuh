@@ -151,6 +151,8 @@ struct GemmParams {
     const int* oz_ca;       // c^(1) of every row of A
     const int* oz_cb;       // c^(1) of every column of B
     int oz_slices, oz_d, oz_beta, oz_pairs, oz_kpad;
+    int selftest_stall;     // 1 (the failure self-test only): the producer issues no
+                            //    loads, so the MMA issuer's bounded wait must give up
 };
 
 // The slice pairs of the Ozaki scheme in the order of the binary64
@@ -624,7 +626,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
-            bool ok = true;
+            bool ok = !p.selftest_stall;  // the failure self-test issues nothing
             if constexpr (kOut == kOutOzaki) {
                 // Slice pairs outermost, then this CTA's tiles: all CTAs work on
                 // the same pair (pa, pb) at a time and share its A and B panels

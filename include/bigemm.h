@@ -405,8 +405,19 @@ BIGEMM_API bigemm_status bigemm_run_splitk_static(const void *A, const void *B, 
  * Returns BIGEMM_OK, BIGEMM_ERR_TIMEOUT or BIGEMM_ERR_CUDA. */
 BIGEMM_API bigemm_status bigemm_device_status(int reset);
 
+/* Self-test of the failure path; the pages have no counterpart.  Enqueues one
+ * split-K partial kernel (16 x 256 x 512, operands in the built-in scratch
+ * array of bigemm_run_splitk_static) whose producer issues no loads, so its
+ * MMA issuer's bounded wait gives up after 2 s: the kernel raises its abort
+ * flag, the other roles leave their waits, nothing is loaded or stored, TMEM
+ * is freed and the kernel ends with the wait's bit set in the device error
+ * word.  A later bigemm_device_status() then returns BIGEMM_ERR_TIMEOUT, and
+ * the context stays usable.  Shares the scratch array with
+ * bigemm_run_splitk_static (calls must not overlap). */
+BIGEMM_API bigemm_status bigemm_selftest_timeout(bigemm_stream stream);
+
 /* Number of kernels the most recent successful call on this host thread
- * enqueued (0, 1 or 2). */
+ * enqueued (0 to 4). */
 BIGEMM_API int bigemm_last_launch_count(void);
 
 #ifdef __cplusplus
