@@ -324,9 +324,10 @@ def matmul(A, B, out_dtype=None, split_k: int = 1, out=None, workspace=None, str
     """C = A @ B for bf16 CUDA tensors A [M, K] and B [K, N] (row-major, unit
     column stride; leading dimensions may be padded).  ``out_dtype`` is
     torch.float32 (default) or torch.bfloat16.  ``split_k``: 1 = none, 0 = the
-    K-only default, S > 1 = S segments through a workspace (allocated here
-    with torch when not given).  ``atomic=True`` runs the nondeterministic
-    atomic-add contrast instead (fp32 only)."""
+    K-only default, S > 1 = S segments added in a fixed order (through a
+    workspace, allocated here with torch when one is needed and not given, or
+    inside the CTA or a cluster; see bigemm_split_path).  ``atomic=True`` runs
+    the nondeterministic atomic-add contrast instead (fp32 only)."""
     import torch
     if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
         raise TypeError("A and B must be bfloat16")

@@ -188,8 +188,11 @@ BIGEMM_API size_t bigemm_partial_workspace_bytes(int64_t M, int64_t N, int64_t K
 
 /* C (fp32) = A * B.  A: bf16 [M, K] (lda), B: bf16 [K, N] (ldb), C: fp32
  * [M, N] (ldc).  split_k: 1 = no split, 0 = bigemm_default_split_k(K), S > 1 =
- * S segments through the workspace and the fixed-order reduction kernel.
- * workspace / workspace_bytes may be NULL / 0 when no workspace is needed. */
+ * S segments whose FP32 partials are added in the order 0..S-1: through the
+ * workspace and the reduction kernel, inside the CTA for products that fill
+ * the GPU with tiles, or inside a thread-block cluster for small ones
+ * (bigemm_split_path names the way; all give the same bits).  workspace /
+ * workspace_bytes may be NULL / 0 when bigemm_workspace_bytes is 0. */
 BIGEMM_API bigemm_status bigemm_run(const void *A, const void *B, float *C,
                          int64_t M, int64_t N, int64_t K,
                          int64_t lda, int64_t ldb, int64_t ldc,
