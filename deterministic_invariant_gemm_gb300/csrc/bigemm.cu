@@ -261,6 +261,10 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t esize, c
 // columns x 64 k-rows, or a weight matrix W [N, K] (wt) in boxes of 64 k x 256
 // rows; all with the 128-byte swizzle the MMA descriptors use.  The second
 // operand again in 256 x 256 boxes without swizzle, used only to warm L2.
+// Rows of A a stage loads: the batch rounded up to 32, 64 or 128 (a function of
+// M that changes no sum -- the other rows of the 128-row MMA operand are zero).
+int a_box_rows(int64_t M) { return M <= 32 ? 32 : (M <= 64 ? 64 : kBM); }
+
 bool encode_operands(CUtensorMap* tmA, CUtensorMap* tmB, CUtensorMap* tmBp, const void* A,
                      const void* B, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                      bool wt, bool fp8) {
@@ -270,7 +274,7 @@ bool encode_operands(CUtensorMap* tmA, CUtensorMap* tmB, CUtensorMap* tmBp, cons
     const uint32_t es = fp8 ? 1u : 2u;
     const int64_t da[2] = {K, M};
     const int64_t db[2] = {wt ? K : N, wt ? N : K};
-    const uint32_t ba[2] = {kb, static_cast<uint32_t>(kBM)};
+    const uint32_t ba[2] = {kb, static_cast<uint32_t>(a_box_rows(M))};
     const uint32_t bb[2] = {wt ? kb : kBChunkCols, wt ? static_cast<uint32_t>(kBN) : kb};
     const uint32_t bp[2] = {wt ? static_cast<uint32_t>(kPrefetchRows) : static_cast<uint32_t>(kBN),
                             wt ? static_cast<uint32_t>(kBN) : static_cast<uint32_t>(kPrefetchRows)};
@@ -487,6 +491,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     p.fold = fold ? 1 : 0;
     p.cluster = cluster ? 1 : 0;
     p.selftest_stall = selftest_stall ? 1 : 0;
+    p.a_rows = a_box_rows(M);
     // the scale and the bias follow the full sum: in this kernel unless a
     // reduction kernel forms that sum
     const bool sum_here = (splits == 1) || fold || cluster;
@@ -973,6 +978,7 @@ bigemm_status bigemm_ozaki_dgemm(const double* A, const double* B, double* C, in
     p.oz_beta = 53 - rho;
     p.oz_pairs = static_cast<int>(pairs);
     p.oz_kpad = static_cast<int>(L.kpad);
+    p.a_rows = kBM;
     const int grid = static_cast<int>(p.units < dev->sm_count ? p.units : dev->sm_count);
     if (launch_gemm<kOutOzaki>(false, false, dim3(static_cast<unsigned>(grid)), dim3(kNumThreads), strm,
                                tmA, tmB, tmBp, tmA, p) != cudaSuccess)

@@ -153,6 +153,8 @@ struct GemmParams {
     int oz_slices, oz_d, oz_beta, oz_pairs, oz_kpad;
     int selftest_stall;     // 1 (the failure self-test only): the producer issues no
                             //    loads, so the MMA issuer's bounded wait must give up
+    int a_rows;             // rows of A each stage loads (32, 64 or 128: the batch
+                            //    rounded up); the stage's other rows stay zero
 };
 
 // The slice pairs of the Ozaki scheme in the order of the binary64
@@ -609,6 +611,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
+    if (p.a_rows < kBM) {
+        // A short batch loads only its first a_rows rows of A per stage; the
+        // MMA still reads all 128 (one instruction shape for every M), so the
+        // rest of every A stage is zeroed once here and never written again.
+        // Those rows feed only output rows >= M, which are never stored.
+        const uint32_t tail = static_cast<uint32_t>(p.a_rows) * 128u;
+        const uint32_t per_stage = (kABytes - tail) / 16u;
+        for (uint32_t i = threadIdx.x; i < kStages * per_stage; i += kNumThreads) {
+            const uint32_t s_ = i / per_stage, c = i - s_ * per_stage;
+            st_shared_v4(sA + s_ * kABytes + tail + c * 16u, 0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // visible to the tensor core's (async-proxy) reads
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -678,7 +693,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         break;
                     }
                     const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, kStageBytes);
+                    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(p.a_rows) * 128u + kBBytes);
                     tma_load_2d(sA + stage * kABytes, &tmA, fb, kb * kKB, m0);
                     if constexpr (kWt) {
                         // one box: 256 weight rows x 64 k (128 bytes each)
