@@ -20,7 +20,8 @@ LIB_PATH = os.path.join(HERE, "libbigemm.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = [os.path.join(CSRC, "bigemm.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("kernels.cuh", "ptx.cuh")] + \
+# every header in csrc/ (kernels, PTX wrappers, the Ozaki split) and the C ABI
+DEPENDS = SOURCES + sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")) + \
     [os.path.join(INCLUDE, "bigemm.h")]
 
 NVCC_FLAGS = [
