@@ -585,6 +585,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
+    // The coordinates of this CTA's first unit, found by the producer thread
+    // while the previous kernel in the stream finishes and reused for its first
+    // loads (working them out after the dependency wait put some 0.5 us between
+    // the wait and the first load of every CTA).
+    int first_mt = 0, first_nt = 0, first_seg = 0;
     if (warp == 0 && lane == 0) {
         // Warm L2 with the weights of this CTA's first unit (its first
         // p.prefetch_rows K rows) while the previous kernel in the stream
@@ -593,8 +598,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // dependency wait below.
         tma_prefetch_desc(&tmBp);
         if (static_cast<int>(blockIdx.x) < p.units) {
-            int mt, nt, seg;
-            unit_coords(p, blockIdx.x, mt, nt, seg);
+            unit_coords(p, blockIdx.x, first_mt, first_nt, first_seg);
+            const int mt = first_mt, nt = first_nt, seg = first_seg;
+            (void)mt;
             const int k0 = seg * p.kb_per_split * kKB;
             const int seg_rows = (p.fold ? p.kb_total : p.kb_per_split) * kKB;
             const int k1 = min(k0 + p.prefetch_rows, min(k0 + seg_rows, p.kb_total * kKB));
@@ -616,13 +622,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // MMA still reads all 128 (one instruction shape for every M), so the
         // rest of every A stage is zeroed once here and never written again.
         // Those rows feed only output rows >= M, which are never stored.
+        // (by the epilogue warps, idle until the first tile is done, so that
+        // the producer thread's prologue stays short)
         const uint32_t tail = static_cast<uint32_t>(p.a_rows) * 128u;
         const uint32_t per_stage = (kABytes - tail) / 16u;
-        for (uint32_t i = threadIdx.x; i < kStages * per_stage; i += kNumThreads) {
+        for (uint32_t i = threadIdx.x - kEpilogueWarp0 * 32; threadIdx.x >= kEpilogueWarp0 * 32 &&
+                                                          i < kStages * per_stage;
+             i += kEpilogueThreads) {
             const uint32_t s_ = i / per_stage, c = i - s_ * per_stage;
             st_shared_v4(sA + s_ * kABytes + tail + c * 16u, 0u, 0u, 0u, 0u);
         }
-        fence_proxy_async_smem();  // visible to the tensor core's (async-proxy) reads
+        if (threadIdx.x >= kEpilogueWarp0 * 32)
+            fence_proxy_async_smem();  // visible to the tensor core's (async-proxy) reads
     }
     tc_fence_before();
     __syncthreads();
@@ -680,8 +691,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
             } else {
             for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-                int mt, nt, seg;
-                unit_coords(p, u, mt, nt, seg);
+                int mt = first_mt, nt = first_nt, seg = first_seg;
+                if (u != static_cast<int>(blockIdx.x)) unit_coords(p, u, mt, nt, seg);
                 // a folded unit streams all of K; its segments follow one another
                 const int kb0 = p.fold ? 0 : seg * p.kb_per_split;
                 const int kb1 = p.fold ? p.kb_total : min(kb0 + p.kb_per_split, p.kb_total);
