@@ -78,35 +78,39 @@ bigemm_status device_info(const DeviceInfo** out) {
         d.sm_count = sms;
         if (d.supported) {
             const int smem = static_cast<int>(kSmemBytes);
-            // Besides the shared-memory opt-in: every GEMM kernel must have been
-            // compiled with kLaunchRegs registers per thread, because its
-            // warpgroups re-divide exactly that allocation (setmaxnreg); with
-            // fewer, the epilogue's register increase could never be granted.
-            const auto opt_in = [smem](const void* fn) {
+            // Besides the shared-memory opt-in: a GEMM kernel whose warpgroups
+            // re-divide their registers (setmaxnreg: the direct-output and Ozaki
+            // epilogues) must have been compiled with kLaunchRegs registers per
+            // thread, the allocation that re-division assumes; with fewer, the
+            // epilogue's register increase could never be granted.
+            const auto opt_in = [smem](const void* fn, bool split_regs) {
                 cudaFuncAttributes fa;
                 if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return BIGEMM_ERR_CUDA;
-                if (fa.numRegs < kLaunchRegs || fa.maxThreadsPerBlock < kNumThreads)
+                if ((split_regs && fa.numRegs < kLaunchRegs) || fa.maxThreadsPerBlock < kNumThreads)
                     return BIGEMM_ERR_UNSUPPORTED;
                 return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
                                cudaSuccess
                            ? BIGEMM_OK
                            : BIGEMM_ERR_CUDA;
             };
-            const void* const kernels[] = {
-                (const void*)bigemm_tc_kernel<kOutF32, false, false>,
-                (const void*)bigemm_tc_kernel<kOutBF16, false, false>,
-                (const void*)bigemm_tc_kernel<kOutSlices, false, false>,
-                (const void*)bigemm_tc_kernel<kOutAtomic, false, false>,
-                (const void*)bigemm_tc_kernel<kOutF32, true, false>,
-                (const void*)bigemm_tc_kernel<kOutBF16, true, false>,
-                (const void*)bigemm_tc_kernel<kOutSlices, true, false>,
-                (const void*)bigemm_tc_kernel<kOutF32, true, true>,
-                (const void*)bigemm_tc_kernel<kOutBF16, true, true>,
-                (const void*)bigemm_tc_kernel<kOutSlices, true, true>,
-                (const void*)bigemm_tc_kernel<kOutOzaki, false, false>,
+            const struct {
+                const void* fn;
+                bool split_regs;
+            } kernels[] = {
+                {(const void*)bigemm_tc_kernel<kOutF32, false, false>, true},
+                {(const void*)bigemm_tc_kernel<kOutBF16, false, false>, true},
+                {(const void*)bigemm_tc_kernel<kOutSlices, false, false>, false},
+                {(const void*)bigemm_tc_kernel<kOutAtomic, false, false>, false},
+                {(const void*)bigemm_tc_kernel<kOutF32, true, false>, true},
+                {(const void*)bigemm_tc_kernel<kOutBF16, true, false>, true},
+                {(const void*)bigemm_tc_kernel<kOutSlices, true, false>, false},
+                {(const void*)bigemm_tc_kernel<kOutF32, true, true>, true},
+                {(const void*)bigemm_tc_kernel<kOutBF16, true, true>, true},
+                {(const void*)bigemm_tc_kernel<kOutSlices, true, true>, false},
+                {(const void*)bigemm_tc_kernel<kOutOzaki, false, false>, true},
             };
-            for (const void* fn : kernels) {
-                const bigemm_status st = opt_in(fn);
+            for (const auto& k : kernels) {
+                const bigemm_status st = opt_in(k.fn, k.split_regs);
                 if (st != BIGEMM_OK) return st;
             }
             void* sym = nullptr;

@@ -193,6 +193,57 @@ __device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& mt,
     nt = r / gm;
 }
 
+// The scheduling parameters the producer thread needs, read from the kernel
+// parameters in one batch: each first read of a parameter line misses the
+// constant cache (the parameters are new at every launch), and read one after
+// another as they are needed these misses lay end to end on the way to every
+// CTA's first load.
+struct Sched {
+    int units, m_tiles, n_tiles, group_m, splits, cluster;
+    int fold, kb_total, kb_per_split, prefetch_rows, a_rows, selftest_stall;
+};
+
+__device__ __forceinline__ Sched load_sched(const GemmParams& p) {
+    Sched s;
+    s.units = p.units;
+    s.m_tiles = p.m_tiles;
+    s.n_tiles = p.n_tiles;
+    s.group_m = p.group_m;
+    s.splits = p.splits;
+    s.cluster = p.cluster;
+    s.fold = p.fold;
+    s.kb_total = p.kb_total;
+    s.kb_per_split = p.kb_per_split;
+    s.prefetch_rows = p.prefetch_rows;
+    s.a_rows = p.a_rows;
+    s.selftest_stall = p.selftest_stall;
+    // all twelve values arrive together here
+    asm volatile("" ::"r"(s.units), "r"(s.m_tiles), "r"(s.n_tiles), "r"(s.group_m), "r"(s.splits),
+                 "r"(s.cluster), "r"(s.fold), "r"(s.kb_total), "r"(s.kb_per_split), "r"(s.prefetch_rows),
+                 "r"(s.a_rows), "r"(s.selftest_stall));
+    return s;
+}
+
+// unit_coords on the preloaded values (the same mapping).
+__device__ __forceinline__ void unit_coords(const Sched& p, int u, int& mt, int& nt, int& seg) {
+    const int tiles = p.m_tiles * p.n_tiles;
+    int tile;
+    if (p.cluster) {
+        tile = u / p.splits;
+        seg = u - tile * p.splits;
+    } else {
+        seg = u / tiles;
+        tile = u - seg * tiles;
+    }
+    const int per_group = p.group_m * p.n_tiles;
+    const int g = tile / per_group;
+    const int first_m = g * p.group_m;
+    const int gm = min(p.m_tiles - first_m, p.group_m);
+    const int r = tile - g * per_group;
+    mt = first_m + r % gm;
+    nt = r / gm;
+}
+
 // Bounded wait on an mbarrier phase.  Gives up when another role has aborted
 // (shared flag) or after kWaitTimeoutNs; a timeout raises the abort flag and
 // records `why` in the device error word.  Never traps.
@@ -590,20 +641,21 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // loads (working them out after the dependency wait put some 0.5 us between
     // the wait and the first load of every CTA).
     int first_mt = 0, first_nt = 0, first_seg = 0;
+    Sched sc{};
     if (warp == 0 && lane == 0) {
+        sc = load_sched(p);
         // Warm L2 with the weights of this CTA's first unit (its first
         // p.prefetch_rows K rows) while the previous kernel in the stream
         // finishes.  An L2 prefetch writes no shared memory and L2 is the
         // device's point of coherence, so it cannot expose data older than the
         // dependency wait below.
         tma_prefetch_desc(&tmBp);
-        if (static_cast<int>(blockIdx.x) < p.units) {
-            unit_coords(p, blockIdx.x, first_mt, first_nt, first_seg);
-            const int mt = first_mt, nt = first_nt, seg = first_seg;
-            (void)mt;
-            const int k0 = seg * p.kb_per_split * kKB;
-            const int seg_rows = (p.fold ? p.kb_total : p.kb_per_split) * kKB;
-            const int k1 = min(k0 + p.prefetch_rows, min(k0 + seg_rows, p.kb_total * kKB));
+        if (static_cast<int>(blockIdx.x) < sc.units) {
+            unit_coords(sc, blockIdx.x, first_mt, first_nt, first_seg);
+            const int nt = first_nt, seg = first_seg;
+            const int k0 = seg * sc.kb_per_split * kKB;
+            const int seg_rows = (sc.fold ? sc.kb_total : sc.kb_per_split) * kKB;
+            const int k1 = min(k0 + sc.prefetch_rows, min(k0 + seg_rows, sc.kb_total * kKB));
             for (int k = k0; k < k1; k += kPrefetchRows) {
                 if constexpr (kWt) tma_prefetch_l2_2d(&tmBp, k, nt * kBN);
                 else tma_prefetch_l2_2d(&tmBp, nt * kBN, k);
@@ -644,15 +696,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // global memory is read and written only after it has completed.
     grid_dependency_wait();
 
+    // Only the direct-output epilogues (the folded running sum) and the Ozaki
+    // epilogue need more than the launch's 168 registers per thread; the
+    // others skip the re-division (it sits between the dependency wait and
+    // the first load).
+    constexpr bool kSplitRegs = (kOut == kOutF32 || kOut == kOutBF16 || kOut == kOutOzaki);
     if (warp < kEpilogueWarp0) {
-      regs_release_to<kFrontRegs>();
+      if constexpr (kSplitRegs) regs_release_to<kFrontRegs>();
       if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer --
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
-            bool ok = !p.selftest_stall;  // the failure self-test issues nothing
+            bool ok = !sc.selftest_stall;  // the failure self-test issues nothing
             if constexpr (kOut == kOutOzaki) {
                 // Slice pairs outermost, then this CTA's tiles: all CTAs work on
                 // the same pair (pa, pb) at a time and share its A and B panels
@@ -690,12 +747,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     ozaki_next_pair(p, pa, pb);
                 }
             } else {
-            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < sc.units; u += gridDim.x) {
                 int mt = first_mt, nt = first_nt, seg = first_seg;
-                if (u != static_cast<int>(blockIdx.x)) unit_coords(p, u, mt, nt, seg);
+                if (u != static_cast<int>(blockIdx.x)) unit_coords(sc, u, mt, nt, seg);
                 // a folded unit streams all of K; its segments follow one another
-                const int kb0 = p.fold ? 0 : seg * p.kb_per_split;
-                const int kb1 = p.fold ? p.kb_total : min(kb0 + p.kb_per_split, p.kb_total);
+                const int kb0 = sc.fold ? 0 : seg * sc.kb_per_split;
+                const int kb1 = sc.fold ? sc.kb_total : min(kb0 + sc.kb_per_split, sc.kb_total);
                 const int m0 = mt * kBM, n0 = nt * kBN;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.status,
@@ -704,7 +761,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         break;
                     }
                     const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(p.a_rows) * 128u + kBBytes);
+                    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(sc.a_rows) * 128u + kBBytes);
                     tma_load_2d(sA + stage * kABytes, &tmA, fb, kb * kKB, m0);
                     if constexpr (kWt) {
                         // one box: 256 weight rows x 64 k (128 bytes each)
@@ -818,7 +875,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
       }
     } else {
-        regs_grow_to<kEpilogueRegs>();
+        if constexpr (kSplitRegs) regs_grow_to<kEpilogueRegs>();
         // ------------------------------------------------------ epilogue --
         // Warp w reads TMEM lanes 32 (w % 4) .. +31, i.e. tile rows q*32 .. q*32+31,
         // and the columns of half h = (w - 4) / 4 of the tile (128 each).
