@@ -706,6 +706,60 @@ def run_single(name, args, world, rank, dev, peaks, peak_src):
         print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ long K --
+
+def run_longk(dev, peaks) -> dict:
+    """M = N = 256, K = 65536 with split_k = 8, 16, 32 through bigemm_run (the
+    path the library picks: a cluster of CTAs or the workspace + reduction
+    kernel; the bits are the workspace path's either way), and the atomic-add
+    contrast at the same splits: its time, and how many distinct results ten
+    runs on the same inputs give (the workspace path gives one).  Four input
+    copies rotate (256 MiB > L2)."""
+    import deterministic_invariant_gemm_gb300 as dig
+    M = N = 256
+    K = 65536
+    copies = 4
+    AB = [workloads.pair(M, N, K, 4321 + c, dist="normal") for c in range(copies)]
+    AB = [(a.to(dev), b.to(dev)) for a, b in AB]
+    C = torch.empty((M, N), dtype=torch.float32, device=dev)
+    alg = 2.0 * (M * K + K * N) + 4.0 * M * N
+    out = {"shape": [M, N, K], "input_copies": copies,
+           "alg_bytes": alg, "peak_gbs": peaks["hbm_gbs"]}
+    iters = 40
+    for S in (8, 16, 32):
+        wsb = dig.bigemm_workspace_bytes(M, N, K, S)
+        ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+
+        def call(i):
+            a, b = AB[i % copies]
+            dig.bigemm_run(a, b, C, M, N, K, K, N, N, S, ws, wsb)
+
+        def atomic(i):
+            a, b = AB[i % copies]
+            dig.bigemm_run_atomic_splitk(a, b, C, M, N, K, K, N, N, S)
+
+        res = {"path": {0: "unsplit", 1: "workspace", 2: "folded", 3: "cluster"}.get(
+            dig.bigemm_split_path(M, N, K, S), "?")}
+        for key, fn in (("bigemm_run", call), ("atomic", atomic)):
+            for i in range(3):
+                fn(i)
+            secs = time_region(fn, iters, 1) / iters
+            res[key] = {"us": round(secs * 1e6, 2),
+                        "hbm_frac": round(alg / secs / 1e9 / peaks["hbm_gbs"], 4),
+                        "tflops": round(2.0 * M * N * K / secs / 1e12, 2)}
+            distinct = set()
+            for _ in range(10):
+                fn(0)
+                torch.cuda.synchronize()
+                distinct.add(hash(C.cpu().numpy().tobytes()))
+            res[key]["distinct_results_in_10_runs"] = len(distinct)
+        out["s%d" % S] = res
+        del ws
+    del AB, C
+    torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------- other shapes --
 
 def run_other_workloads(dev, peaks) -> dict:
@@ -718,7 +772,6 @@ def run_other_workloads(dev, peaks) -> dict:
              ("square_4096", 4096, 4096, 4096, 1, False, "uniform", 10),
              ("square_8192", 8192, 8192, 8192, 1, False, "uniform", 10),
              ("large_16384_bf16out", 16384, 16384, 16384, 1, True, "normal", 5),
-             ("longk_256x256x65536_s16", 256, 256, 65536, 16, False, "normal", 20),
              # split products large enough to fold their segments in the CTA
              ("square_4096_split8_folded", 4096, 4096, 4096, 8, False, "uniform", 10),
              ("square_8192_split16_folded", 8192, 8192, 8192, 16, False, "uniform", 10),
@@ -745,9 +798,6 @@ def run_other_workloads(dev, peaks) -> dict:
                      "ms": round(secs * 1e3 / iters, 4), "split_k": S,
                      "out": "bf16" if bf16 else "fp32", "input_copies": copies,
                      "launches": dig.bigemm_last_launch_count()}
-        if name.startswith("longk"):
-            alg = 2.0 * (M * K + K * N) + 4.0 * M * N
-            out[name]["hbm_frac"] = round(alg / (secs / iters) / 1e9 / peaks["hbm_gbs"], 4)
         del AB, C, ws
         torch.cuda.empty_cache()
     # linear layers, weights [N, K]: BF16 and 8-bit floats (E4M3).  The FP8
@@ -946,6 +996,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_extras:
         line["e2e"] = run_e2e(bench, max(20, args.steps // 20), 5)
         line["workloads"] = run_other_workloads(dev, peaks)
+        line["workloads"]["longk_256x256x65536"] = run_longk(dev, peaks)
         line["workloads"]["decode_linear"] = run_decode_linear(dev, args)
         line["workloads"]["split_paths"] = run_split_paths(dev)
         line["workloads"].update(run_ozaki(dev, peaks))

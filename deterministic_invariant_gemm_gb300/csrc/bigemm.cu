@@ -377,10 +377,14 @@ bigemm_status launch_reduce(const DeviceInfo& d, const float* ws, int splits, in
     const __nv_bfloat16* b = static_cast<const __nv_bfloat16*>(bias);
     const int64_t ws_ld = ws_ld_of(N);
     const int64_t items = M * (ws_ld / 4);
-    // At most one block per SM, so the reduction never crowds out the next
-    // kernel's blocks while it waits for the partial kernel.
+    // One thread per four-column group, all groups in flight at once up to
+    // the SMs' thread capacity (16 blocks of 128 per SM); beyond that the
+    // threads loop.  A decode-sized sum is bound by the latency of its L2
+    // reads, so every read should be issued in the first round: capping the
+    // grid at one block per SM made each thread of an M = 64 sum wait for
+    // four rounds of reads.
     int64_t blocks = ceil_div(items, kReduceThreads);
-    if (blocks > d.sm_count) blocks = d.sm_count;
+    if (blocks > 16LL * d.sm_count) blocks = 16LL * d.sm_count;
     if (blocks < 1) blocks = 1;
     cudaError_t e;
     if (bf16)
