@@ -172,3 +172,60 @@ def test_atomic_contrast_spread(capsys):
         assert bits_equal(det[0], det[1]) and bits_equal(det[0], det[2])
     with capsys.disabled():
         print("\n[atomic split-K contrast] " + "; ".join(report))
+
+
+# ------------------------------- short and long batches in the partial kernel --
+
+@pytest.mark.parametrize("N,K,S", [(256, 512, 2), (296, 1000, 3), (520, 3000, 6), (4096, 4096, 8)])
+def test_partials_same_bits_for_short_and_long_batches(N, K, S):
+    """The split-K partial kernel loads only the batch's rows of A for short
+    batches (a 32- or 64-row A box, the rest of each stage zero) and 128-row
+    boxes otherwise.  Every workspace slice row of a short batch must equal
+    the same row inside a 200-row batch bit for bit (and the long batch's
+    slices are held to the oracle through the full product)."""
+    Mbig = 200
+    A, B = workloads.pair(Mbig, N, K, 700 + N + S)
+    Ad, Bd = A.cuda(), B.cuda()
+    ld = dig.bigemm_workspace_ld(N)
+    Se = dig.bigemm_effective_split_k(K, S)
+
+    def slices(a):
+        M = a.shape[0]
+        nb = dig.bigemm_partial_workspace_bytes(M, N, K, S)
+        ws = torch.full((nb // 4,), float("nan"), device="cuda")
+        dig.bigemm_run_partial(a, Bd, M, N, K, K, N, S, ws, nb)
+        return ws, ws[: Se * M * ld].view(Se, M, ld)[:, :, :N]
+
+    ws_full, full = slices(Ad)
+    C = torch.empty(Mbig, N, device="cuda")
+    dig.bigemm_splitk_reduce(ws_full, Se, Mbig, N, C, N, 0)
+    assert_correct(C, Ad, Bd, rows=[0, 63, 64, 199])
+    for M in (1, 15, 16, 17, 33, 48, 64):
+        for off in (0, 64, Mbig - M):
+            _, part = slices(Ad[off:off + M].contiguous())
+            assert bits_equal(part.contiguous(), full[:, off:off + M].contiguous()), (M, off)
+    torch.cuda.synchronize()
+
+
+def test_linear_short_batches_match_long_batches_both_dtypes():
+    """Linear layers N = K = 4096, split_k = 8 (16 tiles: the workspace path at
+    every M): bf16 and E4M3 rows computed at M <= 64 (short A boxes) equal the
+    same rows inside a 200-row batch (full A boxes)."""
+    N = K = 4096
+    Mbig = 200
+    x = workloads.normal_bf16((Mbig, K), 81).cuda()
+    w = workloads.normal_bf16((N, K), 82, 0.02).cuda()
+    b = workloads.normal_bf16((N,), 83).cuda()
+    full = dig.linear(x, w, b, split_k=8)
+    x8, w8 = x.to(torch.float8_e4m3fn), (w * 16).to(torch.float8_e4m3fn)
+    full8 = dig.linear_fp8(x8, w8, 0.25, b, split_k=8)
+    for fp8 in (False, True):
+        assert dig.bigemm_split_path(Mbig, N, K, 8, fp8) == dig.PATH_WORKSPACE
+    for M, off in ((1, 0), (16, 100), (40, 7), (64, 136)):
+        for fp8 in (False, True):
+            assert dig.bigemm_split_path(M, N, K, 8, fp8) == dig.PATH_WORKSPACE
+        part = dig.linear(x[off:off + M].contiguous(), w, b, split_k=8)
+        assert bits_equal(part, full[off:off + M]), ("bf16", M, off)
+        part8 = dig.linear_fp8(x8[off:off + M].contiguous(), w8, 0.25, b, split_k=8)
+        assert bits_equal(part8, full8[off:off + M]), ("e4m3", M, off)
+    torch.cuda.synchronize()

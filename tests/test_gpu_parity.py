@@ -158,6 +158,34 @@ def test_splitk_reduce_bit_exact(S, bf16_out):
     assert canary_intact(Cbuf, M, N)
 
 
+@pytest.mark.parametrize("bf16_out", [False, True])
+def test_splitk_reduce_more_groups_than_threads(bf16_out):
+    """More four-column groups (80 x 8196) than the reduction launches threads
+    for (16 blocks of 128 per SM), so threads take several groups each: still
+    the serial binary32 sum of the oracle, bit for bit, and nothing written
+    outside C."""
+    S, M, N = 3, 80, 32780
+    ld = dig.bigemm_workspace_ld(N)
+    g = torch.Generator().manual_seed(4242)
+    W = torch.randn(S, M, ld, generator=g, dtype=torch.float32) * \
+        torch.pow(2.0, torch.randint(-12, 13, (S, M, ld), generator=g).to(torch.float32))
+    want = oracle.splitk_reduce_f32(W.numpy())[:, :N]
+    ldc = N + 4
+    if bf16_out:
+        Cbuf = torch.full((M + 2, ldc), 0, dtype=torch.int16, device="cuda").fill_(0x7FC5).view(torch.bfloat16)
+    else:
+        Cbuf = torch.full((M + 2, ldc), float("nan"), device="cuda")
+    dig.bigemm_splitk_reduce(W.cuda(), S, M, N, Cbuf, ldc, bf16_out)
+    torch.cuda.synchronize()
+    got = Cbuf[:M, :N].cpu()
+    if bf16_out:
+        want_bits = oracle.encode_rne(oracle.FMT_BF16, want.astype(np.float64))
+        assert np.array_equal(got.view(torch.int16).numpy().view(np.uint16), want_bits)
+    else:
+        assert np.array_equal(got.numpy().view(np.uint32), want.view(np.uint32))
+    assert canary_intact(Cbuf, M, N)
+
+
 def test_partial_kernel_slices_sum_to_result():
     """bigemm_run_partial + bigemm_splitk_reduce == bigemm_run, bitwise."""
     M, N, K, S = 70, 520, 3000, 6
