@@ -217,7 +217,8 @@ def nvml_index(local: int) -> int:
 def kernel_source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("kernels.cuh", "ptx.cuh"):
+    # the kernels and the host code that sizes and configures their launches
+    for f in ("kernels.cuh", "ptx.cuh", "ozaki.cuh", "bigemm.cu"):
         with open(os.path.join(ROOT, "deterministic_invariant_gemm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -869,6 +870,39 @@ def cpu_baseline(budget_s: float = 10.0) -> dict:
                       "OpenMP over rows), %.1f s" % (reps, total)}
 
 
+def cpu_baseline_configs() -> dict:
+    """The oracle on the other workloads, as SURVEY-style per-config context:
+    the small product and long K in full, the squares on a 256-row sample of
+    A (every column of C; the full-size time extrapolated by rows).  The
+    oracle also forms D = sum |a b| for the tolerance, so it does twice the
+    arithmetic counted here."""
+    import oracle
+    oracle.build()
+    out = {}
+    cases = [("small_64x256x512", "small", 64, 256, 512, None),
+             ("square_2048", "square", 2048, 2048, 2048, 256),
+             ("square_4096", "square", 4096, 4096, 4096, 256),
+             ("square_8192", "square", 8192, 8192, 8192, 256),
+             ("large_16384", "large", 16384, 16384, 16384, 256),
+             ("longk_256x256x65536", "longk", 256, 256, 65536, None)]
+    threads = 1
+    for name, wname, M, N, K, sample in cases:
+        w = workloads.WORKLOADS[wname]
+        dist = {"small": "normal", "square": "uniform", "large": "normal", "longk": "normal"}[wname]
+        rows_m = M if sample is None else sample
+        # only the sampled rows of A are drawn (their values do not change the time)
+        A, B = workloads.pair(rows_m, N, K, workloads.BASE_SEED + w["index"], dist=dist)
+        t0 = time.perf_counter()
+        oracle.gemm_rows(A, B, rows_m, N, K)
+        dt = time.perf_counter() - t0
+        threads = oracle.num_threads()
+        flops = 2.0 * rows_m * N * K
+        out[name] = {"tflops": flops / dt / 1e12, "seconds": round(dt, 3), "rows_timed": rows_m,
+                     "full_size_seconds": round(dt * M / rows_m, 2),
+                     "extrapolated": sample is not None, "cores": threads}
+    return out
+
+
 def run_reference(args, world: int, rank: int):
     """--impl reference: the CPU oracle on the decode step, K timed steps."""
     if rank != 0:
@@ -1001,6 +1035,7 @@ def main():
         line["workloads"]["split_paths"] = run_split_paths(dev)
         line["workloads"].update(run_ozaki(dev, peaks))
         line["cpu_baseline"] = cpu_baseline()
+        line["cpu_baseline"]["per_config"] = cpu_baseline_configs()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
