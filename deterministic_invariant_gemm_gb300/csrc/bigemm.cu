@@ -630,18 +630,27 @@ cudaError_t launch_ozaki_split(const DeviceInfo& d, const double* X, int64_t row
                                int64_t ld, int axis, int rho, int slices, __nv_bfloat16* out,
                                int64_t out_ld, int64_t out_rows, int* exps, cudaStream_t stream) {
     if (axis == 0) {
-        int64_t blocks = ceil_div(rows, kOzakiRowWarps);
-        if (blocks > 8 * static_cast<int64_t>(d.sm_count)) blocks = 8 * static_cast<int64_t>(d.sm_count);
-        ozaki_split_rows_kernel<<<static_cast<unsigned>(blocks), kOzakiRowWarps * 32, 0, stream>>>(
+        // one block per row, at most 16 resident blocks' worth per SM at a time
+        int64_t blocks = rows;
+        if (blocks > 16 * static_cast<int64_t>(d.sm_count)) blocks = 16 * static_cast<int64_t>(d.sm_count);
+        ozaki_split_rows_kernel<<<static_cast<unsigned>(blocks), kOzakiRowThreads, 0, stream>>>(
             X, rows, cols, ld, rho, slices, out, out_ld, rows * out_ld, exps);
         return cudaGetLastError();
     }
-    ozaki_col_exps_kernel<<<static_cast<unsigned>(ceil_div(cols, 32)), 256, 0, stream>>>(X, rows, cols,
-                                                                                        ld, exps);
-    cudaError_t e = cudaGetLastError();
+    // column maxima: every exponent starts below any c^(1), then chunks of
+    // rows merge theirs with an integer atomicMax
+    cudaError_t e = cudaMemsetAsync(exps, 0x80, static_cast<size_t>(cols) * sizeof(int), stream);
     if (e != cudaSuccess) return e;
-    // columns across threads, rows across blockIdx.y: about 16 blocks per SM
-    const int64_t bx = ceil_div(cols, 256);
+    // chunks of at least kOzakiColChunk rows, at most 65535 of them
+    int64_t chunk = ceil_div(ceil_div(rows, 65535), 8) * 8;
+    if (chunk < kOzakiColChunk) chunk = kOzakiColChunk;
+    const int64_t chunks = ceil_div(rows, chunk);
+    ozaki_col_exps_kernel<<<dim3(static_cast<unsigned>(ceil_div(cols, 32)), static_cast<unsigned>(chunks)), 256,
+                            0, stream>>>(X, rows, cols, ld, chunk, exps);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // column pairs across threads, rows across blockIdx.y: about 16 blocks per SM
+    const int64_t bx = ceil_div(ceil_div(cols, 2), 256);
     int64_t by = ceil_div(16 * static_cast<int64_t>(d.sm_count), bx);
     if (by > out_rows) by = out_rows;
     if (by > 65535) by = 65535;

@@ -37,110 +37,228 @@ __device__ __forceinline__ int ozaki_ceil_log2_bits(uint64_t m) {
     return fl - 1074 + ((frac & (frac - 1)) != 0 ? 1 : 0);
 }
 
-// Writes the `slices` bfloat16 slices of x (vector exponent c1) to
-// out[0], out[plane], out[2 plane], ...
-__device__ __forceinline__ void ozaki_split_value(double x, int c1, int rho, int slices,
-                                                  __nv_bfloat16* out, int64_t plane) {
-    const int beta = 53 - rho;
+// One element's split state: x = R 2^E with R a signed integer of at most
+// 53 bits.
+struct OzakiElem {
+    int64_t R;
+    int E;
+};
+
+__device__ __forceinline__ OzakiElem ozaki_elem(double x) {
     const uint64_t bits = static_cast<uint64_t>(__double_as_longlong(x));
     const int eb = static_cast<int>((bits >> 52) & 0x7FF);
     const uint64_t frac = bits & ((1ull << 52) - 1);
-    // x = R 2^E with R a signed integer of at most 53 bits
-    int64_t R = static_cast<int64_t>(eb != 0 ? (frac | (1ull << 52)) : frac);
-    if (bits >> 63) R = -R;
-    const int E = eb != 0 ? eb - 1075 : -1074;
-    const float unit = __int_as_float((127 + rho - 53) << 23);   // 2^(rho - 53), exact in binary32
-    for (int p = 0; p < slices; ++p) {
-        const int g = c1 - p * (beta + 1) + rho - 53;   // exponent of sigma's last place
-        int64_t n = 0;
-        if (R != 0) {
-            if (E >= g) {
-                // x^(p) is a multiple of 2^g already: no rounding, nothing left
-                n = R * (int64_t(1) << (E - g));
-                R = 0;
-            } else if (g - E <= 60) {
-                const int shift = g - E;
-                int64_t q = R >> shift;                            // floor
-                const int64_t rem = R - q * (int64_t(1) << shift); // in [0, 2^shift)
-                const int64_t half = int64_t(1) << (shift - 1);
-                if (rem > half || (rem == half && (q & 1))) ++q;   // to nearest, ties to even
-                n = q;
-                R -= n * (int64_t(1) << shift);
-            }
-            // g - E > 60: |x^(p)| < 2^(g - 7), n = 0
+    OzakiElem e;
+    e.R = static_cast<int64_t>(eb != 0 ? (frac | (1ull << 52)) : frac);
+    if (bits >> 63) e.R = -e.R;
+    e.E = eb != 0 ? eb - 1075 : -1074;
+    return e;
+}
+
+// The slices from single roundings.  With s_p = g_p - E the shift of slice
+// p and F_p = n_0 2^(s_0) + ... + n_p 2^(s_p) (in units of 2^E), the
+// sequential split gives F_p = round-half-even(R / 2^(s_p)) 2^(s_p): F_(p-1)
+// is a multiple of 2^(s_(p-1)) = 2^(s_p + beta + 1), an even multiple of
+// 2^(s_p), and rounding to a grid commutes with adding an even number of
+// grid steps, ties included.  So
+//   n_p = Q_p - 2^(beta+1) Q_(p-1),   Q_p = round-half-even(R / 2^(s_p)),
+// Q_(-1) = 0 (|x| <= 2^(c^(1)) makes |Q_0| <= 2^beta).  |n_p| <= 2^beta, so
+// the low 32 bits of each Q suffice (arithmetic modulo 2^32).
+//
+// Low 32 bits of round-half-even(R / 2^s): for s > 0 the quotient is
+// floor((R + 2^(s-1)) / 2^s), round-half-up; a tie is exactly the case where
+// R + 2^(s-1) is a multiple of 2^s, and there an odd result moves down by one
+// to its even neighbour.  s >= 54 leaves 0 (|R| < 2^53 <= 2^(s-1)); s <= 0 is
+// an exact left shift.
+__device__ __forceinline__ uint32_t ozaki_round_lo32(int64_t R, int s) {
+    if (s <= 0) return -s < 32 ? static_cast<uint32_t>(static_cast<uint64_t>(R) << (-s)) : 0u;
+    if (s >= 54) return 0u;
+    const int64_t t = R + (int64_t(1) << (s - 1));
+    int64_t q = t >> s;  // arithmetic shift: floor
+    if ((q & 1) && (t & ((int64_t(1) << s) - 1)) == 0) --q;
+    return static_cast<uint32_t>(q);
+}
+
+// n 2^(rho - 53) in binary32, exactly: n (|n| <= 256) through the bit
+// pattern of 1.5 * 2^23 + n (the integers of that binade are exact), then a
+// power-of-two scale.
+__device__ __forceinline__ float ozaki_slice_value(int n, float unit) {
+    return (__int_as_float(0x4B400000 + n) - 12582912.0f) * unit;
+}
+
+__device__ __forceinline__ float ozaki_unit(int rho) {
+    return __int_as_float((127 + rho - 53) << 23);  // 2^(rho - 53), exact in binary32
+}
+
+// Splits two adjacent elements (vector exponents c1a, c1b) into `slices`
+// slices each; slice p of the pair goes to out[p * plane] and out[p * plane
+// + 1], as one 4-byte store when `paired`.  Every value is a bfloat16 exactly.
+__device__ __forceinline__ void ozaki_split_two(double xa, double xb, int c1a, int c1b, int rho,
+                                                int slices, __nv_bfloat16* out, int64_t plane,
+                                                bool paired) {
+    const int w = 54 - rho;  // beta + 1
+    const float unit = ozaki_unit(rho);
+    const OzakiElem a = ozaki_elem(xa), b = ozaki_elem(xb);
+    int sa = c1a + rho - 53 - a.E, sb = c1b + rho - 53 - b.E;
+    uint32_t pa = 0, pb = 0;
+    for (int p = 0; p < slices; ++p, sa -= w, sb -= w) {
+        const uint32_t qa = ozaki_round_lo32(a.R, sa), qb = ozaki_round_lo32(b.R, sb);
+        const int na = static_cast<int>(qa - (pa << w)), nb = static_cast<int>(qb - (pb << w));
+        pa = qa;
+        pb = qb;
+        const __nv_bfloat162 v =
+            __floats2bfloat162_rn(ozaki_slice_value(na, unit), ozaki_slice_value(nb, unit));
+        __nv_bfloat16* o = out + p * plane;
+        if (paired) {
+            *reinterpret_cast<__nv_bfloat162*>(o) = v;
+        } else {
+            o[0] = __low2bfloat16(v);
+            o[1] = __high2bfloat16(v);
         }
-        out[p * plane] = __float2bfloat16_rn(static_cast<float>(n) * unit);
     }
 }
 
-// Rows of X [rows][cols] (leading dimension ld): one warp per row finds the
-// row's maximum (integer max of the magnitude bit patterns: exact and
-// order-free), stores c^(1) in exps[row], then splits the row into
-// out[p * plane + row * out_ld + k].
-constexpr int kOzakiRowWarps = 8;
+// One element alone (an odd vector's last element).
+__device__ __forceinline__ void ozaki_split_one(double x, int c1, int rho, int slices,
+                                                __nv_bfloat16* out, int64_t plane) {
+    const int w = 54 - rho;
+    const float unit = ozaki_unit(rho);
+    const OzakiElem a = ozaki_elem(x);
+    int s = c1 + rho - 53 - a.E;
+    uint32_t prev = 0;
+    for (int p = 0; p < slices; ++p, s -= w) {
+        const uint32_t q = ozaki_round_lo32(a.R, s);
+        out[p * plane] = __float2bfloat16_rn(ozaki_slice_value(static_cast<int>(q - (prev << w)), unit));
+        prev = q;
+    }
+}
 
-__global__ void __launch_bounds__(kOzakiRowWarps * 32)
+// Rows of X [rows][cols] (leading dimension ld): one block per row.  Each
+// thread holds up to kOzakiRowCache elements (pairs of adjacent columns) in
+// registers, so the row is read from memory once when cols <= 256 *
+// kOzakiRowCache; the block finds the row's maximum (integer max of the
+// magnitude bit patterns: exact and order-free), stores c^(1) in exps[row],
+// and splits the row into out[p * plane + row * out_ld + k].
+constexpr int kOzakiRowThreads = 256;
+constexpr int kOzakiRowCache = 32;  // elements per thread kept in registers
+
+__device__ __forceinline__ uint64_t ozaki_abs_bits(double x) {
+    return static_cast<uint64_t>(__double_as_longlong(x)) & 0x7FFFFFFFFFFFFFFFull;
+}
+
+__global__ void __launch_bounds__(kOzakiRowThreads)
     ozaki_split_rows_kernel(const double* __restrict__ X, int64_t rows, int64_t cols, int64_t ld,
                             int rho, int slices, __nv_bfloat16* __restrict__ out, int64_t out_ld,
                             int64_t plane, int* __restrict__ exps) {
-    const int lane = threadIdx.x & 31;
-    const int64_t warps = static_cast<int64_t>(gridDim.x) * kOzakiRowWarps;
-    for (int64_t r = static_cast<int64_t>(blockIdx.x) * kOzakiRowWarps + (threadIdx.x >> 5); r < rows;
-         r += warps) {
+    __shared__ uint64_t wmax[kOzakiRowThreads / 32];
+    const int tid = threadIdx.x;
+    const int64_t pairs = cols / 2;
+    const bool paired = (out_ld % 2 == 0) && ((reinterpret_cast<uintptr_t>(out) & 3u) == 0);
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         const double* x = X + r * ld;
+        double cache[kOzakiRowCache];
         uint64_t m = 0;
-        for (int64_t k = lane; k < cols; k += 32) {
-            const uint64_t a = static_cast<uint64_t>(__double_as_longlong(x[k])) & 0x7FFFFFFFFFFFFFFFull;
-            m = a > m ? a : m;
-        }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const uint64_t b = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-            m = b > m ? b : m;
+        for (int i = 0; i < kOzakiRowCache / 2; ++i) {
+            const int64_t pr = tid + static_cast<int64_t>(i) * kOzakiRowThreads;
+            cache[2 * i] = pr < pairs ? x[2 * pr] : 0.0;
+            cache[2 * i + 1] = pr < pairs ? x[2 * pr + 1] : 0.0;
+            m = max(m, max(ozaki_abs_bits(cache[2 * i]), ozaki_abs_bits(cache[2 * i + 1])));
         }
+        // the rest of a long row (read again for the split)
+        for (int64_t pr = tid + static_cast<int64_t>(kOzakiRowCache / 2) * kOzakiRowThreads; pr < pairs;
+             pr += kOzakiRowThreads)
+            m = max(m, max(ozaki_abs_bits(x[2 * pr]), ozaki_abs_bits(x[2 * pr + 1])));
+        if ((cols & 1) && tid == 0) m = max(m, ozaki_abs_bits(x[cols - 1]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        if ((tid & 31) == 0) wmax[tid >> 5] = m;
+        __syncthreads();
+        m = wmax[0];
+#pragma unroll
+        for (int w = 1; w < kOzakiRowThreads / 32; ++w) m = max(m, wmax[w]);
+        __syncthreads();  // wmax is reused by the next row
         const int c1 = ozaki_ceil_log2_bits(m);
-        if (lane == 0) exps[r] = c1;
-        for (int64_t k = lane; k < cols; k += 32)
-            ozaki_split_value(x[k], c1, rho, slices, out + r * out_ld + k, plane);
+        if (tid == 0) exps[r] = c1;
+        __nv_bfloat16* orow = out + r * out_ld;
+#pragma unroll
+        for (int i = 0; i < kOzakiRowCache / 2; ++i) {
+            const int64_t pr = tid + static_cast<int64_t>(i) * kOzakiRowThreads;
+            if (pr < pairs)
+                ozaki_split_two(cache[2 * i], cache[2 * i + 1], c1, c1, rho, slices, orow + 2 * pr, plane,
+                                paired);
+        }
+        for (int64_t pr = tid + static_cast<int64_t>(kOzakiRowCache / 2) * kOzakiRowThreads; pr < pairs;
+             pr += kOzakiRowThreads)
+            ozaki_split_two(x[2 * pr], x[2 * pr + 1], c1, c1, rho, slices, orow + 2 * pr, plane, paired);
+        if ((cols & 1) && tid == 0) ozaki_split_one(x[cols - 1], c1, rho, slices, orow + cols - 1, plane);
     }
 }
 
-// Column maxima of X [rows][cols]: block (32 columns) x (8 row phases); each
-// thread scans every eighth row of its column, the block combines the eight.
+// Column maxima of X [rows][cols]: block (32 columns) x (8 row phases) over a
+// chunk of `chunk` rows (blockIdx.y; at least kOzakiColChunk, a multiple of
+// 8); each thread scans every eighth
+// row of its column in the chunk, the block combines the eight, and the
+// chunk's ceil(log2(max)) is merged into exps[j] with an integer atomicMax
+// (ceil(log2) is monotone, so the merged value is ceil(log2) of the column
+// maximum whatever the order).  exps must hold kOzakiNoExp beforehand; a
+// chunk of zeros merges nothing, and an all-zero column keeps kOzakiNoExp
+// (read as 0 by the split below).
+constexpr int kOzakiColChunk = 256;
+constexpr int kOzakiNoExp = static_cast<int>(0x80808080u);  // every byte 0x80: below any c^(1)
+
 __global__ void __launch_bounds__(256)
     ozaki_col_exps_kernel(const double* __restrict__ X, int64_t rows, int64_t cols, int64_t ld,
-                          int* __restrict__ exps) {
+                          int64_t chunk, int* __restrict__ exps) {
     __shared__ uint64_t part[8][32];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
     const int64_t j = static_cast<int64_t>(blockIdx.x) * 32 + tx;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * chunk;
+    const int64_t r1 = min(rows, r0 + chunk);
     uint64_t m = 0;
-    if (j < cols)
-        for (int64_t r = ty; r < rows; r += 8) {
-            const uint64_t a = static_cast<uint64_t>(__double_as_longlong(X[r * ld + j])) & 0x7FFFFFFFFFFFFFFFull;
-            m = a > m ? a : m;
-        }
+    if (j < cols) {
+#pragma unroll 8
+        for (int64_t r = r0 + ty; r < r1; r += 8) m = max(m, ozaki_abs_bits(X[r * ld + j]));
+    }
     part[ty][tx] = m;
     __syncthreads();
     if (ty == 0 && j < cols) {
-        for (int t = 1; t < 8; ++t) m = part[t][tx] > m ? part[t][tx] : m;
-        exps[j] = ozaki_ceil_log2_bits(m);
+        for (int t = 1; t < 8; ++t) m = max(m, part[t][tx]);
+        if (m != 0) atomicMax(exps + j, ozaki_ceil_log2_bits(m));
     }
 }
 
 // The column split: element (r, j) of X [rows][cols] goes to
 // out[p * plane + r * out_ld + j]; rows rows .. out_rows-1 of every slice
-// (the padding up to a whole K block) are written as zeros.  Threads run
-// along a row (coalesced), blocks along y step through the rows.
+// (the padding up to a whole K block) are written as zeros.  A thread takes
+// two adjacent columns (one 4-byte store per slice when out_ld is even),
+// blocks along y step through the rows.  Blocks with blockIdx.y == 0 also
+// turn an all-zero column's kOzakiNoExp into its c^(1) = 0.
 __global__ void __launch_bounds__(256)
     ozaki_split_cols_kernel(const double* __restrict__ X, int64_t rows, int64_t cols, int64_t ld,
                             int64_t out_rows, int rho, int slices, __nv_bfloat16* __restrict__ out,
-                            int64_t out_ld, int64_t plane, const int* __restrict__ exps) {
-    const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+                            int64_t out_ld, int64_t plane, int* __restrict__ exps) {
+    const int64_t j = 2 * (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
     if (j >= cols) return;
-    const int c1 = exps[j];
+    const bool two = j + 1 < cols;
+    const bool paired = two && (out_ld % 2 == 0) && ((reinterpret_cast<uintptr_t>(out) & 3u) == 0);
+    int ea = exps[j];
+    int eb = two ? exps[j + 1] : 0;
+    ea = ea == kOzakiNoExp ? 0 : ea;
+    eb = eb == kOzakiNoExp ? 0 : eb;
+    if (blockIdx.y == 0) {
+        exps[j] = ea;
+        if (two) exps[j + 1] = eb;
+    }
     for (int64_t r = blockIdx.y; r < out_rows; r += gridDim.y) {
-        const double x = r < rows ? X[r * ld + j] : 0.0;
-        ozaki_split_value(x, c1, rho, slices, out + r * out_ld + j, plane);
+        __nv_bfloat16* o = out + r * out_ld + j;
+        if (two) {
+            const double xa = r < rows ? X[r * ld + j] : 0.0;
+            const double xb = r < rows ? X[r * ld + j + 1] : 0.0;
+            ozaki_split_two(xa, xb, ea, eb, rho, slices, o, plane, paired);
+        } else {
+            ozaki_split_one(r < rows ? X[r * ld + j] : 0.0, ea, rho, slices, o, plane);
+        }
     }
 }
 

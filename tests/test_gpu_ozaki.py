@@ -72,6 +72,28 @@ def test_split_matches_the_oracle_bit_for_bit(axis, rows, cols, K):
         assert (got[:, rows:, :cols].float() == 0).all()    # the padding rows are zeros
 
 
+@pytest.mark.parametrize("axis", [0, 1])
+def test_split_rounding_ties_match_the_oracle(axis):
+    """Small integers, halves and quarters put many residuals exactly halfway
+    between two multiples of a slice's unit, where the split rounds to the
+    even neighbour: the GPU's slices must still equal the oracle's bit for
+    bit, on a row long enough to take the register-cached and the re-read
+    parts of the row kernel (9000 > 8192 columns) and an odd column count."""
+    g = workloads.generator(515)
+    rows, cols = (6, 9001) if axis == 0 else (9001, 6)
+    X = torch.randint(-1000, 1001, (rows, cols), generator=g).double()
+    X = X * torch.tensor([1.0, 0.5, 0.25, 8.0])[torch.randint(0, 4, (rows, cols), generator=g)]
+    X[0, 0] = 1024.0 if axis == 0 else X[0, 0]
+    for K in (4096, 1 << 16):
+        rho = dig.bigemm_ozaki_rho(K)
+        slices = dig.bigemm_ozaki_default_slices(K)
+        S, c1, _ = oracle.ozaki_split(X, axis, rho, slices)
+        got, exps = gpu_split(X, axis, rho, slices, rows + 3 if axis == 1 else None)
+        assert np.array_equal(exps.cpu().numpy(), c1)
+        have = got[:, :rows, :cols].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(oracle.decode(oracle.FMT_BF16, have), S), K
+
+
 def run_dgemm(A, B, slices=0, d=0, ldc_pad=0):
     M, K = A.shape
     N = B.shape[1]
