@@ -481,7 +481,8 @@ def run_split_paths(dev) -> dict:
                 dig.bigemm_splitk_reduce(ws, s_eff, M, N, C, N, 0)
 
         res = {"path": {0: "unsplit", 1: "workspace", 2: "folded", 3: "cluster"}.get(
-            dig.bigemm_split_path(M, N, K, S), "?"), "weights": pool}
+            dig.bigemm_split_path(M, N, K, S), "?"), "tile_n": dig.bigemm_tile_n(M, N, K, S),
+            "weights": pool}
         for name, fn in (("bigemm_run_us", one_call), ("two_kernel_us", two_kernels)):
             s = torch.cuda.Stream(device=dev)
             s.wait_stream(torch.cuda.current_stream())
@@ -740,7 +741,7 @@ def run_longk(dev, peaks) -> dict:
             dig.bigemm_run_atomic_splitk(a, b, C, M, N, K, K, N, N, S)
 
         res = {"path": {0: "unsplit", 1: "workspace", 2: "folded", 3: "cluster"}.get(
-            dig.bigemm_split_path(M, N, K, S), "?")}
+            dig.bigemm_split_path(M, N, K, S), "?"), "tile_n": dig.bigemm_tile_n(M, N, K, S)}
         for key, fn in (("bigemm_run", call), ("atomic", atomic)):
             for i in range(3):
                 fn(i)

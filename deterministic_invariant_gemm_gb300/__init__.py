@@ -35,7 +35,7 @@ __all__ = [
     "bigemm_run_bf16out", "bigemm_run_partial", "bigemm_splitk_reduce",
     "bigemm_run_atomic_splitk", "bigemm_device_status", "bigemm_last_launch_count",
     "bigemm_run_splitk_static", "bigemm_linear", "bigemm_fp8_effective_split_k",
-    "bigemm_fp8_workspace_bytes", "bigemm_linear_fp8", "bigemm_split_is_folded", "bigemm_split_path",
+    "bigemm_fp8_workspace_bytes", "bigemm_linear_fp8", "bigemm_split_is_folded", "bigemm_split_path", "bigemm_tile_n",
     "bigemm_cluster_capacity", "bigemm_ozaki_rho", "bigemm_ozaki_default_slices",
     "bigemm_ozaki_pairs", "bigemm_ozaki_workspace_bytes", "bigemm_ozaki_split", "bigemm_ozaki_dgemm",
     "ozaki_matmul", "bigemm_selftest_timeout", "PATH_UNSPLIT", "PATH_WORKSPACE", "PATH_FOLDED", "PATH_CLUSTER", "FP8_E4M3",
@@ -67,7 +67,7 @@ EXPORTED_SYMBOLS = (
     "bigemm_splitk_reduce", "bigemm_run_atomic_splitk", "bigemm_device_status",
     "bigemm_last_launch_count", "bigemm_run_splitk_static", "bigemm_linear",
     "bigemm_fp8_effective_split_k", "bigemm_fp8_workspace_bytes", "bigemm_linear_fp8",
-    "bigemm_split_is_folded", "bigemm_split_path", "bigemm_cluster_capacity",
+    "bigemm_split_is_folded", "bigemm_split_path", "bigemm_tile_n", "bigemm_cluster_capacity",
     "bigemm_ozaki_rho", "bigemm_ozaki_default_slices", "bigemm_ozaki_pairs",
     "bigemm_ozaki_workspace_bytes", "bigemm_ozaki_split", "bigemm_ozaki_dgemm",
     "bigemm_selftest_timeout",
@@ -111,6 +111,7 @@ def load():
         "bigemm_workspace_bytes": ([i64, i64, i64, i32], sz),
         "bigemm_split_is_folded": ([i64, i64, i64, i32], i32),
         "bigemm_split_path": ([i64, i64, i64, i32, i32], i32),
+        "bigemm_tile_n": ([i64, i64, i64, i32, i32], i32),
         "bigemm_cluster_capacity": ([i32], i32),
         "bigemm_ozaki_rho": ([i64], i32),
         "bigemm_selftest_timeout": ([vp], i32),
@@ -217,6 +218,12 @@ def bigemm_split_path(M: int, N: int, K: int, split_k: int, fp8: bool = False) -
     """How a direct-output product of this shape runs on the current device:
     PATH_UNSPLIT, PATH_WORKSPACE, PATH_FOLDED or PATH_CLUSTER (-1: invalid)."""
     return int(load().bigemm_split_path(M, N, K, split_k, 1 if fp8 else 0))
+
+
+def bigemm_tile_n(M: int, N: int, K: int, split_k: int, fp8: bool = False) -> int:
+    """Output-tile width (256, 128 or 64 columns) a product of this shape runs
+    with on the current device (-1: invalid)."""
+    return int(load().bigemm_tile_n(M, N, K, split_k, 1 if fp8 else 0))
 
 
 def bigemm_partial_workspace_bytes(M: int, N: int, K: int, split_k: int) -> int:

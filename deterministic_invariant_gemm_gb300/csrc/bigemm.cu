@@ -77,40 +77,51 @@ bigemm_status device_info(const DeviceInfo** out) {
         d.supported = (major == 10 && minor == 3);
         d.sm_count = sms;
         if (d.supported) {
-            const int smem = static_cast<int>(kSmemBytes);
             // Besides the shared-memory opt-in: a GEMM kernel whose warpgroups
             // re-divide their registers (setmaxnreg: the direct-output and Ozaki
             // epilogues) must have been compiled with kLaunchRegs registers per
             // thread, the allocation that re-division assumes; with fewer, the
             // epilogue's register increase could never be granted.
-            const auto opt_in = [smem](const void* fn, bool split_regs) {
+            const auto opt_in = [](const void* fn, bool split_regs, uint32_t smem) {
                 cudaFuncAttributes fa;
                 if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return BIGEMM_ERR_CUDA;
                 if ((split_regs && fa.numRegs < kLaunchRegs) || fa.maxThreadsPerBlock < kNumThreads)
                     return BIGEMM_ERR_UNSUPPORTED;
-                return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
-                               cudaSuccess
+                return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(smem)) == cudaSuccess
                            ? BIGEMM_OK
                            : BIGEMM_ERR_CUDA;
             };
             const struct {
                 const void* fn;
                 bool split_regs;
+                uint32_t smem;
             } kernels[] = {
-                {(const void*)bigemm_tc_kernel<kOutF32, false, false>, true},
-                {(const void*)bigemm_tc_kernel<kOutBF16, false, false>, true},
-                {(const void*)bigemm_tc_kernel<kOutSlices, false, false>, false},
-                {(const void*)bigemm_tc_kernel<kOutAtomic, false, false>, false},
-                {(const void*)bigemm_tc_kernel<kOutF32, true, false>, true},
-                {(const void*)bigemm_tc_kernel<kOutBF16, true, false>, true},
-                {(const void*)bigemm_tc_kernel<kOutSlices, true, false>, false},
-                {(const void*)bigemm_tc_kernel<kOutF32, true, true>, true},
-                {(const void*)bigemm_tc_kernel<kOutBF16, true, true>, true},
-                {(const void*)bigemm_tc_kernel<kOutSlices, true, true>, false},
-                {(const void*)bigemm_tc_kernel<kOutOzaki, false, false>, true},
+                {(const void*)bigemm_tc_kernel<kOutF32, false, false>, true, kSmemBytes},
+                {(const void*)bigemm_tc_kernel<kOutBF16, false, false>, true, kSmemBytes},
+                {(const void*)bigemm_tc_kernel<kOutSlices, false, false>, false, kSmemBytes},
+                {(const void*)bigemm_tc_kernel<kOutAtomic, false, false>, false, kSmemBytes},
+                {(const void*)bigemm_tc_kernel<kOutF32, true, false>, true, kSmemBytes},
+                {(const void*)bigemm_tc_kernel<kOutBF16, true, false>, true, kSmemBytes},
+                {(const void*)bigemm_tc_kernel<kOutSlices, true, false>, false, kSmemBytes},
+                {(const void*)bigemm_tc_kernel<kOutF32, true, true>, true, kSmemBytes},
+                {(const void*)bigemm_tc_kernel<kOutBF16, true, true>, true, kSmemBytes},
+                {(const void*)bigemm_tc_kernel<kOutSlices, true, true>, false, kSmemBytes},
+                {(const void*)bigemm_tc_kernel<kOutOzaki, false, false>, true, kSmemBytes},
+#define BIGEMM_NARROW_KERNELS(TN)                                                                  \
+    {(const void*)bigemm_tc_kernel<kOutF32, false, false, TN>, true, Tile<TN>::kSmemBytes},        \
+        {(const void*)bigemm_tc_kernel<kOutBF16, false, false, TN>, true, Tile<TN>::kSmemBytes},   \
+        {(const void*)bigemm_tc_kernel<kOutSlices, false, false, TN>, false, Tile<TN>::kSmemBytes}, \
+        {(const void*)bigemm_tc_kernel<kOutAtomic, false, false, TN>, false, Tile<TN>::kSmemBytes}, \
+        {(const void*)bigemm_tc_kernel<kOutF32, true, false, TN>, true, Tile<TN>::kSmemBytes},     \
+        {(const void*)bigemm_tc_kernel<kOutBF16, true, false, TN>, true, Tile<TN>::kSmemBytes},    \
+        {(const void*)bigemm_tc_kernel<kOutSlices, true, false, TN>, false, Tile<TN>::kSmemBytes}
+                BIGEMM_NARROW_KERNELS(128),
+                BIGEMM_NARROW_KERNELS(64),
+#undef BIGEMM_NARROW_KERNELS
             };
             for (const auto& k : kernels) {
-                const bigemm_status st = opt_in(k.fn, k.split_regs);
+                const bigemm_status st = opt_in(k.fn, k.split_regs, k.smem);
                 if (st != BIGEMM_OK) return st;
             }
             void* sym = nullptr;
@@ -159,6 +170,26 @@ static_assert(epi_batch_for(BIGEMM_FOLD_MIN_ROWS) == 1 && epi_boxes_for(BIGEMM_F
 bool folds(int64_t M, int64_t N, int splits) {
     if (splits <= 1 || M < BIGEMM_FOLD_MIN_ROWS || N <= 0) return false;
     return ceil_div(M, kBM) * ceil_div(N, kBN) >= BIGEMM_FOLD_MIN_TILES;
+}
+
+// Tile width of a product (kBN = 256, or 128 / 64).  The wide tile unless
+// its units (tiles x K segments) would occupy fewer than half of the SMs and
+// each unit streams at least kNarrowMinBlocks K blocks: then a single SM's
+// load rate, not HBM, sets the pace, and narrower tiles put more SMs to work
+// -- the widest width whose units reach half the SMs, else 64.  Short
+// segments keep the wide tile: their time is launch and pipeline latency,
+// which narrower tiles do not shorten.  Folded and 8-bit products are always
+// wide.  Speed only: every width forms every sum the same way.
+constexpr int kNarrowMinBlocks = 32;
+
+int tile_width(int64_t M, int64_t N, int splits, int kb_per_split, bool fold, bool fp8,
+               int sm_count) {
+    if (fp8 || fold || M <= 0 || N <= 0 || kb_per_split < kNarrowMinBlocks) return kBN;
+    const int64_t m_tiles = ceil_div(M, kBM);
+    const int64_t half = sm_count / 2;
+    if (m_tiles * ceil_div(N, kBN) * splits >= half) return kBN;
+    if (m_tiles * ceil_div(N, 128) * splits >= half) return 128;
+    return 64;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -262,16 +293,17 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t esize, c
 }
 
 // Operand maps: A [M, K] in boxes of 64 k x 128 rows; B [K, N] in boxes of 64
-// columns x 64 k-rows, or a weight matrix W [N, K] (wt) in boxes of 64 k x 256
-// rows; all with the 128-byte swizzle the MMA descriptors use.  The second
-// operand again in 256 x 256 boxes without swizzle, used only to warm L2.
+// columns x 64 k-rows, or a weight matrix W [N, K] (wt) in boxes of 64 k x
+// tile_n rows; all with the 128-byte swizzle the MMA descriptors use.  The
+// second operand again in tile_n x 256 boxes without swizzle, used only to
+// warm L2.
 // Rows of A a stage loads: the batch rounded up to 32, 64 or 128 (a function of
 // M that changes no sum -- the other rows of the 128-row MMA operand are zero).
 int a_box_rows(int64_t M) { return M <= 32 ? 32 : (M <= 64 ? 64 : kBM); }
 
 bool encode_operands(CUtensorMap* tmA, CUtensorMap* tmB, CUtensorMap* tmBp, const void* A,
                      const void* B, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
-                     bool wt, bool fp8) {
+                     bool wt, bool fp8, int tile_n = kBN) {
     // 8-bit operands: a K block of 128 elements is still 128 bytes per row
     const uint32_t kb = fp8 ? 128u : static_cast<uint32_t>(kBK);
     const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -279,9 +311,10 @@ bool encode_operands(CUtensorMap* tmA, CUtensorMap* tmB, CUtensorMap* tmBp, cons
     const int64_t da[2] = {K, M};
     const int64_t db[2] = {wt ? K : N, wt ? N : K};
     const uint32_t ba[2] = {kb, static_cast<uint32_t>(a_box_rows(M))};
-    const uint32_t bb[2] = {wt ? kb : kBChunkCols, wt ? static_cast<uint32_t>(kBN) : kb};
-    const uint32_t bp[2] = {wt ? static_cast<uint32_t>(kPrefetchRows) : static_cast<uint32_t>(kBN),
-                            wt ? static_cast<uint32_t>(kBN) : static_cast<uint32_t>(kPrefetchRows)};
+    const uint32_t tn = static_cast<uint32_t>(tile_n);
+    const uint32_t bb[2] = {wt ? kb : kBChunkCols, wt ? tn : kb};
+    const uint32_t bp[2] = {wt ? static_cast<uint32_t>(kPrefetchRows) : tn,
+                            wt ? tn : static_cast<uint32_t>(kPrefetchRows)};
     return encode_tiled(tmA, dt, es, A, 2, da, lda, 0, ba, CU_TENSOR_MAP_SWIZZLE_128B) &&
            encode_tiled(tmB, dt, es, B, 2, db, ldb, 0, bb, CU_TENSOR_MAP_SWIZZLE_128B) &&
            encode_tiled(tmBp, dt, es, B, 2, db, ldb, 0, bp, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -343,10 +376,38 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaSt
     return launch_pdl_cluster(kernel, grid, block, smem, stream, 1u, args...);
 }
 
+// A bf16 product with narrow tiles (128 or 64 columns; never clustered).
+template <int kOut, int kTN>
+cudaError_t launch_narrow(bool wt, dim3 g, dim3 blk, cudaStream_t stream, const CUtensorMap& tmA,
+                          const CUtensorMap& tmB, const CUtensorMap& tmBp, const CUtensorMap& tmC,
+                          const GemmParams& p) {
+    constexpr uint32_t smem = Tile<kTN>::kSmemBytes;
+    if constexpr (kOut == kOutAtomic) {
+        if (wt) return cudaErrorInvalidValue;
+        return launch_pdl(bigemm_tc_kernel<kOut, false, false, kTN>, g, blk, smem, stream, tmA, tmB,
+                          tmBp, tmC, p);
+    } else {
+        if (wt)
+            return launch_pdl(bigemm_tc_kernel<kOut, true, false, kTN>, g, blk, smem, stream, tmA, tmB,
+                              tmBp, tmC, p);
+        return launch_pdl(bigemm_tc_kernel<kOut, false, false, kTN>, g, blk, smem, stream, tmA, tmB,
+                          tmBp, tmC, p);
+    }
+}
+
 template <int kOut>
 cudaError_t launch_gemm(bool wt, bool fp8, dim3 g, dim3 blk, cudaStream_t stream,
                         const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBp,
-                        const CUtensorMap& tmC, const GemmParams& p, unsigned cluster_x = 1) {
+                        const CUtensorMap& tmC, const GemmParams& p, unsigned cluster_x = 1,
+                        int tile_n = kBN) {
+    if constexpr (kOut != kOutOzaki) {
+        if (tile_n != kBN) {
+            if (fp8 || cluster_x > 1 || p.fold) return cudaErrorInvalidValue;
+            if (tile_n == 128) return launch_narrow<kOut, 128>(wt, g, blk, stream, tmA, tmB, tmBp, tmC, p);
+            if (tile_n == 64) return launch_narrow<kOut, 64>(wt, g, blk, stream, tmA, tmB, tmBp, tmC, p);
+            return cudaErrorInvalidValue;
+        }
+    }
     if constexpr (kOut == kOutOzaki) {
         if (wt || fp8) return cudaErrorInvalidValue;  // bfloat16 slices of B [K, N] only
         return launch_pdl(bigemm_tc_kernel<kOut, false, false>, g, blk, kSmemBytes, stream, tmA, tmB,
@@ -440,19 +501,21 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
             return BIGEMM_ERR_WORKSPACE;
     }
     if (M == 0 || N == 0) return BIGEMM_OK;
-    const int64_t m_tiles = ceil_div(M, kBM);
-    const int64_t n_tiles = ceil_div(N, kBN);
-    const int64_t units = m_tiles * n_tiles * (fold ? 1 : splits);
-    if (units > INT_MAX) return BIGEMM_ERR_ARG;
 
     const DeviceInfo* d = nullptr;
     bigemm_status st = device_info(&d);
     if (st != BIGEMM_OK) return st;
+    const int tile_n = tile_width(M, N, splits, kb_per_split, fold, fp8, d->sm_count);
+    const int64_t m_tiles = ceil_div(M, kBM);
+    const int64_t n_tiles = ceil_div(N, tile_n);
+    const int64_t units = m_tiles * n_tiles * (fold ? 1 : splits);
+    if (units > INT_MAX) return BIGEMM_ERR_ARG;
     // A split product that is not folded sums its segments inside clusters of
     // `splits` CTAs when all of its clusters can be resident at once (one
-    // wave); otherwise through the workspace and the reduction kernel.  Same
-    // bits either way; the workspace is required in both cases.
-    const bool cluster = direct && !fold && splits >= 2 && splits <= 8 && K > 0 &&
+    // wave) and its tiles are wide; otherwise through the workspace and the
+    // reduction kernel.  Same bits either way; the workspace is required in
+    // both cases.
+    const bool cluster = direct && !fold && tile_n == kBN && splits >= 2 && splits <= 8 && K > 0 &&
                          m_tiles * n_tiles <= d->max_clusters[splits];
 
     // ---- K == 0: the empty sum is +0.0 everywhere (plus the bias, if any)
@@ -475,7 +538,8 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
 
     CUtensorMap tmA, tmB, tmBp, tmC;
     std::memset(&tmC, 0, sizeof(tmC));
-    if (!encode_operands(&tmA, &tmB, &tmBp, A, B, M, N, K, lda, ldb, wt, fp8)) return BIGEMM_ERR_CUDA;
+    if (!encode_operands(&tmA, &tmB, &tmBp, A, B, M, N, K, lda, ldb, wt, fp8, tile_n))
+        return BIGEMM_ERR_CUDA;
 
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
@@ -489,9 +553,13 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     p.kb_per_split = kb_per_split;
     p.units = static_cast<int>(units);
     p.epi_boxes = epi_boxes_for(static_cast<int>(M));
+    // a batch of 32-column blocks never spans past the warp's half of a tile
     p.epi_batch = epi_batch_for(static_cast<int>(M));
+    if (p.epi_batch > tile_n / 64) p.epi_batch = tile_n / 64;
     p.grouped = 0;
-    p.prefetch_rows = kStages * kb_elems;  // what the ring holds: the first four K blocks
+    // what the ring holds: its first 4 (wide), 6 or 8 (narrow) K blocks
+    p.prefetch_rows = (tile_n == 128 ? Tile<128>::kStages : (tile_n == 64 ? Tile<64>::kStages : kStages)) *
+                      kb_elems;
     // GROUP_M swizzle: 16 tile rows per group once there are four or more waves
     // of tiles (the concurrent tiles then span about 16 x 9 tiles, whose A and
     // B panels stay in L2), else 8.  It orders tiles only; no sum changes.
@@ -522,7 +590,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
         if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
         p.out = C;
         p.ld_out = ldc;
-        e = launch_gemm<kOutAtomic>(wt, fp8, g, blk, stream, tmA, tmB, tmBp, tmC, p);
+        e = launch_gemm<kOutAtomic>(wt, fp8, g, blk, stream, tmA, tmB, tmBp, tmC, p, 1u, tile_n);
         launches = 1;
     } else if (mode == kModePartial || (splits > 1 && !fold && !cluster)) {
         p.out = ws;
@@ -533,7 +601,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
             p.grouped = 1;
         else if (!encode_out_slices(&tmC, ws, M, N, splits))
             return BIGEMM_ERR_CUDA;
-        e = launch_gemm<kOutSlices>(wt, fp8, g, blk, stream, tmA, tmB, tmBp, tmC, p);
+        e = launch_gemm<kOutSlices>(wt, fp8, g, blk, stream, tmA, tmB, tmBp, tmC, p, 1u, tile_n);
         launches = 1;
         if (e == cudaSuccess && mode != kModePartial) {
             st = launch_reduce(*d, static_cast<const float*>(ws), splits, M, N, C, ldc,
@@ -551,7 +619,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
             else if (!encode_out_bf16(&tmC, C, M, N, ldc))
                 return BIGEMM_ERR_CUDA;
             e = launch_gemm<kOutBF16>(wt, fp8, g, blk, stream, tmA, tmB, tmBp, tmC, p,
-                                      cluster ? static_cast<unsigned>(splits) : 1u);
+                                      cluster ? static_cast<unsigned>(splits) : 1u, tile_n);
         } else {
             if (encode_out_grouped(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, M, N, ldc, 0, 0,
                                    p.epi_batch))
@@ -559,7 +627,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
             else if (!encode_out_f32(&tmC, C, M, N, ldc))
                 return BIGEMM_ERR_CUDA;
             e = launch_gemm<kOutF32>(wt, fp8, g, blk, stream, tmA, tmB, tmBp, tmC, p,
-                                     cluster ? static_cast<unsigned>(splits) : 1u);
+                                     cluster ? static_cast<unsigned>(splits) : 1u, tile_n);
         }
         launches = 1;
     }
@@ -738,14 +806,27 @@ int bigemm_cluster_capacity(int splits) {
 
 int bigemm_split_path(int64_t M, int64_t N, int64_t K, int split_k, int fp8) {
     if (M < 0 || N < 0 || K < 0) return -1;
-    const int s = effective_split(K, split_k, nullptr, fp8 ? 128 : kBK);
+    int L = 0;
+    const int s = effective_split(K, split_k, &L, fp8 ? 128 : kBK);
     if (s == 0) return -1;
     if (s == 1 || K == 0) return BIGEMM_PATH_UNSPLIT;
     if (folds(M, N, s)) return BIGEMM_PATH_FOLDED;
     const DeviceInfo* d = nullptr;
     if (device_info(&d) != BIGEMM_OK) return -1;
+    if (tile_width(M, N, s, L, false, fp8 != 0, d->sm_count) != kBN) return BIGEMM_PATH_WORKSPACE;
     if (s <= 8 && ceil_div(M, kBM) * ceil_div(N, kBN) <= d->max_clusters[s]) return BIGEMM_PATH_CLUSTER;
     return BIGEMM_PATH_WORKSPACE;
+}
+
+int bigemm_tile_n(int64_t M, int64_t N, int64_t K, int split_k, int fp8) {
+    if (M < 0 || N < 0 || K < 0) return -1;
+    int L = 0;
+    const int s = effective_split(K, split_k, &L, fp8 ? 128 : kBK);
+    if (s == 0) return -1;
+    if (M == 0 || N == 0 || K == 0) return kBN;
+    const DeviceInfo* d = nullptr;
+    if (device_info(&d) != BIGEMM_OK) return -1;
+    return tile_width(M, N, s, L, folds(M, N, s), fp8 != 0, d->sm_count);
 }
 
 size_t bigemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {

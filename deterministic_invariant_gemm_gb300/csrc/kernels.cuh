@@ -100,6 +100,35 @@ __host__ __device__ constexpr int epi_batch_for(int M) {
 constexpr uint32_t kIdescBN = idesc_bf16_f32(kBM, kBN, /*A MN-major*/ false, /*B MN-major*/ true);
 constexpr uint32_t kIdescWt = idesc_bf16_f32(kBM, kBN, /*A MN-major*/ false, /*B MN-major*/ false);
 
+// Tile widths.  kBN = 256 columns is the default.  A product whose 256-wide
+// units would leave most SMs idle (few tiles and few K segments: small N,
+// small M, long K) runs with 128- or 64-column tiles instead, so that more
+// SMs stream its operands.  Every output element is still formed by the same
+// 128-row instructions over the same K blocks in ascending order -- the tile
+// width sets only the N extent of each instruction -- and the GPU tests check
+// that every width gives the same bits.  A narrower tile has a smaller B
+// stage, so the ring holds more stages in the same shared memory: 4 stages of
+// 48 KiB (256), 6 of 32 KiB (128), 8 of 24 KiB (64).
+template <int kTN>
+struct Tile {
+    static_assert(kTN == 256 || kTN == 128 || kTN == 64, "tile width");
+    static constexpr uint32_t kBBytes = kBK * kTN * 2;
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr int kStages = static_cast<int>((4u * (kABytes + kBK * kBN * 2)) / kStageBytes);
+    static constexpr int kTmemCols = kAccStages * kTN;
+    static constexpr int kNumBarriers = 2 * kStages + 2 * kAccStages + 1;
+    static constexpr uint32_t kSmemBytes =
+        kStages * kStageBytes + kStagingBytes + kNumBarriers * 8 + 16;
+    static constexpr int kHalfBlocks = kTN / 64;  // 32-column blocks per epilogue warp
+    static constexpr uint32_t kIdescBN = idesc_bf16_f32(kBM, kTN, false, true);
+    static constexpr uint32_t kIdescWt = idesc_bf16_f32(kBM, kTN, false, false);
+    static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103 CTA");
+    static_assert(kBBytes % 1024 == 0, "B stages on 1024-byte boundaries (128-byte swizzle)");
+};
+static_assert(Tile<kBN>::kStages == kStages && Tile<kBN>::kSmemBytes == kSmemBytes &&
+                  Tile<kBN>::kTmemCols == kTmemCols && Tile<kBN>::kIdescBN == kIdescBN,
+              "the default tile width keeps the default layout");
+
 // A wait that gives up: 2 s of global time, checked every 256 polls.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
@@ -589,12 +618,21 @@ __device__ __forceinline__ void ozaki_accumulate_block(double* crow, const int* 
 // kFp8: 8-bit float operands (both K-major, kWt): a K block is 128 elements,
 // still 128 bytes per row, consumed by four tcgen05.mma.kind::f8f6f4 of K = 32;
 // the shared-memory layout and descriptors are byte for byte those of BF16.
-template <int kOut, bool kWt, bool kFp8>
+template <int kOut, bool kWt, bool kFp8, int kTN = kBN>
 __global__ void __launch_bounds__(kNumThreads, 1)
     bigemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmBp, const __grid_constant__ CUtensorMap tmC,
                      const GemmParams p) {
     static_assert(!kFp8 || kWt, "8-bit operands are read K-major only");
+    static_assert(kTN == kBN || (!kFp8 && kOut != kOutOzaki),
+                  "narrow tiles serve the bf16 products only");
+    // this tile width's ring, accumulators and barriers
+    using TileT = Tile<kTN>;
+    constexpr int kRing = TileT::kStages;
+    constexpr uint32_t kRingB = TileT::kBBytes;
+    constexpr uint32_t kRingStage = TileT::kStageBytes;
+    constexpr int kBars = TileT::kNumBarriers;
+    constexpr int kHB = TileT::kHalfBlocks;
     constexpr int kKB = kFp8 ? 128 : kBK;  // elements per K block (128 bytes per row)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 128-byte-swizzled tiles must start on 1024-byte boundaries; the layout
@@ -607,24 +645,24 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     uint8_t* gbase = smem_raw;
     const uint32_t sA = base;                                // stage s: sA + s * kABytes
-    const uint32_t sB = base + kStages * kABytes;            // stage s: sB + s * kBBytes
-    const uint32_t sOut = base + kStages * kStageBytes;      // epilogue staging boxes
-    uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kStages * kStageBytes + kStagingBytes);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBarriers);
+    const uint32_t sB = base + kRing * kABytes;              // stage s: sB + s * kRingB
+    const uint32_t sOut = base + kRing * kRingStage;         // epilogue staging boxes
+    uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kRing * kRingStage + kStagingBytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const uint32_t bar0 = smem_addr(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
-    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + kAccStages + a); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 2 * kAccStages);
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kRing + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kRing + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kRing + kAccStages + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kRing + 2 * kAccStages);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (warp == 2 && lane == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kRing; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
@@ -657,8 +695,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int seg_rows = (sc.fold ? sc.kb_total : sc.kb_per_split) * kKB;
             const int k1 = min(k0 + sc.prefetch_rows, min(k0 + seg_rows, sc.kb_total * kKB));
             for (int k = k0; k < k1; k += kPrefetchRows) {
-                if constexpr (kWt) tma_prefetch_l2_2d(&tmBp, k, nt * kBN);
-                else tma_prefetch_l2_2d(&tmBp, nt * kBN, k);
+                if constexpr (kWt) tma_prefetch_l2_2d(&tmBp, k, nt * kTN);
+                else tma_prefetch_l2_2d(&tmBp, nt * kTN, k);
             }
         }
         tma_prefetch_desc(&tmA);
@@ -666,7 +704,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if constexpr (kOut != kOutAtomic && kOut != kOutOzaki) tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
-        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_alloc(smem_addr(tmem_slot), TileT::kTmemCols);
         tmem_relinquish();
     }
     if (p.a_rows < kBM) {
@@ -679,7 +717,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const uint32_t tail = static_cast<uint32_t>(p.a_rows) * 128u;
         const uint32_t per_stage = (kABytes - tail) / 16u;
         for (uint32_t i = threadIdx.x - kEpilogueWarp0 * 32; threadIdx.x >= kEpilogueWarp0 * 32 &&
-                                                          i < kStages * per_stage;
+                                                          i < kRing * per_stage;
              i += kEpilogueThreads) {
             const uint32_t s_ = i / per_stage, c = i - s_ * per_stage;
             st_shared_v4(sA + s_ * kABytes + tail + c * 16u, 0u, 0u, 0u, 0u);
@@ -730,15 +768,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                 break;
                             }
                             const uint32_t fb = full_bar(stage);
-                            mbar_arrive_expect_tx(fb, kStageBytes);
+                            mbar_arrive_expect_tx(fb, kRingStage);
                             tma_load_2d(sA + stage * kABytes, &tmA, fb, kb * kBK, a_row);
 #pragma unroll
                             for (int c = 0; c < kBN / static_cast<int>(kBChunkCols); ++c)
-                                tma_load_2d(sB + stage * kBBytes + c * kBChunkBytes, &tmB, fb,
+                                tma_load_2d(sB + stage * kRingB + c * kBChunkBytes, &tmB, fb,
                                             n0 + c * static_cast<int>(kBChunkCols), b_row + kb * kBK);
                             issued_mask |= 1u << stage;
                             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                            if (++stage == kStages) {
+                            if (++stage == kRing) {
                                 stage = 0;
                                 phase ^= 1u;
                             }
@@ -753,7 +791,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 // a folded unit streams all of K; its segments follow one another
                 const int kb0 = sc.fold ? 0 : seg * sc.kb_per_split;
                 const int kb1 = sc.fold ? sc.kb_total : min(kb0 + sc.kb_per_split, sc.kb_total);
-                const int m0 = mt * kBM, n0 = nt * kBN;
+                const int m0 = mt * kBM, n0 = nt * kTN;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.status,
                                       kErrWaitProducer)) {
@@ -761,20 +799,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         break;
                     }
                     const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(sc.a_rows) * 128u + kBBytes);
+                    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(sc.a_rows) * 128u + kRingB);
                     tma_load_2d(sA + stage * kABytes, &tmA, fb, kb * kKB, m0);
                     if constexpr (kWt) {
                         // one box: 256 weight rows x 64 k (128 bytes each)
-                        tma_load_2d(sB + stage * kBBytes, &tmB, fb, kb * kKB, n0);
+                        tma_load_2d(sB + stage * kRingB, &tmB, fb, kb * kKB, n0);
                     } else {
 #pragma unroll
-                        for (int c = 0; c < kBN / static_cast<int>(kBChunkCols); ++c)
-                            tma_load_2d(sB + stage * kBBytes + c * kBChunkBytes, &tmB, fb,
+                        for (int c = 0; c < kTN / static_cast<int>(kBChunkCols); ++c)
+                            tma_load_2d(sB + stage * kRingB + c * kBChunkBytes, &tmB, fb,
                                         n0 + c * static_cast<int>(kBChunkCols), kb * kBK);
                     }
                     issued_mask |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == kStages) {
+                    if (++stage == kRing) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -790,7 +828,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             grid_launch_dependents();
             // No copy may still be in flight when the CTA exits: wait (bounded)
             // for the last load issued into every stage.
-            for (int s = 0; s < kStages; ++s)
+            for (int s = 0; s < kRing; ++s)
                 if (issued_mask & (1u << s))
                     wait_bounded(full_bar(s), (issued_parity >> s) & 1u, abort_flag, p.status,
                                  kErrWaitDrain, /*honour_abort=*/false);
@@ -821,7 +859,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kTN);
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!wait_bounded(full_bar(stage), phase, abort_flag, p.status, kErrWaitMma)) {
                             ok = false;
@@ -829,7 +867,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         }
                         tc_fence_after();
                         const uint32_t a0 = sA + stage * kABytes;
-                        const uint32_t b0 = sB + stage * kBBytes;
+                        const uint32_t b0 = sB + stage * kRingB;
     #pragma unroll
                         for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
                             // A: K-major, 128-byte rows; advance 16 elements = 32 bytes.
@@ -846,11 +884,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             if constexpr (kFp8)
                                 mma_fp8(d_tmem, ad, bd, p.idesc_fp8, (kb > kb0 || kk > 0) ? 1u : 0u);
                             else
-                                mma_bf16(d_tmem, ad, bd, kWt ? kIdescWt : kIdescBN,
+                                mma_bf16(d_tmem, ad, bd, kWt ? TileT::kIdescWt : TileT::kIdescBN,
                                          (kb > kb0 || kk > 0) ? 1u : 0u);
                         }
                         mma_commit(empty_bar(stage));
-                        if (++stage == kStages) {
+                        if (++stage == kRing) {
                             stage = 0;
                             phase ^= 1u;
                         }
@@ -866,7 +904,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       }
       // The cluster's two barriers (see the epilogue): every thread of every
       // CTA passes both, on every path.
-      if constexpr (kOut == kOutF32 || kOut == kOutBF16) {
+      if constexpr ((kOut == kOutF32 || kOut == kOutBF16) && kTN == kBN) {
           if (p.cluster) {
               cluster_arrive_release();
               cluster_wait_acquire();
@@ -955,7 +993,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 ozaki_next_pair(p, pa, pb);
             }
         }
-        if constexpr (kOut == kOutF32 || kOut == kOutBF16) {
+        if constexpr ((kOut == kOutF32 || kOut == kOutBF16) && kTN == kBN) {
             if (p.cluster) {
                 // ---- one K segment of a clustered tile: the FP32 partial goes
                 // to this CTA's shared memory (the pipeline stages, idle once
@@ -1068,9 +1106,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
                 int mt, nt, seg;
                 unit_coords(p, u, mt, nt, seg);
-                const int m0 = mt * kBM + q * 32, n0 = nt * kBN;
-                // this warp's 32-column blocks: [h * 4, nchunks)
-                const int nchunks = min(h * 4 + 4, min(kBN / 32, (p.N - n0 + 31) / 32));
+                const int m0 = mt * kBM + q * 32, n0 = nt * kTN;
+                // this warp's 32-column blocks: [h * kHB, nchunks)
+                const int nchunks = min(h * kHB + kHB, min(kTN / 32, (p.N - n0 + 31) / 32));
                 const int acc = t % kAccStages;
                 const uint32_t acc_phase = static_cast<uint32_t>(t / kAccStages) & 1u;
                 if (!wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.status, kErrWaitEpilogue))
@@ -1079,9 +1117,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 bool released = false;
                 if (m0 < p.M) {  // uniform per warp: a warp whose rows are all past M skips
                     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                           static_cast<uint32_t>(acc * kBN);
+                                           static_cast<uint32_t>(acc * kTN);
 #pragma unroll 1
-                    for (int c0 = h * 4; c0 < nchunks; c0 += batch) {
+                    for (int c0 = h * kHB; c0 < nchunks; c0 += batch) {
                         const int nb = min(batch, nchunks - c0);
                         uint32_t r[kMaxBatch * 32];
                         if (batch == 4) tmem_ld_32x32b_x128(tbase + c0 * 32, r);
@@ -1112,7 +1150,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc(tmem_base, TileT::kTmemCols);
     }
 }
 

@@ -174,6 +174,21 @@ BIGEMM_API int bigemm_cluster_capacity(int splits);
 #define BIGEMM_PATH_CLUSTER 3
 BIGEMM_API int bigemm_split_path(int64_t M, int64_t N, int64_t K, int split_k, int fp8);
 
+/* Width in columns of the output tiles a product of this shape runs with on
+ * the current device: BIGEMM_TILE_N (256), or 128 / 64 for a bf16 product
+ * whose 256-wide work units (tiles x K segments) would occupy fewer than half
+ * of the SMs while each unit streams at least 32 K blocks (small M and N,
+ * long K: "Split-K" on the Tencent page names exactly this case, few output
+ * tiles and a long K).  Narrow tiles put more SMs to work on such a product;
+ * they never run on the folded or cluster paths (a split product with narrow
+ * tiles takes BIGEMM_PATH_WORKSPACE).  Speed only: the tile width sets the N
+ * extent of each 128-row tensor-core instruction, never which K blocks an
+ * element sums or in what order, so every width gives the same bits (the GPU
+ * tests compare rows computed at widths 64, 128 and 256).  fp8 = 1 asks for
+ * bigemm_linear_fp8, always 256.  -1 for invalid arguments or when the device
+ * cannot be queried. */
+BIGEMM_API int bigemm_tile_n(int64_t M, int64_t N, int64_t K, int split_k, int fp8);
+
 /* Workspace bytes bigemm_run / bigemm_run_bf16out / bigemm_linear need for
  * (M, N, K, split_k): effective_split * M * bigemm_workspace_ld(N) * 4 when
  * the effective split is > 1 and the product is not folded

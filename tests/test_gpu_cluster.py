@@ -46,9 +46,9 @@ def tiles(M, N):
 
 
 def test_path_rule(capsys):
-    """A split product (S = 2..8) that is not folded clusters exactly when its
-    tiles are no more than the device's cluster capacity for S; the capacity
-    is the device's (printed)."""
+    """A split product (S = 2..8) that is not folded and runs wide tiles
+    clusters exactly when its tiles are no more than the device's cluster
+    capacity for S; the capacity is the device's (printed)."""
     caps = {S: dig.bigemm_cluster_capacity(S) for S in range(2, 9)}
     with capsys.disabled():
         print("\n[cluster path] capacity for S = 2..8: %s" % [caps[S] for S in range(2, 9)])
@@ -61,6 +61,8 @@ def test_path_rule(capsys):
                     want = dig.PATH_UNSPLIT
                 elif dig.bigemm_split_is_folded(M, N, K, S):
                     want = dig.PATH_FOLDED
+                elif dig.bigemm_tile_n(M, N, K, S) != 256:
+                    want = dig.PATH_WORKSPACE
                 elif s <= 8 and tiles(M, N) <= caps[s]:
                     want = dig.PATH_CLUSTER
                 else:
