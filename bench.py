@@ -600,6 +600,8 @@ SINGLE = {
     "square8192": (8192, 8192, 8192, 1, False, "uniform", "tensor"),
     "large16384": (16384, 16384, 16384, 1, True, "normal", "tensor"),
     "longk": (256, 256, 65536, 16, False, "normal", "hbm"),
+    "longk8": (256, 256, 65536, 8, False, "normal", "hbm"),
+    "longk32": (256, 256, 65536, 32, False, "normal", "hbm"),
     # linear layers, weights [N, K], bf16 out: bf16 and 8-bit float (E4M3) operands
     "linear8192": (8192, 8192, 8192, 1, True, "linear", "tensor"),
     "linearfp8_8192": (8192, 8192, 8192, 1, True, "linear_fp8", "tensor_fp8"),
@@ -712,8 +714,8 @@ def run_single(name, args, world, rank, dev, peaks, peak_src):
 
 def run_longk(dev, peaks) -> dict:
     """M = N = 256, K = 65536 with split_k = 8, 16, 32 through bigemm_run (the
-    path the library picks: a cluster of CTAs or the workspace + reduction
-    kernel; the bits are the workspace path's either way), and the atomic-add
+    path and tile width the library picks -- at this shape narrow tiles and
+    the workspace + reduction kernel; the bits are the same every way), and the atomic-add
     contrast at the same splits: its time, and how many distinct results ten
     runs on the same inputs give (the workspace path gives one).  Four input
     copies rotate (256 MiB > L2)."""
