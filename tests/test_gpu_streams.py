@@ -15,8 +15,10 @@ from gemm_check import bits_equal
 
 pytestmark = pytest.mark.gpu
 
-# (M, N, K, split_k): decode-like, ragged, folded-size and unsplit products
-CASES = [(16, 4096, 4096, 8), (300, 600, 1000, 3), (1024, 4096, 2048, 4), (256, 512, 1536, 1)]
+# (M, N, K, split_k): decode-like, ragged, folded-size and unsplit products, and
+# a small long-K product on narrow (64-column) tiles
+CASES = [(16, 4096, 4096, 8), (300, 600, 1000, 3), (1024, 4096, 2048, 4), (256, 512, 1536, 1),
+         (64, 256, 16384, 8)]
 
 
 @pytest.fixture(scope="module", autouse=True)
