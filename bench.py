@@ -214,13 +214,43 @@ def nvml_index(local: int) -> int:
     return local
 
 
+def code_only(text: str) -> str:
+    """C/C++ source with each comment and each run of whitespace replaced by
+    one space: what the compiler sees of it, up to layout.  String literals (the
+    inline PTX) are kept as they are."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(" " if c.isspace() else c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the kernels and of the host code that sizes and configures their
+    launches, comments and whitespace excluded: an edit to a comment changes no
+    kernel, so it does not make an ncu capture stale."""
     import hashlib
     h = hashlib.sha256()
-    # the kernels and the host code that sizes and configures their launches
     for f in ("kernels.cuh", "ptx.cuh", "ozaki.cuh", "bigemm.cu"):
-        with open(os.path.join(ROOT, "deterministic_invariant_gemm_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "deterministic_invariant_gemm_gb300", "csrc", f),
+                  encoding="utf-8") as fh:
+            h.update(code_only(fh.read()).encode("utf-8"))
     return h.hexdigest()[:16]
 
 

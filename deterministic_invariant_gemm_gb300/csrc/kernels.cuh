@@ -14,9 +14,11 @@
 //     blockIdx.x, blockIdx.x + gridDim.x, ... -- a static schedule.
 // None of the three changes the order in which any single C element's terms
 // are added, so the bits of row i depend only on (row i of A, B, K, S).  The
-// same MMA instruction shape (M = 128, N = 256, K = 16) and operand roles are
-// used for every M: short batches are padded by the TMA unit's zero fill, never
-// served by a different code path.
+// same 128-row, K = 16 MMA instruction and operand roles are used for every M:
+// short batches are padded by the TMA unit's zero fill, never served by a
+// different code path.  The instruction's N extent is the tile width, 256,
+// or 128 / 64 for small products with long K (Tile<kTN> below); it sets which
+// columns an instruction covers, not how any column's sum is formed.
 //
 // CTA roles (384 threads = three warpgroups, one CTA per SM):
 //   warp 0       TMA producer: fills a kStages-deep shared-memory ring.
