@@ -759,6 +759,26 @@ def run_longk(dev, peaks) -> dict:
     alg = 2.0 * (M * K + K * N) + 4.0 * M * N
     out = {"shape": [M, N, K], "input_copies": copies,
            "alg_bytes": alg, "peak_gbs": peaks["hbm_gbs"]}
+    # The accumulate chain, measured: one CTA computing a 128 x 64 tile of a
+    # one-row product over all of K (M = 1, N = 64, split_k = 1) runs 4 * K/64
+    # dependent K = 16 MMAs into one accumulator while its loads (12 KB per
+    # K block for one SM) take a fraction of that; its time over the MMA count
+    # is the latency of one dependent MMA.  A K segment of L blocks cannot take
+    # less than 4 L of them, whatever the tile width or the memory system.
+    kb = -(-K // 64)
+    a1 = AB[0][0][:1].contiguous()
+    b1 = AB[0][1][:, :64].contiguous()
+    c1 = torch.empty((1, 64), dtype=torch.float32, device=dev)
+
+    def chain_call(i):
+        dig.bigemm_run(a1, b1, c1, 1, 64, K, K, 64, 64, 1, None, 0)
+
+    for i in range(2):
+        chain_call(i)
+    t_mma = time_region(chain_call, 10, 1) / 10 / (4 * kb)
+    out["mma_chain_ns"] = round(t_mma * 1e9, 1)
+    out["mma_chain_probe"] = "1 x 64 x %d, split_k 1, tile width %d: %d dependent MMAs" % (
+        K, dig.bigemm_tile_n(1, 64, K, 1), 4 * kb)
     iters = 40
     for S in (8, 16, 32):
         wsb = dig.bigemm_workspace_bytes(M, N, K, S)
@@ -772,15 +792,18 @@ def run_longk(dev, peaks) -> dict:
             a, b = AB[i % copies]
             dig.bigemm_run_atomic_splitk(a, b, C, M, N, K, K, N, N, S)
 
+        floor_s = -(-kb // S) * 4 * t_mma
         res = {"path": {0: "unsplit", 1: "workspace", 2: "folded", 3: "cluster"}.get(
-            dig.bigemm_split_path(M, N, K, S), "?"), "tile_n": dig.bigemm_tile_n(M, N, K, S)}
+            dig.bigemm_split_path(M, N, K, S), "?"), "tile_n": dig.bigemm_tile_n(M, N, K, S),
+            "chain_floor_us": round(floor_s * 1e6, 2)}
         for key, fn in (("bigemm_run", call), ("atomic", atomic)):
             for i in range(3):
                 fn(i)
             secs = time_region(fn, iters, 1) / iters
             res[key] = {"us": round(secs * 1e6, 2),
                         "hbm_frac": round(alg / secs / 1e9 / peaks["hbm_gbs"], 4),
-                        "tflops": round(2.0 * M * N * K / secs / 1e12, 2)}
+                        "tflops": round(2.0 * M * N * K / secs / 1e12, 2),
+                        "frac_of_chain_floor": round(floor_s / secs, 4)}
             distinct = set()
             for _ in range(10):
                 fn(0)
