@@ -669,10 +669,11 @@ int64_t round_up(int64_t x, int64_t m) { return ceil_div(x, m) * m; }
 
 // Workspace of bigemm_ozaki_dgemm, in this order, each part 256-byte aligned:
 // A slices [s][M][lda_s] bf16, B slices [s][kpad][ldb_s] bf16, c^(1) of the
-// rows of A [M] int32, c^(1) of the columns of B [N] int32.
+// rows of A [M] int32, c^(1) of the columns of B [N] int32, and one int32
+// count per 128 x 256 output tile (the slice pairs added so far).
 struct OzakiLayout {
-    int64_t lda_s, ldb_s, kpad;
-    size_t off_b, off_ca, off_cb, total;
+    int64_t lda_s, ldb_s, kpad, tiles;
+    size_t off_b, off_ca, off_cb, off_cnt, total;
 };
 
 OzakiLayout ozaki_layout(int64_t M, int64_t N, int64_t K, int slices) {
@@ -685,10 +686,13 @@ OzakiLayout ozaki_layout(int64_t M, int64_t N, int64_t K, int slices) {
     const size_t b = up(static_cast<size_t>(slices) * L.kpad * L.ldb_s * 2);
     const size_t ca = up(static_cast<size_t>(M) * 4);
     const size_t cb = up(static_cast<size_t>(N) * 4);
+    L.tiles = ceil_div(M, kBM) * ceil_div(N, kBN);
+    const size_t cnt = up(static_cast<size_t>(L.tiles) * 4);
     L.off_b = a;
     L.off_ca = a + b;
     L.off_cb = a + b + ca;
-    L.total = a + b + ca + cb;
+    L.off_cnt = a + b + ca + cb;
+    L.total = a + b + ca + cb + cnt;
     return L;
 }
 
@@ -1028,6 +1032,7 @@ bigemm_status bigemm_ozaki_dgemm(const double* A, const double* B, double* C, in
     __nv_bfloat16* Bs = reinterpret_cast<__nv_bfloat16*>(ws + L.off_b);
     int* ca = reinterpret_cast<int*>(ws + L.off_ca);
     int* cb = reinterpret_cast<int*>(ws + L.off_cb);
+    int* cnt = reinterpret_cast<int*>(ws + L.off_cnt);
     // 1-3: split A by rows and B by columns (plain launches: they read the
     // caller's A and B, so they wait for everything before them)
     if (launch_ozaki_split(*dev, A, M, K, lda, 0, rho, slices, As, L.lda_s, M, ca, strm) != cudaSuccess ||
@@ -1050,7 +1055,10 @@ bigemm_status bigemm_ozaki_dgemm(const double* A, const double* B, double* C, in
             return BIGEMM_ERR_CUDA;
     }
     const int64_t m_tiles = ceil_div(M, kBM), n_tiles = ceil_div(N, kBN);
-    if (m_tiles * n_tiles > INT_MAX) return BIGEMM_ERR_ARG;
+    if (m_tiles * n_tiles * pairs > INT_MAX) return BIGEMM_ERR_ARG;
+    // every tile's count of added slice pairs starts at zero
+    if (cudaMemsetAsync(cnt, 0, static_cast<size_t>(L.tiles) * sizeof(int), strm) != cudaSuccess)
+        return BIGEMM_ERR_CUDA;
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
     p.out = C;
@@ -1071,13 +1079,17 @@ bigemm_status bigemm_ozaki_dgemm(const double* A, const double* B, double* C, in
     p.scale = 1.0f;
     p.oz_ca = ca;
     p.oz_cb = cb;
+    p.oz_count = cnt;
     p.oz_slices = slices;
     p.oz_d = d;
     p.oz_beta = 53 - rho;
     p.oz_pairs = static_cast<int>(pairs);
     p.oz_kpad = static_cast<int>(L.kpad);
     p.a_rows = kBM;
-    const int grid = static_cast<int>(p.units < dev->sm_count ? p.units : dev->sm_count);
+    // one CTA per SM at most, over all (slice pair, tile) items: a tile's pairs
+    // may run on different CTAs at once, their additions ordered by the counts
+    const int64_t items = static_cast<int64_t>(p.units) * pairs;
+    const int grid = static_cast<int>(items < dev->sm_count ? items : dev->sm_count);
     if (launch_gemm<kOutOzaki>(false, false, dim3(static_cast<unsigned>(grid)), dim3(kNumThreads), strm,
                                tmA, tmB, tmBp, tmA, p) != cudaSuccess)
         return BIGEMM_ERR_CUDA;

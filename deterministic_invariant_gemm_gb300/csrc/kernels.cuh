@@ -47,6 +47,7 @@ constexpr int kBK = 64;
 constexpr int kUmmaK = 16;
 constexpr int kNumThreads = 384;       // warp 0 TMA, warp 1 MMA, warps 4..11 epilogue
 constexpr int kEpilogueThreads = 256;
+constexpr int kEpilogueWarps = kEpilogueThreads / 32;
 constexpr int kEpilogueWarp0 = 4;      // first epilogue warp: the second warpgroup
 
 // Register split.  The block is launched with kLaunchRegs registers per thread
@@ -140,6 +141,7 @@ constexpr unsigned kErrWaitMma = 2u;
 constexpr unsigned kErrWaitEpilogue = 4u;
 constexpr unsigned kErrWaitDrain = 8u;
 constexpr unsigned kErrSmemAlign = 16u;
+constexpr unsigned kErrWaitOzakiOrder = 32u;
 
 enum OutKind : int {
     kOutF32 = 0,     // C fp32, plain stores
@@ -177,10 +179,17 @@ struct GemmParams {
                             //    sum their partials through distributed shared memory
                             //    (splits in 2..8, direct output, one unit per CTA)
     // Ozaki scheme (kOutOzaki): A is `oz_slices` bfloat16 slices of M rows each
-    // (slice p at rows p * M), B the same number of slices of oz_kpad rows;
-    // a unit is a tile, run once for every slice pair (p, q) with p + q < oz_d.
+    // (slice p at rows p * M), B the same number of slices of oz_kpad rows.
+    // The work items are (slice pair, tile) pairs, pair-major: item L is pair
+    // L / units of tile L % units, for the pairs (p, q) with p + q < oz_d, and
+    // CTA c takes items c, c + grid, ...  A tile's pairs may run on different
+    // CTAs; oz_count[tile] (zero at launch) counts the epilogue warps that have
+    // added a pair into the tile's C (kEpilogueWarps per pair), and pair k's
+    // warps wait until it reaches k * kEpilogueWarps, so every element of C
+    // still takes its pairs in order.
     const int* oz_ca;       // c^(1) of every row of A
     const int* oz_cb;       // c^(1) of every column of B
+    int* oz_count;          // per tile
     int oz_slices, oz_d, oz_beta, oz_pairs, oz_kpad;
     int selftest_stall;     // 1 (the failure self-test only): the producer issues no
                             //    loads, so the MMA issuer's bounded wait must give up
@@ -292,6 +301,25 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
     }
     *abort_flag = 1;
     atomicOr(status, why);
+    return false;
+}
+
+// Bounded wait until *count >= want (an acquire load per poll).  Gives up
+// like wait_bounded: when another role has aborted, or after
+// kWaitTimeoutNs, raising the abort flag and the error bit.
+__device__ __forceinline__ bool wait_count_bounded(const int* count, int want, volatile int* abort_flag,
+                                                   unsigned* status) {
+    if (ld_acquire_gpu(count) >= want) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1; it != 0u; ++it) {
+        if (ld_acquire_gpu(count) >= want) return true;
+        if ((it & 63u) == 0u) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
+        }
+    }
+    *abort_flag = 1;
+    atomicOr(status, kErrWaitOzakiOrder);
     return false;
 }
 
@@ -751,13 +779,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = !sc.selftest_stall;  // the failure self-test issues nothing
             if constexpr (kOut == kOutOzaki) {
-                // Slice pairs outermost, then this CTA's tiles: all CTAs work on
-                // the same pair (pa, pb) at a time and share its A and B panels
-                // in L2.  Per tile: rows pa * M + m0 of the A slices, rows
-                // pb * oz_kpad + k of the B slices.
-                int pa = 0, pb = 0;
-                for (int pair = 0; ok && pair < p.oz_pairs; ++pair) {
-                    for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+                // Items pair-major: all CTAs work on the same one or two slice
+                // pairs at a time and share their A and B panels in L2.  Per
+                // item: rows pa * M + m0 of the A slices, rows pb * oz_kpad + k
+                // of the B slices.
+                int pa = 0, pb = 0, pk = 0;  // pair pk is (pa, pb)
+                const int items = p.units * p.oz_pairs;
+                for (int L = blockIdx.x; ok && L < items; L += gridDim.x) {
+                    const int pair = L / p.units, u = L - pair * p.units;
+                    for (; pk < pair; ++pk) ozaki_next_pair(p, pa, pb);
+                    {
                         int mt, nt, seg;
                         unit_coords(p, u, mt, nt, seg);
                         const int n0 = nt * kBN;
@@ -784,7 +815,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             }
                         }
                     }
-                    ozaki_next_pair(p, pa, pb);
                 }
             } else {
             for (int u = blockIdx.x; ok && u < sc.units; u += gridDim.x) {
@@ -842,13 +872,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t phase = 0;
             int t = 0;  // accumulators filled so far (one per segment)
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-                int mt, nt, seg0;
-                unit_coords(p, u, mt, nt, seg0);
+            // an Ozaki item is one (slice pair, tile), over all of K
+            const int n_items = (kOut == kOutOzaki) ? p.units * p.oz_pairs : p.units;
+            for (int u = blockIdx.x; ok && u < n_items; u += gridDim.x) {
+                int mt = 0, nt = 0, seg0 = 0;
+                if constexpr (kOut != kOutOzaki) unit_coords(p, u, mt, nt, seg0);
                 // A folded unit fills one accumulator per K segment, in order; the
-                // epilogue adds them.  An Ozaki unit fills one per slice pair, each
-                // over all of K.  Otherwise the unit is the single segment seg0.
-                const int nseg = (kOut == kOutOzaki) ? p.oz_pairs : (p.fold ? p.splits : 1);
+                // epilogue adds them.  Otherwise the unit is the single segment seg0.
+                const int nseg = (kOut != kOutOzaki && p.fold) ? p.splits : 1;
                 for (int sg = 0; ok && sg < nseg; ++sg, ++t) {
                     const int seg = p.fold ? sg : seg0;
                     const int kb0 = seg * p.kb_per_split;
@@ -942,20 +973,27 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         int t = 0;          // accumulators drained so far (one per segment)
         bool folded = false;
         if constexpr (kOut == kOutOzaki) {
-            // ---- Ozaki scheme: for every slice pair (pa, pb) of the tile, in the
-            // order of the binary64 sum, C[row][col] += 2^e * P with P the FP32
-            // slice-pair product (exact) and e = c_a^(pa)[row] + c_b^(pb)[col];
-            // the first pair starts the sum at +0.0.  Each thread owns its row
-            // and its half of the tile's columns, so it alone reads and writes
-            // those elements of C, pair after pair.
+            // ---- Ozaki scheme: for the item's slice pair (pa, pb), C[row][col] +=
+            // 2^e * P with P the FP32 slice-pair product (exact) and e =
+            // c_a^(pa)[row] + c_b^(pb)[col]; the first pair starts the sum at
+            // +0.0.  A warp adds pair k into its 32 rows x 128 columns only
+            // once the tile's count shows that all warps have added pair k - 1
+            // (whichever CTA ran it), then raises the count: every element
+            // takes its pairs in the order of the binary64 sum.  Each lane's
+            // acquiring read of the count orders its reads of C after the
+            // stores that raised it (each writer lane fences before the count
+            // is raised).
             folded = true;
             double* C = static_cast<double*>(p.out);
             const int step = p.oz_beta + 1;
             bool ok = true;
-            // the producer's order: slice pairs outermost, then this CTA's tiles
-            int pa = 0, pb = 0;
-            for (int pair = 0; ok && pair < p.oz_pairs; ++pair) {
-                for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
+            // the producer's order: items pair-major
+            int pa = 0, pb = 0, pk = 0;
+            const int items = p.units * p.oz_pairs;
+            for (int L = blockIdx.x; ok && L < items; L += gridDim.x) {
+                const int pair = L / p.units, u = L - pair * p.units;
+                for (; pk < pair; ++pk) ozaki_next_pair(p, pa, pb);
+                {
                     int mt, nt, seg;
                     unit_coords(p, u, mt, nt, seg);
                     const int m0 = mt * kBM + q * 32, n0 = nt * kBN;
@@ -968,6 +1006,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         break;
                     }
                     tc_fence_after();
+                    if (pair > 0) {
+                        // wait (bounded) for pair - 1 of this tile in every warp
+                        bool in_order = true;
+                        if (lane == 0)
+                            in_order = wait_count_bounded(p.oz_count + u, pair * kEpilogueWarps,
+                                                          abort_flag, p.status);
+                        in_order = __shfl_sync(0xffffffffu, in_order ? 1 : 0, 0) != 0;
+                        if (!in_order) {
+                            tc_fence_before();
+                            mbar_arrive(tempty_bar(acc));
+                            ok = false;
+                            break;
+                        }
+                        // every lane acquires the count itself, so that its own
+                        // loads of C below come after the previous pair's stores
+                        (void)ld_acquire_gpu(p.oz_count + u);
+                    }
                     if (m0 < p.M) {
                         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                                static_cast<uint32_t>(acc * kBN);
@@ -991,8 +1046,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         tc_fence_before();
                         mbar_arrive(tempty_bar(acc));
                     }
+                    // this warp's part of the pair is in C: count it
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) atomicAdd(p.oz_count + u, 1);
+                    ++t;
                 }
-                ozaki_next_pair(p, pa, pb);
             }
         }
         if constexpr ((kOut == kOutF32 || kOut == kOutBF16) && kTN == kBN) {

@@ -345,7 +345,9 @@ BIGEMM_API int64_t bigemm_ozaki_pairs(int slices, int d);
 /* Workspace bytes of bigemm_ozaki_dgemm (slices = 0: the default): the
  * slices of A [s][M][round_up(K, 8)] and of B [s][round_up(K, 64)]
  * [round_up(N, 8)] in bf16, then c^(1) of every row of A and every column
- * of B (int32), each part 256-byte aligned.  0 for invalid arguments. */
+ * of B (int32), then one int32 per 128 x 256 tile of C (how many slice
+ * pairs the tile has taken so far), each part 256-byte aligned.  0 for
+ * invalid arguments. */
 BIGEMM_API size_t bigemm_ozaki_workspace_bytes(int64_t M, int64_t N, int64_t K, int slices);
 
 /* The split alone.  X: binary64 [rows][ld].  axis 0: every row is a vector,
@@ -365,8 +367,12 @@ BIGEMM_API bigemm_status bigemm_ozaki_split(const double *X, int64_t rows, int64
  * smaller for Fast Mode's trade of accuracy for speed.  K <= 2^22.  Four
  * launches: the row split of A, the column maxima and column split of B, and
  * one tensor-core kernel that runs every kept slice pair of each output tile
- * and keeps the binary64 sum in C.  Workspace: bigemm_ozaki_workspace_bytes,
- * 256-byte aligned. */
+ * and keeps the binary64 sum in C (plus one memset of the tile counts).  The
+ * kernel deals the (slice pair, tile) products over the SMs pair by pair, so
+ * the pairs of one tile may run on different SMs at once; each element of C
+ * still takes its pairs' terms one after another in the fixed pair order (a
+ * tile's epilogue waits, bounded, for its count to show the previous pair).
+ * Workspace: bigemm_ozaki_workspace_bytes, 256-byte aligned. */
 BIGEMM_API bigemm_status bigemm_ozaki_dgemm(const double *A, const double *B, double *C,
                                             int64_t M, int64_t N, int64_t K,
                                             int64_t lda, int64_t ldb, int64_t ldc,
