@@ -174,12 +174,14 @@ bool folds(int64_t M, int64_t N, int splits) {
 
 // Tile width of a product (kBN = 256, or 128 / 64).  The wide tile unless
 // its units (tiles x K segments) would occupy fewer than half of the SMs and
-// each unit streams at least kNarrowMinBlocks K blocks: then a single SM's
-// load rate, not HBM, sets the pace, and narrower tiles put more SMs to work
-// -- the widest width whose units reach half the SMs, else 64.  Short
-// segments keep the wide tile: their time is launch and pipeline latency,
-// which narrower tiles do not shorten.  Folded and 8-bit products are always
-// wide.  Speed only: every width forms every sum the same way.
+// each unit streams at least kNarrowMinBlocks K blocks: then each unit's K
+// loop, not HBM, sets the pace -- an SM takes in at most about 140 GB/s, and
+// a unit's dependent MMAs run one after another -- and narrower tiles put
+// more SMs to work with fewer bytes each, down to the MMA chain's floor: the
+// widest width whose units reach half the SMs, else 64.  Short segments keep
+// the wide tile: their time is launch and pipeline latency, which narrower
+// tiles do not shorten.  Folded and 8-bit products are always wide.  Speed
+// only: every width forms every sum the same way.
 constexpr int kNarrowMinBlocks = 32;
 
 int tile_width(int64_t M, int64_t N, int splits, int kb_per_split, bool fold, bool fp8,
