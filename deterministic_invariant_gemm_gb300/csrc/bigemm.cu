@@ -412,8 +412,23 @@ cudaError_t launch_gemm(bool wt, bool fp8, dim3 g, dim3 blk, cudaStream_t stream
     }
     if constexpr (kOut == kOutOzaki) {
         if (wt || fp8) return cudaErrorInvalidValue;  // bfloat16 slices of B [K, N] only
-        return launch_pdl(bigemm_tc_kernel<kOut, false, false>, g, blk, kSmemBytes, stream, tmA, tmB,
-                          tmBp, tmC, p);
+        // A cooperative launch: the CTAs of an Ozaki product wait on one
+        // another (a tile's pairs run on different CTAs, in order), so CUDA
+        // must start the grid only when all of its CTAs can be resident at
+        // once -- also while other kernels, another Ozaki product among
+        // them, hold SMs.  (No programmatic serialisation here: the kernel's
+        // dependency wait is then a no-op and it starts after its predecessor.)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = g;
+        cfg.blockDim = blk;
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, bigemm_tc_kernel<kOut, false, false>, tmA, tmB, tmBp, tmC, p);
     } else if constexpr (kOut == kOutAtomic) {
         if (wt || fp8) return cudaErrorInvalidValue;  // the contrast exists for bf16 B [K, N] only
         return launch_pdl(bigemm_tc_kernel<kOut, false, false>, g, blk, kSmemBytes, stream, tmA, tmB,

@@ -372,9 +372,9 @@ BIGEMM_API bigemm_status bigemm_ozaki_split(const double *X, int64_t rows, int64
  * the pairs of one tile may run on different SMs at once; each element of C
  * still takes its pairs' terms one after another in the fixed pair order (a
  * tile's epilogue waits, bounded, for its count to show the previous pair).
- * Those waits assume the kernel's CTAs (at most one per SM) are all resident
- * within 2 s; should other work hold the SMs longer, the kernel gives up and
- * bigemm_device_status reports BIGEMM_ERR_TIMEOUT.
+ * The kernel is a cooperative launch: CUDA starts it only when all of its
+ * CTAs (at most one per SM) can be resident together, so those waits end
+ * whatever else runs on the device, concurrent Ozaki products included.
  * Workspace: bigemm_ozaki_workspace_bytes, 256-byte aligned. */
 BIGEMM_API bigemm_status bigemm_ozaki_dgemm(const double *A, const double *B, double *C,
                                             int64_t M, int64_t N, int64_t K,

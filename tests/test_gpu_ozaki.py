@@ -193,3 +193,47 @@ def test_dgemm_wrapper_and_edge_cases():
     c2 = torch.empty(40, 34, dtype=torch.float64, device="cuda")
     assert dig.bigemm_ozaki_dgemm(A, B, c2, 40, 33, 50, 50, 33, 34, 0, 0, None, 0, check=False) == 3
     assert dig.bigemm_ozaki_dgemm(A, B, c2, 40, 33, 50, 50, 33, 34, 33, 0, None, 0, check=False) == 1
+
+
+def test_concurrent_products_on_two_streams_and_a_graph_replay():
+    """The slice-pair kernel's CTAs wait on one another (a tile's pairs run on
+    different CTAs, in pair order), so it is a cooperative launch: two products
+    enqueued on two streams at once, each with a CTA on every SM, must both
+    finish (no bounded wait may run out) with the serial results' bits, and so
+    must a CUDA graph replay of one."""
+    shapes = [(512, 768, 1024, 21), (640, 512, 2048, 22)]
+    data = []
+    for M, N, K, seed in shapes:
+        A = wide((M, K), seed, 8).cuda()
+        B = wide((K, N), seed + 1, 8).cuda()
+        data.append((A, B))
+    serial = [dig.ozaki_matmul(A, B) for A, B in data]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in data]
+    outs = []
+    for _ in range(3):
+        outs = []
+        torch.cuda.current_stream().synchronize()
+        for (A, B), st in zip(data, streams):
+            with torch.cuda.stream(st):
+                outs.append(dig.ozaki_matmul(A, B, stream=st))
+        torch.cuda.synchronize()
+        assert dig.bigemm_device_status(reset=True) == 0
+        for got, want in zip(outs, serial):
+            assert torch.equal(got.view(torch.int64), want.view(torch.int64))
+    A, B = data[0]
+    M, K = A.shape
+    N = B.shape[1]
+    C = torch.empty((M, N), dtype=torch.float64, device="cuda")
+    ws = torch.empty(dig.bigemm_ozaki_workspace_bytes(M, N, K, 0), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dig.ozaki_matmul(A, B, out=C, workspace=ws, stream=s)
+    for _ in range(2):
+        C.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(C.view(torch.int64), serial[0].view(torch.int64))
+    assert dig.bigemm_device_status(reset=True) == 0
