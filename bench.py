@@ -857,6 +857,44 @@ def run_other_workloads(dev, peaks) -> dict:
                      "launches": dig.bigemm_last_launch_count()}
         del AB, C, ws
         torch.cuda.empty_cache()
+    # The small product (64 x 256 x 512, split_k 1, FP32 out): a latency case
+    # with no roofline target.  Per-call device time from a CUDA graph of 50
+    # back-to-back calls (programmatic launches overlap their prologues), and
+    # the time of one call alone between two events on its stream.
+    M, N, K = 64, 256, 512
+    a, b = workloads.pair(M, N, K, workloads.BASE_SEED)
+    a, b = a.to(dev), b.to(dev)
+    C = torch.empty((M, N), dtype=torch.float32, device=dev)
+    st = torch.cuda.Stream(device=dev)
+    st.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        for _ in range(50):
+            dig.bigemm_run(a, b, C, M, N, K, K, N, N, 1, None, 0, stream=st)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(20):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    chained_us = e0.elapsed_time(e1) * 1e3 / (20 * 50)
+    alone = []
+    with torch.cuda.stream(st):
+        for _ in range(30):
+            e0.record(st)
+            dig.bigemm_run(a, b, C, M, N, K, K, N, N, 1, None, 0, stream=st)
+            e1.record(st)
+            st.synchronize()
+            alone.append(e0.elapsed_time(e1) * 1e3)
+    alone.sort()
+    out["small_64x256x512"] = {"us_per_call_chained": round(chained_us, 2),
+                               "us_one_call_median": round(alone[len(alone) // 2], 2),
+                               "tflops_chained": round(2.0 * M * N * K / (chained_us * 1e-6) / 1e12, 3),
+                               "split_k": 1, "out": "fp32", "launches": 1}
+    del g, a, b, C
     # linear layers, weights [N, K]: BF16 and 8-bit floats (E4M3).  The FP8
     # peak is the measured BF16 peak times the nominal FP8 / BF16 ratio (2).
     fp8_peak = 2.0 * bf16_peak
