@@ -105,3 +105,14 @@ def test_calls_from_two_host_threads():
     for t in threads:
         t.join()
     assert not errors, errors
+
+
+def test_default_stream_is_torchs_current_stream():
+    """stream=None means torch's current stream, read through its raw
+    accessor: the same handle as torch.cuda.current_stream(), inside and
+    outside a stream context."""
+    assert dig._current_raw_stream() == torch.cuda.current_stream().cuda_stream
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        assert dig._current_raw_stream() == s.cuda_stream
+    assert dig._current_raw_stream() == torch.cuda.current_stream().cuda_stream
