@@ -38,7 +38,7 @@ __all__ = [
     "bigemm_fp8_workspace_bytes", "bigemm_linear_fp8", "bigemm_split_is_folded", "bigemm_split_path", "bigemm_tile_n",
     "bigemm_cluster_capacity", "bigemm_ozaki_rho", "bigemm_ozaki_default_slices",
     "bigemm_ozaki_pairs", "bigemm_ozaki_workspace_bytes", "bigemm_ozaki_split", "bigemm_ozaki_dgemm",
-    "ozaki_matmul", "bigemm_selftest_timeout", "PATH_UNSPLIT", "PATH_WORKSPACE", "PATH_FOLDED", "PATH_CLUSTER", "FP8_E4M3",
+    "ozaki_matmul", "bigemm_selftest_timeout", "bigemm_selftest_ozaki_order_timeout", "PATH_UNSPLIT", "PATH_WORKSPACE", "PATH_FOLDED", "PATH_CLUSTER", "FP8_E4M3",
     "FP8_E5M2", "FOLD_MIN_ROWS", "FOLD_MIN_TILES",
     "STATIC_SCRATCH_BYTES", "matmul", "linear", "linear_fp8", "EXPORTED_SYMBOLS",
 ]
@@ -70,7 +70,7 @@ EXPORTED_SYMBOLS = (
     "bigemm_split_is_folded", "bigemm_split_path", "bigemm_tile_n", "bigemm_cluster_capacity",
     "bigemm_ozaki_rho", "bigemm_ozaki_default_slices", "bigemm_ozaki_pairs",
     "bigemm_ozaki_workspace_bytes", "bigemm_ozaki_split", "bigemm_ozaki_dgemm",
-    "bigemm_selftest_timeout",
+    "bigemm_selftest_timeout", "bigemm_selftest_ozaki_order_timeout",
 )
 
 FP8_E4M3 = 0
@@ -115,6 +115,7 @@ def load():
         "bigemm_cluster_capacity": ([i32], i32),
         "bigemm_ozaki_rho": ([i64], i32),
         "bigemm_selftest_timeout": ([vp], i32),
+        "bigemm_selftest_ozaki_order_timeout": ([vp], i32),
         "bigemm_ozaki_default_slices": ([i64], i32),
         "bigemm_ozaki_pairs": ([i32, i32], i64),
         "bigemm_ozaki_workspace_bytes": ([i64, i64, i64, i32], sz),
@@ -467,6 +468,13 @@ def bigemm_selftest_timeout(stream=None, check=True) -> int:
     st = load().bigemm_selftest_timeout(_stream(stream))
     if check:
         _check(st, "bigemm_selftest_timeout")
+    return st
+
+
+def bigemm_selftest_ozaki_order_timeout(stream=None, check=True) -> int:
+    st = load().bigemm_selftest_ozaki_order_timeout(_stream(stream))
+    if check:
+        _check(st, "bigemm_selftest_ozaki_order_timeout")
     return st
 
 

@@ -686,8 +686,9 @@ int64_t round_up(int64_t x, int64_t m) { return ceil_div(x, m) * m; }
 
 // Workspace of bigemm_ozaki_dgemm, in this order, each part 256-byte aligned:
 // A slices [s][M][lda_s] bf16, B slices [s][kpad][ldb_s] bf16, c^(1) of the
-// rows of A [M] int32, c^(1) of the columns of B [N] int32, and one int32
-// count per 128 x 256 output tile (the slice pairs added so far).
+// rows of A [M] int32, c^(1) of the columns of B [N] int32, one int32 count
+// per 128 x 256 output tile (the slice pairs added so far) and one int32
+// abort word for the launch.
 struct OzakiLayout {
     int64_t lda_s, ldb_s, kpad, tiles;
     size_t off_b, off_ca, off_cb, off_cnt, total;
@@ -704,7 +705,7 @@ OzakiLayout ozaki_layout(int64_t M, int64_t N, int64_t K, int slices) {
     const size_t ca = up(static_cast<size_t>(M) * 4);
     const size_t cb = up(static_cast<size_t>(N) * 4);
     L.tiles = ceil_div(M, kBM) * ceil_div(N, kBN);
-    const size_t cnt = up(static_cast<size_t>(L.tiles) * 4);
+    const size_t cnt = up(static_cast<size_t>(L.tiles + 1) * 4);
     L.off_b = a;
     L.off_ca = a + b;
     L.off_cb = a + b + ca;
@@ -971,6 +972,31 @@ bigemm_status bigemm_selftest_timeout(bigemm_stream stream) {
                     -1, -1, 1.0f, /*selftest_stall=*/true);
 }
 
+static bigemm_status ozaki_dgemm_impl(const double* A, const double* B, double* C, int64_t M, int64_t N,
+                                      int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int slices, int d,
+                                      void* workspace, size_t workspace_bytes, bigemm_stream stream,
+                                      bool stall_order);
+
+bigemm_status bigemm_selftest_ozaki_order_timeout(bigemm_stream stream) {
+    g_last_launches = 0;
+    void* scratch = nullptr;
+    const bigemm_status st = static_scratch_address(&scratch);
+    if (st != BIGEMM_OK) return st;
+    // a 256 x 256 x 128 product of zero matrices in the built-in array:
+    // A and B (256 KiB each), C (512 KiB), then the workspace
+    constexpr int64_t M = 256, N = 256, K = 128;
+    unsigned char* base = static_cast<unsigned char*>(scratch);
+    double* A = reinterpret_cast<double*>(base);
+    double* B = reinterpret_cast<double*>(base + (256 << 10));
+    double* C = reinterpret_cast<double*>(base + (512 << 10));
+    unsigned char* ws = base + (1 << 20);
+    const size_t need = ozaki_layout(M, N, K, ozaki_default_slices(ozaki_rho(K))).total;
+    if (need + (1u << 20) > BIGEMM_STATIC_SCRATCH_BYTES) return BIGEMM_ERR_STATIC_LIMIT;
+    if (cudaMemsetAsync(base, 0, 512 << 10, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return BIGEMM_ERR_CUDA;
+    return ozaki_dgemm_impl(A, B, C, M, N, K, K, N, N, 0, 0, ws, need, stream, /*stall_order=*/true);
+}
+
 int bigemm_ozaki_rho(int64_t K) { return (K < 1 || K > kOzakiMaxK) ? -1 : ozaki_rho(K); }
 
 int bigemm_ozaki_default_slices(int64_t K) {
@@ -1010,9 +1036,12 @@ bigemm_status bigemm_ozaki_split(const double* X, int64_t rows, int64_t cols, in
     return BIGEMM_OK;
 }
 
-bigemm_status bigemm_ozaki_dgemm(const double* A, const double* B, double* C, int64_t M, int64_t N,
-                                 int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int slices, int d,
-                                 void* workspace, size_t workspace_bytes, bigemm_stream stream) {
+// stall_order (the failure self-test only): every tile's count starts far
+// below zero, so no epilogue wait for a previous slice pair is ever met.
+static bigemm_status ozaki_dgemm_impl(const double* A, const double* B, double* C, int64_t M, int64_t N,
+                                      int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int slices, int d,
+                                      void* workspace, size_t workspace_bytes, bigemm_stream stream,
+                                      bool stall_order) {
     g_last_launches = 0;
     const cudaStream_t strm = static_cast<cudaStream_t>(stream);
     if (M < 0 || N < 0 || K < 0 || K > kOzakiMaxK || M > INT_MAX || N > INT_MAX) return BIGEMM_ERR_ARG;
@@ -1073,8 +1102,12 @@ bigemm_status bigemm_ozaki_dgemm(const double* A, const double* B, double* C, in
     }
     const int64_t m_tiles = ceil_div(M, kBM), n_tiles = ceil_div(N, kBN);
     if (m_tiles * n_tiles * pairs > INT_MAX) return BIGEMM_ERR_ARG;
-    // every tile's count of added slice pairs starts at zero
-    if (cudaMemsetAsync(cnt, 0, static_cast<size_t>(L.tiles) * sizeof(int), strm) != cudaSuccess)
+    // every tile's count of added slice pairs starts at zero, and so does the
+    // launch's abort word after them
+    if (cudaMemsetAsync(cnt, 0, static_cast<size_t>(L.tiles + 1) * sizeof(int), strm) != cudaSuccess)
+        return BIGEMM_ERR_CUDA;
+    if (stall_order &&
+        cudaMemsetAsync(cnt, 0x80, static_cast<size_t>(L.tiles) * sizeof(int), strm) != cudaSuccess)
         return BIGEMM_ERR_CUDA;
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
@@ -1112,6 +1145,13 @@ bigemm_status bigemm_ozaki_dgemm(const double* A, const double* B, double* C, in
         return BIGEMM_ERR_CUDA;
     g_last_launches = 4;
     return BIGEMM_OK;
+}
+
+bigemm_status bigemm_ozaki_dgemm(const double* A, const double* B, double* C, int64_t M, int64_t N,
+                                 int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int slices, int d,
+                                 void* workspace, size_t workspace_bytes, bigemm_stream stream) {
+    return ozaki_dgemm_impl(A, B, C, M, N, K, lda, ldb, ldc, slices, d, workspace, workspace_bytes, stream,
+                            false);
 }
 
 bigemm_status bigemm_device_status(int reset) {

@@ -189,7 +189,7 @@ struct GemmParams {
     // still takes its pairs in order.
     const int* oz_ca;       // c^(1) of every row of A
     const int* oz_cb;       // c^(1) of every column of B
-    int* oz_count;          // per tile
+    int* oz_count;          // per tile, then the grid's abort word (oz_count[units])
     int oz_slices, oz_d, oz_beta, oz_pairs, oz_kpad;
     int selftest_stall;     // 1 (the failure self-test only): the producer issues no
                             //    loads, so the MMA issuer's bounded wait must give up
@@ -305,20 +305,28 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
 }
 
 // Bounded wait until *count >= want (an acquire load per poll).  Gives up
-// like wait_bounded: when another role has aborted, or after
-// kWaitTimeoutNs, raising the abort flag and the error bit.
+// like wait_bounded: when another role of this CTA has aborted, when another
+// CTA of the grid has given up (*grid_abort, a word of the launch's
+// workspace, zero at launch), or after kWaitTimeoutNs; a timeout raises the
+// CTA's abort flag, the grid's abort word and the error bit, so that the
+// CTAs waiting behind this one stop at once instead of each running out its
+// own time.
 __device__ __forceinline__ bool wait_count_bounded(const int* count, int want, volatile int* abort_flag,
-                                                   unsigned* status) {
+                                                   int* grid_abort, unsigned* status) {
     if (ld_acquire_gpu(count) >= want) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1; it != 0u; ++it) {
         if (ld_acquire_gpu(count) >= want) return true;
         if ((it & 63u) == 0u) {
-            if (*abort_flag) return false;
+            if (*abort_flag || *reinterpret_cast<volatile int*>(grid_abort)) {
+                *abort_flag = 1;
+                return false;
+            }
             if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
         }
     }
     *abort_flag = 1;
+    atomicExch(grid_abort, 1);
     atomicOr(status, kErrWaitOzakiOrder);
     return false;
 }
@@ -1011,7 +1019,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         bool in_order = true;
                         if (lane == 0)
                             in_order = wait_count_bounded(p.oz_count + u, pair * kEpilogueWarps,
-                                                          abort_flag, p.status);
+                                                          abort_flag, p.oz_count + p.units, p.status);
                         in_order = __shfl_sync(0xffffffffu, in_order ? 1 : 0, 0) != 0;
                         if (!in_order) {
                             tc_fence_before();

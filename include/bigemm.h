@@ -346,8 +346,8 @@ BIGEMM_API int64_t bigemm_ozaki_pairs(int slices, int d);
  * slices of A [s][M][round_up(K, 8)] and of B [s][round_up(K, 64)]
  * [round_up(N, 8)] in bf16, then c^(1) of every row of A and every column
  * of B (int32), then one int32 per 128 x 256 tile of C (how many slice
- * pairs the tile has taken so far), each part 256-byte aligned.  0 for
- * invalid arguments. */
+ * pairs the tile has taken so far) and one more (set when a wait gives up),
+ * each part 256-byte aligned.  0 for invalid arguments. */
 BIGEMM_API size_t bigemm_ozaki_workspace_bytes(int64_t M, int64_t N, int64_t K, int slices);
 
 /* The split alone.  X: binary64 [rows][ld].  axis 0: every row is a vector,
@@ -442,6 +442,19 @@ BIGEMM_API bigemm_status bigemm_device_status(int reset);
  * the context stays usable.  Shares the scratch array with
  * bigemm_run_splitk_static (calls must not overlap). */
 BIGEMM_API bigemm_status bigemm_selftest_timeout(bigemm_stream stream);
+
+/* Self-test of the Ozaki kernel's failure path; the pages have no counterpart.
+ * Enqueues a 256 x 256 x 128 binary64 product of zero matrices, with its
+ * operands, output and workspace in the built-in scratch array, whose tile
+ * counts start far below zero, so that no epilogue's bounded wait for the
+ * previous slice pair of its tile is ever met.  The first wait to give up
+ * after 2 s sets the launch's abort word, and every other CTA then leaves its
+ * waits at once (rather than each running out its own 2 s); the kernel ends
+ * with the wait's bit in the device error word, so a later
+ * bigemm_device_status() returns BIGEMM_ERR_TIMEOUT, and the context stays
+ * usable.  Shares the scratch array with bigemm_run_splitk_static (calls
+ * must not overlap). */
+BIGEMM_API bigemm_status bigemm_selftest_ozaki_order_timeout(bigemm_stream stream);
 
 /* Number of kernels the most recent successful call on this host thread
  * enqueued (0 to 4). */

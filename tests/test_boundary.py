@@ -193,8 +193,11 @@ def test_ozaki_host_helpers_agree_with_the_oracle(lib):
     M, N, K, s = 100, 70, 300, 0
     s = dig.bigemm_ozaki_default_slices(K)
     up = lambda x: (x + 255) // 256 * 256
-    want = up(s * M * 304 * 2) + up(s * 320 * 72 * 2) + up(M * 4) + up(N * 4) + up(1 * 4)
+    want = up(s * M * 304 * 2) + up(s * 320 * 72 * 2) + up(M * 4) + up(N * 4) + up((1 + 1) * 4)
     assert dig.bigemm_ozaki_workspace_bytes(M, N, K, 0) == want
     M, N = 1000, 3000              # 8 x 12 tiles
-    want = up(s * M * 304 * 2) + up(s * 320 * 3000 * 2) + up(M * 4) + up(N * 4) + up(96 * 4)
+    want = up(s * M * 304 * 2) + up(s * 320 * 3000 * 2) + up(M * 4) + up(N * 4) + up((96 + 1) * 4)
+    assert dig.bigemm_ozaki_workspace_bytes(M, N, K, 0) == want
+    M, N = 1024, 4096              # 8 x 16 tiles: the abort word starts a second 256-byte block
+    want = up(s * M * 304 * 2) + up(s * 320 * 4096 * 2) + up(M * 4) + up(N * 4) + up((128 + 1) * 4)
     assert dig.bigemm_ozaki_workspace_bytes(M, N, K, 0) == want

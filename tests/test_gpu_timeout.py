@@ -40,3 +40,33 @@ def test_expired_wait_is_reported_and_the_context_survives(cuda_device):
     torch.cuda.synchronize()
     assert bits_equal(after, before)
     assert dig.bigemm_device_status(reset=False) == 0
+
+
+def test_ozaki_order_wait_gives_up_once_for_the_whole_grid(cuda_device):
+    """The Ozaki kernel's epilogues wait for the previous slice pair of their
+    tile, possibly on another CTA.  bigemm_selftest_ozaki_order_timeout starts
+    every tile's count far below zero, so no such wait is ever met: the first
+    to give up (after 2 s) sets the launch's abort word and every other CTA
+    leaves at once -- one 2 s limit for the grid, not one per CTA or per pair
+    in turn.  The error word reports the timeout, and a later product is
+    still right."""
+    dig.load()
+    assert dig.bigemm_device_status(reset=True) == 0
+    g = workloads.generator(5)
+    A = torch.randn(200, 300, generator=g, dtype=torch.float64).cuda()
+    B = torch.randn(300, 100, generator=g, dtype=torch.float64).cuda()
+    before = dig.ozaki_matmul(A, B)
+    torch.cuda.synchronize()
+
+    t0 = time.time()
+    assert dig.bigemm_selftest_ozaki_order_timeout() == 0
+    st = dig.bigemm_device_status(reset=True)          # synchronises
+    elapsed = time.time() - t0
+    assert st == ERR_TIMEOUT, st
+    assert 1.5 < elapsed < 8.0, elapsed                # one limit for the grid
+    assert dig.bigemm_device_status(reset=False) == 0
+
+    after = dig.ozaki_matmul(A, B)
+    torch.cuda.synchronize()
+    assert torch.equal(after.view(torch.int64), before.view(torch.int64))
+    assert dig.bigemm_device_status(reset=False) == 0
