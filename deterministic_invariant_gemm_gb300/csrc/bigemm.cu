@@ -465,14 +465,14 @@ bigemm_status launch_reduce(const DeviceInfo& d, const float* ws, int splits, in
     if (blocks > 16LL * d.sm_count) blocks = 16LL * d.sm_count;
     if (blocks < 1) blocks = 1;
     cudaError_t e;
+    const dim3 g(static_cast<unsigned>(blocks)), blk(kReduceThreads);
+    const int m = static_cast<int>(M), n = static_cast<int>(N);
     if (bf16)
-        e = launch_pdl(splitk_reduce_kernel<true>, dim3(static_cast<unsigned>(blocks)),
-                       dim3(kReduceThreads), 0, stream, ws, C, static_cast<int>(M), static_cast<int>(N),
-                       ldc, ws_ld, splits, b, scale);
+        e = b ? launch_pdl(splitk_reduce_kernel<true, true>, g, blk, 0, stream, ws, C, m, n, ldc, ws_ld, splits, b, scale)
+              : launch_pdl(splitk_reduce_kernel<true, false>, g, blk, 0, stream, ws, C, m, n, ldc, ws_ld, splits, b, scale);
     else
-        e = launch_pdl(splitk_reduce_kernel<false>, dim3(static_cast<unsigned>(blocks)),
-                       dim3(kReduceThreads), 0, stream, ws, C, static_cast<int>(M), static_cast<int>(N),
-                       ldc, ws_ld, splits, b, scale);
+        e = b ? launch_pdl(splitk_reduce_kernel<false, true>, g, blk, 0, stream, ws, C, m, n, ldc, ws_ld, splits, b, scale)
+              : launch_pdl(splitk_reduce_kernel<false, false>, g, blk, 0, stream, ws, C, m, n, ldc, ws_ld, splits, b, scale);
     return e == cudaSuccess ? BIGEMM_OK : BIGEMM_ERR_CUDA;
 }
 

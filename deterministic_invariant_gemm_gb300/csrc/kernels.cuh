@@ -736,6 +736,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 if constexpr (kWt) tma_prefetch_l2_2d(&tmBp, k, nt * kTN);
                 else tma_prefetch_l2_2d(&tmBp, nt * kTN, k);
             }
+            // and the tile's bias values, which the epilogue adds (one line
+            // per 64 columns, none past N)
+            if constexpr (kOut == kOutF32 || kOut == kOutBF16) {
+                if (p.bias != nullptr)
+                    for (int c = nt * kTN; c < min(nt * kTN + kTN, p.N); c += 64) prefetch_l2(p.bias + c);
+            }
         }
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
@@ -1231,7 +1237,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 // up to eight slices are issued before their additions.
 constexpr int kReduceThreads = 128;
 
-template <bool kBF16Out>
+// kBias: a linear layer's bias[N] is added (the pointer is then non-null);
+// the products without one run the kernel without any of that code.
+template <bool kBF16Out, bool kBias>
 __global__ void __launch_bounds__(kReduceThreads)
     splitk_reduce_kernel(const float* __restrict__ ws, void* __restrict__ C, int M, int N,
                          int64_t ldc, int64_t ws_ld, int S, const __nv_bfloat16* __restrict__ bias,
@@ -1240,8 +1248,19 @@ __global__ void __launch_bounds__(kReduceThreads)
     // this grid to complete before touching memory, and this kernel holds no
     // tensor memory a dependent could need.
     grid_launch_dependents();
-    grid_dependency_wait();
     const int64_t vec_per_row = ws_ld / 4;
+    if constexpr (kBias) {
+        // Warm L2 with this thread's first bias values while the partial
+        // kernel finishes: a linear layer's bias is read once per product and
+        // is usually gone from L2 by then, and its trip from DRAM would
+        // otherwise come after the slices'.  An L2 prefetch fills nothing in
+        // the SM and L2 is the device's point of coherence, so it cannot
+        // expose data older than the dependency wait below.
+        const int64_t v0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+        if (v0 < static_cast<int64_t>(M) * vec_per_row)
+            prefetch_l2(bias + static_cast<int>(v0 % vec_per_row) * 4);
+    }
+    grid_dependency_wait();
     const int64_t total = static_cast<int64_t>(M) * vec_per_row;
     const int64_t slice = static_cast<int64_t>(M) * ws_ld;
     for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < total;
@@ -1249,6 +1268,16 @@ __global__ void __launch_bounds__(kReduceThreads)
         const int64_t m = v / vec_per_row;
         const int col = static_cast<int>(v - m * vec_per_row) * 4;
         const float* src = ws + m * ws_ld + col;
+        int valid = 0;
+        uint2 bw = make_uint2(0u, 0u);
+        if constexpr (kBias) {
+            // four bf16 values in one 8-byte load (col is a multiple of 4 and
+            // the bias 16-byte aligned), issued before the slices' loads so
+            // that the two latencies overlap: this kernel's time is the
+            // latency of its loads
+            valid = min(4, N - col);
+            if (valid == 4) bw = __ldg(reinterpret_cast<const uint2*>(bias + col));
+        }
         // S == 0: no slices (an empty K); the sum is +0.0 and only a bias remains
         float4 acc = S > 0 ? __ldcs(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int s0 = 1; s0 < S; s0 += 8) {
@@ -1266,7 +1295,7 @@ __global__ void __launch_bounds__(kReduceThreads)
                 }
             }
         }
-        const int valid = min(4, N - col);
+        if constexpr (!kBias) valid = min(4, N - col);
         if (valid <= 0) continue;
         if (scale != 1.0f) {  // an 8-bit product's output scale, after the split sum
             acc.x = __fmul_rn(acc.x, scale);
@@ -1274,9 +1303,17 @@ __global__ void __launch_bounds__(kReduceThreads)
             acc.z = __fmul_rn(acc.z, scale);
             acc.w = __fmul_rn(acc.w, scale);
         }
-        if (bias != nullptr) {  // a linear layer's bias, added after the split sum
-            float* a = &acc.x;
-            for (int c = 0; c < valid; ++c) a[c] = __fadd_rn(a[c], __bfloat162float(bias[col + c]));
+        if constexpr (kBias) {  // added after the split sum (and the scale)
+            if (valid == 4) {
+                // a bf16 value is the upper half of the FP32 with the same value
+                acc.x = __fadd_rn(acc.x, __uint_as_float(bw.x << 16));
+                acc.y = __fadd_rn(acc.y, __uint_as_float(bw.x & 0xFFFF0000u));
+                acc.z = __fadd_rn(acc.z, __uint_as_float(bw.y << 16));
+                acc.w = __fadd_rn(acc.w, __uint_as_float(bw.y & 0xFFFF0000u));
+            } else {
+                float* a = &acc.x;
+                for (int c = 0; c < valid; ++c) a[c] = __fadd_rn(a[c], __bfloat162float(bias[col + c]));
+            }
         }
         if constexpr (kBF16Out) {
             __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(C) + m * ldc + col;

@@ -39,6 +39,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Brings the cache line holding `p` into L2 (no register, no shared memory).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // A 32-bit global load with acquire semantics at GPU scope: the writes that
 // the releasing thread made before its matching store or atomic are visible
 // to this thread's later reads.
