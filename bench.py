@@ -4,25 +4,32 @@
 
 Prints ONE JSON line (rank 0).  The headline workload is the decode-shaped
 product: M in {1, 4, 16, 64} rows against N = K = 4096 weights drawn N(0, 0.02),
-split_k = 8 chosen from K alone.  One step = the four products, each through
-the split-K partial kernel and the fixed-order reduction kernel; every product
-of a step multiplies a different weight matrix from a rotating pool of 16
-(512 MiB, four times the 129 MB L2), so the weights stream from HBM as they
-do in decoding.  Steps are replayed from a CUDA graph (one per rotation
-period).  The metric is the whole job's TFLOP/s (2 M N K per product).
+split_k = 8 chosen from K alone.  One step decodes through four layers at each
+batch size: for each M, four products through bigemm_run, each against a
+different weight matrix of a pool of 16 (512 MiB, four times the 129 MB L2),
+so a step streams every weight once from HBM, as decoding does.  The step is
+replayed from a CUDA graph.  The metric is the whole job's TFLOP/s (2 M N K
+per product).  After the timed region the results are checked: the device
+error word, every product of the last step against an eager call (bits), and
+sampled rows against the binary64 oracle ("checked").
 
 Also reported (N = 1, rank 0):
-  roofline      the split-K partial kernel (the dominant kernel): algorithmic
-                bytes 2MK + 2KN + 4MN per launch over its measured duration,
-                against the measured HBM copy bandwidth.
-  e2e           the same step through the public API with host buffers:
-                A and B copied from pinned host memory, C read back, every step.
-  cpu_baseline  the CPU oracle (binary64 triple loop) on the same decode step.
-  workloads     the other shapes: large squares (tensor-core bound) and long K.
-  clocks        SM clock and throttle reasons sampled during the timed region.
+  roofline        the few-row kernel (the whole product at M <= 32, the
+                  dominant kernel): algorithmic bytes 2MK + 2KN + 4MN per
+                  product over its measured duration, against the measured HBM
+                  copy bandwidth; per-M whole-product times and fractions.
+  e2e             one product per M through the public API with host buffers:
+                  A and B copied from pinned host memory, C read back, every step.
+  cpu_baseline    the CPU oracle (binary64 triple loop) on one product per M.
+  workloads       the other shapes in brief: squares (tensor-core bound), long
+                  K, the small product, linear layers, the Ozaki products;
+                  the full record goes to gpurun_out/bench_detail.json.
+  roofline_tensor the 16384^3 product against the dense BF16 peak, with the
+                  SM clock sampled during its own timed region.
+  clocks          SM clock and throttle reasons sampled during the timed region.
 
 --impl reference times the CPU oracle (the reference for this build) on the
-same workload and prints its line with "impl": "reference".
+same products and prints its line with "impl": "reference".
 
 For N > 1 (torchrun) every rank runs the same step on its own GPU (replicas:
 the product shards by rows or columns with no exchange); ranks meet at a
@@ -57,6 +64,7 @@ MS = tuple(DECODE["Ms"])
 N_DEC = DECODE["N"]
 K_DEC = DECODE["K"]
 POOL = 16
+PER_M = POOL // len(MS)          # products (layers) per batch size in one step
 L2_BYTES = 129 * 1000 * 1000
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -74,8 +82,14 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def flops_of(ms) -> float:
+    """2 M N K summed over products of the decode shape with the given M."""
+    return float(sum(2.0 * M * N_DEC * K_DEC for M in ms))
+
+
 def decode_flops_per_step() -> float:
-    return float(sum(2.0 * M * N_DEC * K_DEC for M in MS))
+    """The timed step: PER_M products at each M."""
+    return PER_M * flops_of(MS)
 
 
 def decode_alg_bytes(M: int) -> float:
@@ -247,17 +261,20 @@ def kernel_source_hash() -> str:
     kernel, so it does not make an ncu capture stale."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("kernels.cuh", "ptx.cuh", "ozaki.cuh", "bigemm.cu"):
+    for f in ("kernels.cuh", "ptx.cuh", "ozaki.cuh", "skinny.cuh", "bigemm.cu"):
         with open(os.path.join(ROOT, "deterministic_invariant_gemm_gb300", "csrc", f),
                   encoding="utf-8") as fh:
             h.update(code_only(fh.read()).encode("utf-8"))
     return h.hexdigest()[:16]
 
 
+TRAFFIC_PROFILE = "profiles/bigemm_skinny_decode_N4096_K4096.md"
+
+
 def profiled_traffic():
-    """DRAM bytes per launch of the decode partial kernel from the committed
+    """DRAM bytes per launch of the few-row decode kernel from the committed
     ncu summary, or None when that capture was taken on other kernel sources."""
-    path = os.path.join(ROOT, "profiles", "bigemm_partial_decode_N4096_K4096.md")
+    path = os.path.join(ROOT, TRAFFIC_PROFILE)
     try:
         text = open(path, encoding="utf-8").read()
     except OSError:
@@ -282,9 +299,12 @@ def external_events_supported() -> bool:
 # --------------------------------------------------------- decode workload --
 
 class DecodeBench:
-    """Inputs, workspaces and the captured step graphs of the headline workload.
-    linear=True: the same step as a stack of linear layers, weights stored
-    [N, K] with a bias, through bigemm_linear."""
+    """Inputs, outputs and the captured step graph of the headline workload.
+    One step: for each batch size M in (1, 4, 16, 64), PER_M products through
+    bigemm_run against PER_M different weight matrices -- decoding through
+    PER_M layers at that batch size -- so a step streams every weight of the
+    pool once (512 MiB, four times L2).  linear=True: the same step as linear
+    layers, weights stored [N, K] with a bias, through bigemm_linear."""
 
     def __init__(self, dev: torch.device, linear: bool = False):
         import deterministic_invariant_gemm_gb300 as dig
@@ -299,34 +319,36 @@ class DecodeBench:
                   for j in range(POOL)]
         self.bias = [workloads.normal_bf16((N_DEC,), seed + 2000 + j, 0.02).to(dev)
                      for j in range(POOL)] if linear else None
-        self.C = {M: torch.empty((M, N_DEC), dtype=torch.float32, device=dev) for M in MS}
-        self.ws_bytes = {M: dig.bigemm_partial_workspace_bytes(M, N_DEC, K_DEC, self.split) for M in MS}
-        self.ws = {M: torch.empty(self.ws_bytes[M], dtype=torch.uint8, device=dev) for M in MS}
-        self.eff = dig.bigemm_effective_split_k(K_DEC, self.split)
-        self.period = POOL // len(MS)            # steps per rotation of the weight pool
-        self.launches_per_step = 2 * len(MS)
-        self.full = None
-        self.single = []
+        # one output per product of a step, so that every product can be checked
+        self.C = {(M, r): torch.empty((M, N_DEC), dtype=torch.float32, device=dev)
+                  for M in MS for r in range(PER_M)}
+        self.ws_bytes = {M: dig.bigemm_workspace_bytes(M, N_DEC, K_DEC, self.split) for M in MS}
+        self.ws = {M: torch.empty(max(self.ws_bytes[M], 16), dtype=torch.uint8, device=dev) for M in MS}
+        self.path = {M: dig.bigemm_split_path(M, N_DEC, K_DEC, self.split) for M in MS}
+        self.graph = None
+        self.launches_per_step = 0
 
-    def product(self, M: int, B: torch.Tensor, ev=None, j: int = 0):
+    @staticmethod
+    def weight(idx: int, r: int) -> int:
+        return idx * PER_M + r
+
+    def product(self, M: int, j: int, C: torch.Tensor):
         dig = self.dig
         if self.linear:
-            need = dig.bigemm_workspace_bytes(M, N_DEC, K_DEC, self.split)
-            dig.bigemm_linear(self.A[M], B, self.bias[j], self.C[M], M, N_DEC, K_DEC, K_DEC, K_DEC,
-                              N_DEC, self.split, 0, self.ws[M], need)
-            return
-        if ev is not None:
-            ev[0].record()
-        dig.bigemm_run_partial(self.A[M], B, M, N_DEC, K_DEC, K_DEC, N_DEC, self.split,
-                               self.ws[M], self.ws_bytes[M])
-        if ev is not None:
-            ev[1].record()
-        dig.bigemm_splitk_reduce(self.ws[M], self.eff, M, N_DEC, self.C[M], N_DEC, 0)
+            dig.bigemm_linear(self.A[M], self.B[j], self.bias[j], C, M, N_DEC, K_DEC, K_DEC, K_DEC,
+                              N_DEC, self.split, 0, self.ws[M], self.ws_bytes[M])
+        else:
+            dig.bigemm_run(self.A[M], self.B[j], C, M, N_DEC, K_DEC, K_DEC, N_DEC, N_DEC,
+                           self.split, self.ws[M], self.ws_bytes[M])
 
-    def step(self, i: int, events=None):
+    def step(self, count_launches: bool = False):
+        n = 0
         for idx, M in enumerate(MS):
-            j = (i * len(MS) + idx) % POOL
-            self.product(M, self.B[j], None if events is None else events[idx], j)
+            for r in range(PER_M):
+                self.product(M, self.weight(idx, r), self.C[(M, r)])
+                n += self.dig.bigemm_last_launch_count()
+        if count_launches:
+            self.launches_per_step = n
 
     def _capture(self, fn):
         s = torch.cuda.Stream(device=self.dev)
@@ -339,34 +361,25 @@ class DecodeBench:
         return g
 
     def capture(self):
-        """The timed graphs hold kernels only, so consecutive launches keep their
-        programmatic (early-launch) dependencies: one graph for a whole
-        rotation of the weight pool (`period` steps) and one per single step
-        for a remainder."""
-        self.full = self._capture(lambda: [self.step(i) for i in range(self.period)])
-        self.single = [self._capture(lambda i=i: self.step(i)) for i in range(self.period)]
+        """The timed graph holds kernels only, so consecutive launches keep
+        their programmatic (early-launch) dependencies."""
+        self.graph = self._capture(self.step)
 
-    def run_steps(self, first: int, count: int):
-        """Replay `count` steps starting at step index `first`."""
-        i = first
-        while count >= self.period and i % self.period == 0:
-            self.full.replay()
-            i += self.period
-            count -= self.period
+    def run_steps(self, count: int):
         for _ in range(count):
-            self.single[i % self.period].replay()
-            i += 1
+            self.graph.replay()
 
-    def partial_chain_us(self, reps: int = 50):
-        """Average duration of the split-K partial kernel per M, launched back to
-        back (16 launches rotating through the weight pool, one graph, CUDA
-        events around `reps` replays).  Returns {M: microseconds}."""
+    def chain_us(self, reps: int = 40):
+        """Per M: the average time of one whole product (every kernel it
+        launches) in a graph of POOL back-to-back products of that M against
+        every weight of the pool, CUDA events around `reps` replays."""
         out = {}
         for M in MS:
-            def chain(M=M):
+            C = torch.empty((M, N_DEC), dtype=torch.float32, device=self.dev)
+
+            def chain(M=M, C=C):
                 for j in range(POOL):
-                    self.dig.bigemm_run_partial(self.A[M], self.B[j], M, N_DEC, K_DEC, K_DEC, N_DEC,
-                                                self.split, self.ws[M], self.ws_bytes[M])
+                    self.product(M, j, C)
             g = self._capture(chain)
             for _ in range(3):
                 g.replay()
@@ -381,21 +394,41 @@ class DecodeBench:
             out[M] = e0.elapsed_time(e1) * 1e3 / (reps * POOL)
         return out
 
-    def partial_isolated_us(self, rounds: int = 25):
-        """Durations of partial launches separated by events inside the step
-        graph (each duration then includes its kernel's start-up).  {M: us}"""
-        if not external_events_supported():
-            return {}
-        evs = [(torch.cuda.Event(enable_timing=True, external=True),
-                torch.cuda.Event(enable_timing=True, external=True)) for _ in MS]
-        g = self._capture(lambda: self.step(0, evs))
-        acc = {M: [] for M in MS}
-        for _ in range(rounds):
-            g.replay()
-            torch.cuda.synchronize()
-            for M, (a, b) in zip(MS, evs):
-                acc[M].append(a.elapsed_time(b) * 1e3)
-        return {M: sum(v) / len(v) for M, v in acc.items()}
+    def verify(self) -> dict:
+        """After the timed region: the device error word is clear, every
+        product of the last replayed step equals the same product computed
+        again by an eager call, bit for bit, and rows 0 and M - 1 of the last
+        product of each M are within 1e-5 * sum_k |a_ik b_kj| of the binary64
+        oracle (plus |bias_j| for linear layers)."""
+        import numpy as np
+        import oracle
+        dig = self.dig
+        torch.cuda.synchronize()
+        status = int(dig.bigemm_device_status(reset=True))
+        bits_ok = True
+        for idx, M in enumerate(MS):
+            for r in range(PER_M):
+                again = torch.empty_like(self.C[(M, r)])
+                self.product(M, self.weight(idx, r), again)
+                torch.cuda.synchronize()
+                bits_ok &= bool(torch.equal(again.view(torch.int32), self.C[(M, r)].view(torch.int32)))
+        worst = 0.0
+        for idx, M in enumerate(MS):
+            j = self.weight(idx, PER_M - 1)
+            rows = sorted({0, M - 1})
+            A = self.A[M].cpu()
+            B = self.B[j].cpu()
+            if self.linear:
+                Cref, D = oracle.linear_rows(A, B, self.bias[j].cpu(), M, N_DEC, K_DEC, rows=rows)
+            else:
+                Cref, D = oracle.gemm_rows(A, B, M, N_DEC, K_DEC, rows=rows)
+            got = self.C[(M, PER_M - 1)][rows].double().cpu().numpy()
+            with np.errstate(divide="ignore", invalid="ignore"):
+                rel = np.where(D > 0, np.abs(got - Cref) / D, np.abs(got - Cref))
+            worst = max(worst, float(rel.max()))
+        return {"device_status": status, "bits_equal_eager": bits_ok,
+                "oracle_max_err_over_D": worst, "oracle_ok": worst <= 1e-5,
+                "checked": status == 0 and bits_ok and worst <= 1e-5}
 
 
 def time_region(fn, steps: int, world: int) -> float:
@@ -418,7 +451,7 @@ def time_region(fn, steps: int, world: int) -> float:
 
 
 def time_region_steps(bench: DecodeBench, steps: int, world: int) -> float:
-    """time_region for the decode step graphs (whole rotations in one replay)."""
+    """time_region for the decode step graph."""
     import torch.distributed as dist
     if world > 1:
         dist.barrier()
@@ -426,7 +459,7 @@ def time_region_steps(bench: DecodeBench, steps: int, world: int) -> float:
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
-    bench.run_steps(0, steps)
+    bench.run_steps(steps)
     e1.record()
     torch.cuda.synchronize()
     if world > 1:
@@ -435,9 +468,9 @@ def time_region_steps(bench: DecodeBench, steps: int, world: int) -> float:
 
 
 def run_e2e(bench: DecodeBench, steps: int, warmup: int) -> dict:
-    """The decode step through the public API with host buffers: every step
-    copies its A and B matrices from pinned host memory, runs the four
-    products, and reads the four results back.  The copies go on their own
+    """The decode products through the public API with host buffers: every
+    step copies one A and one B matrix per M from pinned host memory, runs the
+    four products, and reads the four results back.  The copies go on their own
     stream and each product waits only for its own inputs, so a step's
     products and result reads overlap the copies still in flight (the
     host-to-device link, about 200 GB/s here, is the bound)."""
@@ -469,19 +502,19 @@ def run_e2e(bench: DecodeBench, steps: int, warmup: int) -> dict:
             loaded[idx].record(copy)
         for idx, M in enumerate(MS):
             compute.wait_event(loaded[idx])
-            dig.bigemm_run(devA[M], devB[idx], bench.C[M], M, N_DEC, K_DEC, K_DEC, N_DEC, N_DEC,
+            dig.bigemm_run(devA[M], devB[idx], bench.C[(M, 0)], M, N_DEC, K_DEC, K_DEC, N_DEC, N_DEC,
                            bench.split, bench.ws[M], bench.ws_bytes[M], stream=compute)
             consumed[idx].record(compute)
-            hostC[M].copy_(bench.C[M], non_blocking=True)
+            hostC[M].copy_(bench.C[(M, 0)], non_blocking=True)
 
     for i in range(warmup):
         one(i)
     torch.cuda.synchronize()
     secs = time_region(one, steps, 1)
-    return {"value": decode_flops_per_step() * steps / secs / 1e12, "unit": UNIT,
+    return {"value": flops_of(MS) * steps / secs / 1e12, "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": secs * 1e3 / steps,
-            "h2d_note": "pinned host -> device copies on a second stream; products wait per input"}
+            "step": "one product per M, its A and weight copied in from pinned host memory"}
 
 
 def run_split_paths(dev) -> dict:
@@ -510,7 +543,7 @@ def run_split_paths(dev) -> dict:
                 dig.bigemm_run_partial(A, B, M, N, K, K, N, S, ws, need)
                 dig.bigemm_splitk_reduce(ws, s_eff, M, N, C, N, 0)
 
-        res = {"path": {0: "unsplit", 1: "workspace", 2: "folded", 3: "cluster"}.get(
+        res = {"path": {0: "unsplit", 1: "workspace", 2: "folded", 3: "cluster", 4: "skinny"}.get(
             dig.bigemm_split_path(M, N, K, S), "?"), "tile_n": dig.bigemm_tile_n(M, N, K, S),
             "weights": pool}
         for name, fn in (("bigemm_run_us", one_call), ("two_kernel_us", two_kernels)):
@@ -604,17 +637,18 @@ def run_decode_linear(dev, args) -> dict:
     """The headline step as linear layers (bigemm_linear, weights [N, K] plus a
     bias), timed the same way."""
     lb = DecodeBench(dev, linear=True)
-    for i in range(5):
-        lb.step(i)
+    for i in range(3):
+        lb.step()
     torch.cuda.synchronize()
     lb.capture()
-    lb.run_steps(0, 8)
+    lb.run_steps(5)
     torch.cuda.synchronize()
-    steps = max(200, args.steps // 4)
+    steps = max(50, args.steps // 4)
     secs = time_region_steps(lb, steps, 1)
+    check = lb.verify()
     out = {"tflops": round(decode_flops_per_step() * steps / secs / 1e12, 2),
            "us_per_step": round(secs * 1e6 / steps, 2), "split_k": lb.split,
-           "weights": "[N, K] + bias (bigemm_linear)"}
+           "weights": "[N, K] + bias (bigemm_linear)", "checked": check["checked"]}
     del lb
     torch.cuda.empty_cache()
     return out
@@ -629,6 +663,10 @@ SINGLE = {
     "square4096": (4096, 4096, 4096, 1, False, "uniform", "tensor"),
     "square8192": (8192, 8192, 8192, 1, False, "uniform", "tensor"),
     "large16384": (16384, 16384, 16384, 1, True, "normal", "tensor"),
+    # one decode product (the few-row kernel), for profiling one launch
+    "decode_m1": (1, 4096, 4096, 8, False, "normal", "hbm"),
+    "decode_m16": (16, 4096, 4096, 8, False, "normal", "hbm"),
+    "decode_m64": (64, 4096, 4096, 8, False, "normal", "hbm"),
     "longk": (256, 256, 65536, 16, False, "normal", "hbm"),
     "longk8": (256, 256, 65536, 8, False, "normal", "hbm"),
     "longk32": (256, 256, 65536, 32, False, "normal", "hbm"),
@@ -684,12 +722,13 @@ def run_single(name, args, world, rank, dev, peaks, peak_src):
         wsb = dig.bigemm_workspace_bytes(M, N, K, S)
         ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
         fn = dig.bigemm_run_bf16out if bf16 else dig.bigemm_run
-        launches = 1 if (dig.bigemm_effective_split_k(K, S) == 1 or
-                         dig.bigemm_split_is_folded(M, N, K, S)) else 2
 
         def call(i):
             a, b = AB[i % copies]
             fn(a, b, C, M, N, K, K, N, N, S, ws, wsb)
+
+        call(0)
+        launches = dig.bigemm_last_launch_count()
 
     for i in range(args.warmup):
         call(i)
@@ -732,7 +771,10 @@ def run_single(name, args, world, rank, dev, peaks, peak_src):
                             "frac": round(flops / per / 1e12 / peak, 4), "traffic": None}
     elif bound == "hbm":
         alg = 2.0 * (M * K + K * N) + 4.0 * M * N
-        line["roofline"] = {"kernel": "bigemm_tc_kernel + splitk_reduce_kernel", "bound": "hbm",
+        kern = {0: "bigemm_tc_kernel", 1: "bigemm_tc_kernel + splitk_reduce_kernel",
+                3: "bigemm_tc_kernel (cluster)", 4: "bigemm_skinny_kernel"}.get(
+                    dig.bigemm_split_path(M, N, K, S), "bigemm_tc_kernel")
+        line["roofline"] = {"kernel": kern, "bound": "hbm",
                             "achieved": round(alg / per / 1e9, 1), "peak": peaks["hbm_gbs"],
                             "peak_source": peak_src, "unit": "GB/s",
                             "frac": round(alg / per / 1e9 / peaks["hbm_gbs"], 4), "traffic": None}
@@ -793,7 +835,7 @@ def run_longk(dev, peaks) -> dict:
             dig.bigemm_run_atomic_splitk(a, b, C, M, N, K, K, N, N, S)
 
         floor_s = -(-kb // S) * 4 * t_mma
-        res = {"path": {0: "unsplit", 1: "workspace", 2: "folded", 3: "cluster"}.get(
+        res = {"path": {0: "unsplit", 1: "workspace", 2: "folded", 3: "cluster", 4: "skinny"}.get(
             dig.bigemm_split_path(M, N, K, S), "?"), "tile_n": dig.bigemm_tile_n(M, N, K, S),
             "chain_floor_us": round(floor_s * 1e6, 2)}
         for key, fn in (("bigemm_run", call), ("atomic", atomic)):
@@ -849,12 +891,15 @@ def run_other_workloads(dev, peaks) -> dict:
 
         for i in range(3):
             call(i)
+        sampler = ClockSampler(nvml_index(dev.index or 0))
+        sampler.start()
         secs = time_region(call, iters, 1)
+        clocks = sampler.stop()
         tflops = 2.0 * M * N * K * iters / secs / 1e12
         out[name] = {"tflops": round(tflops, 2), "frac_of_bf16_peak": round(tflops / bf16_peak, 4),
                      "ms": round(secs * 1e3 / iters, 4), "split_k": S,
                      "out": "bf16" if bf16 else "fp32", "input_copies": copies,
-                     "launches": dig.bigemm_last_launch_count()}
+                     "launches": dig.bigemm_last_launch_count(), "clocks": clocks}
         del AB, C, ws
         torch.cuda.empty_cache()
     # The small product (64 x 256 x 512, split_k 1, FP32 out): a latency case
@@ -958,7 +1003,7 @@ def cpu_baseline(budget_s: float = 10.0) -> dict:
         reps += 1
         if reps >= 200:
             break
-    value = decode_flops_per_step() * reps / total / 1e12
+    value = flops_of(MS) * reps / total / 1e12
     return {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": "%d whole decode steps (M=1,4,16,64 x N=K=4096, binary64 triple loop, "
                       "OpenMP over rows), %.1f s" % (reps, total)}
@@ -1007,7 +1052,7 @@ def run_reference(args, world: int, rank: int):
     for _ in range(args.steps):
         dt, threads = oracle_decode_step()
         total += dt
-    value = decode_flops_per_step() * args.steps / total / 1e12
+    value = flops_of(MS) * args.steps / total / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -1023,11 +1068,74 @@ def run_reference(args, world: int, rank: int):
 
 def decode_config(split: int) -> dict:
     return {"workload": "decode-shaped BF16 GEMM: M in {1,4,16,64}, N=K=4096, A~N(0,1), "
-                        "B~N(0,0.02) bf16, FP32 out, split_k=%d from K only" % split,
-            "M": list(MS), "N": N_DEC, "K": K_DEC, "split_k": split,
-            "l2": "weights rotate through a pool of %d matrices (%d MiB > L2)"
-                  % (POOL, POOL * N_DEC * K_DEC * 2 >> 20),
+                        "B~N(0,0.02) bf16, FP32 out, split_k=%d from K only; a step is %d products "
+                        "(layers) at each M" % (split, PER_M),
+            "M": list(MS), "N": N_DEC, "K": K_DEC, "split_k": split, "products_per_M": PER_M,
+            "l2": "every product of a step multiplies a different weight of a pool of %d "
+                  "(%d MiB > L2): inputs larger than L2" % (POOL, POOL * N_DEC * K_DEC * 2 >> 20),
             "parallelism": "replicas"}
+
+
+# ------------------------------------------------------------ the record --
+
+def write_detail(detail: dict) -> str:
+    """The full per-workload record (Ozaki d-sweeps, split-path A/Bs, per-config
+    CPU times, ...) goes to a side file; the JSON line keeps a summary."""
+    out_dir = os.path.join(ROOT, "gpurun_out")
+    try:
+        os.makedirs(out_dir, exist_ok=True)
+        path = os.path.join(out_dir, "bench_detail.json")
+        with open(path, "w") as f:
+            json.dump(detail, f, indent=1)
+        return os.path.relpath(path, ROOT)
+    except OSError:
+        return None
+
+
+def compact_workloads(detail: dict, peaks: dict, peak_src: str):
+    """Per shape only what the metric needs: TFLOP/s and the fraction of the
+    dense BF16 peak for the tensor-bound shapes, time and HBM fraction for the
+    long-K ones; and a roofline object for the largest square."""
+    out = {}
+    for k in ("square_2048", "square_4096", "square_8192", "large_16384_bf16out",
+              "square_8192_split16_folded", "prefill_1024x4096x4096_split8_folded"):
+        d = detail.get(k)
+        if d:
+            out[k] = {"tflops": d["tflops"], "frac": d["frac_of_bf16_peak"], "ms": d["ms"]}
+    for k in ("linear_bf16_8192", "linear_fp8_e4m3_16384"):
+        d = detail.get(k)
+        if d:
+            out[k] = {"tflops": d["tflops"], "frac": d["frac_of_peak"], "ms": d["ms"]}
+    lk = detail.get("longk_256x256x65536")
+    if lk:
+        out["longk_256x256x65536"] = {
+            "s%d" % S: {"us": lk["s%d" % S]["bigemm_run"]["us"],
+                        "hbm_frac": lk["s%d" % S]["bigemm_run"]["hbm_frac"],
+                        "frac_of_chain_floor": lk["s%d" % S]["bigemm_run"]["frac_of_chain_floor"],
+                        "distinct_in_10": lk["s%d" % S]["bigemm_run"]["distinct_results_in_10_runs"],
+                        "atomic_distinct_in_10": lk["s%d" % S]["atomic"]["distinct_results_in_10_runs"]}
+            for S in (8, 16, 32)}
+    sm = detail.get("small_64x256x512")
+    if sm:
+        out["small_64x256x512"] = {"us_chained": sm["us_per_call_chained"], "us_alone": sm["us_one_call_median"]}
+    dl = detail.get("decode_linear")
+    if dl:
+        out["decode_linear"] = {"tflops": dl["tflops"], "us_per_step": dl["us_per_step"], "checked": dl["checked"]}
+    for n in (4096, 8192):
+        oz = detail.get("ozaki_%d" % n)
+        if oz:
+            full = oz["d%d" % oz["slices"]]
+            out["ozaki_%d" % n] = {"ms": full["ms"], "fp64_equiv_tflops": full["fp64_equiv_tflops"],
+                                   "products_frac_of_bf16_peak": oz["products_frac_of_bf16_peak"]}
+    big = detail.get("large_16384_bf16out")
+    roof = None
+    if big:
+        roof = {"kernel": "bigemm_tc_kernel<kOutBF16> (16384^3, bf16 out)", "bound": "tensor",
+                "achieved": big["tflops"], "peak": peaks["bf16_tflops"], "peak_source": peak_src,
+                "peak_kind": "burst (the product is timed alone)", "unit": "TFLOP/s",
+                "frac": round(big["tflops"] / peaks["bf16_tflops"], 4), "traffic": None,
+                "clocks": big.get("clocks")}
+    return out, roof
 
 
 # ------------------------------------------------------------------- main --
@@ -1035,7 +1143,7 @@ def decode_config(split: int) -> dict:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-extras", action="store_true",
@@ -1066,11 +1174,12 @@ def main():
         return
 
     bench = DecodeBench(dev)
-    for i in range(args.warmup):          # eager warm-up (loads the module)
-        bench.step(i)
+    bench.step(count_launches=True)       # eager warm-up (loads the module)
+    for i in range(args.warmup - 1):
+        bench.step()
     torch.cuda.synchronize()
     bench.capture()
-    bench.run_steps(0, args.warmup)
+    bench.run_steps(args.warmup)
     torch.cuda.synchronize()
 
     sampler = ClockSampler(nvml_index(local))
@@ -1082,8 +1191,8 @@ def main():
         if not ClockSampler.rejected(clocks):
             break
         remeasured = True
-    chain = bench.partial_chain_us()
-    isolated = bench.partial_isolated_us()
+    check = bench.verify()
+    chain = bench.chain_us()
 
     flops_step = decode_flops_per_step()
     value = job_throughput(flops_step * args.steps, world, secs)
@@ -1093,43 +1202,54 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": decode_config(bench.split),
         "gpu_launches": bench.launches_per_step * args.steps,
-        "clocks": clocks,
+        "clocks": clocks, "checked": check,
     }
     if remeasured:
         line["clocks"]["remeasured"] = True
-    alg = sum(decode_alg_bytes(M) for M in MS)
-    dur_s = sum(chain[M] for M in MS) / 1e6
+    # The dominant kernel: the few-row kernel, which is the whole product at
+    # M = 1, 4, 16 (one launch each; 12 of the step's 16 products).
+    few = [M for M in MS if bench.path[M] == 4]   # PATH_SKINNY
+    alg = sum(decode_alg_bytes(M) for M in few)
+    dur_s = sum(chain[M] for M in few) / 1e6
     achieved = alg / dur_s / 1e9
+    step_bytes = PER_M * sum(decode_alg_bytes(M) for M in MS)
     line["roofline"] = {
-        "kernel": "bigemm_tc_kernel<kOutSlices> (split-K partial, split_k=%d)" % bench.split,
+        "kernel": "bigemm_skinny_kernel (split_k=%d summed in 8-CTA clusters), M=%s"
+                  % (bench.split, ",".join(str(M) for M in few)),
         "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
         "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
         "traffic": None,
-        "bytes_per_launch": {str(M): decode_alg_bytes(M) for M in MS},
-        "us_per_launch": {str(M): round(chain[M], 3) for M in MS},
-        "hbm_frac_per_M": {str(M): round(decode_alg_bytes(M) / (chain[M] / 1e6) / 1e9 / peaks["hbm_gbs"], 4)
-                           for M in MS},
-        "timing": "CUDA events on the launching stream around graph replays of %d back-to-back "
-                  "partial launches per M (weights rotating through the pool); achieved = sum of "
-                  "algorithmic bytes over sum of per-launch times for M=1,4,16,64" % POOL,
-        "isolated_us_per_launch": {str(M): round(v, 3) for M, v in isolated.items()},
+        "bytes_per_launch": {str(M): decode_alg_bytes(M) for M in few},
+        "timing": "CUDA events around graph replays of %d back-to-back products per M (every "
+                  "weight of the pool); achieved = sum of bytes / sum of times" % POOL,
+        "whole_product_us": {str(M): round(chain[M], 3) for M in MS},
+        "whole_product_hbm_frac": {str(M): round(decode_alg_bytes(M) / (chain[M] / 1e6) / 1e9 /
+                                                 peaks["hbm_gbs"], 4) for M in MS},
+        "paths": {str(M): {0: "unsplit", 1: "workspace", 2: "folded", 3: "cluster", 4: "skinny"}.get(
+            bench.path[M], "?") for M in MS},
+        "step_hbm_frac": round(step_bytes / (secs / args.steps) / 1e9 / peaks["hbm_gbs"], 4),
     }
     traffic = profiled_traffic()
     if traffic:
-        line["roofline"]["traffic"] = sum(traffic.values()) / len(traffic)
-        line["roofline"]["traffic_source"] = (
-            "dram__bytes_read.sum + dram__bytes_write.sum per launch, ncu capture of the current "
-            "kernel sources (profiles/bigemm_partial_decode_N4096_K4096.md), mean of M=%s"
-            % ",".join(str(m) for m in sorted(traffic)))
+        tm = {M: v for M, v in traffic.items() if M in few}
+        if tm:
+            line["roofline"]["traffic"] = sum(tm.values()) / len(tm)
+            line["roofline"]["traffic_source"] = (
+                "dram__bytes_read.sum + dram__bytes_write.sum per launch, ncu capture of the current "
+                "kernel sources (%s), mean of M=%s" % (TRAFFIC_PROFILE, ",".join(str(m) for m in sorted(tm))))
     if rank == 0 and world == 1 and not args.no_extras:
         line["e2e"] = run_e2e(bench, max(20, args.steps // 20), 5)
-        line["workloads"] = run_other_workloads(dev, peaks)
-        line["workloads"]["longk_256x256x65536"] = run_longk(dev, peaks)
-        line["workloads"]["decode_linear"] = run_decode_linear(dev, args)
-        line["workloads"]["split_paths"] = run_split_paths(dev)
-        line["workloads"].update(run_ozaki(dev, peaks))
+        del bench
+        torch.cuda.empty_cache()
+        detail = run_other_workloads(dev, peaks)
+        detail["longk_256x256x65536"] = run_longk(dev, peaks)
+        detail["decode_linear"] = run_decode_linear(dev, args)
+        detail["split_paths"] = run_split_paths(dev)
+        detail.update(run_ozaki(dev, peaks))
         line["cpu_baseline"] = cpu_baseline()
-        line["cpu_baseline"]["per_config"] = cpu_baseline_configs()
+        detail["cpu_baseline_per_config"] = cpu_baseline_configs()
+        line["workloads"], line["roofline_tensor"] = compact_workloads(detail, peaks, peak_src)
+        line["workloads"]["detail_file"] = write_detail(detail)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -38,8 +38,8 @@ __all__ = [
     "bigemm_fp8_workspace_bytes", "bigemm_linear_fp8", "bigemm_split_is_folded", "bigemm_split_path", "bigemm_tile_n",
     "bigemm_cluster_capacity", "bigemm_ozaki_rho", "bigemm_ozaki_default_slices",
     "bigemm_ozaki_pairs", "bigemm_ozaki_workspace_bytes", "bigemm_ozaki_split", "bigemm_ozaki_dgemm",
-    "ozaki_matmul", "bigemm_selftest_timeout", "bigemm_selftest_ozaki_order_timeout", "PATH_UNSPLIT", "PATH_WORKSPACE", "PATH_FOLDED", "PATH_CLUSTER", "FP8_E4M3",
-    "FP8_E5M2", "FOLD_MIN_ROWS", "FOLD_MIN_TILES",
+    "ozaki_matmul", "bigemm_selftest_timeout", "bigemm_selftest_ozaki_order_timeout", "PATH_UNSPLIT", "PATH_WORKSPACE", "PATH_FOLDED", "PATH_CLUSTER", "PATH_SKINNY", "FP8_E4M3",
+    "FP8_E5M2", "FOLD_MIN_ROWS", "FOLD_MIN_TILES", "SKINNY_MAX_ROWS", "SKINNY_MAX_SPLIT",
     "STATIC_SCRATCH_BYTES", "matmul", "linear", "linear_fp8", "EXPORTED_SYMBOLS",
 ]
 
@@ -59,6 +59,12 @@ STATIC_SCRATCH_BYTES = 16 << 20
 # segments inside the CTA (no workspace); see bigemm_split_is_folded
 FOLD_MIN_ROWS = 97
 FOLD_MIN_TILES = 128
+
+# a bf16 product of at most this many rows and at most this many K segments
+# runs the few-row kernel, which sums its segments in one launch (no
+# workspace); see bigemm_split_path (PATH_SKINNY)
+SKINNY_MAX_ROWS = 32
+SKINNY_MAX_SPLIT = 8
 
 EXPORTED_SYMBOLS = (
     "bigemm_version", "bigemm_status_string", "bigemm_max_split_k", "bigemm_default_split_k",
@@ -219,7 +225,7 @@ def bigemm_split_is_folded(M: int, N: int, K: int, split_k: int) -> bool:
     return bool(load().bigemm_split_is_folded(M, N, K, split_k))
 
 
-PATH_UNSPLIT, PATH_WORKSPACE, PATH_FOLDED, PATH_CLUSTER = 0, 1, 2, 3
+PATH_UNSPLIT, PATH_WORKSPACE, PATH_FOLDED, PATH_CLUSTER, PATH_SKINNY = 0, 1, 2, 3, 4
 
 
 def bigemm_cluster_capacity(splits: int) -> int:
@@ -228,7 +234,8 @@ def bigemm_cluster_capacity(splits: int) -> int:
 
 def bigemm_split_path(M: int, N: int, K: int, split_k: int, fp8: bool = False) -> int:
     """How a direct-output product of this shape runs on the current device:
-    PATH_UNSPLIT, PATH_WORKSPACE, PATH_FOLDED or PATH_CLUSTER (-1: invalid)."""
+    PATH_UNSPLIT, PATH_WORKSPACE, PATH_FOLDED, PATH_CLUSTER or PATH_SKINNY
+    (-1: invalid)."""
     return int(load().bigemm_split_path(M, N, K, split_k, 1 if fp8 else 0))
 
 

@@ -15,6 +15,7 @@
 #include "../../include/bigemm.h"
 #include "kernels.cuh"
 #include "ozaki.cuh"
+#include "skinny.cuh"
 
 namespace bigemm {
 
@@ -124,6 +125,15 @@ bigemm_status device_info(const DeviceInfo** out) {
                 const bigemm_status st = opt_in(k.fn, k.split_regs, k.smem);
                 if (st != BIGEMM_OK) return st;
             }
+            // the few-row kernels: up to the wide kernel's shared memory
+            const void* skinny[] = {(const void*)bigemm_skinny_kernel<kOutF32, false>,
+                                    (const void*)bigemm_skinny_kernel<kOutBF16, false>,
+                                    (const void*)bigemm_skinny_kernel<kOutF32, true>,
+                                    (const void*)bigemm_skinny_kernel<kOutBF16, true>};
+            for (const void* fn : skinny)
+                if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes)) != cudaSuccess)
+                    return BIGEMM_ERR_CUDA;
             void* sym = nullptr;
             if (cudaGetSymbolAddress(&sym, g_device_status) != cudaSuccess) return BIGEMM_ERR_CUDA;
             d.status = static_cast<unsigned*>(sym);
@@ -170,6 +180,17 @@ static_assert(epi_batch_for(BIGEMM_FOLD_MIN_ROWS) == 1 && epi_boxes_for(BIGEMM_F
 bool folds(int64_t M, int64_t N, int splits) {
     if (splits <= 1 || M < BIGEMM_FOLD_MIN_ROWS || N <= 0) return false;
     return ceil_div(M, kBM) * ceil_div(N, kBN) >= BIGEMM_FOLD_MIN_TILES;
+}
+
+// A product of at most kSkMaxM rows with bf16 operands and at most
+// kSkMaxCluster K segments runs bigemm_skinny_kernel, which forms
+// its split sum inside the launch: no workspace, one kernel.  A rule on the
+// shape alone (a cluster of up to 8 CTAs always fits); the same bits as the
+// other paths.
+static_assert(kSkMaxM == BIGEMM_SKINNY_MAX_ROWS && kSkMaxCluster == BIGEMM_SKINNY_MAX_SPLIT,
+              "header and kernel disagree on the few-row rule");
+bool skinny(int64_t M, int splits, bool fp8) {
+    return !fp8 && M >= 1 && M <= kSkMaxM && splits >= 1 && splits <= kSkMaxCluster;
 }
 
 // Tile width of a product (kBN = 256, or 128 / 64).  The wide tile unless
@@ -476,6 +497,59 @@ bigemm_status launch_reduce(const DeviceInfo& d, const float* ws, int splits, in
     return e == cudaSuccess ? BIGEMM_OK : BIGEMM_ERR_CUDA;
 }
 
+// A product of at most kSkMaxM rows with at most kSkMaxCluster K segments
+// (skinny()): one launch of bigemm_skinny_kernel, a cluster of S CTAs per
+// 128 x 256 output tile.
+bigemm_status run_skinny(const DeviceInfo& d, bool bf16, const void* A, const void* B, void* C, int64_t M,
+                         int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int splits,
+                         int kb_per_split, bool wt, const void* bias, cudaStream_t stream) {
+    const int64_t tiles = ceil_div(N, kBN);
+    if (tiles * splits > INT_MAX) return BIGEMM_ERR_ARG;
+    CUtensorMap tmA, tmB;
+    const int64_t da[2] = {K, M};
+    const uint32_t ba[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(sk_a_rows(static_cast<int>(M)))};
+    const int64_t db[2] = {wt ? K : N, wt ? N : K};
+    const uint32_t bb[2] = {wt ? static_cast<uint32_t>(kBK) : kBChunkCols,
+                            wt ? static_cast<uint32_t>(kBN) : static_cast<uint32_t>(kBK)};
+    if (!encode_tiled(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, 2, da, lda, 0, ba,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, 2, db, ldb, 0, bb,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+        return BIGEMM_ERR_CUDA;
+    SkinnyParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.out = C;
+    p.ldc = ldc;
+    p.w = static_cast<const __nv_bfloat16*>(B);
+    p.ldw = ldb;
+    p.status = d.status;
+    p.bias = static_cast<const __nv_bfloat16*>(bias);
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.splits = splits;
+    p.kb_total = static_cast<int>(ceil_div(K, kBK));
+    p.kb_per_split = kb_per_split;
+    // ring depth: as deep as fits in half an SM's shared memory, so that the
+    // next product's CTAs can be resident beside this product's; the ring
+    // also holds the partials once the last instruction is done
+    const uint32_t stage = sk_stage_bytes(p.M);
+    int stages = static_cast<int>(kSkHalfSmBytes / stage);
+    if (stages > kSkMaxStages) stages = kSkMaxStages;
+    p.stages = stages;
+    const dim3 g(static_cast<unsigned>(tiles * splits)), blk(kSkThreads);
+    const uint32_t smem = sk_smem_bytes(p.M, stages);
+    const unsigned cx = static_cast<unsigned>(splits);
+    cudaError_t e;
+    if (wt)
+        e = bf16 ? launch_pdl_cluster(bigemm_skinny_kernel<kOutBF16, true>, g, blk, smem, stream, cx, tmA, tmB, p)
+                 : launch_pdl_cluster(bigemm_skinny_kernel<kOutF32, true>, g, blk, smem, stream, cx, tmA, tmB, p);
+    else
+        e = bf16 ? launch_pdl_cluster(bigemm_skinny_kernel<kOutBF16, false>, g, blk, smem, stream, cx, tmA, tmB, p)
+                 : launch_pdl_cluster(bigemm_skinny_kernel<kOutF32, false>, g, blk, smem, stream, cx, tmA, tmB, p);
+    return e == cudaSuccess ? BIGEMM_OK : BIGEMM_ERR_CUDA;
+}
+
 // wt: the second operand is a weight matrix W [N, K] (ldb is its row stride);
 // otherwise B [K, N].  bias: bf16 [N] added to every row (linear layers), or
 // nullptr.
@@ -510,7 +584,8 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     // ---- workspace
     const bool direct = (mode == kModeF32 || mode == kModeBF16);
     const bool fold = direct && folds(M, N, splits);
-    const bool need_ws = (mode == kModePartial) || (direct && splits > 1 && !fold);
+    const bool few_rows = direct && skinny(M, splits, fp8);
+    const bool need_ws = (mode == kModePartial) || (direct && splits > 1 && !fold && !few_rows);
     if (need_ws) {
         const size_t need = slice_bytes(M, N, splits);
         if (need == SIZE_MAX) return BIGEMM_ERR_ARG;
@@ -551,6 +626,13 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
                                   static_cast<size_t>(M), stream);
         }
         return e == cudaSuccess ? BIGEMM_OK : BIGEMM_ERR_CUDA;
+    }
+
+    if (few_rows) {
+        st = run_skinny(*d, mode == kModeBF16, A, B, C, M, N, K, lda, ldb, ldc, splits, kb_per_split, wt,
+                        bias, stream);
+        if (st == BIGEMM_OK) g_last_launches = 1;
+        return st;
     }
 
     CUtensorMap tmA, tmB, tmBp, tmC;
@@ -832,6 +914,7 @@ int bigemm_split_path(int64_t M, int64_t N, int64_t K, int split_k, int fp8) {
     const int s = effective_split(K, split_k, &L, fp8 ? 128 : kBK);
     if (s == 0) return -1;
     if (s == 1 || K == 0) return BIGEMM_PATH_UNSPLIT;
+    if (skinny(M, s, fp8 != 0)) return BIGEMM_PATH_SKINNY;
     if (folds(M, N, s)) return BIGEMM_PATH_FOLDED;
     const DeviceInfo* d = nullptr;
     if (device_info(&d) != BIGEMM_OK) return -1;
@@ -846,6 +929,7 @@ int bigemm_tile_n(int64_t M, int64_t N, int64_t K, int split_k, int fp8) {
     const int s = effective_split(K, split_k, &L, fp8 ? 128 : kBK);
     if (s == 0) return -1;
     if (M == 0 || N == 0 || K == 0) return kBN;
+    if (skinny(M, s, fp8 != 0)) return kBN;
     const DeviceInfo* d = nullptr;
     if (device_info(&d) != BIGEMM_OK) return -1;
     return tile_width(M, N, s, L, folds(M, N, s), fp8 != 0, d->sm_count);
@@ -854,7 +938,7 @@ int bigemm_tile_n(int64_t M, int64_t N, int64_t K, int split_k, int fp8) {
 size_t bigemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {
     if (M < 0 || N < 0) return 0;
     const int s = effective_split(K, split_k, nullptr);
-    if (s <= 1 || folds(M, N, s)) return 0;
+    if (s <= 1 || folds(M, N, s) || skinny(M, s, false)) return 0;
     return slice_bytes(M, N, s);
 }
 

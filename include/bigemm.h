@@ -19,11 +19,12 @@
  *     kernel) -- no atomics.  A product large enough to fill the GPU with
  *     whole tiles (bigemm_split_is_folded) instead has the CTA that owns a
  *     tile compute its S segment partials one after another and add them in
- *     the same order with the same FP32 additions; a smaller one (S <= 8)
- *     may have the S CTAs of a thread-block cluster compute one segment each
- *     and add the partials through distributed shared memory, again in that
- *     order with those additions (bigemm_split_path).  The same bits every
- *     way, with no workspace traffic and no second kernel;
+ *     the same order with the same FP32 additions; a smaller one (S <= 8),
+ *     and every batch of at most 32 rows (the few-row kernel), may have the
+ *     S CTAs of a thread-block cluster compute one segment each and add the
+ *     partials through distributed shared memory, again in that order with
+ *     those additions (bigemm_split_path).  The same bits every way, with no
+ *     workspace traffic and no second kernel;
  *   - the M and N tile sizes and the order in which tiles run (a GROUP_M
  *     swizzle, "GROUP_M - Swizzle L2 Cache") change no sum.
  * So row i of C is bit-for-bit a function of (row i of A, B, K, split_k,
@@ -110,6 +111,15 @@ typedef void *bigemm_stream;
 #define BIGEMM_FOLD_MIN_ROWS 97
 #define BIGEMM_FOLD_MIN_TILES 128
 
+/* A bf16 product (bigemm_run, bigemm_run_bf16out, bigemm_linear) of 1 ..
+ * BIGEMM_SKINNY_MAX_ROWS rows whose effective split is at most
+ * BIGEMM_SKINNY_MAX_SPLIT runs the few-row kernel: the S CTAs of each
+ * 128 x 256 output tile form a thread-block cluster, one K segment each, and
+ * add their partials through distributed shared memory (one launch, no
+ * workspace); see BIGEMM_PATH_SKINNY. */
+#define BIGEMM_SKINNY_MAX_ROWS 32
+#define BIGEMM_SKINNY_MAX_SPLIT 8
+
 /* Library version, (major << 16) | minor. */
 BIGEMM_API int bigemm_version(void);
 
@@ -160,7 +170,17 @@ BIGEMM_API int bigemm_split_is_folded(int64_t M, int64_t N, int64_t K, int split
  *                          of S CTAs resident at once: each CTA computes one
  *                          segment and the cluster adds the partials through
  *                          distributed shared memory in the order 0..S-1
- *                          (one kernel).
+ *                          (one kernel);
+ *   BIGEMM_PATH_SKINNY     a bf16 product of 1 .. BIGEMM_SKINNY_MAX_ROWS rows
+ *                          with effective split 2 .. BIGEMM_SKINNY_MAX_SPLIT:
+ *                          the few-row kernel, clusters of S CTAs of a
+ *                          footprint small enough that the next product's
+ *                          CTAs start beside them and warm L2 with their
+ *                          weights (one kernel, no workspace).  It also
+ *                          serves such products unsplit (reported as
+ *                          BIGEMM_PATH_UNSPLIT).
+ * The choice is by shape alone except between CLUSTER and WORKSPACE, which
+ * depends on the device's cluster capacity.
  * -1 for invalid arguments or when the device cannot be queried. */
 /* Number of clusters of `splits` GEMM CTAs (one CTA per SM) the current
  * device can hold at once, as the CUDA occupancy calculator reports it; a
@@ -172,6 +192,7 @@ BIGEMM_API int bigemm_cluster_capacity(int splits);
 #define BIGEMM_PATH_WORKSPACE 1
 #define BIGEMM_PATH_FOLDED 2
 #define BIGEMM_PATH_CLUSTER 3
+#define BIGEMM_PATH_SKINNY 4
 BIGEMM_API int bigemm_split_path(int64_t M, int64_t N, int64_t K, int split_k, int fp8);
 
 /* Width in columns of the output tiles a product of this shape runs with on
@@ -191,8 +212,9 @@ BIGEMM_API int bigemm_tile_n(int64_t M, int64_t N, int64_t K, int split_k, int f
 
 /* Workspace bytes bigemm_run / bigemm_run_bf16out / bigemm_linear need for
  * (M, N, K, split_k): effective_split * M * bigemm_workspace_ld(N) * 4 when
- * the effective split is > 1 and the product is not folded
- * (bigemm_split_is_folded), else 0.  A function of the shape alone: the
+ * the effective split is > 1 and the product is neither folded
+ * (bigemm_split_is_folded) nor a few-row one (M <= BIGEMM_SKINNY_MAX_ROWS
+ * and effective split <= BIGEMM_SKINNY_MAX_SPLIT), else 0.  A function of the shape alone: the
  * workspace is required even when the product then runs on the cluster path,
  * which leaves it untouched.  Returns 0 for invalid arguments too. */
 BIGEMM_API size_t bigemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);

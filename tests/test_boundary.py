@@ -77,11 +77,20 @@ def test_workspace_sizes(lib):
     assert dig.bigemm_workspace_ld(1) == 4
     assert dig.bigemm_workspace_ld(4096) == 4096
     assert dig.bigemm_workspace_ld(4097) == 4100
-    assert dig.bigemm_workspace_bytes(16, 4096, 4096, 8) == 8 * 16 * 4096 * 4
-    assert dig.bigemm_workspace_bytes(16, 4096, 4096, 1) == 0
+    assert dig.bigemm_workspace_bytes(64, 4096, 4096, 8) == 8 * 64 * 4096 * 4
+    assert dig.bigemm_workspace_bytes(64, 4096, 4096, 1) == 0
     assert dig.bigemm_partial_workspace_bytes(16, 4096, 4096, 1) == 16 * 4096 * 4
-    assert dig.bigemm_workspace_bytes(3, 5, 640, 7) == 5 * 3 * 8 * 4
+    assert dig.bigemm_workspace_bytes(33, 5, 640, 7) == 5 * 33 * 8 * 4
     assert dig.bigemm_workspace_bytes(-1, 5, 640, 2) == 0
+    # a few-row product (M <= 32, at most 8 segments) sums its segments
+    # inside one launch: no workspace
+    assert dig.bigemm_workspace_bytes(16, 4096, 4096, 8) == 0
+    assert dig.bigemm_workspace_bytes(3, 5, 640, 7) == 0
+    assert dig.bigemm_workspace_bytes(32, 4096, 4096, 8) == 0
+    assert dig.bigemm_workspace_bytes(33, 4096, 4096, 8) == 8 * 33 * 4096 * 4
+    assert dig.bigemm_workspace_bytes(16, 4096, 8192, 16) == 16 * 16 * 4096 * 4   # 16 segments
+    # the 8-bit entry point has no few-row kernel
+    assert dig.bigemm_fp8_workspace_bytes(16, 4096, 8192, 8) == 8 * 16 * 4096 * 4
 
 
 def test_fold_rule_is_a_function_of_the_shape(lib):
@@ -91,14 +100,15 @@ def test_fold_rule_is_a_function_of_the_shape(lib):
     def tiles(M, N):
         return -(-M // 128) * -(-N // 256)
 
-    for M in (1, 16, 96, 97, 128, 511, 512, 1024, 1025, 4096, 8192):
+    for M in (1, 16, 32, 33, 96, 97, 128, 511, 512, 1024, 1025, 4096, 8192):
         for N in (256, 4096, 4100, 6144, 32768, 65536):
             for K, S in ((4096, 8), (4096, 1), (4096, 0), (65536, 16), (640, 7), (64, 4)):
                 s = dig.bigemm_effective_split_k(K, S)
                 want = s > 1 and M >= dig.FOLD_MIN_ROWS and tiles(M, N) >= dig.FOLD_MIN_TILES
                 assert dig.bigemm_split_is_folded(M, N, K, S) == want, (M, N, K, S)
                 ws = dig.bigemm_workspace_bytes(M, N, K, S)
-                assert ws == (0 if (s <= 1 or want) else s * M * dig.bigemm_workspace_ld(N) * 4)
+                few_rows = 1 <= M <= dig.SKINNY_MAX_ROWS and s <= dig.SKINNY_MAX_SPLIT
+                assert ws == (0 if (s <= 1 or want or few_rows) else s * M * dig.bigemm_workspace_ld(N) * 4)
                 s8 = dig.bigemm_fp8_effective_split_k(K, S)
                 want8 = s8 > 1 and M >= dig.FOLD_MIN_ROWS and tiles(M, N) >= dig.FOLD_MIN_TILES
                 ws8 = dig.bigemm_fp8_workspace_bytes(M, N, K, S)
@@ -137,9 +147,10 @@ W16 = 4 << 20
     ((A16, B16, C16, 8, 8, 12, 12, 8, 8, 1, None, 0), ALIGN),    # lda % 8
     ((A16, B16, C16, 8, 12, 8, 8, 12, 12, 1, None, 0), ALIGN),   # ldb % 8
     ((A16, B16, C16, 8, 8, 8, 8, 8, 10, 1, None, 0), ALIGN),     # ldc % 4
-    ((A16, B16, C16, 8, 8, 4096, 4096, 8, 8, 8, None, 0), WS),   # no workspace
-    ((A16, B16, C16, 8, 8, 4096, 4096, 8, 8, 8, W16, 100), WS),  # too small
-    ((A16, B16, C16, 8, 8, 4096, 4096, 8, 8, 8, W16 + 4, 1 << 20), WS),
+    # (40 rows: past the few-row kernel, which needs no workspace)
+    ((A16, B16, C16, 40, 8, 4096, 4096, 8, 8, 8, None, 0), WS),   # no workspace
+    ((A16, B16, C16, 40, 8, 4096, 4096, 8, 8, 8, W16, 100), WS),  # too small
+    ((A16, B16, C16, 40, 8, 4096, 4096, 8, 8, 8, W16 + 4, 1 << 20), WS),
     ((A16, B16, C16, 0, 8, 8, 8, 8, 8, 1, None, 0), OK),         # empty: nothing enqueued
     ((A16, B16, C16, 8, 0, 8, 8, 8, 8, 1, None, 0), OK),
 ])

@@ -53,12 +53,14 @@ def test_path_rule(capsys):
     with capsys.disabled():
         print("\n[cluster path] capacity for S = 2..8: %s" % [caps[S] for S in range(2, 9)])
     assert all(c >= 1 for c in caps.values())
-    for M in (1, 16, 64, 128, 200, 640):
+    for M in (1, 16, 32, 33, 64, 128, 200, 640):
         for N in (256, 1024, 2048, 3840, 4096, 6144):
             for K, S in ((4096, 8), (4096, 4), (3000, 3), (640, 2), (8192, 16), (4096, 1)):
                 s = dig.bigemm_effective_split_k(K, S)
                 if s == 1:
                     want = dig.PATH_UNSPLIT
+                elif M <= dig.SKINNY_MAX_ROWS and s <= dig.SKINNY_MAX_SPLIT:
+                    want = dig.PATH_SKINNY
                 elif dig.bigemm_split_is_folded(M, N, K, S):
                     want = dig.PATH_FOLDED
                 elif dig.bigemm_tile_n(M, N, K, S) != 256:
@@ -71,15 +73,15 @@ def test_path_rule(capsys):
 
 
 @pytest.mark.parametrize("M,N,K,S", [
-    (1, 2048, 4096, 8),          # decode rows against a 2048-wide weight: 8 clusters of 8
-    (16, 2048, 4096, 8),
+    (40, 2048, 4096, 8),         # rows against a 2048-wide weight: 8 clusters of 8
+    (33, 2048, 4096, 8),
     (64, 3840, 4096, 8),         # 15 tiles
     (128, 2048, 4096, 8),
-    (16, 4096, 4096, 4),         # 16 clusters of 4
+    (48, 4096, 4096, 4),         # 16 clusters of 4
     (64, 4096, 4096, 6),         # 11 blocks per segment, the last 9
     (200, 1024, 4096, 8),        # two tile rows, the second ragged
     (37, 1000, 3000, 3),         # ragged N (4 tiles, the last 232 wide), S = 3 segments of 16, 16, 15
-    (5, 300, 1000, 5),           # N not a multiple of 4: the last columns stored one by one
+    (35, 300, 1000, 5),          # N not a multiple of 4: the last columns stored one by one
     (64, 2048, 640, 2),          # two segments of 5 blocks
     (33, 512, 8192, 7),          # 128 blocks in 7 segments of 19 (the last 14)
 ])
@@ -102,9 +104,9 @@ def test_cluster_equals_the_two_kernel_path(M, N, K, S, bf16_out):
 
 
 def test_cluster_rows_equal_workspace_rows_of_a_larger_batch():
-    """Rows computed at M = 1, 4, 16 (cluster path) equal the same rows inside a
-    640-row batch, which has too many tiles to cluster and is not folded
-    (workspace path)."""
+    """Rows computed at M = 1, 4, 16 (few-row kernel) and 33, 48 (cluster path)
+    equal the same rows inside a 640-row batch, which has too many tiles to
+    cluster and is not folded (workspace path)."""
     N, K, S = 2048, 4096, 8
     M = 640
     assert dig.bigemm_split_path(M, N, K, S) == dig.PATH_WORKSPACE
@@ -112,7 +114,7 @@ def test_cluster_rows_equal_workspace_rows_of_a_larger_batch():
     A, B = A.cuda(), B.cuda()
     full = dig.matmul(A, B, split_k=S)
     assert dig.bigemm_last_launch_count() == 2
-    for m in (1, 4, 16):
+    for m in (1, 4, 16, 33, 48):
         for off in (0, 300, M - m):
             part = dig.matmul(A[off:off + m].contiguous(), B, split_k=S)
             assert dig.bigemm_last_launch_count() == 1
@@ -120,9 +122,9 @@ def test_cluster_rows_equal_workspace_rows_of_a_larger_batch():
 
 
 def test_cluster_bit_stable_over_10_runs():
-    A, B = workloads.pair(16, 2048, 4096, 8)
+    A, B = workloads.pair(40, 2048, 4096, 8)
     A, B = A.cuda(), B.cuda()
-    assert dig.bigemm_split_path(16, 2048, 4096, 8) == dig.PATH_CLUSTER
+    assert dig.bigemm_split_path(40, 2048, 4096, 8) == dig.PATH_CLUSTER
     first = dig.matmul(A, B, split_k=8)
     for _ in range(9):
         assert bits_equal(dig.matmul(A, B, split_k=8), first)
@@ -174,7 +176,7 @@ def test_clustered_fp8_linear_with_scale_and_bias():
 def test_cluster_path_leaves_the_workspace_alone():
     """The workspace is required by the shape rule but the cluster path does
     not touch it."""
-    M, N, K, S = 16, 2048, 4096, 8
+    M, N, K, S = 40, 2048, 4096, 8
     assert dig.bigemm_split_path(M, N, K, S) == dig.PATH_CLUSTER
     A, B = workloads.pair(M, N, K, 9)
     A, B = A.cuda(), B.cuda()

@@ -208,9 +208,10 @@ def test_partials_same_bits_for_short_and_long_batches(N, K, S):
 
 
 def test_linear_short_batches_match_long_batches_both_dtypes():
-    """Linear layers N = K = 4096, split_k = 8 (16 tiles: the workspace path at
-    every M): bf16 and E4M3 rows computed at M <= 64 (short A boxes) equal the
-    same rows inside a 200-row batch (full A boxes)."""
+    """Linear layers N = K = 4096, split_k = 8 (16 tiles: the workspace path,
+    or for bf16 at M <= 32 the few-row kernel): bf16 and E4M3 rows computed at
+    M <= 64 (short A boxes) equal the same rows inside a 200-row batch (full A
+    boxes)."""
     N = K = 4096
     Mbig = 200
     x = workloads.normal_bf16((Mbig, K), 81).cuda()
@@ -221,9 +222,10 @@ def test_linear_short_batches_match_long_batches_both_dtypes():
     full8 = dig.linear_fp8(x8, w8, 0.25, b, split_k=8)
     for fp8 in (False, True):
         assert dig.bigemm_split_path(Mbig, N, K, 8, fp8) == dig.PATH_WORKSPACE
-    for M, off in ((1, 0), (16, 100), (40, 7), (64, 136)):
-        for fp8 in (False, True):
-            assert dig.bigemm_split_path(M, N, K, 8, fp8) == dig.PATH_WORKSPACE
+    for M, off in ((1, 0), (16, 100), (32, 9), (33, 50), (40, 7), (64, 136)):
+        assert dig.bigemm_split_path(M, N, K, 8, True) == dig.PATH_WORKSPACE
+        assert dig.bigemm_split_path(M, N, K, 8, False) == (
+            dig.PATH_SKINNY if M <= dig.SKINNY_MAX_ROWS else dig.PATH_WORKSPACE)
         part = dig.linear(x[off:off + M].contiguous(), w, b, split_k=8)
         assert bits_equal(part, full[off:off + M]), ("bf16", M, off)
         part8 = dig.linear_fp8(x8[off:off + M].contiguous(), w8, 0.25, b, split_k=8)

@@ -45,6 +45,9 @@ def expected_width(M, N, K, S):
     L = cdiv(cdiv(K, 64), s_req)
     if M == 0 or N == 0 or K == 0 or L < 32 or dig.bigemm_split_is_folded(M, N, K, S):
         return 256
+    if M <= dig.SKINNY_MAX_ROWS and s <= dig.SKINNY_MAX_SPLIT:
+        return 256      # the few-row kernel, always 256 wide
+    
     mt, half = cdiv(M, 128), half_the_sms()
     for w in (256, 128):
         if mt * cdiv(N, w) * s >= half:
@@ -54,7 +57,7 @@ def expected_width(M, N, K, S):
 
 def test_width_rule_and_paths():
     seen = set()
-    for M in (1, 16, 128, 200, 640, 1280, 4096):
+    for M in (1, 16, 33, 48, 128, 200, 640, 1280, 4096):
         for N in (64, 256, 300, 512, 1024, 2048, 4096):
             for K, S in ((65536, 8), (65536, 16), (65536, 32), (16384, 8), (4096, 1), (2048, 1),
                          (4096, 8), (1984, 1), (8192, 0)):
@@ -65,6 +68,10 @@ def test_width_rule_and_paths():
                     # narrow split products sum through the workspace
                     assert dig.bigemm_split_path(M, N, K, S) == dig.PATH_WORKSPACE
     assert seen == {64, 128, 256}
+    # the few-row kernel takes the small batches of split counts up to 8
+    assert dig.bigemm_tile_n(1, 256, 65536, 8) == 256
+    assert dig.bigemm_split_path(1, 256, 65536, 8) == dig.PATH_SKINNY
+    assert dig.bigemm_tile_n(33, 256, 65536, 8) == 64
     # the decode shape of the pages' linear layers stays wide
     for M in (1, 4, 16, 64):
         assert dig.bigemm_tile_n(M, 4096, 4096, 8) == 256
@@ -80,7 +87,8 @@ def batch_sizes(N, K, S):
     half = half_the_sms()
     m128 = 128 * cdiv(half, cdiv(N, 128) * s)
     m256 = 128 * cdiv(half, cdiv(N, 256) * s)
-    return {64: 1, 128: m128, 256: m256}
+    # one tile row, but more rows than the few-row kernel takes
+    return {64: dig.SKINNY_MAX_ROWS + 1, 128: m128, 256: m256}
 
 
 @pytest.mark.parametrize("N,K,S", [
@@ -101,9 +109,12 @@ def test_rows_equal_across_widths(N, K, S, bf16_out):
     full = dig.matmul(Ad, Bd, out_dtype=dt, split_k=S)            # 256 wide
     mid = dig.matmul(Ad[:sizes[128]].contiguous(), Bd, out_dtype=dt, split_k=S)   # 128 wide
     assert bits_equal(mid, full[:sizes[128]])
-    for lo, hi in ((0, 1), (77, 78), (Mbig - 1, Mbig), (130, 194), (Mbig - 100, Mbig)):
-        part = dig.matmul(Ad[lo:hi].contiguous(), Bd, out_dtype=dt, split_k=S)   # 64 wide
-        assert dig.bigemm_tile_n(hi - lo, N, K, S) == 64
+    for lo, hi in ((0, 1), (77, 78), (Mbig - 1, Mbig), (130, 194), (Mbig - 100, Mbig), (40, 73)):
+        part = dig.matmul(Ad[lo:hi].contiguous(), Bd, out_dtype=dt, split_k=S)
+        if hi - lo > dig.SKINNY_MAX_ROWS:
+            assert dig.bigemm_tile_n(hi - lo, N, K, S) == 64
+        else:
+            assert dig.bigemm_split_path(hi - lo, N, K, S) in (dig.PATH_SKINNY, dig.PATH_UNSPLIT)
         assert bits_equal(part, full[lo:hi]), (lo, hi)
     rows = [0, 77, Mbig - 1]
     Cref, D = oracle.gemm_rows(A, B, Mbig, N, K, rows=rows)
@@ -139,7 +150,7 @@ def test_linear_rows_equal_across_widths(bf16_out):
     (37, 300, 4096, 1),      # 64 wide: five tiles, the last 44 columns
     (37, 301, 4096, 1),      # N not a multiple of 4: the last columns stored one by one
     (200, 200, 4096, 2),     # two tile rows (the second ragged), two segments of 32 blocks
-    (5, 130, 2112, 1),       # 33 K blocks
+    (35, 130, 2112, 1),      # 33 K blocks
     (1200, 1000, 2048, 1),   # 128 wide: ten tile rows of eight tiles
 ])
 @pytest.mark.parametrize("bf16_out", [False, True])
@@ -185,7 +196,7 @@ def test_narrow_atomic_contrast_within_tolerance():
 def test_integer_exact_narrow_equals_the_oracle_bitwise():
     """Small integers, every partial sum below 2^24: FP32 is exact in any
     order, so the narrow path equals the binary64 oracle exactly."""
-    M, N, K, S = 3, 192, 4096, 2
+    M, N, K, S = 34, 192, 4096, 2
     assert dig.bigemm_tile_n(M, N, K, S) == 64
     g = workloads.generator(91)
     A = torch.randint(-8, 9, (M, K), generator=g).to(torch.bfloat16)
