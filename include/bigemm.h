@@ -438,7 +438,10 @@ BIGEMM_API bigemm_status bigemm_run_atomic_splitk(const void *A, const void *B, 
  *     nothing; use bigemm_run with a workspace, or a smaller split_k.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and keeps it; make
- *     that first call before any stream capture on the device.
+ *     that first call before any stream capture on the device.  The kept
+ *     address belongs to the device's primary context: it does not survive
+ *     cudaDeviceReset (or any teardown of that context), after which this
+ *     call must not be used again in the process.
  *   - Every call on a device shares the one array, which keeps the last
  *     call's contents.  Nothing in it needs to start at zero: each call's
  *     partial kernel writes every element its reduction reads.  Calls that

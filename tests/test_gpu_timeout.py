@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 ERR_TIMEOUT = 6
 
 
-def test_expired_wait_is_reported_and_the_context_survives(cuda_device):
+def test_expired_wait_is_reported_and_the_context_survives(builtin_scratch):
     dig.load()
     assert dig.bigemm_device_status(reset=True) == 0
     A, B = workloads.pair(16, 256, 512, 3)
@@ -42,7 +42,7 @@ def test_expired_wait_is_reported_and_the_context_survives(cuda_device):
     assert dig.bigemm_device_status(reset=False) == 0
 
 
-def test_ozaki_order_wait_gives_up_once_for_the_whole_grid(cuda_device):
+def test_ozaki_order_wait_gives_up_once_for_the_whole_grid(builtin_scratch):
     """The Ozaki kernel's epilogues wait for the previous slice pair of their
     tile, possibly on another CTA.  bigemm_selftest_ozaki_order_timeout starts
     every tile's count far below zero, so no such wait is ever met: the first

@@ -8,11 +8,14 @@ host framework that owns all device memory through its own allocator and does
 not expose it over a C interface.  For them the library keeps a fixed 16 MiB
 array of split-K scratch in its device image.
 
-This file runs last on purpose: the call shares one array across calls, so
+This file is collected last, so that a run stopping at its first failure has
+run every other test before it.  The call shares one array across calls, so
 the check below covers two calls in a row, with the second one finding the
-first one's partial sums still in the array.  Each result must equal the
-ordinary entry point's (bigemm_run with a caller workspace) within the
-parity tolerance, and in fact bit for bit, since the same kernels run.
+first one's partial sums still in the array; the tests that use the array
+hold the `builtin_scratch` fixture, which keeps them from overlapping.  Each
+result must equal the ordinary entry point's (bigemm_run with a caller
+workspace) within the parity tolerance, and in fact bit for bit, since the
+same kernels run.
 """
 import numpy as np
 import pytest
@@ -36,7 +39,7 @@ def _device_pair(M, N, K, seed):
 
 
 @pytest.mark.parametrize("order", ["static_first", "workspace_first"])
-def test_static_scratch_matches_workspace_entry_point(cuda_device, order):
+def test_static_scratch_matches_workspace_entry_point(builtin_scratch, order):
     # Two calls in a row with different shapes and splits; the second finds
     # the first call's partials in the shared array.
     # splits above 8 always take the workspace path (partial + reduction), so
@@ -75,7 +78,7 @@ def test_static_scratch_matches_workspace_entry_point(cuda_device, order):
     assert dig.bigemm_device_status(reset=True) == 0
 
 
-def test_static_scratch_rejects_products_past_its_size(cuda_device):
+def test_static_scratch_rejects_products_past_its_size(builtin_scratch):
     M, N, K, S = 512, 4096, 4096, 8             # needs 64 MiB of split-K scratch
     assert not dig.bigemm_split_is_folded(M, N, K, S)   # 64 tiles: the workspace path
     assert dig.bigemm_workspace_bytes(M, N, K, S) > dig.STATIC_SCRATCH_BYTES
