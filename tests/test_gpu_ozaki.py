@@ -237,3 +237,22 @@ def test_concurrent_products_on_two_streams_and_a_graph_replay():
         torch.cuda.synchronize()
         assert torch.equal(C.view(torch.int64), serial[0].view(torch.int64))
     assert dig.bigemm_device_status(reset=True) == 0
+
+
+def test_dgemm_4096_rows_equal_the_oracle_and_one_row_products():
+    """A 4096^3 product (36 slice pairs dealt over every SM, 18432 items):
+    sampled rows equal the oracle's exactly and the same rows of one-row
+    products, bit for bit; also with Fast Mode's d."""
+    M = N = K = 4096
+    g = workloads.generator(79)
+    A = torch.randn(M, K, generator=g, dtype=torch.float64)
+    B = torch.randn(K, N, generator=g, dtype=torch.float64)
+    rows = [0, 3071, 3072, 4095]
+    for d in (0, 6):
+        C = run_dgemm(A, B, 0, d)
+        s = oracle.ozaki_default_slices(oracle.ozaki_rho(K))
+        Cref, _ = oracle.ozaki_gemm(A[rows], B, d=d or s)
+        assert np.array_equal(C[rows], Cref), d
+        for r in rows[1:3]:
+            one = run_dgemm(A[r:r + 1].clone(), B, 0, d)
+            assert np.array_equal(one.view(np.int64), C[r:r + 1].view(np.int64)), (d, r)
