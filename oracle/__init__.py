@@ -23,9 +23,10 @@ passage of the pages it follows in ``oracle.c``'s header:
   おける GEMM の Batch Invariance サポート": linear_batch_invariant(x, weight,
   bias)).
 * :func:`ozaki_rho`, :func:`ozaki_split`, :func:`ozaki_pairs`,
-  :func:`ozaki_gemm` -- the Ozaki scheme's binary64 product from bfloat16
-  slices (cuTile article, "倍精度行列積エミュレーション": the Veltkamp split of
-  eqs. (1)-(5), the slice-pair products of eqs. (10)-(11), Fast Mode's d).
+  :func:`ozaki_gemm`, :func:`ozaki_fast_d` -- the Ozaki scheme's binary64
+  product from bfloat16 slices (cuTile article, "倍精度行列積エミュレーション":
+  the Veltkamp split of eqs. (1)-(5), the slice-pair products of eqs.
+  (10)-(11), Fast Mode's d, fixed or chosen per element).
 
 Pins (tests/test_oracle.py) tie each function to something other than itself:
 identity and permutation products, small-integer products checked against
@@ -118,6 +119,9 @@ def _load():
     lib.oracle_ozaki_gemm.argtypes = [vp, vp, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, vp, i64, vp]
     lib.oracle_ozaki_gemm.restype = ctypes.c_int
+    lib.oracle_ozaki_fast_d.argtypes = [vp, vp, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                        vp, vp, vp]
+    lib.oracle_ozaki_fast_d.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -332,10 +336,31 @@ def ozaki_split(X, axis: int, rho: int, slices: int):
     return S, c1, R
 
 
+def ozaki_fast_d(A, B, rho: int | None = None, slices: int | None = None):
+    """Fast Mode's automatic d for every element of A B (cuTile article,
+    "Fast Mode（GEMMの削減）"; the per-element reading in oracle.c): returns
+    (D [M, N] int32, T_a [M] and T_b [N] uint64, the vectors' integer masses
+    sum_k floor(|x_k| 2^(40 - c^(1))))."""
+    a, b = _f64(A), _f64(B)
+    M, K = a.shape
+    N = b.shape[1]
+    rho = ozaki_rho(max(K, 1)) if rho is None else rho
+    slices = ozaki_default_slices(rho) if slices is None else slices
+    D = np.empty((M, N), dtype=np.int32)
+    Ta = np.empty(M, dtype=np.uint64)
+    Tb = np.empty(N, dtype=np.uint64)
+    st = _load().oracle_ozaki_fast_d(_ptr(a), _ptr(b), M, N, K, K, N, rho, slices, _ptr(D), _ptr(Ta),
+                                     _ptr(Tb))
+    if st != 0:
+        raise ValueError("oracle_ozaki_fast_d failed")
+    return D, Ta, Tb
+
+
 def ozaki_gemm(A, B, rho: int | None = None, slices: int | None = None, d: int | None = None):
     """C = A B (binary64) by the Ozaki scheme; returns (C, inexact) where
     inexact counts slice-pair sums that a binary32 accumulation could round
-    (0 when rho fits K)."""
+    (0 when rho fits K).  d = -1: Fast Mode's automatic d per element
+    (ozaki_fast_d)."""
     a, b = _f64(A), _f64(B)
     M, K = a.shape
     K2, N = b.shape

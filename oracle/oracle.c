@@ -42,7 +42,8 @@
  *                         from bfloat16 slices -- the Veltkamp split, eqs.
  *                         (1)-(5); slice-pair products, eqs. (10)-(11); the
  *                         binary64 outer accumulation; Fast Mode's skip of the
- *                         pairs with p + q >= d.
+ *                         pairs with p + q >= d, a fixed d or its automatic
+ *                         choice per output element (oracle_ozaki_fast_d).
  *
  * Build: a C99 compiler with -O2 -ffp-contract=off (no fused multiply-add, no
  * fast-math); OpenMP is optional and only splits the rows between threads --
@@ -413,6 +414,90 @@ int oracle_ozaki_split(const double *X, int64_t rows, int64_t cols, int64_t ld, 
 }
 
 /*
+ * Fast Mode's choice of d (cuTile article, "Fast Mode（GEMMの削減）": the
+ * smallest d for which the pairs with p + q >= d may be skipped while
+ * |fl(AB) - AB| <= 2 sqrt(k) u |A||B|, u = 2^-53).  The page states the bound
+ * and not the procedure; the reading here is made per output element, from
+ * its row of A and its column of B only, so that a row's bits stay
+ * independent of the rest of the batch:
+ *
+ *   - The skipped pairs of element (i, j) add sum_{p+q>=d} 2^(c_x^(p) +
+ *     c_y^(q)) xbar^(p) . ybar^(q).  Every slice entry is at most 1 and
+ *     c^(p) = c^(1) - p (beta + 1), so with w = beta + 1, at most `slices`
+ *     pairs per diagonal p + q = t and the page's probabilistic sqrt(k) for a
+ *     k-term dot product, they amount to at most
+ *       sqrt(k) 2^(c_x + c_y) sum_{t>=d} slices 2^(-t w)
+ *         <= sqrt(k) 2^(c_x + c_y + 1 + L_s - d w),   L_s = ceil(log2 slices).
+ *   - |A||B|_ij = sum_k |x_k| |y_k| is estimated by its mean-field value
+ *     mu_x mu_y / k (mu the 1-norm of the vector), from below: mu_x >=
+ *     T_x 2^(c_x - 40) with the integer mass T_x = sum_k floor(|x_k| 2^(40 -
+ *     c_x)) (exact and order-free; < 2^62 for k <= 2^22), and k <= 2^kappa,
+ *     kappa = ceil(log2 k).
+ *   - So the skip is within the bound when 2^(1 + L_s - d w) <= 2^(-52) T_x
+ *     T_y 2^(-80 - kappa), i.e. when T_x T_y >= 2^(133 + L_s + kappa - d w),
+ *     which holds exactly when d w >= 134 + L_s + kappa - bitlen(T_x T_y)
+ *     (bitlen of the 128-bit product).
+ *   - d_ij = the least such d, at least 1 and at most `slices` (the
+ *     deterministic default d: Fast Mode only ever removes pairs).
+ * Element (i, j) then takes pair (p, q) iff p + q < d_ij, in the usual
+ * order; every element takes pair (0, 0).
+ */
+static uint64_t oz_mass(const double *x, int64_t n, int64_t inc, int c) {
+    uint64_t t = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        const double a = fabs(x[i * inc]);
+        if (a != 0.0) t += (uint64_t)floor(ldexp(a, 40 - c));  /* exact: a power-of-two scale */
+    }
+    return t;
+}
+
+static int oz_ceil_log2_int(int64_t v) {
+    int l = 0;
+    while (((int64_t)1 << l) < v) ++l;
+    return l;
+}
+
+/* 134 + ceil(log2 slices) + ceil(log2 k) - bitlen(tx * ty): d_ij = the least
+ * d >= 1 with d (beta + 1) >= this, capped at slices. */
+static int oz_fast_need(uint64_t tx, uint64_t ty, int slices, int64_t k) {
+    unsigned __int128 prod = (unsigned __int128)tx * ty;
+    int bl = 0;
+    while (prod != 0) {
+        ++bl;
+        prod >>= 1;
+    }
+    return 134 + oz_ceil_log2_int(slices) + oz_ceil_log2_int(k) - bl;
+}
+
+static int oz_fast_d(uint64_t tx, uint64_t ty, int slices, int beta, int64_t k) {
+    const int need = oz_fast_need(tx, ty, slices, k), w = beta + 1;
+    int d = need <= w ? 1 : (need + w - 1) / w;
+    return d > slices ? slices : d;
+}
+
+/* The per-element d of Fast Mode for A B (see above): D [M][N] int32, and the
+ * masses T of the rows of A and columns of B.  Returns 0 or -1. */
+int oracle_ozaki_fast_d(const double *A, const double *B, int64_t M, int64_t N, int64_t K, int64_t lda,
+                        int64_t ldb, int rho, int slices, int *D, uint64_t *Ta, uint64_t *Tb) {
+    if (M < 0 || N < 0 || K < 1 || slices < 1 || lda < K || ldb < N) return -1;
+    if (rho < OZ_M1 - OZ_M2 || rho >= OZ_M1) return -1;
+    const int beta = OZ_M1 - rho;
+    for (int64_t i = 0; i < M; ++i) {
+        double m = 0.0;
+        for (int64_t k = 0; k < K; ++k) if (fabs(A[i * lda + k]) > m) m = fabs(A[i * lda + k]);
+        Ta[i] = m == 0.0 ? 0 : oz_mass(A + i * lda, K, 1, oz_ceil_log2(m));
+    }
+    for (int64_t j = 0; j < N; ++j) {
+        double m = 0.0;
+        for (int64_t k = 0; k < K; ++k) if (fabs(B[k * ldb + j]) > m) m = fabs(B[k * ldb + j]);
+        Tb[j] = m == 0.0 ? 0 : oz_mass(B + j, K, ldb, oz_ceil_log2(m));
+    }
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) D[i * N + j] = oz_fast_d(Ta[i], Tb[j], slices, beta, K);
+    return 0;
+}
+
+/*
  * C = A B in the Ozaki scheme.  A: [M][lda], B: [K][ldb] binary64; C: [M][ldc].
  * A is split by rows and B by columns (each row of A and column of B is one
  * vector x, y of eq. (10)); then, for p = 0 .. slices-1 and, inside, q = 0 ..
@@ -425,12 +510,14 @@ int oracle_ozaki_split(const double *X, int64_t rows, int64_t cols, int64_t ld, 
  * some order could round -- rho is chosen so that this count is 0
  * ("行列積の計算": no rounding error in the Type3 accumulation).  The scaling
  * by a power of two is exact (inputs within the normal range), so each pair
- * costs one binary64 rounding, in the addition.  Returns 0 or -1.
+ * costs one binary64 rounding, in the addition.  d = -1: Fast Mode's
+ * automatic choice, element by element (oracle_ozaki_fast_d): element (i, j)
+ * takes the pairs with p + q < d_ij, in the same order.  Returns 0 or -1.
  */
 int oracle_ozaki_gemm(const double *A, const double *B, int64_t M, int64_t N, int64_t K,
                       int64_t lda, int64_t ldb, int rho, int slices, int d, double *C, int64_t ldc,
                       int64_t *inexact) {
-    if (M < 0 || N < 0 || K < 0 || slices < 1 || d < 0) return -1;
+    if (M < 0 || N < 0 || K < 0 || slices < 1 || d < -1) return -1;
     if ((K > 0 && (lda < K || ldb < N)) || ldc < N) return -1;
     if (rho < OZ_M1 - OZ_M2 || rho >= OZ_M1) return -1;
     const int beta = OZ_M1 - rho;
@@ -438,9 +525,16 @@ int oracle_ozaki_gemm(const double *A, const double *B, int64_t M, int64_t N, in
     double *Sb = (double *)malloc(sizeof(double) * (size_t)(slices * (K > 0 ? K : 1) * N));
     int *ca = (int *)malloc(sizeof(int) * (size_t)(M > 0 ? M : 1));
     int *cb = (int *)malloc(sizeof(int) * (size_t)(N > 0 ? N : 1));
-    int st = (Sa && Sb && ca && cb) ? 0 : -1;
+    const int fast = (d == -1);
+    int *Dij = fast ? (int *)malloc(sizeof(int) * (size_t)(M > 0 && N > 0 ? M * N : 1)) : NULL;
+    uint64_t *Ta = fast ? (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(M > 0 ? M : 1)) : NULL;
+    uint64_t *Tb = fast ? (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(N > 0 ? N : 1)) : NULL;
+    int st = (Sa && Sb && ca && cb && (!fast || (Dij && Ta && Tb))) ? 0 : -1;
     if (st == 0 && K > 0) st = oracle_ozaki_split(A, M, K, lda, 0, rho, slices, Sa, ca, NULL);
     if (st == 0 && K > 0) st = oracle_ozaki_split(B, K, N, ldb, 1, rho, slices, Sb, cb, NULL);
+    if (st == 0 && K > 0 && fast)
+        st = oracle_ozaki_fast_d(A, B, M, N, K, lda, ldb, rho, slices, Dij, Ta, Tb);
+    if (fast) d = slices;
     int64_t bad = 0;
     if (st == 0) {
         const double unit_bound = ldexp(1.0, OZ_M3 + 2 * (rho - OZ_M1));
@@ -464,6 +558,7 @@ int oracle_ozaki_gemm(const double *A, const double *B, int64_t M, int64_t N, in
                                 D = D + fabs(t);
                             }
                             if (D > unit_bound) ++bad;
+                            if (fast && p + q >= Dij[i * N + j]) continue;
                             const int e = (ca[i] - p * (beta + 1)) + (cb[j] - q * (beta + 1));
                             C[i * ldc + j] = C[i * ldc + j] + ldexp(P, e);
                         }
@@ -477,6 +572,9 @@ int oracle_ozaki_gemm(const double *A, const double *B, int64_t M, int64_t N, in
     free(Sb);
     free(ca);
     free(cb);
+    free(Dij);
+    free(Ta);
+    free(Tb);
     return st;
 }
 

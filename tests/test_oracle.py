@@ -600,3 +600,103 @@ def test_ozaki_inexact_count_flags_too_wide_slices():
     _, bad_wide = oracle.ozaki_gemm(A, B, rho=45, slices=7, d=7)
     _, bad_rho = oracle.ozaki_gemm(A, B)
     assert bad_wide > 0 and bad_rho == 0
+
+
+# --- Fast Mode's automatic d (cuTile article, "Fast Mode（GEMMの削減）") ---
+
+def _mass(x):
+    """sum_k floor(|x_k| 2^(40 - c)), c = ceil(log2 max |x|), in exact rationals."""
+    m = max(abs(Fraction(v)) for v in x)
+    if m == 0:
+        return 0
+    c = 0
+    while Fraction(2) ** c < m:
+        c += 1
+    while Fraction(2) ** (c - 1) >= m:
+        c -= 1
+    return sum(int(abs(Fraction(v)) * Fraction(2) ** (40 - c)) for v in x)
+
+
+def _fast_d_brute(tx, ty, slices, beta, k):
+    """The least d in 1 .. slices whose skipped pairs meet the bound:
+    T_x T_y >= 2^(133 + ceil(log2 slices) + ceil(log2 k) - d (beta + 1)),
+    compared as exact integers (Python), else slices."""
+    ls = (slices - 1).bit_length()
+    kap = (k - 1).bit_length()
+    for d in range(1, slices + 1):
+        e = 133 + ls + kap - d * (beta + 1)
+        if (tx * ty) * (2 ** max(-e, 0)) >= 2 ** max(e, 0):
+            return d
+    return slices
+
+
+def test_ozaki_fast_mode_masses_and_d_against_exact_integers():
+    """The vectors' masses against exact rational floors (subnormals, zeros,
+    powers of two and wide exponent ranges included), and every element's d
+    against a brute-force search of the inequality in exact integers."""
+    rng = np.random.default_rng(21)
+    M, N, K = 6, 5, 300
+    A = rng.standard_normal((M, K)) * np.exp2(rng.integers(-30, 30, (M, K)))
+    B = rng.standard_normal((K, N))
+    A[0, :] = 0.0                                  # a zero row: mass 0
+    A[1, :] = 0.0
+    A[1, 7] = 2.0 ** -1070                         # a subnormal alone
+    A[2, 3] = 2.0 ** 40                            # a power-of-two maximum
+    B[:, 0] = 1.0                                  # equal values
+    B[5, 1] = 0.0
+    rho = oracle.ozaki_rho(K)
+    s = oracle.ozaki_default_slices(rho)
+    D, Ta, Tb = oracle.ozaki_fast_d(A, B, rho=rho, slices=s)
+    for i in range(M):
+        assert int(Ta[i]) == _mass(A[i]), i
+    for j in range(N):
+        assert int(Tb[j]) == _mass(B[:, j]), j
+    assert Ta[0] == 0 and Ta[1] == 2 ** 40         # one element at the maximum: 2^40
+    assert int(Tb[0]) == K * 2 ** 40               # all equal to the maximum (a power of two)
+    for i in range(M):
+        for j in range(N):
+            assert D[i, j] == _fast_d_brute(int(Ta[i]), int(Tb[j]), s, 53 - rho, K), (i, j)
+    assert (D[0] == s).all()                       # nothing known about a zero row: every pair
+
+
+def test_ozaki_fast_mode_meets_the_pages_bound_and_skips_pairs():
+    """On normal data the automatic d skips pairs the default keeps (about a
+    quarter at K = 4096), and every element stays within the page's bound
+    2 sqrt(k) u |A||B| against exact rational products."""
+    rng = np.random.default_rng(22)
+    M, N, K = 6, 7, 4096
+    A = rng.standard_normal((M, K))
+    B = rng.standard_normal((K, N))
+    rho = oracle.ozaki_rho(K)
+    s = oracle.ozaki_default_slices(rho)
+    D, _, _ = oracle.ozaki_fast_d(A, B, rho=rho, slices=s)
+    assert D.max() <= s and D.min() >= 1
+    assert (D < s).mean() > 0.5                    # most elements drop the last diagonal
+    C, inexact = oracle.ozaki_gemm(A, B, rho=rho, slices=s, d=-1)
+    assert inexact == 0
+    scale = np.abs(A) @ np.abs(B)
+    for i in range(M):
+        for j in range(N):
+            exact = sum((Fraction(A[i, k]) * Fraction(B[k, j]) for k in range(K)), Fraction(0))
+            err = abs(float(Fraction(C[i, j]) - exact))
+            assert err <= 2 * np.sqrt(K) * 2.0 ** -53 * scale[i, j], (i, j)
+
+
+def test_ozaki_fast_mode_is_the_fixed_d_product_where_d_is_uniform():
+    """Where every element's automatic d is the same d, the product is the
+    fixed-d product, bit for bit; rows computed alone take the same d and give
+    the same bits (d depends on the row and the column only)."""
+    rng = np.random.default_rng(23)
+    A = rng.standard_normal((5, 4096))
+    B = rng.standard_normal((4096, 9))
+    rho = oracle.ozaki_rho(4096)
+    s = oracle.ozaki_default_slices(rho)
+    D, _, _ = oracle.ozaki_fast_d(A, B, rho=rho, slices=s)
+    C, _ = oracle.ozaki_gemm(A, B, rho=rho, slices=s, d=-1)
+    for d in np.unique(D):
+        Cd, _ = oracle.ozaki_gemm(A, B, rho=rho, slices=s, d=int(d))
+        assert np.array_equal(C[D == d], Cd[D == d])
+    for i in range(5):
+        Di, _, _ = oracle.ozaki_fast_d(A[i:i + 1], B, rho=rho, slices=s)
+        Ci, _ = oracle.ozaki_gemm(A[i:i + 1], B, rho=rho, slices=s, d=-1)
+        assert np.array_equal(Di[0], D[i]) and np.array_equal(Ci[0], C[i])
