@@ -575,7 +575,8 @@ def run_ozaki(dev, peaks) -> dict:
     float64 squares: time per call, the split's share, FP64-equivalent
     TFLOP/s (2 M N K per call), the tensor-core rate of the slice-pair
     products against the measured BF16 peak, and the error against cuBLAS's
-    own binary64 product.  At 8192 also a Fast Mode sweep of d."""
+    own binary64 product.  At 8192 also a Fast Mode sweep of d; at both
+    sizes Fast Mode's automatic d (d = -1, chosen per element)."""
     import deterministic_invariant_gemm_gb300 as dig
     out = {}
     bf16_peak = peaks["bf16_tflops"]
@@ -590,7 +591,7 @@ def run_ozaki(dev, peaks) -> dict:
         ws = torch.empty(need, dtype=torch.uint8, device=dev)
         ref = A @ B                                  # cuBLAS binary64
         scale = A.abs() @ B.abs()
-        cases = [s] if n != 8192 else [s, s - 1, s - 2, s - 3]
+        cases = ([s] if n != 8192 else [s, s - 1, s - 2, s - 3]) + [-1]
         res = {"slices": s, "rho": rho}
         for d in cases:
             def call(i, d=d):
@@ -599,9 +600,9 @@ def run_ozaki(dev, peaks) -> dict:
                 call(i)
             secs = time_region(call, iters, 1)
             per = secs / iters
-            pairs = dig.bigemm_ozaki_pairs(s, d)
+            pairs = dig.bigemm_ozaki_pairs(s, d) if d > 0 else None
             err = float(((C - ref).abs() / scale).max())
-            res["d%d" % d] = {"pairs": pairs, "ms": round(per * 1e3, 3),
+            res["d%d" % d if d > 0 else "d_auto"] = {"pairs": pairs, "ms": round(per * 1e3, 3),
                               "fp64_equiv_tflops": round(2.0 * n ** 3 / per / 1e12, 2),
                               "max_err_vs_cublas_fp64_over_absAabsB": err}
         # the split alone (rows of A, columns of B), to separate it from the products
@@ -1127,6 +1128,10 @@ def compact_workloads(detail: dict, peaks: dict, peak_src: str):
             full = oz["d%d" % oz["slices"]]
             out["ozaki_%d" % n] = {"ms": full["ms"], "fp64_equiv_tflops": full["fp64_equiv_tflops"],
                                    "products_frac_of_bf16_peak": oz["products_frac_of_bf16_peak"]}
+            auto = oz.get("d_auto")
+            if auto:
+                out["ozaki_%d" % n]["fast_auto_d"] = {"ms": auto["ms"], "fp64_equiv_tflops": auto["fp64_equiv_tflops"],
+                                                      "max_err": auto["max_err_vs_cublas_fp64_over_absAabsB"]}
     big = detail.get("large_16384_bf16out")
     roof = None
     if big:

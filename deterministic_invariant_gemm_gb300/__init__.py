@@ -522,7 +522,8 @@ def bigemm_ozaki_dgemm(A, B, C, M, N, K, lda, ldb, ldc, slices=0, d=0, workspace
 def ozaki_matmul(A, B, slices: int = 0, d: int = 0, out=None, workspace=None, stream=None):
     """C = A @ B for float64 CUDA tensors A [M, K] and B [K, N] (row-major), by
     the Ozaki scheme on the bf16 tensor cores (bigemm_ozaki_dgemm).  slices /
-    d: 0 for the defaults (binary64 accuracy).  Returns C float64 [M, N]."""
+    d: 0 for the defaults (binary64 accuracy); d = -1 for Fast Mode's
+    automatic d, chosen per element.  Returns C float64 [M, N]."""
     import torch
     if A.dtype != torch.float64 or B.dtype != torch.float64:
         raise TypeError("A and B must be float64")

@@ -773,7 +773,7 @@ int64_t round_up(int64_t x, int64_t m) { return ceil_div(x, m) * m; }
 // abort word for the launch.
 struct OzakiLayout {
     int64_t lda_s, ldb_s, kpad, tiles;
-    size_t off_b, off_ca, off_cb, off_cnt, total;
+    size_t off_b, off_ca, off_cb, off_cnt, off_ta, off_tb, total;
 };
 
 OzakiLayout ozaki_layout(int64_t M, int64_t N, int64_t K, int slices) {
@@ -788,31 +788,47 @@ OzakiLayout ozaki_layout(int64_t M, int64_t N, int64_t K, int slices) {
     const size_t cb = up(static_cast<size_t>(N) * 4);
     L.tiles = ceil_div(M, kBM) * ceil_div(N, kBN);
     const size_t cnt = up(static_cast<size_t>(L.tiles + 1) * 4);
+    const size_t ta = up(static_cast<size_t>(M) * 8);
+    const size_t tb = up(static_cast<size_t>(N) * 8);
     L.off_b = a;
     L.off_ca = a + b;
     L.off_cb = a + b + ca;
     L.off_cnt = a + b + ca + cb;
-    L.total = a + b + ca + cb + cnt;
+    L.off_ta = L.off_cnt + cnt;
+    L.off_tb = L.off_ta + ta;
+    L.total = L.off_tb + tb;
     return L;
+}
+
+int ceil_log2_int(int64_t v) {
+    int l = 0;
+    while ((int64_t(1) << l) < v) ++l;
+    return l;
 }
 
 bool aligned_to(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
+// mass: Fast Mode's vector masses (zeroed here for the columns), or nullptr.
 cudaError_t launch_ozaki_split(const DeviceInfo& d, const double* X, int64_t rows, int64_t cols,
                                int64_t ld, int axis, int rho, int slices, __nv_bfloat16* out,
-                               int64_t out_ld, int64_t out_rows, int* exps, cudaStream_t stream) {
+                               int64_t out_ld, int64_t out_rows, int* exps, cudaStream_t stream,
+                               unsigned long long* mass = nullptr) {
     if (axis == 0) {
         // one block per row, at most 16 resident blocks' worth per SM at a time
         int64_t blocks = rows;
         if (blocks > 16 * static_cast<int64_t>(d.sm_count)) blocks = 16 * static_cast<int64_t>(d.sm_count);
         ozaki_split_rows_kernel<<<static_cast<unsigned>(blocks), kOzakiRowThreads, 0, stream>>>(
-            X, rows, cols, ld, rho, slices, out, out_ld, rows * out_ld, exps);
+            X, rows, cols, ld, rho, slices, out, out_ld, rows * out_ld, exps, mass);
         return cudaGetLastError();
     }
     // column maxima: every exponent starts below any c^(1), then chunks of
     // rows merge theirs with an integer atomicMax
     cudaError_t e = cudaMemsetAsync(exps, 0x80, static_cast<size_t>(cols) * sizeof(int), stream);
     if (e != cudaSuccess) return e;
+    if (mass != nullptr) {
+        e = cudaMemsetAsync(mass, 0, static_cast<size_t>(cols) * sizeof(unsigned long long), stream);
+        if (e != cudaSuccess) return e;
+    }
     // chunks of at least kOzakiColChunk rows, at most 65535 of them
     int64_t chunk = ceil_div(ceil_div(rows, 65535), 8) * 8;
     if (chunk < kOzakiColChunk) chunk = kOzakiColChunk;
@@ -828,7 +844,7 @@ cudaError_t launch_ozaki_split(const DeviceInfo& d, const double* X, int64_t row
     if (by > 65535) by = 65535;
     if (by < 1) by = 1;
     ozaki_split_cols_kernel<<<dim3(static_cast<unsigned>(bx), static_cast<unsigned>(by)), 256, 0, stream>>>(
-        X, rows, cols, ld, out_rows, rho, slices, out, out_ld, out_rows * out_ld, exps);
+        X, rows, cols, ld, out_rows, rho, slices, out, out_ld, out_rows * out_ld, exps, mass);
     return cudaGetLastError();
 }
 
@@ -1131,8 +1147,9 @@ static bigemm_status ozaki_dgemm_impl(const double* A, const double* B, double* 
     if (M < 0 || N < 0 || K < 0 || K > kOzakiMaxK || M > INT_MAX || N > INT_MAX) return BIGEMM_ERR_ARG;
     const int rho = K > 0 ? ozaki_rho(K) : 52;
     if (slices == 0) slices = ozaki_default_slices(rho);
-    if (slices < 1 || slices > kOzakiMaxSlices || d < 0) return BIGEMM_ERR_ARG;
-    if (d == 0) d = slices;
+    if (slices < 1 || slices > kOzakiMaxSlices || d < -1) return BIGEMM_ERR_ARG;
+    const bool fast = (d == -1);  // Fast Mode's automatic d, per element
+    if (d == 0 || fast) d = slices;
     if (K > 0 && (A == nullptr || B == nullptr || lda < K || ldb < N)) return BIGEMM_ERR_ARG;
     if (C == nullptr || ldc < N) return BIGEMM_ERR_ARG;
     if (K > 0 && (!aligned_to(A, 8) || !aligned_to(B, 8))) return BIGEMM_ERR_ALIGN;
@@ -1163,10 +1180,13 @@ static bigemm_status ozaki_dgemm_impl(const double* A, const double* B, double* 
     int* ca = reinterpret_cast<int*>(ws + L.off_ca);
     int* cb = reinterpret_cast<int*>(ws + L.off_cb);
     int* cnt = reinterpret_cast<int*>(ws + L.off_cnt);
+    unsigned long long* ta = fast ? reinterpret_cast<unsigned long long*>(ws + L.off_ta) : nullptr;
+    unsigned long long* tb = fast ? reinterpret_cast<unsigned long long*>(ws + L.off_tb) : nullptr;
     // 1-3: split A by rows and B by columns (plain launches: they read the
-    // caller's A and B, so they wait for everything before them)
-    if (launch_ozaki_split(*dev, A, M, K, lda, 0, rho, slices, As, L.lda_s, M, ca, strm) != cudaSuccess ||
-        launch_ozaki_split(*dev, B, K, N, ldb, 1, rho, slices, Bs, L.ldb_s, L.kpad, cb, strm) != cudaSuccess)
+    // caller's A and B, so they wait for everything before them); with Fast
+    // Mode's automatic d also the vectors' masses
+    if (launch_ozaki_split(*dev, A, M, K, lda, 0, rho, slices, As, L.lda_s, M, ca, strm, ta) != cudaSuccess ||
+        launch_ozaki_split(*dev, B, K, N, ldb, 1, rho, slices, Bs, L.ldb_s, L.kpad, cb, strm, tb) != cudaSuccess)
         return BIGEMM_ERR_CUDA;
     // 4: every slice pair's product on the tensor cores, summed in binary64
     CUtensorMap tmA, tmB, tmBp;
@@ -1219,6 +1239,10 @@ static bigemm_status ozaki_dgemm_impl(const double* A, const double* B, double* 
     p.oz_beta = 53 - rho;
     p.oz_pairs = static_cast<int>(pairs);
     p.oz_kpad = static_cast<int>(L.kpad);
+    p.oz_fast = fast ? 1 : 0;
+    p.oz_ta = ta;
+    p.oz_tb = tb;
+    p.oz_need0 = 134 + ceil_log2_int(slices) + ceil_log2_int(K);
     p.a_rows = kBM;
     // one CTA per SM at most, over all (slice pair, tile) items: a tile's pairs
     // may run on different CTAs at once, their additions ordered by the counts

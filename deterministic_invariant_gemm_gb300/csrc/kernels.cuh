@@ -191,6 +191,13 @@ struct GemmParams {
     const int* oz_cb;       // c^(1) of every column of B
     int* oz_count;          // per tile, then the grid's abort word (oz_count[units])
     int oz_slices, oz_d, oz_beta, oz_pairs, oz_kpad;
+    // Fast Mode's automatic d (oz_fast): element (i, j) takes the pairs with
+    // p + q < d_ij, d_ij the least d >= 1 with d (beta + 1) >= oz_need0 -
+    // bitlen(T_a[i] T_b[j]) (at most oz_slices), T the vectors' integer masses;
+    // the kernel enumerates the pairs with p + q < the largest d_ij.
+    const unsigned long long* oz_ta;  // mass of every row of A
+    const unsigned long long* oz_tb;  // mass of every column of B
+    int oz_fast, oz_need0;
     int selftest_stall;     // 1 (the failure self-test only): the producer issues no
                             //    loads, so the MMA issuer's bounded wait must give up
     int a_rows;             // rows of A each stage loads (32, 64 or 128: the batch
@@ -199,12 +206,28 @@ struct GemmParams {
 
 // The slice pairs of the Ozaki scheme in the order of the binary64
 // accumulation: p outer, q inner, skipping p + q >= d (Fast Mode).
-__device__ __forceinline__ void ozaki_next_pair(const GemmParams& p, int& a, int& b) {
+__device__ __forceinline__ void ozaki_next_pair(const GemmParams& p, int d, int& a, int& b) {
     ++b;
-    if (b >= p.oz_slices || a + b >= p.oz_d) {
+    if (b >= p.oz_slices || a + b >= d) {
         ++a;
         b = 0;
     }
+}
+
+// Bit length of the 128-bit product x y.
+__device__ __forceinline__ int ozaki_bitlen_product(unsigned long long x, unsigned long long y) {
+    const unsigned long long hi = __umul64hi(x, y), lo = x * y;
+    if (hi != 0) return 128 - __clzll(static_cast<long long>(hi));
+    return lo != 0 ? 64 - __clzll(static_cast<long long>(lo)) : 0;
+}
+
+// Fast Mode's d for masses (tx, ty): the least d >= 1 with d (beta + 1) >=
+// need0 - bitlen(tx ty), at most the slice count.
+__device__ __forceinline__ int ozaki_fast_d(const GemmParams& p, unsigned long long tx,
+                                            unsigned long long ty) {
+    const int need = p.oz_need0 - ozaki_bitlen_product(tx, ty), w = p.oz_beta + 1;
+    const int d = need <= w ? 1 : (need + w - 1) / w;
+    return d < p.oz_slices ? d : p.oz_slices;
 }
 
 // Unit u -> (tile row, tile column, K segment).  All tiles of segment 0 come
@@ -596,9 +619,68 @@ __device__ __forceinline__ double ozaki_scaled(uint32_t pbits, int e) {
     return mag != 0u ? __longlong_as_double(static_cast<long long>(bits)) : 0.0;
 }
 
+// Fast Mode's per-element choice (fast.tb not NULL): element j takes the
+// pair iff t == 0 or t (beta + 1) < need0 - bitlen(ta tb[j]) (t = p + q),
+// i.e. iff p + q < its d; an element that does not keep C unchanged (no
+// addition of zero, which would turn -0.0 into +0.0).  For t > 0 and
+// E = need0 - t (beta + 1) - 1 >= 0 the test is ta tb[j] < 2^E, i.e. (for
+// ta > 0) tb[j] <= lim = floor((2^E - 1) / ta): one comparison per element
+// against a limit the row computes once per pair.
+struct OzakiFastRow {
+    const unsigned long long* tb;  // masses of the block's columns, or NULL: every element
+    unsigned long long lim;        // the largest column mass that takes the pair
+    bool none;                     // no element of the row takes it
+};
+
+// The row's limit for diagonal t of the pairs (tw = t (beta + 1)): none
+// passes when E < 0; every column mass passes (lim = 2^64 - 1) when t == 0,
+// ta == 0 or 2^E / ta >= 2^64; otherwise floor((2^E - 1) / ta) by restoring
+// division, starting after the bits of 2^E - 1 that stay below ta (at most
+// 64 steps).
+__device__ __forceinline__ OzakiFastRow ozaki_fast_row(const unsigned long long* tb,
+                                                       unsigned long long ta, int tw, int need0) {
+    OzakiFastRow f;
+    f.tb = tb;
+    f.lim = ~0ull;
+    f.none = false;
+    if (tb == nullptr || tw == 0) return f;
+    const int E = need0 - tw - 1;
+    if (E < 0) {  // bitlen(ta tb) < 0: never
+        f.none = true;
+        return f;
+    }
+    if (ta == 0) return f;  // a zero product: bitlen 0 <= E
+    const int la = 64 - __clzll(static_cast<long long>(ta));
+    if (E - la >= 64) return f;  // ta tb < 2^(la + 64) <= 2^E for every tb
+    if (E < la - 1) {            // 2^E - 1 < ta: only a zero mass
+        f.lim = 0;
+        return f;
+    }
+    // 2^E - 1 is E one bits; its first la - 1 leave a remainder 2^(la-1) - 1 < ta
+    unsigned long long rem = (la == 64) ? 0x7FFFFFFFFFFFFFFFull : ((1ull << (la - 1)) - 1);
+    unsigned long long q = 0;
+    for (int pos = E - la; pos >= 0; --pos) {
+        const bool carry = (rem >> 63) != 0;
+        const unsigned long long r2 = (rem << 1) | 1ull;
+        if (carry || r2 >= ta) {
+            rem = r2 - ta;  // the true difference is below ta < 2^64
+            q |= 1ull << pos;
+        } else {
+            rem = r2;
+        }
+    }
+    f.lim = q;
+    return f;
+}
+
+__device__ __forceinline__ bool ozaki_takes(const OzakiFastRow& f, int j) {
+    if (f.tb == nullptr) return true;
+    return !f.none && __ldg(f.tb + j) <= f.lim;
+}
+
 __device__ __forceinline__ void ozaki_accumulate_block(double* crow, const int* cb, int valid,
                                                        int e_pair, const uint32_t (&r)[32],
-                                                       bool first) {
+                                                       bool first, const OzakiFastRow& fast) {
     if (valid == 32) {
         // all loads first (C and the column exponents), then the arithmetic,
         // then the stores: 32 independent memory operations in flight
@@ -630,16 +712,25 @@ __device__ __forceinline__ void ozaki_accumulate_block(double* crow, const int* 
             // normal binary64 for e in this range: build it from P's bits
             // (exponent rebiased, fraction widened) -- exact, integer work only
             // -- and spend one binary64 addition per element.
+            if (fast.tb == nullptr || fast.lim == ~0ull) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                c[j].x = __dadd_rn(c[j].x, ozaki_scaled(r[2 * j], e[2 * j]));
-                c[j].y = __dadd_rn(c[j].y, ozaki_scaled(r[2 * j + 1], e[2 * j + 1]));
+                for (int j = 0; j < 16; ++j) {
+                    c[j].x = __dadd_rn(c[j].x, ozaki_scaled(r[2 * j], e[2 * j]));
+                    c[j].y = __dadd_rn(c[j].y, ozaki_scaled(r[2 * j + 1], e[2 * j + 1]));
+                }
+            } else if (!fast.none) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const ulonglong2 t = __ldg(reinterpret_cast<const ulonglong2*>(fast.tb) + j);
+                    if (t.x <= fast.lim) c[j].x = __dadd_rn(c[j].x, ozaki_scaled(r[2 * j], e[2 * j]));
+                    if (t.y <= fast.lim) c[j].y = __dadd_rn(c[j].y, ozaki_scaled(r[2 * j + 1], e[2 * j + 1]));
+                }
             }
         } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                c[j].x = ozaki_term(c[j].x, r[2 * j], e[2 * j]);
-                c[j].y = ozaki_term(c[j].y, r[2 * j + 1], e[2 * j + 1]);
+                if (ozaki_takes(fast, 2 * j)) c[j].x = ozaki_term(c[j].x, r[2 * j], e[2 * j]);
+                if (ozaki_takes(fast, 2 * j + 1)) c[j].y = ozaki_term(c[j].y, r[2 * j + 1], e[2 * j + 1]);
             }
         }
 #pragma unroll
@@ -647,7 +738,8 @@ __device__ __forceinline__ void ozaki_accumulate_block(double* crow, const int* 
     } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            if (j < valid) crow[j] = ozaki_term(first ? 0.0 : crow[j], r[j], e_pair + __ldg(cb + j));
+            if (j < valid && ozaki_takes(fast, j))
+                crow[j] = ozaki_term(first ? 0.0 : crow[j], r[j], e_pair + __ldg(cb + j));
     }
 }
 
@@ -778,6 +870,40 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // global memory is read and written only after it has completed.
     grid_dependency_wait();
 
+    // The slice pairs this product enumerates: p + q < oz_d.  With Fast Mode's
+    // automatic d, oz_d is the largest per-element d of the product, that of
+    // the least row mass and the least column mass (d_ij falls as the masses
+    // grow), found by every CTA from the split kernels' masses.
+    int oz_d = 0, oz_pairs = 0;
+    if constexpr (kOut == kOutOzaki) {
+        oz_d = p.oz_d;
+        oz_pairs = p.oz_pairs;
+        if (p.oz_fast) {
+            __shared__ unsigned long long oz_min[2];
+            if (threadIdx.x == 0) {
+                oz_min[0] = ~0ull;
+                oz_min[1] = ~0ull;
+            }
+            __syncthreads();
+            unsigned long long ma = ~0ull, mb = ~0ull;
+            for (int i = threadIdx.x; i < p.M; i += kNumThreads) ma = min(ma, p.oz_ta[i]);
+            for (int j = threadIdx.x; j < p.N; j += kNumThreads) mb = min(mb, p.oz_tb[j]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                ma = min(ma, __shfl_xor_sync(0xffffffffu, ma, o));
+                mb = min(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+            }
+            if (lane == 0) {
+                atomicMin(&oz_min[0], ma);
+                atomicMin(&oz_min[1], mb);
+            }
+            __syncthreads();
+            oz_d = ozaki_fast_d(p, oz_min[0], oz_min[1]);
+            oz_pairs = 0;
+            for (int a = 0; a < p.oz_slices; ++a) oz_pairs += max(0, min(p.oz_slices, oz_d - a));
+        }
+    }
+
     // Only the direct-output epilogues (the folded running sum) and the Ozaki
     // epilogue need more than the launch's 168 registers per thread; the
     // others skip the re-division (it sits between the dependency wait and
@@ -798,10 +924,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 // item: rows pa * M + m0 of the A slices, rows pb * oz_kpad + k
                 // of the B slices.
                 int pa = 0, pb = 0, pk = 0;  // pair pk is (pa, pb)
-                const int items = p.units * p.oz_pairs;
+                const int items = p.units * oz_pairs;
                 for (int L = blockIdx.x; ok && L < items; L += gridDim.x) {
                     const int pair = L / p.units, u = L - pair * p.units;
-                    for (; pk < pair; ++pk) ozaki_next_pair(p, pa, pb);
+                    for (; pk < pair; ++pk) ozaki_next_pair(p, oz_d, pa, pb);
                     {
                         int mt, nt, seg;
                         unit_coords(p, u, mt, nt, seg);
@@ -887,7 +1013,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             int t = 0;  // accumulators filled so far (one per segment)
             bool ok = true;
             // an Ozaki item is one (slice pair, tile), over all of K
-            const int n_items = (kOut == kOutOzaki) ? p.units * p.oz_pairs : p.units;
+            const int n_items = (kOut == kOutOzaki) ? p.units * oz_pairs : p.units;
             for (int u = blockIdx.x; ok && u < n_items; u += gridDim.x) {
                 int mt = 0, nt = 0, seg0 = 0;
                 if constexpr (kOut != kOutOzaki) unit_coords(p, u, mt, nt, seg0);
@@ -1003,10 +1129,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             bool ok = true;
             // the producer's order: items pair-major
             int pa = 0, pb = 0, pk = 0;
-            const int items = p.units * p.oz_pairs;
+            const int items = p.units * oz_pairs;
             for (int L = blockIdx.x; ok && L < items; L += gridDim.x) {
                 const int pair = L / p.units, u = L - pair * p.units;
-                for (; pk < pair; ++pk) ozaki_next_pair(p, pa, pb);
+                for (; pk < pair; ++pk) ozaki_next_pair(p, oz_d, pa, pb);
                 {
                     int mt, nt, seg;
                     unit_coords(p, u, mt, nt, seg);
@@ -1041,6 +1167,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                                static_cast<uint32_t>(acc * kBN);
                         const int e_pair = row_ok ? (p.oz_ca[row] - pa * step) - pb * step : 0;
+                        // Fast Mode: the row's limit on the column masses for this pair
+                        OzakiFastRow fast = ozaki_fast_row(p.oz_fast ? p.oz_tb : nullptr,
+                                                           (p.oz_fast && row_ok) ? p.oz_ta[row] : 0ull,
+                                                           (pa + pb) * step, p.oz_need0);
 #pragma unroll 1
                         for (int i = 0; i < 4; ++i) {
                             uint32_t r[32];
@@ -1051,10 +1181,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                 mbar_arrive(tempty_bar(acc));
                             }
                             const int col0 = n0 + (h * 4 + i) * 32;
+                            if (p.oz_fast) fast.tb = p.oz_tb + col0;  // 256-byte aligned: col0 % 32 == 0
                             if (row_ok && col0 < p.N)
                                 ozaki_accumulate_block(C + static_cast<int64_t>(row) * p.ld_out + col0,
                                                        p.oz_cb + col0, min(32, p.N - col0), e_pair, r,
-                                                       pair == 0);
+                                                       pair == 0, fast);
                         }
                     } else {
                         tc_fence_before();

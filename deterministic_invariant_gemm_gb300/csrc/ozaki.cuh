@@ -133,12 +133,26 @@ __device__ __forceinline__ void ozaki_split_one(double x, int c1, int rho, int s
     }
 }
 
+// Fast Mode's mass of a vector (its 1-norm from below, exactly and in any
+// order): sum_k floor(|x_k| 2^(40 - c^(1))), each term at most 2^40 since
+// |x_k| <= 2^(c^(1)), so the sum fits 64 bits for up to 2^23 terms.  The term
+// of one element from its bit pattern: |x| = R 2^E, shifted by E + 40 - c.
+__device__ __forceinline__ unsigned long long ozaki_mass_term(double x, int c1) {
+    const OzakiElem a = ozaki_elem(x);
+    const unsigned long long R = static_cast<unsigned long long>(a.R < 0 ? -a.R : a.R);
+    if (R == 0) return 0ull;
+    const int sh = a.E + 40 - c1;
+    if (sh >= 0) return R << sh;  // < 2^41: |x| <= 2^c1
+    return -sh >= 64 ? 0ull : (R >> -sh);
+}
+
 // Rows of X [rows][cols] (leading dimension ld): one block per row.  Each
 // thread holds up to kOzakiRowCache elements (pairs of adjacent columns) in
 // registers, so the row is read from memory once when cols <= 256 *
 // kOzakiRowCache; the block finds the row's maximum (integer max of the
 // magnitude bit patterns: exact and order-free), stores c^(1) in exps[row],
-// and splits the row into out[p * plane + row * out_ld + k].
+// and splits the row into out[p * plane + row * out_ld + k]; with `mass`
+// not NULL it also stores the row's Fast Mode mass in mass[row].
 constexpr int kOzakiRowThreads = 256;
 constexpr int kOzakiRowCache = 32;  // elements per thread kept in registers
 
@@ -149,7 +163,7 @@ __device__ __forceinline__ uint64_t ozaki_abs_bits(double x) {
 __global__ void __launch_bounds__(kOzakiRowThreads)
     ozaki_split_rows_kernel(const double* __restrict__ X, int64_t rows, int64_t cols, int64_t ld,
                             int rho, int slices, __nv_bfloat16* __restrict__ out, int64_t out_ld,
-                            int64_t plane, int* __restrict__ exps) {
+                            int64_t plane, int* __restrict__ exps, unsigned long long* __restrict__ mass) {
     __shared__ uint64_t wmax[kOzakiRowThreads / 32];
     const int tid = threadIdx.x;
     const int64_t pairs = cols / 2;
@@ -180,6 +194,28 @@ __global__ void __launch_bounds__(kOzakiRowThreads)
         __syncthreads();  // wmax is reused by the next row
         const int c1 = ozaki_ceil_log2_bits(m);
         if (tid == 0) exps[r] = c1;
+        if (mass != nullptr) {
+            // integer sums: the same total in any order
+            unsigned long long t = 0;
+#pragma unroll
+            for (int i = 0; i < kOzakiRowCache / 2; ++i) {
+                const int64_t pr = tid + static_cast<int64_t>(i) * kOzakiRowThreads;
+                if (pr < pairs) t += ozaki_mass_term(cache[2 * i], c1) + ozaki_mass_term(cache[2 * i + 1], c1);
+            }
+            for (int64_t pr = tid + static_cast<int64_t>(kOzakiRowCache / 2) * kOzakiRowThreads; pr < pairs;
+                 pr += kOzakiRowThreads)
+                t += ozaki_mass_term(x[2 * pr], c1) + ozaki_mass_term(x[2 * pr + 1], c1);
+            if ((cols & 1) && tid == 0) t += ozaki_mass_term(x[cols - 1], c1);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+            if ((tid & 31) == 0) wmax[tid >> 5] = t;
+            __syncthreads();
+            if (tid == 0) {
+                for (int w = 1; w < kOzakiRowThreads / 32; ++w) t += wmax[w];
+                mass[r] = t;
+            }
+            __syncthreads();  // wmax is reused by the next row
+        }
         __nv_bfloat16* orow = out + r * out_ld;
 #pragma unroll
         for (int i = 0; i < kOzakiRowCache / 2; ++i) {
@@ -233,11 +269,14 @@ __global__ void __launch_bounds__(256)
 // (the padding up to a whole K block) are written as zeros.  A thread takes
 // two adjacent columns (one 4-byte store per slice when out_ld is even),
 // blocks along y step through the rows.  Blocks with blockIdx.y == 0 also
-// turn an all-zero column's kOzakiNoExp into its c^(1) = 0.
+// turn an all-zero column's kOzakiNoExp into its c^(1) = 0.  With `mass` not
+// NULL (zero beforehand) every thread adds its rows' Fast Mode mass terms
+// into mass[j] with one integer atomic addition per column: order-free.
 __global__ void __launch_bounds__(256)
     ozaki_split_cols_kernel(const double* __restrict__ X, int64_t rows, int64_t cols, int64_t ld,
                             int64_t out_rows, int rho, int slices, __nv_bfloat16* __restrict__ out,
-                            int64_t out_ld, int64_t plane, int* __restrict__ exps) {
+                            int64_t out_ld, int64_t plane, int* __restrict__ exps,
+                            unsigned long long* __restrict__ mass) {
     const int64_t j = 2 * (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
     if (j >= cols) return;
     const bool two = j + 1 < cols;
@@ -250,15 +289,26 @@ __global__ void __launch_bounds__(256)
         exps[j] = ea;
         if (two) exps[j + 1] = eb;
     }
+    unsigned long long ta = 0, tb = 0;
     for (int64_t r = blockIdx.y; r < out_rows; r += gridDim.y) {
         __nv_bfloat16* o = out + r * out_ld + j;
         if (two) {
             const double xa = r < rows ? X[r * ld + j] : 0.0;
             const double xb = r < rows ? X[r * ld + j + 1] : 0.0;
             ozaki_split_two(xa, xb, ea, eb, rho, slices, o, plane, paired);
+            if (mass != nullptr) {
+                ta += ozaki_mass_term(xa, ea);
+                tb += ozaki_mass_term(xb, eb);
+            }
         } else {
-            ozaki_split_one(r < rows ? X[r * ld + j] : 0.0, ea, rho, slices, o, plane);
+            const double xa = r < rows ? X[r * ld + j] : 0.0;
+            ozaki_split_one(xa, ea, rho, slices, o, plane);
+            if (mass != nullptr) ta += ozaki_mass_term(xa, ea);
         }
+    }
+    if (mass != nullptr) {
+        if (ta != 0) atomicAdd(mass + j, ta);
+        if (two && tb != 0) atomicAdd(mass + j + 1, tb);
     }
 }
 

@@ -369,6 +369,7 @@ BIGEMM_API int64_t bigemm_ozaki_pairs(int slices, int d);
  * [round_up(N, 8)] in bf16, then c^(1) of every row of A and every column
  * of B (int32), then one int32 per 128 x 256 tile of C (how many slice
  * pairs the tile has taken so far) and one more (set when a wait gives up),
+ * then Fast Mode's masses of the rows of A and the columns of B (uint64),
  * each part 256-byte aligned.  0 for invalid arguments. */
 BIGEMM_API size_t bigemm_ozaki_workspace_bytes(int64_t M, int64_t N, int64_t K, int slices);
 
@@ -386,7 +387,18 @@ BIGEMM_API bigemm_status bigemm_ozaki_split(const double *X, int64_t rows, int64
  * C [M][ldc] binary64 (16-byte aligned, ldc even).  slices: 0 = the default
  * (bigemm_ozaki_default_slices), else 1 .. 32; d: 0 = slices (the deterministic
  * binary64 bound: every skipped pair is below 2^-54 of its vectors' maxima),
- * smaller for Fast Mode's trade of accuracy for speed.  K <= 2^22.  Four
+ * smaller for Fast Mode's trade of accuracy for speed, or -1 for Fast Mode's
+ * automatic d ("Fast Mode（GEMMの削減）": the smallest d meeting
+ * |fl(AB) - AB| <= 2 sqrt(k) u |A||B|).  The page gives that bound, not its
+ * procedure; here each element (i, j) takes its own d_ij, from row i of A
+ * and column j of B only (so rows stay batch-invariant): with the vectors'
+ * masses T = sum_k floor(|x_k| 2^(40 - c^(1))) (exact integers), d_ij is the
+ * least d >= 1 with d (54 - rho) >= 134 + ceil(log2 slices) + ceil(log2 K) -
+ * bitlen(T_a[i] T_b[j]), at most `slices` -- the skipped pairs' probabilistic
+ * size (at most `slices` pairs per diagonal, sqrt(K) per dot product) against
+ * 2 sqrt(K) 2^-53 times a mean-field estimate T_a T_b 2^(c_a + c_b - 80) / K
+ * of |A||B|_ij.  The element adds the pairs with p + q < d_ij, in the usual
+ * order; the kernel runs the pairs up to the largest d_ij.  K <= 2^22.  Four
  * launches: the row split of A, the column maxima and column split of B, and
  * one tensor-core kernel that runs every kept slice pair of each output tile
  * and keeps the binary64 sum in C (plus one memset of the tile counts).  The

@@ -199,16 +199,18 @@ def test_ozaki_host_helpers_agree_with_the_oracle(lib):
     for s in range(1, 12):
         for d in range(0, 2 * s + 1):
             assert dig.bigemm_ozaki_pairs(s, d) == oracle.ozaki_pairs(s, d)
-    # workspace: slices of A and B in bf16, then the two exponent vectors and
-    # one count per 128 x 256 output tile, 256-byte parts
+    # workspace: slices of A and B in bf16, then the two exponent vectors,
+    # one count per 128 x 256 output tile and the abort word, then Fast
+    # Mode's 64-bit masses of the rows of A and the columns of B, 256-byte parts
     M, N, K, s = 100, 70, 300, 0
     s = dig.bigemm_ozaki_default_slices(K)
     up = lambda x: (x + 255) // 256 * 256
+    masses = lambda M, N: up(M * 8) + up(N * 8)
     want = up(s * M * 304 * 2) + up(s * 320 * 72 * 2) + up(M * 4) + up(N * 4) + up((1 + 1) * 4)
-    assert dig.bigemm_ozaki_workspace_bytes(M, N, K, 0) == want
+    assert dig.bigemm_ozaki_workspace_bytes(M, N, K, 0) == want + masses(M, N)
     M, N = 1000, 3000              # 8 x 12 tiles
     want = up(s * M * 304 * 2) + up(s * 320 * 3000 * 2) + up(M * 4) + up(N * 4) + up((96 + 1) * 4)
-    assert dig.bigemm_ozaki_workspace_bytes(M, N, K, 0) == want
+    assert dig.bigemm_ozaki_workspace_bytes(M, N, K, 0) == want + masses(M, N)
     M, N = 1024, 4096              # 8 x 16 tiles: the abort word starts a second 256-byte block
     want = up(s * M * 304 * 2) + up(s * 320 * 4096 * 2) + up(M * 4) + up(N * 4) + up((128 + 1) * 4)
-    assert dig.bigemm_ozaki_workspace_bytes(M, N, K, 0) == want
+    assert dig.bigemm_ozaki_workspace_bytes(M, N, K, 0) == want + masses(M, N)

@@ -127,6 +127,84 @@ def test_dgemm_equals_the_oracle_exactly(M, N, K, slices, d):
     assert np.array_equal(C, Cref)
 
 
+def banded(shape, seed, axis):
+    """Vectors (rows for axis 0, columns for axis 1) of different magnitude
+    profiles -- flat (every entry near the maximum), normal, one dominant
+    entry, wide exponents, now and then all zero -- so that Fast Mode's
+    automatic d differs from element to element."""
+    g = workloads.generator(seed)
+    n, k = (shape[0], shape[1]) if axis == 0 else (shape[1], shape[0])
+    x = torch.randn((n, k), generator=g, dtype=torch.float64)
+    for v in range(n):
+        kind = v % 5
+        if kind == 0:                                       # flat: |x| in [0.75, 1]
+            x[v] = torch.sign(x[v]) * (0.75 + 0.25 * torch.rand(k, generator=g, dtype=torch.float64))
+        elif kind == 2:                                     # one entry dominates
+            x[v] *= 2.0 ** -30
+            x[v, v % k] = 2.0 ** 10
+        elif kind == 3:                                     # wide exponents
+            x[v] *= torch.exp2(torch.randint(-20, 21, (k,), generator=g).double())
+        elif kind == 4 and v % 10 == 4:
+            x[v] = 0.0
+    return x if axis == 0 else x.t().contiguous()
+
+
+@pytest.mark.parametrize("M,N,K,slices", [
+    (100, 70, 300, 12),          # ragged, one partial tile; more slices than the default 7
+    (257, 300, 1000, 11),        # three tile rows, two tile columns
+    (130, 512, 4096, 0),         # the default slices (8 at rho = 47)
+    (5, 40, 70000, 0),           # long K (14 slices)
+])
+def test_fast_mode_automatic_d_equals_the_oracle_exactly(M, N, K, slices):
+    """d = -1 (Fast Mode's automatic d, "Fast Mode（GEMMの削減）"): each
+    element takes the pairs p + q < d_ij that the oracle takes, so C equals the
+    oracle's bit for bit; the inputs make d_ij vary, and some pairs are skipped."""
+    A = banded((M, K), 3 * M + K, 0)
+    B = banded((K, N), 5 * N + K, 1)
+    rho = oracle.ozaki_rho(K)
+    s = slices or oracle.ozaki_default_slices(rho)
+    D, _, _ = oracle.ozaki_fast_d(A, B, rho=rho, slices=s)
+    assert D.min() < D.max() == s              # d varies; the zero vectors take every pair
+    C = run_dgemm(A, B, slices, -1, ldc_pad=6)
+    Cref, inexact = oracle.ozaki_gemm(A, B, rho=rho, slices=s, d=-1)
+    assert inexact == 0
+    assert np.array_equal(C.view(np.int64), Cref.view(np.int64))
+
+
+def test_fast_mode_rows_are_batch_invariant():
+    """d_ij depends on row i of A and column j of B only (their masses), so
+    Fast Mode's rows are the same at M = 1, in a window and in the full batch."""
+    M, N, K = 300, 384, 777
+    A = banded((M, K), 15, 0)
+    B = banded((K, N), 16, 1)
+    full = run_dgemm(A, B, 10, -1)
+    for lo, hi in ((0, 1), (1, 2), (2, 3), (128, 129), (299, 300), (37, 170)):
+        part = run_dgemm(A[lo:hi].clone(), B, 10, -1)
+        assert np.array_equal(part.view(np.int64), full[lo:hi].view(np.int64)), (lo, hi)
+
+
+def test_fast_mode_meets_the_pages_bound_on_normal_data():
+    """On normal data with K = 4096 the automatic d skips pairs the default
+    keeps (d < slices for most elements), C equals the oracle's, and the error
+    against exact rational products stays within the page's 2 sqrt(k) u |A||B|."""
+    M, N, K = 64, 96, 4096
+    g = workloads.generator(81)
+    A = torch.randn(M, K, generator=g, dtype=torch.float64)
+    B = torch.randn(K, N, generator=g, dtype=torch.float64)
+    C = run_dgemm(A, B, 0, -1)
+    D, _, _ = oracle.ozaki_fast_d(A, B)
+    s = oracle.ozaki_default_slices(oracle.ozaki_rho(K))
+    assert (D < s).mean() > 0.5
+    Cref, _ = oracle.ozaki_gemm(A, B, d=-1)
+    assert np.array_equal(C.view(np.int64), Cref.view(np.int64))
+    a, b = A.numpy(), B.numpy()
+    scale = np.abs(a) @ np.abs(b)
+    for i, j in ((0, 0), (10, 40), (63, 95), (7, 70)):
+        exact = sum((Fraction(a[i, k]) * Fraction(b[k, j]) for k in range(K)), Fraction(0))
+        err = abs(float(Fraction(C[i, j]) - exact))
+        assert err <= 2 * np.sqrt(K) * 2.0 ** -53 * scale[i, j], (i, j, err / scale[i, j])
+
+
 def test_dgemm_accuracy_against_exact_products():
     """1024^3 normal inputs: rows computed by the oracle match exactly, and
     the error against exact rational products on a sample is binary64's."""
@@ -242,13 +320,13 @@ def test_concurrent_products_on_two_streams_and_a_graph_replay():
 def test_dgemm_4096_rows_equal_the_oracle_and_one_row_products():
     """A 4096^3 product (36 slice pairs dealt over every SM, 18432 items):
     sampled rows equal the oracle's exactly and the same rows of one-row
-    products, bit for bit; also with Fast Mode's d."""
+    products, bit for bit; also with Fast Mode's fixed and automatic d."""
     M = N = K = 4096
     g = workloads.generator(79)
     A = torch.randn(M, K, generator=g, dtype=torch.float64)
     B = torch.randn(K, N, generator=g, dtype=torch.float64)
     rows = [0, 3071, 3072, 4095]
-    for d in (0, 6):
+    for d in (0, 6, -1):
         C = run_dgemm(A, B, 0, d)
         s = oracle.ozaki_default_slices(oracle.ozaki_rho(K))
         Cref, _ = oracle.ozaki_gemm(A[rows], B, d=d or s)
