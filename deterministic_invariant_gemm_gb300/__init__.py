@@ -74,6 +74,7 @@ EXPORTED_SYMBOLS = (
     "bigemm_last_launch_count", "bigemm_run_splitk_static", "bigemm_linear",
     "bigemm_fp8_effective_split_k", "bigemm_fp8_workspace_bytes", "bigemm_linear_fp8",
     "bigemm_split_is_folded", "bigemm_split_path", "bigemm_tile_n", "bigemm_cluster_capacity",
+    "bigemm_uses_pair", "bigemm_set_pair_mode", "bigemm_pair_capacity",
     "bigemm_ozaki_rho", "bigemm_ozaki_default_slices", "bigemm_ozaki_pairs",
     "bigemm_ozaki_workspace_bytes", "bigemm_ozaki_split", "bigemm_ozaki_dgemm",
     "bigemm_selftest_timeout", "bigemm_selftest_ozaki_order_timeout",
@@ -119,6 +120,9 @@ def load():
         "bigemm_split_path": ([i64, i64, i64, i32, i32], i32),
         "bigemm_tile_n": ([i64, i64, i64, i32, i32], i32),
         "bigemm_cluster_capacity": ([i32], i32),
+        "bigemm_uses_pair": ([i64, i64, i64, i32, i32], i32),
+        "bigemm_set_pair_mode": ([i32], i32),
+        "bigemm_pair_capacity": ([], i32),
         "bigemm_ozaki_rho": ([i64], i32),
         "bigemm_selftest_timeout": ([vp], i32),
         "bigemm_selftest_ozaki_order_timeout": ([vp], i32),
@@ -237,6 +241,29 @@ def bigemm_split_path(M: int, N: int, K: int, split_k: int, fp8: bool = False) -
     PATH_UNSPLIT, PATH_WORKSPACE, PATH_FOLDED, PATH_CLUSTER or PATH_SKINNY
     (-1: invalid)."""
     return int(load().bigemm_split_path(M, N, K, split_k, 1 if fp8 else 0))
+
+
+def bigemm_uses_pair(M: int, N: int, K: int, split_k: int, fp8: bool = False) -> int:
+    """1 when a product of this shape runs the 2-SM kernel (256 x 256 tiles
+    on CTA pairs), 0 when single CTAs (-1: invalid)."""
+    return int(load().bigemm_uses_pair(M, N, K, split_k, 1 if fp8 else 0))
+
+
+PAIR_NEVER, PAIR_AUTO, PAIR_ALWAYS = 0, 1, 2
+
+
+def bigemm_set_pair_mode(mode: int) -> int:
+    """When the 2-SM kernel runs for later products: PAIR_NEVER, PAIR_AUTO
+    (the default rule) or PAIR_ALWAYS (every shape it serves); returns the
+    previous mode."""
+    prev = int(load().bigemm_set_pair_mode(int(mode)))
+    if prev < 0:
+        raise ValueError("pair mode must be 0, 1 or 2")
+    return prev
+
+
+def bigemm_pair_capacity() -> int:
+    return int(load().bigemm_pair_capacity())
 
 
 def bigemm_tile_n(M: int, N: int, K: int, split_k: int, fp8: bool = False) -> int:

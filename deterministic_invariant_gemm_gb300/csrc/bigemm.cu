@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <cstring>
@@ -15,6 +16,7 @@
 #include "../../include/bigemm.h"
 #include "kernels.cuh"
 #include "ozaki.cuh"
+#include "pair.cuh"
 #include "skinny.cuh"
 
 namespace bigemm {
@@ -55,6 +57,8 @@ struct DeviceInfo {
     unsigned* status = nullptr;
     // clusters of S GEMM CTAs that can be resident at once, S = 0..8 (0: none)
     int max_clusters[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+    // CTA pairs of the 2-SM kernel that can be resident at once (0: never used)
+    int pair_clusters = 0;
 };
 
 constexpr int kMaxDevices = 64;
@@ -109,6 +113,10 @@ bigemm_status device_info(const DeviceInfo** out) {
                 {(const void*)bigemm_tc_kernel<kOutBF16, true, true>, true, kSmemBytes},
                 {(const void*)bigemm_tc_kernel<kOutSlices, true, true>, false, kSmemBytes},
                 {(const void*)bigemm_tc_kernel<kOutOzaki, false, false>, true, kSmemBytes},
+                {(const void*)bigemm_pair_kernel<kOutF32, false>, true, kPairSmemBytes},
+                {(const void*)bigemm_pair_kernel<kOutBF16, false>, true, kPairSmemBytes},
+                {(const void*)bigemm_pair_kernel<kOutF32, true>, true, kPairSmemBytes},
+                {(const void*)bigemm_pair_kernel<kOutBF16, true>, true, kPairSmemBytes},
 #define BIGEMM_NARROW_KERNELS(TN)                                                                  \
     {(const void*)bigemm_tc_kernel<kOutF32, false, false, TN>, true, Tile<TN>::kSmemBytes},        \
         {(const void*)bigemm_tc_kernel<kOutBF16, false, false, TN>, true, Tile<TN>::kSmemBytes},   \
@@ -159,6 +167,26 @@ bigemm_status device_info(const DeviceInfo** out) {
                     n = 0;
                 }
                 d.max_clusters[S] = n;
+            }
+            {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(2);
+                cfg.blockDim = dim3(kNumThreads);
+                cfg.dynamicSmemBytes = kPairSmemBytes;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = 2;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                int n = 0;
+                if (cudaOccupancyMaxActiveClusters(&n, (const void*)bigemm_pair_kernel<kOutF32, false>,
+                                                   &cfg) != cudaSuccess) {
+                    (void)cudaGetLastError();
+                    n = 0;
+                }
+                d.pair_clusters = n;
             }
         }
         d.ready = true;
@@ -216,6 +244,23 @@ int tile_width(int64_t M, int64_t N, int splits, int kb_per_split, bool fold, bo
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// An unsplit bf16 product of at least 256 rows with wide tiles can run on
+// CTA pairs (bigemm_pair_kernel): 256 x 256 tiles, each CTA loading half of
+// the A and B panels.  A pair instruction takes about as long per SM as a
+// 1-SM one, so the gain is the lighter loads of the main loop (measured 3 to
+// 15 %), while a pair's start and finish cost more: the rule takes the
+// 2-SM kernel once the pair tiles fill at least two waves of the device's
+// pairs.  Every output element is the same accumulation chain either way.
+// bigemm_set_pair_mode: 0 never, 1 by this rule, 2 for every eligible shape
+// (comparisons and tests).
+std::atomic<int> g_pair_mode{1};
+
+bool pairs_tiles(int64_t M, int64_t N, int splits, bool fp8, int tile_n, int pair_clusters) {
+    const int mode = g_pair_mode.load(std::memory_order_relaxed);
+    if (mode == 0 || fp8 || splits != 1 || M < kPairBM || tile_n != kBN || pair_clusters <= 0) return false;
+    return mode == 2 || ceil_div(M, kPairBM) * ceil_div(N, kBN) >= 2 * static_cast<int64_t>(pair_clusters);
+}
 
 // kb_elems: elements per K block -- 64 for BF16, 128 for 8-bit floats (both
 // 128 bytes per row).
@@ -553,6 +598,62 @@ bigemm_status run_skinny(const DeviceInfo& d, bool bf16, const void* A, const vo
 // wt: the second operand is a weight matrix W [N, K] (ldb is its row stride);
 // otherwise B [K, N].  bias: bf16 [N] added to every row (linear layers), or
 // nullptr.
+// The 2-SM product (pairs_tiles): A [M, K] in boxes of 64 k x 128 rows, B
+// [K, N] in boxes of 64 columns x 64 k-rows or W [N, K] in boxes of 64 k x
+// 128 rows (a CTA's half of a 256-column tile), C in 32 x 32 boxes.
+bigemm_status run_pair(const DeviceInfo& d, bool bf16, const void* A, const void* B, void* C, int64_t M,
+                       int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, bool wt,
+                       const void* bias, float scale, cudaStream_t stream) {
+    CUtensorMap tmA, tmB, tmBp, tmC;
+    std::memset(&tmC, 0, sizeof(tmC));
+    if (!encode_operands(&tmA, &tmB, &tmBp, A, B, M, N, K, lda, ldb, wt, false, kBN / 2))
+        return BIGEMM_ERR_CUDA;
+    const int64_t m_tiles = ceil_div(M, kPairBM), n_tiles = ceil_div(N, kBN);
+    const int64_t units = m_tiles * n_tiles;
+    if (units > INT_MAX) return BIGEMM_ERR_ARG;
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.status = d.status;
+    p.out = C;
+    p.ld_out = ldc;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.m_tiles = static_cast<int>(m_tiles);
+    p.n_tiles = static_cast<int>(n_tiles);
+    p.splits = 1;
+    p.kb_total = static_cast<int>(ceil_div(K, kBK));
+    p.kb_per_split = p.kb_total;
+    p.units = static_cast<int>(units);
+    p.epi_boxes = epi_boxes_for(static_cast<int>(M));
+    p.epi_batch = epi_batch_for(static_cast<int>(M));
+    // GROUP_M swizzle over 256-row tiles: the same rows per group as the
+    // 1-SM rule (8 pair tile rows once there are four waves, else 4)
+    p.group_m = (units >= 4 * static_cast<int64_t>(d.pair_clusters)) ? 8 : 4;
+    p.a_rows = kBM;
+    p.bias = static_cast<const __nv_bfloat16*>(bias);
+    p.scale = scale;
+    const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    if (encode_out_grouped(&tmC, dt, bf16 ? 2u : 4u, C, M, N, ldc, 0, 0, p.epi_batch))
+        p.grouped = 1;
+    else if (!(bf16 ? encode_out_bf16(&tmC, C, M, N, ldc) : encode_out_f32(&tmC, C, M, N, ldc)))
+        return BIGEMM_ERR_CUDA;
+    // persistent: at most one pair per two SMs, as many as fit at once
+    const int64_t pairs = units < d.pair_clusters ? units : d.pair_clusters;
+    const dim3 g(static_cast<unsigned>(2 * pairs)), blk(kNumThreads);
+    cudaError_t e;
+    if (bf16)
+        e = wt ? launch_pdl_cluster(bigemm_pair_kernel<kOutBF16, true>, g, blk, kPairSmemBytes, stream, 2u,
+                                    tmA, tmB, tmC, p)
+               : launch_pdl_cluster(bigemm_pair_kernel<kOutBF16, false>, g, blk, kPairSmemBytes, stream, 2u,
+                                    tmA, tmB, tmC, p);
+    else
+        e = wt ? launch_pdl_cluster(bigemm_pair_kernel<kOutF32, true>, g, blk, kPairSmemBytes, stream, 2u,
+                                    tmA, tmB, tmC, p)
+               : launch_pdl_cluster(bigemm_pair_kernel<kOutF32, false>, g, blk, kPairSmemBytes, stream, 2u,
+                                    tmA, tmB, tmC, p);
+    return e == cudaSuccess ? BIGEMM_OK : BIGEMM_ERR_CUDA;
+}
+
 bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t M, int64_t N,
                        int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int split_k, void* ws,
                        size_t ws_bytes, cudaStream_t stream, bool wt = false,
@@ -609,6 +710,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     // both cases.
     const bool cluster = direct && !fold && tile_n == kBN && splits >= 2 && splits <= 8 && K > 0 &&
                          m_tiles * n_tiles <= d->max_clusters[splits];
+    const bool pair = direct && K > 0 && pairs_tiles(M, N, splits, fp8, tile_n, d->pair_clusters);
 
     // ---- K == 0: the empty sum is +0.0 everywhere (plus the bias, if any)
     if (K == 0 && bias != nullptr) {
@@ -631,6 +733,11 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     if (few_rows) {
         st = run_skinny(*d, mode == kModeBF16, A, B, C, M, N, K, lda, ldb, ldc, splits, kb_per_split, wt,
                         bias, stream);
+        if (st == BIGEMM_OK) g_last_launches = 1;
+        return st;
+    }
+    if (pair) {
+        st = run_pair(*d, mode == kModeBF16, A, B, C, M, N, K, lda, ldb, ldc, wt, bias, scale, stream);
         if (st == BIGEMM_OK) g_last_launches = 1;
         return st;
     }
@@ -949,6 +1056,29 @@ int bigemm_tile_n(int64_t M, int64_t N, int64_t K, int split_k, int fp8) {
     const DeviceInfo* d = nullptr;
     if (device_info(&d) != BIGEMM_OK) return -1;
     return tile_width(M, N, s, L, folds(M, N, s), fp8 != 0, d->sm_count);
+}
+
+int bigemm_uses_pair(int64_t M, int64_t N, int64_t K, int split_k, int fp8) {
+    if (M < 0 || N < 0 || K < 0) return -1;
+    int L = 0;
+    const int s = effective_split(K, split_k, &L, fp8 ? 128 : kBK);
+    if (s == 0) return -1;
+    if (M == 0 || N == 0 || K == 0 || skinny(M, s, fp8 != 0)) return 0;
+    const DeviceInfo* d = nullptr;
+    if (device_info(&d) != BIGEMM_OK) return -1;
+    const int tn = tile_width(M, N, s, L, folds(M, N, s), fp8 != 0, d->sm_count);
+    return pairs_tiles(M, N, s, fp8 != 0, tn, d->pair_clusters) ? 1 : 0;
+}
+
+int bigemm_set_pair_mode(int mode) {
+    if (mode < 0 || mode > 2) return -1;
+    return g_pair_mode.exchange(mode);
+}
+
+int bigemm_pair_capacity(void) {
+    const DeviceInfo* d = nullptr;
+    if (device_info(&d) != BIGEMM_OK) return -1;
+    return d->pair_clusters;
 }
 
 size_t bigemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {

@@ -310,13 +310,19 @@ __device__ __forceinline__ void unit_coords(const Sched& p, int u, int& mt, int&
 // Bounded wait on an mbarrier phase.  Gives up when another role has aborted
 // (shared flag) or after kWaitTimeoutNs; a timeout raises the abort flag and
 // records `why` in the device error word.  Never traps.
+// kCluster: acquire at cluster scope (a barrier the other CTA of a pair
+// arrives on).
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                              volatile int* abort_flag, unsigned* status,
                                              unsigned why, bool honour_abort = true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    const auto done = [&]() {
+        return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (done()) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1; it != 0u; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (done()) return true;
         if ((it & 255u) == 0u) {
             if (honour_abort && *abort_flag) return false;
             if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
