@@ -117,6 +117,8 @@ bigemm_status device_info(const DeviceInfo** out) {
                 {(const void*)bigemm_pair_kernel<kOutBF16, false>, true, kPairSmemBytes},
                 {(const void*)bigemm_pair_kernel<kOutF32, true>, true, kPairSmemBytes},
                 {(const void*)bigemm_pair_kernel<kOutBF16, true>, true, kPairSmemBytes},
+                {(const void*)bigemm_pair_kernel<kOutF32, true, true>, true, kPairSmemBytes},
+                {(const void*)bigemm_pair_kernel<kOutBF16, true, true>, true, kPairSmemBytes},
 #define BIGEMM_NARROW_KERNELS(TN)                                                                  \
     {(const void*)bigemm_tc_kernel<kOutF32, false, false, TN>, true, Tile<TN>::kSmemBytes},        \
         {(const void*)bigemm_tc_kernel<kOutBF16, false, false, TN>, true, Tile<TN>::kSmemBytes},   \
@@ -245,9 +247,9 @@ int tile_width(int64_t M, int64_t N, int splits, int kb_per_split, bool fold, bo
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// An unsplit bf16 product of at least 256 rows with wide tiles can run on
-// CTA pairs (bigemm_pair_kernel): 256 x 256 tiles, each CTA loading half of
-// the A and B panels.  A pair instruction takes about as long per SM as a
+// An unsplit (or folded) product of at least 256 rows with wide tiles, bf16
+// or 8-bit floats, can run on CTA pairs (bigemm_pair_kernel): 256 x 256
+// tiles, each CTA loading half of the A and B panels.  A pair instruction takes about as long per SM as a
 // 1-SM one, so the gain is the lighter loads of the main loop (measured 3 to
 // 15 %), while a pair's start and finish cost more: the rule takes the
 // 2-SM kernel once the pair tiles fill at least two waves of the device's
@@ -256,9 +258,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // (comparisons and tests).
 std::atomic<int> g_pair_mode{1};
 
-bool pairs_tiles(int64_t M, int64_t N, int splits, bool fp8, int tile_n, int pair_clusters) {
+// A split product qualifies when it folds (folds(): then every 128-row tile
+// of it would also sum its segments in the CTA).
+bool pairs_tiles(int64_t M, int64_t N, int splits, int tile_n, int pair_clusters) {
     const int mode = g_pair_mode.load(std::memory_order_relaxed);
-    if (mode == 0 || fp8 || splits != 1 || M < kPairBM || tile_n != kBN || pair_clusters <= 0) return false;
+    if (mode == 0 || M < kPairBM || tile_n != kBN || pair_clusters <= 0) return false;
+    if (splits != 1 && !folds(M, N, splits)) return false;
     return mode == 2 || ceil_div(M, kPairBM) * ceil_div(N, kBN) >= 2 * static_cast<int64_t>(pair_clusters);
 }
 
@@ -602,11 +607,14 @@ bigemm_status run_skinny(const DeviceInfo& d, bool bf16, const void* A, const vo
 // [K, N] in boxes of 64 columns x 64 k-rows or W [N, K] in boxes of 64 k x
 // 128 rows (a CTA's half of a 256-column tile), C in 32 x 32 boxes.
 bigemm_status run_pair(const DeviceInfo& d, bool bf16, const void* A, const void* B, void* C, int64_t M,
-                       int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, bool wt,
-                       const void* bias, float scale, cudaStream_t stream) {
+                       int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int splits,
+                       int kb_per_split, bool wt, const void* bias, float scale, int fp8_fmt_a,
+                       int fp8_fmt_b, cudaStream_t stream) {
+    const bool fp8 = fp8_fmt_a >= 0;  // 8-bit float operands, W layout
+    if (fp8 && !wt) return BIGEMM_ERR_ARG;
     CUtensorMap tmA, tmB, tmBp, tmC;
     std::memset(&tmC, 0, sizeof(tmC));
-    if (!encode_operands(&tmA, &tmB, &tmBp, A, B, M, N, K, lda, ldb, wt, false, kBN / 2))
+    if (!encode_operands(&tmA, &tmB, &tmBp, A, B, M, N, K, lda, ldb, wt, fp8, kBN / 2))
         return BIGEMM_ERR_CUDA;
     const int64_t m_tiles = ceil_div(M, kPairBM), n_tiles = ceil_div(N, kBN);
     const int64_t units = m_tiles * n_tiles;
@@ -620,9 +628,13 @@ bigemm_status run_pair(const DeviceInfo& d, bool bf16, const void* A, const void
     p.N = static_cast<int>(N);
     p.m_tiles = static_cast<int>(m_tiles);
     p.n_tiles = static_cast<int>(n_tiles);
-    p.splits = 1;
-    p.kb_total = static_cast<int>(ceil_div(K, kBK));
-    p.kb_per_split = p.kb_total;
+    p.splits = splits;
+    p.kb_total = static_cast<int>(ceil_div(K, fp8 ? 128 : kBK));
+    p.kb_per_split = splits > 1 ? kb_per_split : p.kb_total;
+    p.fold = splits > 1 ? 1 : 0;
+    p.idesc_fp8 = fp8 ? idesc_fp8_f32(kPairBM, kBN, static_cast<uint32_t>(fp8_fmt_a),
+                                      static_cast<uint32_t>(fp8_fmt_b))
+                      : 0u;
     p.units = static_cast<int>(units);
     p.epi_boxes = epi_boxes_for(static_cast<int>(M));
     p.epi_batch = epi_batch_for(static_cast<int>(M));
@@ -641,7 +653,12 @@ bigemm_status run_pair(const DeviceInfo& d, bool bf16, const void* A, const void
     const int64_t pairs = units < d.pair_clusters ? units : d.pair_clusters;
     const dim3 g(static_cast<unsigned>(2 * pairs)), blk(kNumThreads);
     cudaError_t e;
-    if (bf16)
+    if (fp8)
+        e = bf16 ? launch_pdl_cluster(bigemm_pair_kernel<kOutBF16, true, true>, g, blk, kPairSmemBytes, stream,
+                                      2u, tmA, tmB, tmC, p)
+                 : launch_pdl_cluster(bigemm_pair_kernel<kOutF32, true, true>, g, blk, kPairSmemBytes, stream,
+                                      2u, tmA, tmB, tmC, p);
+    else if (bf16)
         e = wt ? launch_pdl_cluster(bigemm_pair_kernel<kOutBF16, true>, g, blk, kPairSmemBytes, stream, 2u,
                                     tmA, tmB, tmC, p)
                : launch_pdl_cluster(bigemm_pair_kernel<kOutBF16, false>, g, blk, kPairSmemBytes, stream, 2u,
@@ -710,7 +727,7 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
     // both cases.
     const bool cluster = direct && !fold && tile_n == kBN && splits >= 2 && splits <= 8 && K > 0 &&
                          m_tiles * n_tiles <= d->max_clusters[splits];
-    const bool pair = direct && K > 0 && pairs_tiles(M, N, splits, fp8, tile_n, d->pair_clusters);
+    const bool pair = direct && K > 0 && pairs_tiles(M, N, splits, tile_n, d->pair_clusters);
 
     // ---- K == 0: the empty sum is +0.0 everywhere (plus the bias, if any)
     if (K == 0 && bias != nullptr) {
@@ -737,7 +754,8 @@ bigemm_status run_impl(Mode mode, const void* A, const void* B, void* C, int64_t
         return st;
     }
     if (pair) {
-        st = run_pair(*d, mode == kModeBF16, A, B, C, M, N, K, lda, ldb, ldc, wt, bias, scale, stream);
+        st = run_pair(*d, mode == kModeBF16, A, B, C, M, N, K, lda, ldb, ldc, splits, kb_per_split, wt, bias,
+                      scale, fp8_fmt_a, fp8_fmt_b, stream);
         if (st == BIGEMM_OK) g_last_launches = 1;
         return st;
     }
@@ -1067,7 +1085,7 @@ int bigemm_uses_pair(int64_t M, int64_t N, int64_t K, int split_k, int fp8) {
     const DeviceInfo* d = nullptr;
     if (device_info(&d) != BIGEMM_OK) return -1;
     const int tn = tile_width(M, N, s, L, folds(M, N, s), fp8 != 0, d->sm_count);
-    return pairs_tiles(M, N, s, fp8 != 0, tn, d->pair_clusters) ? 1 : 0;
+    return pairs_tiles(M, N, s, tn, d->pair_clusters) ? 1 : 0;
 }
 
 int bigemm_set_pair_mode(int mode) {

@@ -49,14 +49,22 @@ constexpr uint32_t kPairIdescBN = idesc_bf16_f32(kPairBM, kBN, /*A MN-major*/ fa
 constexpr uint32_t kPairIdescWt = idesc_bf16_f32(kPairBM, kBN, false, false);
 
 // GemmParams as the 1-SM kernel reads them, with m_tiles counting 256-row
-// pair tiles, splits == 1 and no fold, cluster or Ozaki fields.  kWt: W [N, K]
+// pair tiles, no cluster or Ozaki fields, and either splits == 1 or a folded
+// split (p.fold: the unit is a whole tile whose K segments fill one
+// accumulator each, summed by the epilogue in the order 0..splits-1 with the
+// reduction kernel's FP32 additions, as in the 1-SM kernel).  kWt: W [N, K]
 // (K-major, boxes of 64 k x 128 rows); otherwise B [K, N] (N-major, boxes of
-// 64 columns x 64 k-rows).
-template <int kOut, bool kWt>
+// 64 columns x 64 k-rows).  kFp8: 8-bit float operands, both K-major (kWt): a
+// K block is 128 elements, still 128 bytes per row, consumed by four
+// instructions of K = 32 (kind::f8f6f4) -- shared-memory layout and
+// descriptors byte for byte those of BF16.
+template <int kOut, bool kWt, bool kFp8 = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
     bigemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
     static_assert(kOut == kOutF32 || kOut == kOutBF16, "the 2-SM kernel writes C directly");
+    static_assert(!kFp8 || kWt, "8-bit operands are read K-major only");
+    constexpr int kKB = kFp8 ? 128 : kBK;  // elements per K block (128 bytes per row)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Both CTAs of a pair have the same layout, so both stop here or neither
     // does (before any barrier, allocation or remote access).
@@ -139,9 +147,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     // CTA 0's barrier counts both CTAs' bytes of the stage
                     const uint32_t fb = map_shared_rank(full_bar(stage), 0u);
                     if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kPairStageBytes);
-                    tma_load_2d_pair(sA + stage * kABytes, &tmA, fb, kb * kBK, m0);
+                    tma_load_2d_pair(sA + stage * kABytes, &tmA, fb, kb * kKB, m0);
                     if constexpr (kWt) {
-                        tma_load_2d_pair(sB + stage * kPairBBytes, &tmB, fb, kb * kBK, nb0);
+                        tma_load_2d_pair(sB + stage * kPairBBytes, &tmB, fb, kb * kKB, nb0);
                     } else {
 #pragma unroll
                         for (int c = 0; c < 2; ++c)
@@ -169,12 +177,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                        abort_flag, p.status, kErrWaitDrain, /*honour_abort=*/false);
         } else if (warp == 1 && lane == 0 && rank == 0) {
             // ------------------------------------------------- MMA issuer --
-            const uint32_t idesc = kWt ? kPairIdescWt : kPairIdescBN;
+            const uint32_t idesc = kFp8 ? p.idesc_fp8 : (kWt ? kPairIdescWt : kPairIdescBN);
             int stage = 0;
             uint32_t phase = 0;
             int t = 0;
             bool ok = true;
-            for (int u = pair_id; ok && u < p.units; u += n_pairs, ++t) {
+            const int nseg = p.fold ? p.splits : 1;
+            for (int u = pair_id; ok && u < p.units; u += n_pairs) {
+              for (int sg = 0; ok && sg < nseg; ++sg, ++t) {
+                // one accumulator per K segment (the whole of K when unsplit)
+                const int kb0 = p.fold ? sg * p.kb_per_split : 0;
+                const int kb1 = p.fold ? min(kb0 + p.kb_per_split, p.kb_total) : p.kb_total;
                 const int acc = t % kPairAccStages;
                 const uint32_t acc_phase = static_cast<uint32_t>(t / kPairAccStages) & 1u;
                 if (!wait_bounded<true>(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status,
@@ -184,7 +197,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-                for (int kb = 0; kb < p.kb_total; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded<true>(full_bar(stage), phase, abort_flag, p.status, kErrWaitMma)) {
                         ok = false;
                         break;
@@ -199,7 +212,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         // two 64-column chunks, 16 k-rows = 2 KiB per step.
                         const uint64_t bd = kWt ? smem_desc_sw128(b0 + kk * kUmmaK * 2, 16, 1024)
                                                 : smem_desc_sw128(b0 + kk * kUmmaK * 128, kBChunkBytes, 1024);
-                        mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        if constexpr (kFp8)
+                            mma_fp8_pair(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                        else
+                            mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
                     }
                     // stage s is free again in both CTAs once these have read it
                     mma_commit_pair(empty_bar(stage));
@@ -212,6 +228,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 if (!ok) break;
                 mma_commit_pair(tfull_bar(acc));
                 mma_commit_pair(map_shared_rank(tfull_bar(acc), 1u));
+              }
             }
             // every instruction completes before the TMEM and the stages are released
             mma_commit_pair(drain_bar);
@@ -237,7 +254,67 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (rank == 0) mbar_arrive(tempty_bar(acc));
             else mbar_arrive_remote(map_shared_rank(tempty_bar(acc), 0u));
         };
-        for (int u = pair_id; u < p.units; u += n_pairs, ++t) {
+        if (p.fold) {
+            // ---- folded tiles: sum = w_0, then sum = sum + w_s for s = 1 ..
+            // splits-1 (FP32, round to nearest even) in 128 registers, then the
+            // scale, the bias and the stores -- the 1-SM fold's arithmetic in its
+            // order.  The host folds only when every warp with rows stores one
+            // block per batch (p.epi_batch == 1).
+            for (int u = pair_id; u < p.units; u += n_pairs) {
+                int mt, nt, seg;
+                unit_coords(p, u, mt, nt, seg);
+                const int m0 = mt * kPairBM + static_cast<int>(rank) * kBM + q * 32, n0 = nt * kBN;
+                const int nchunks = min(h * 4 + 4, min(kBN / 32, (p.N - n0 + 31) / 32));
+                uint32_t sum[128];
+                bool ok = true;
+#pragma unroll 1
+                for (int sg = 0; sg < p.splits; ++sg, ++t) {
+                    const int acc = t % kPairAccStages;
+                    const uint32_t acc_phase = static_cast<uint32_t>(t / kPairAccStages) & 1u;
+                    if (!wait_bounded<true>(tfull_bar(acc), acc_phase, abort_flag, p.status,
+                                            kErrWaitEpilogue)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (m0 < p.M) {
+                        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                               static_cast<uint32_t>(acc * kBN);
+                        if (sg == 0) {  // sum = w_0 itself (a -0.0 stays -0.0)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                if (h * 4 + i < nchunks)
+                                    tmem_ld_32x32b_x32(tbase + (h * 4 + i) * 32,
+                                                       *reinterpret_cast<uint32_t(*)[32]>(sum + 32 * i));
+                            tmem_ld_wait();
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                if (h * 4 + i < nchunks) {
+                                    uint32_t w[32];
+                                    tmem_ld_32x32b_x32(tbase + (h * 4 + i) * 32, w);
+                                    tmem_ld_wait();
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j)
+                                        sum[32 * i + j] = __float_as_uint(
+                                            __fadd_rn(__uint_as_float(sum[32 * i + j]), __uint_as_float(w[j])));
+                                }
+                            }
+                        }
+                    }
+                    release_acc(acc);
+                }
+                if (!ok) break;
+                if (m0 < p.M) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (h * 4 + i < nchunks)
+                            emit_blocks<kOut, 1>(p, &tmC, sum + 32 * i, 1, h * 4 + i, n0, m0, seg, lane,
+                                                 my_boxes, 1, slots, nbat);
+                }
+            }
+        }
+        for (int u = pair_id; !p.fold && u < p.units; u += n_pairs, ++t) {
             int mt, nt, seg;
             unit_coords(p, u, mt, nt, seg);
             const int m0 = mt * kPairBM + static_cast<int>(rank) * kBM + q * 32, n0 = nt * kBN;

@@ -248,6 +248,18 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, 
         : "memory");
 }
 
+// The 8-bit float form of mma_bf16_pair (formats in the instruction
+// descriptor, K = 32 per instruction).
+__device__ __forceinline__ void mma_fp8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` (a shared::cluster address: this CTA's barrier or
 // the peer's) when every pair instruction this thread issued so far has
 // completed.

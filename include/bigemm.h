@@ -195,26 +195,28 @@ BIGEMM_API int bigemm_cluster_capacity(int splits);
 #define BIGEMM_PATH_SKINNY 4
 BIGEMM_API int bigemm_split_path(int64_t M, int64_t N, int64_t K, int split_k, int fp8);
 
-/* 1 when bigemm_run, bigemm_run_bf16out or bigemm_linear (fp8 = 0) runs a
- * product of this shape on CTA pairs, 0 when on single CTAs, -1 for invalid
- * arguments or when the device cannot be queried.  The 2-SM kernel serves
- * unsplit (effective split 1) bf16 products of at least 256 rows with
- * 256-wide tiles (bigemm_tile_n): a thread-block cluster of two CTAs on two
+/* 1 when bigemm_run, bigemm_run_bf16out, bigemm_linear (fp8 = 0) or
+ * bigemm_linear_fp8 (fp8 = 1) runs a product of this shape on CTA pairs, 0
+ * when on single CTAs, -1 for invalid arguments or when the device cannot be
+ * queried.  The 2-SM kernel serves products of at least 256 rows with
+ * 256-wide tiles (bigemm_tile_n) that are unsplit (effective split 1) or
+ * folded (bigemm_split_is_folded): a thread-block cluster of two CTAs on two
  * SMs computes a 256 x 256 output tile with tcgen05.mma.cta_group::2 (M =
- * 256, N = 256, K = 16); each CTA loads its own 128 rows of A and its own 128
- * columns of B with plain TMA loads and holds its 128 rows of the FP32 sum
- * in its TMEM.  By default (bigemm_set_pair_mode 1) it takes such a product
+ * 256, N = 256, K = 16 for bf16, 32 for 8-bit floats); each CTA loads its own
+ * 128 rows of A and its own 128 columns of B (rows of W) with plain TMA loads
+ * and holds its 128 rows of the FP32 sums in its TMEM; a folded split keeps
+ * one sum per K segment and adds them in the order 0..S-1, as on one CTA.  By default (bigemm_set_pair_mode 1) it takes such a product
  * when its 256 x 256 tiles number at least twice bigemm_pair_capacity(): a
  * pair's lighter loads then outweigh its costlier start and finish.  A
  * choice of speed only (Tencent AI-infra article, "Tiling"): every output
- * element is the same FP32 accumulation chain over K, 16 k per instruction
- * in ascending order, as on one CTA -- the GPU tests compare the two bit for
- * bit. */
+ * element is the same FP32 accumulation chain over K, 16 k (bf16) or 32 k
+ * (8-bit) per instruction in ascending order, as on one CTA -- the GPU tests
+ * compare the two bit for bit. */
 BIGEMM_API int bigemm_uses_pair(int64_t M, int64_t N, int64_t K, int split_k, int fp8);
 
 /* When the 2-SM kernel runs, for products launched afterwards in this
  * process: 0 never, 1 by the rule above (the default), 2 for every product
- * it can serve (at least 256 rows, unsplit, bf16, 256-wide tiles) -- for
+ * it can serve (at least 256 rows, unsplit or folded, 256-wide tiles) -- for
  * comparisons and tests.  Returns the previous mode, or -1 for a mode
  * outside 0..2 (nothing changes). */
 BIGEMM_API int bigemm_set_pair_mode(int mode);

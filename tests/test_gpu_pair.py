@@ -48,8 +48,9 @@ def product(A, B, mode, bf16_out=False, wt=False, bias=None):
 
 
 def test_rule():
-    """Eligible: unsplit bf16 products of at least 256 rows with 256-wide
-    tiles.  AUTO takes those whose 256 x 256 tiles fill two waves of pairs."""
+    """Eligible: bf16 products of at least 256 rows with 256-wide tiles,
+    unsplit or folded.  AUTO takes those whose 256 x 256 tiles fill two waves
+    of pairs."""
     cap = dig.bigemm_pair_capacity()
     assert cap >= 1
     dig.bigemm_set_pair_mode(dig.PAIR_AUTO)
@@ -58,14 +59,18 @@ def test_rule():
     assert dig.bigemm_uses_pair(4096, n_two_waves - 256, 1024, 1) == (1 if 16 * (cdiv(2 * cap, 16) - 1) >= 2 * cap else 0)
     assert dig.bigemm_uses_pair(8192, 8192, 8192, 1) == 1
     assert dig.bigemm_uses_pair(2048, 2048, 2048, 1) == 0      # 64 tiles: one wave
-    assert dig.bigemm_uses_pair(8192, 8192, 8192, 2) == 0      # split
-    assert dig.bigemm_uses_pair(8192, 8192, 8192, 1, fp8=True) == 0
+    assert dig.bigemm_uses_pair(8192, 8192, 8192, 2) == 1      # a folded split
+    assert dig.bigemm_uses_pair(8192, 8192, 8192, 0) == 1      # the default split, 16, folds
+    assert dig.bigemm_uses_pair(256, 2048, 4096, 8) == 0       # split, not folded (16 tiles)
+    assert dig.bigemm_uses_pair(8192, 8192, 8192, 1, fp8=True) == 1
+    assert dig.bigemm_uses_pair(2048, 2048, 2048, 1, fp8=True) == 0
     assert dig.bigemm_uses_pair(255, 65536, 1024, 1) == 0       # fewer than 256 rows
     dig.bigemm_set_pair_mode(dig.PAIR_ALWAYS)
     assert dig.bigemm_uses_pair(256, 256, 128, 1) == 1
     assert dig.bigemm_uses_pair(255, 256, 128, 1) == 0
     assert dig.bigemm_uses_pair(256, 256, 65536, 1) == 0        # narrow tiles (long K, one tile)
-    assert dig.bigemm_uses_pair(4096, 4096, 4096, 0) == 0       # the default split of K = 4096 is 8
+    assert dig.bigemm_uses_pair(4096, 4096, 4096, 0) == 1       # the default split 8 folds
+    assert dig.bigemm_uses_pair(256, 4096, 4096, 8) == 0        # split, 64 tiles: not folded
     dig.bigemm_set_pair_mode(dig.PAIR_NEVER)
     assert dig.bigemm_uses_pair(8192, 8192, 8192, 1) == 0
     with pytest.raises(ValueError):
@@ -91,6 +96,68 @@ def test_equals_the_1sm_kernel_bit_for_bit(M, N, K, bf16_out):
     assert dig.bigemm_last_launch_count() == 1
     single = product(A, B, dig.PAIR_NEVER, bf16_out)
     assert bits_equal(pair, single)
+
+
+@pytest.mark.parametrize("M,N,K,S", [
+    (4096, 4096, 4096, 8),       # the default split of K = 4096, folded; AUTO takes pairs
+    (1024, 8192, 2048, 4),       # 256 tiles of 128 x 256: folds; 4 x 32 pair tiles
+    (300, 32768, 1000, 3),       # ragged rows and K (16 blocks in segments of 6, 6, 4)
+    (512, 33024, 8192, 16),      # 16 segments; a ragged last tile column (N = 129 x 256)
+])
+@pytest.mark.parametrize("bf16_out", [False, True])
+def test_folded_split_equals_the_1sm_fold_and_the_workspace_path(M, N, K, S, bf16_out):
+    """A folded split on pairs: each CTA's epilogue adds the segment partials
+    in the order 0..S-1 -- the bits of the 1-SM fold and of the two-kernel
+    path (partial kernel + reduction kernel, run explicitly)."""
+    assert dig.bigemm_split_is_folded(M, N, K, S)
+    A = workloads.normal_bf16((M, K), M + S).cuda()
+    B = workloads.normal_bf16((K, N), N + S, 0.05).cuda()
+    dt = torch.bfloat16 if bf16_out else torch.float32
+    dig.bigemm_set_pair_mode(dig.PAIR_ALWAYS)
+    assert dig.bigemm_uses_pair(M, N, K, S) == 1
+    pair = dig.matmul(A, B, out_dtype=dt, split_k=S)
+    assert dig.bigemm_last_launch_count() == 1
+    dig.bigemm_set_pair_mode(dig.PAIR_NEVER)
+    single = dig.matmul(A, B, out_dtype=dt, split_k=S)
+    torch.cuda.synchronize()
+    assert bits_equal(pair, single)
+    s_eff = dig.bigemm_effective_split_k(K, S)
+    need = dig.bigemm_partial_workspace_bytes(M, N, K, S)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    dig.bigemm_run_partial(A, B, M, N, K, K, N, S, ws, need)
+    C = torch.empty((M, N), dtype=dt, device="cuda")
+    dig.bigemm_splitk_reduce(ws, s_eff, M, N, C, N, bf16_out)
+    torch.cuda.synchronize()
+    assert bits_equal(pair, C)
+
+
+@pytest.mark.parametrize("M,N,K,S", [
+    (256, 512, 1024, 1),         # one K block of 128 elements per 128 bytes
+    (300, 600, 992, 1),          # ragged rows, columns and K (not a multiple of 128)
+    (1024, 8192, 4096, 4),       # folded split
+])
+@pytest.mark.parametrize("fa,fb", [(dig.FP8_E4M3, dig.FP8_E4M3), (dig.FP8_E5M2, dig.FP8_E4M3)])
+@pytest.mark.parametrize("bf16_out", [False, True])
+def test_fp8_linear_equals_the_1sm_kernel(M, N, K, S, fa, fb, bf16_out):
+    """8-bit float operands on pairs (kind::f8f6f4, K = 32 per instruction)
+    with the output scale and a bias: the 1-SM kernel's bits."""
+    tda = torch.float8_e4m3fn if fa == dig.FP8_E4M3 else torch.float8_e5m2
+    tdb = torch.float8_e4m3fn if fb == dig.FP8_E4M3 else torch.float8_e5m2
+    g = workloads.generator(M + N + K)
+    A = torch.randn(M, K, generator=g).to(tda).cuda()
+    W = (torch.randn(N, K, generator=g) * 0.05).to(tdb).cuda()
+    b = workloads.normal_bf16((N,), 4).cuda()
+    dt = torch.bfloat16 if bf16_out else torch.float32
+    dig.bigemm_set_pair_mode(dig.PAIR_ALWAYS)
+    assert dig.bigemm_uses_pair(M, N, K, S, fp8=True) == 1
+    pair = dig.linear_fp8(A, W, 0.5, b, out_dtype=dt, split_k=S)
+    dig.bigemm_set_pair_mode(dig.PAIR_NEVER)
+    single = dig.linear_fp8(A, W, 0.5, b, out_dtype=dt, split_k=S)
+    torch.cuda.synchronize()
+    assert bits_equal(pair, single)
+    for r in (0, 255, M - 1):
+        one = dig.linear_fp8(A[r:r + 1].contiguous(), W, 0.5, b, out_dtype=dt, split_k=S)
+        assert bits_equal(one, pair[r:r + 1]), r
 
 
 @pytest.mark.parametrize("M,N,K", [(256, 512, 1024), (520, 6144, 4096), (768, 1280, 1984)])
