@@ -62,8 +62,10 @@ template <int kOut, bool kWt, bool kFp8 = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
     bigemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-    static_assert(kOut == kOutF32 || kOut == kOutBF16, "the 2-SM kernel writes C directly");
+    static_assert(kOut == kOutF32 || kOut == kOutBF16 || kOut == kOutOzaki,
+                  "the 2-SM kernel writes C directly or adds Ozaki slice pairs");
     static_assert(!kFp8 || kWt, "8-bit operands are read K-major only");
+    static_assert(kOut != kOutOzaki || (!kWt && !kFp8), "Ozaki slices: bf16, B [K, N]");
     constexpr int kKB = kFp8 ? 128 : kBK;  // elements per K block (128 bytes per row)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Both CTAs of a pair have the same layout, so both stop here or neither
@@ -124,6 +126,41 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // global memory is touched only after the previous kernel has completed
     grid_dependency_wait();
 
+    // Ozaki scheme: the slice pairs p + q < oz_d this product enumerates (with
+    // Fast Mode's automatic d, the largest per-element d, that of the least
+    // row mass and the least column mass -- as in the 1-SM kernel).
+    int oz_d = 0, oz_pairs = 0;
+    if constexpr (kOut == kOutOzaki) {
+        oz_d = p.oz_d;
+        oz_pairs = p.oz_pairs;
+        if (p.oz_fast) {
+            __shared__ unsigned long long oz_min[2];
+            if (threadIdx.x == 0) {
+                oz_min[0] = ~0ull;
+                oz_min[1] = ~0ull;
+            }
+            __syncthreads();
+            unsigned long long ma = ~0ull, mb = ~0ull;
+            for (int i = threadIdx.x; i < p.M; i += kNumThreads) ma = min(ma, p.oz_ta[i]);
+            for (int j = threadIdx.x; j < p.N; j += kNumThreads) mb = min(mb, p.oz_tb[j]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                ma = min(ma, __shfl_xor_sync(0xffffffffu, ma, o));
+                mb = min(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+            }
+            if (lane == 0) {
+                atomicMin(&oz_min[0], ma);
+                atomicMin(&oz_min[1], mb);
+            }
+            __syncthreads();
+            oz_d = ozaki_fast_d(p, oz_min[0], oz_min[1]);
+            oz_pairs = 0;
+            for (int a = 0; a < p.oz_slices; ++a) oz_pairs += max(0, min(p.oz_slices, oz_d - a));
+        }
+    }
+    // work items: tiles, or (slice pair, tile) items pair-major for Ozaki
+    const int n_work = (kOut == kOutOzaki) ? p.units * oz_pairs : p.units;
+
     if (warp < kEpilogueWarp0) {
         regs_release_to<kFrontRegs>();
         if (warp == 0 && lane == 0) {
@@ -133,10 +170,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
-            for (int u = pair_id; ok && u < p.units; u += n_pairs) {
+            int pa = 0, pb = 0, pk = 0;  // Ozaki: slice pair pk is (pa, pb)
+            for (int L = pair_id; ok && L < n_work; L += n_pairs) {
+                int u = L, a_off = 0, b_off = 0;
+                if constexpr (kOut == kOutOzaki) {
+                    // rows pa * M + m0 of the A slices, rows pb * oz_kpad + k of the B slices
+                    const int pair = L / p.units;
+                    u = L - pair * p.units;
+                    for (; pk < pair; ++pk) ozaki_next_pair(p, oz_d, pa, pb);
+                    a_off = pa * p.M;
+                    b_off = pb * p.oz_kpad;
+                }
                 int mt, nt, seg;
                 unit_coords(p, u, mt, nt, seg);
-                const int m0 = mt * kPairBM + static_cast<int>(rank) * kBM;
+                const int m0 = mt * kPairBM + static_cast<int>(rank) * kBM + a_off;
                 const int nb0 = nt * kBN + static_cast<int>(rank) * (kBN / 2);
                 for (int kb = 0; kb < p.kb_total; ++kb) {
                     if (!wait_bounded<true>(empty_bar(stage), phase ^ 1u, abort_flag, p.status,
@@ -154,7 +201,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
                         for (int c = 0; c < 2; ++c)
                             tma_load_2d_pair(sB + stage * kPairBBytes + c * kBChunkBytes, &tmB, fb,
-                                             nb0 + c * static_cast<int>(kBChunkCols), kb * kBK);
+                                             nb0 + c * static_cast<int>(kBChunkCols), b_off + kb * kBK);
                     }
                     issued_mask |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -171,10 +218,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // waits until CTA 0's instructions have consumed its last load of
             // every stage -- in a run that gave up early, until the bounded wait
             // expires, long after any load has landed.
+            // (after one wait has run out, every load has had its 2 s to land)
+            bool waited_out = false;
             for (int s = 0; s < kPairStages; ++s)
-                if (issued_mask & (1u << s))
-                    wait_bounded<true>(rank == 0 ? full_bar(s) : empty_bar(s), (issued_parity >> s) & 1u,
-                                       abort_flag, p.status, kErrWaitDrain, /*honour_abort=*/false);
+                if (!waited_out && (issued_mask & (1u << s)))
+                    waited_out = !wait_bounded<true>(rank == 0 ? full_bar(s) : empty_bar(s),
+                                                     (issued_parity >> s) & 1u, abort_flag, p.status,
+                                                     kErrWaitDrain, /*honour_abort=*/false);
         } else if (warp == 1 && lane == 0 && rank == 0) {
             // ------------------------------------------------- MMA issuer --
             const uint32_t idesc = kFp8 ? p.idesc_fp8 : (kWt ? kPairIdescWt : kPairIdescBN);
@@ -183,7 +233,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             int t = 0;
             bool ok = true;
             const int nseg = p.fold ? p.splits : 1;
-            for (int u = pair_id; ok && u < p.units; u += n_pairs) {
+            for (int u = pair_id; ok && u < n_work; u += n_pairs) {
               for (int sg = 0; ok && sg < nseg; ++sg, ++t) {
                 // one accumulator per K segment (the whole of K when unsplit)
                 const int kb0 = p.fold ? sg * p.kb_per_split : 0;
@@ -254,7 +304,80 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (rank == 0) mbar_arrive(tempty_bar(acc));
             else mbar_arrive_remote(map_shared_rank(tempty_bar(acc), 0u));
         };
-        if (p.fold) {
+        if constexpr (kOut == kOutOzaki) {
+            // ---- Ozaki scheme, as in the 1-SM kernel: for the item's slice
+            // pair (pa, pb), C[row][col] += 2^e * P (P the exact FP32 slice-pair
+            // product, e = c_a^(pa)[row] + c_b^(pb)[col]), the first pair
+            // starting the sum at +0.0.  This CTA's half of a pair tile is a
+            // 128 x 256 tile of C with its own count: a warp adds pair k into
+            // its 32 rows once the count shows that the 8 warps of that half
+            // (whichever pair of CTAs ran it) have added pair k - 1, then
+            // raises it.  A half with no rows neither waits nor counts.
+            double* C = static_cast<double*>(p.out);
+            const int step = p.oz_beta + 1;
+            const int tiles128 = ((p.M + kBM - 1) / kBM) * p.n_tiles;
+            int* const grid_abort = p.oz_count + tiles128;  // the launch's abort word
+            int pa = 0, pb = 0, pk = 0;
+            for (int L = pair_id; L < n_work; L += n_pairs, ++t) {
+                const int pair = L / p.units, u = L - pair * p.units;
+                for (; pk < pair; ++pk) ozaki_next_pair(p, oz_d, pa, pb);
+                int mt, nt, seg;
+                unit_coords(p, u, mt, nt, seg);
+                const int half = 2 * mt + static_cast<int>(rank);
+                const bool has_rows = half * kBM < p.M;
+                int* const count = p.oz_count + half * p.n_tiles + nt;
+                const int m0 = half * kBM + q * 32, n0 = nt * kBN;
+                const int row = m0 + lane;
+                const bool row_ok = row < p.M;
+                const int acc = t % kPairAccStages;
+                const uint32_t acc_phase = static_cast<uint32_t>(t / kPairAccStages) & 1u;
+                if (!wait_bounded<true>(tfull_bar(acc), acc_phase, abort_flag, p.status, kErrWaitEpilogue))
+                    break;
+                tc_fence_after();
+                if (pair > 0 && has_rows) {
+                    bool in_order = true;
+                    if (lane == 0)
+                        in_order = wait_count_bounded(count, pair * kEpilogueWarps, abort_flag, grid_abort,
+                                                      p.status);
+                    in_order = __shfl_sync(0xffffffffu, in_order ? 1 : 0, 0) != 0;
+                    if (!in_order) {
+                        release_acc(acc);
+                        break;
+                    }
+                    // every lane acquires the count itself (its loads of C come
+                    // after the stores of the previous pair)
+                    (void)ld_acquire_gpu(count);
+                }
+                if (m0 < p.M) {
+                    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                           static_cast<uint32_t>(acc * kBN);
+                    const int e_pair = row_ok ? (p.oz_ca[row] - pa * step) - pb * step : 0;
+                    OzakiFastRow fast = ozaki_fast_row(p.oz_fast ? p.oz_tb : nullptr,
+                                                       (p.oz_fast && row_ok) ? p.oz_ta[row] : 0ull,
+                                                       (pa + pb) * step, p.oz_need0);
+#pragma unroll 1
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(tbase + (h * 4 + i) * 32, r);
+                        tmem_ld_wait();
+                        if (i == 3) release_acc(acc);  // the accumulator is no longer needed
+                        const int col0 = n0 + (h * 4 + i) * 32;
+                        if (p.oz_fast) fast.tb = p.oz_tb + col0;  // 256-byte aligned: col0 % 32 == 0
+                        if (row_ok && col0 < p.N)
+                            ozaki_accumulate_block(C + static_cast<int64_t>(row) * p.ld_out + col0, p.oz_cb + col0,
+                                                   min(32, p.N - col0), e_pair, r, pair == 0, fast);
+                    }
+                } else {
+                    release_acc(acc);
+                }
+                if (has_rows) {
+                    // this warp's part of the pair is in C: count it
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) atomicAdd(count, 1);
+                }
+            }
+        } else if (p.fold) {
             // ---- folded tiles: sum = w_0, then sum = sum + w_s for s = 1 ..
             // splits-1 (FP32, round to nearest even) in 128 registers, then the
             // scale, the bias and the stores -- the 1-SM fold's arithmetic in its
@@ -314,37 +437,39 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
             }
         }
-        for (int u = pair_id; !p.fold && u < p.units; u += n_pairs, ++t) {
-            int mt, nt, seg;
-            unit_coords(p, u, mt, nt, seg);
-            const int m0 = mt * kPairBM + static_cast<int>(rank) * kBM + q * 32, n0 = nt * kBN;
-            const int nchunks = min(h * 4 + 4, min(kBN / 32, (p.N - n0 + 31) / 32));
-            const int acc = t % kPairAccStages;
-            const uint32_t acc_phase = static_cast<uint32_t>(t / kPairAccStages) & 1u;
-            if (!wait_bounded<true>(tfull_bar(acc), acc_phase, abort_flag, p.status, kErrWaitEpilogue))
-                break;
-            tc_fence_after();
-            bool released = false;
-            if (m0 < p.M) {
-                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                       static_cast<uint32_t>(acc * kBN);
+        if constexpr (kOut != kOutOzaki) {
+          for (int u = pair_id; !p.fold && u < p.units; u += n_pairs, ++t) {
+              int mt, nt, seg;
+              unit_coords(p, u, mt, nt, seg);
+              const int m0 = mt * kPairBM + static_cast<int>(rank) * kBM + q * 32, n0 = nt * kBN;
+              const int nchunks = min(h * 4 + 4, min(kBN / 32, (p.N - n0 + 31) / 32));
+              const int acc = t % kPairAccStages;
+              const uint32_t acc_phase = static_cast<uint32_t>(t / kPairAccStages) & 1u;
+              if (!wait_bounded<true>(tfull_bar(acc), acc_phase, abort_flag, p.status, kErrWaitEpilogue))
+                  break;
+              tc_fence_after();
+              bool released = false;
+              if (m0 < p.M) {
+                  const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                         static_cast<uint32_t>(acc * kBN);
 #pragma unroll 1
-                for (int c0 = h * 4; c0 < nchunks; c0 += batch) {
-                    const int nb = min(batch, nchunks - c0);
-                    uint32_t r[kMaxBatch * 32];
-                    if (batch == 4) tmem_ld_32x32b_x128(tbase + c0 * 32, r);
-                    else if (batch == 2) tmem_ld_32x32b_x64(tbase + c0 * 32, r);
-                    else tmem_ld_32x32b_x32(tbase + c0 * 32, *reinterpret_cast<uint32_t(*)[32]>(r));
-                    tmem_ld_wait();
-                    if (c0 + nb >= nchunks) {
-                        release_acc(acc);
-                        released = true;
-                    }
-                    emit_blocks<kOut, kMaxBatch>(p, &tmC, r, nb, c0, n0, m0, seg, lane, my_boxes, batch,
-                                                 slots, nbat);
-                }
-            }
-            if (!released) release_acc(acc);
+                  for (int c0 = h * 4; c0 < nchunks; c0 += batch) {
+                      const int nb = min(batch, nchunks - c0);
+                      uint32_t r[kMaxBatch * 32];
+                      if (batch == 4) tmem_ld_32x32b_x128(tbase + c0 * 32, r);
+                      else if (batch == 2) tmem_ld_32x32b_x64(tbase + c0 * 32, r);
+                      else tmem_ld_32x32b_x32(tbase + c0 * 32, *reinterpret_cast<uint32_t(*)[32]>(r));
+                      tmem_ld_wait();
+                      if (c0 + nb >= nchunks) {
+                          release_acc(acc);
+                          released = true;
+                      }
+                      emit_blocks<kOut, kMaxBatch>(p, &tmC, r, nb, c0, n0, m0, seg, lane, my_boxes, batch,
+                                                   slots, nbat);
+                  }
+              }
+              if (!released) release_acc(acc);
+          }
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();

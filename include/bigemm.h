@@ -437,6 +437,10 @@ BIGEMM_API bigemm_status bigemm_ozaki_split(const double *X, int64_t rows, int64
  * the pairs of one tile may run on different SMs at once; each element of C
  * still takes its pairs' terms one after another in the fixed pair order (a
  * tile's epilogue waits, bounded, for its count to show the previous pair).
+ * With at least 256 rows and K <= 4096 (and enough items for two waves) the
+ * products run on CTA pairs (256 x 256 tiles, tcgen05.mma.cta_group::2; see
+ * bigemm_uses_pair and bigemm_set_pair_mode), each CTA adding its 128 rows
+ * under its 128 x 256 tile's count -- the same additions in the same order.
  * The kernel is a cooperative launch: CUDA starts it only when all of its
  * CTAs (at most one per SM) can be resident together, so those waits end
  * whatever else runs on the device, concurrent Ozaki products included.

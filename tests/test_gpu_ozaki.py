@@ -205,6 +205,32 @@ def test_fast_mode_meets_the_pages_bound_on_normal_data():
         assert err <= 2 * np.sqrt(K) * 2.0 ** -53 * scale[i, j], (i, j, err / scale[i, j])
 
 
+@pytest.mark.parametrize("M,N,K,slices,d", [
+    (257, 300, 1000, 0, 0),      # two pair tile rows, the second with one row
+    (300, 384, 777, 0, 0),       # CTA 1 of the second tile row has no rows
+    (512, 768, 1024, 4, 3),      # Fast Mode, fixed d
+    (256, 512, 4096, 0, -1),     # Fast Mode, automatic d
+])
+def test_pair_kernel_equals_the_1sm_kernel_and_the_oracle(M, N, K, slices, d):
+    """The slice-pair products on CTA pairs (256 x 256 tiles, each CTA adding
+    its 128 rows under its own 128 x 256 tile's count): the bits of the 1-SM
+    kernel and of the oracle."""
+    A = wide((M, K), 2 * M + K, 10)
+    B = wide((K, N), 2 * N + K, 10)
+    prev = dig.bigemm_set_pair_mode(dig.PAIR_ALWAYS)
+    try:
+        pair = run_dgemm(A, B, slices, d)
+        dig.bigemm_set_pair_mode(dig.PAIR_NEVER)
+        single = run_dgemm(A, B, slices, d)
+    finally:
+        dig.bigemm_set_pair_mode(prev)
+    assert np.array_equal(pair.view(np.int64), single.view(np.int64))
+    rho = oracle.ozaki_rho(K)
+    s = slices or oracle.ozaki_default_slices(rho)
+    Cref, _ = oracle.ozaki_gemm(A, B, rho=rho, slices=s, d=d if d < 0 else (d or s))
+    assert np.array_equal(pair.view(np.int64), Cref.view(np.int64))
+
+
 def test_dgemm_accuracy_against_exact_products():
     """1024^3 normal inputs: rows computed by the oracle match exactly, and
     the error against exact rational products on a sample is binary64's."""

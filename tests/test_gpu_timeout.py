@@ -42,14 +42,16 @@ def test_expired_wait_is_reported_and_the_context_survives(builtin_scratch):
     assert dig.bigemm_device_status(reset=False) == 0
 
 
-def test_ozaki_order_wait_gives_up_once_for_the_whole_grid(builtin_scratch):
+@pytest.mark.parametrize("pair_mode", [None, "always"])
+def test_ozaki_order_wait_gives_up_once_for_the_whole_grid(builtin_scratch, pair_mode):
     """The Ozaki kernel's epilogues wait for the previous slice pair of their
     tile, possibly on another CTA.  bigemm_selftest_ozaki_order_timeout starts
     every tile's count far below zero, so no such wait is ever met: the first
     to give up (after 2 s) sets the launch's abort word and every other CTA
     leaves at once -- one 2 s limit for the grid, not one per CTA or per pair
     in turn.  The error word reports the timeout, and a later product is
-    still right."""
+    still right.  Run on single CTAs (the default rule at this size) and on CTA
+    pairs, whose drains also end after one limit."""
     dig.load()
     assert dig.bigemm_device_status(reset=True) == 0
     g = workloads.generator(5)
@@ -58,10 +60,14 @@ def test_ozaki_order_wait_gives_up_once_for_the_whole_grid(builtin_scratch):
     before = dig.ozaki_matmul(A, B)
     torch.cuda.synchronize()
 
-    t0 = time.time()
-    assert dig.bigemm_selftest_ozaki_order_timeout() == 0
-    st = dig.bigemm_device_status(reset=True)          # synchronises
-    elapsed = time.time() - t0
+    prev = dig.bigemm_set_pair_mode(dig.PAIR_ALWAYS if pair_mode else dig.PAIR_AUTO)
+    try:
+        t0 = time.time()
+        assert dig.bigemm_selftest_ozaki_order_timeout() == 0
+        st = dig.bigemm_device_status(reset=True)      # synchronises
+        elapsed = time.time() - t0
+    finally:
+        dig.bigemm_set_pair_mode(prev)
     assert st == ERR_TIMEOUT, st
     assert 1.5 < elapsed < 8.0, elapsed                # one limit for the grid
     assert dig.bigemm_device_status(reset=False) == 0
