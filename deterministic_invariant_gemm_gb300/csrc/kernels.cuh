@@ -749,6 +749,88 @@ __device__ __forceinline__ void ozaki_accumulate_block(double* crow, const int* 
     }
 }
 
+// ozaki_accumulate_block for a warp's full 32 x 32 block (32 columns inside
+// N), with the loads and stores of C coalesced through the warp's 4 KiB of
+// shared memory: per half of 16 columns, the warp reads the block's rows four
+// at a time (8 lanes x 16 bytes per row: 512 contiguous-per-row bytes per
+// instruction) into buf, each lane then takes its own row from buf (16-byte
+// chunk c of row i at chunk c ^ (i % 8): no bank conflict), adds exactly as
+// ozaki_accumulate_block does, puts the row back, and the warp writes the
+// rows out four at a time.  rows: the block's rows inside C (lanes past it
+// compute but nothing of theirs is read or written).  Every lane calls it.
+__device__ __forceinline__ void ozaki_accumulate_block_staged(double* crow0, int64_t ldc, int rows, const int* cb,
+                                                              int e_pair, const uint32_t (&r)[32], bool first,
+                                                              const OzakiFastRow& fast, double* buf, int lane) {
+    const int quarter = lane >> 3, chunk = lane & 7;
+    const auto slot = [](int i, int c) { return i * 16 + ((c ^ (i & 7)) << 1); };  // chunk c of row i
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {  // unrolled: r is indexed by constants
+        double* const ch = crow0 + hb * 16;
+        if (!first) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int i = 4 * k + quarter;
+                const double2 v = i < rows ? *reinterpret_cast<const double2*>(ch + static_cast<int64_t>(i) * ldc + 2 * chunk)
+                                           : make_double2(0.0, 0.0);
+                *reinterpret_cast<double2*>(buf + slot(i, chunk)) = v;
+            }
+            __syncwarp();
+        }
+        int e[16];
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) {
+            const int4 v = __ldg(reinterpret_cast<const int4*>(cb + hb * 16 + j));
+            e[j] = e_pair + v.x;
+            e[j + 1] = e_pair + v.y;
+            e[j + 2] = e_pair + v.z;
+            e[j + 3] = e_pair + v.w;
+        }
+        double c[16];
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+            if (first) {
+                c[j] = 0.0;
+                c[j + 1] = 0.0;
+            } else {
+                const double2 v = *reinterpret_cast<const double2*>(buf + slot(lane, j >> 1));
+                c[j] = v.x;
+                c[j + 1] = v.y;
+            }
+        }
+        int lo = e[0], hi = e[0];
+#pragma unroll
+        for (int j = 1; j < 16; ++j) {
+            lo = min(lo, e[j]);
+            hi = max(hi, e[j]);
+        }
+        // the per-element choice of ozaki_accumulate_block (Fast Mode: the
+        // column masses from hb * 16; an element that does not take the pair
+        // keeps its C)
+        const bool all = fast.tb == nullptr || fast.lim == ~0ull;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const uint32_t pbits = r[hb * 16 + j];
+            bool takes = all;
+            if (!all) takes = !fast.none && __ldg(fast.tb + hb * 16 + j) <= fast.lim;
+            if (takes)
+                c[j] = (lo >= -1006 && hi <= 1001) ? __dadd_rn(c[j], ozaki_scaled(pbits, e[j]))
+                                                   : ozaki_term(c[j], pbits, e[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; j += 2)
+            *reinterpret_cast<double2*>(buf + slot(lane, j >> 1)) = make_double2(c[j], c[j + 1]);
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = 4 * k + quarter;
+            if (i < rows)
+                *reinterpret_cast<double2*>(ch + static_cast<int64_t>(i) * ldc + 2 * chunk) =
+                    *reinterpret_cast<const double2*>(buf + slot(i, chunk));
+        }
+        __syncwarp();  // buf is refilled by the next half
+    }
+}
+
 // kWt: the second operand is the weight matrix W [N, K] (K-major); otherwise
 // B [K, N] (N-major).  Both products run the same K = 16 instruction sequence.
 // kFp8: 8-bit float operands (both K-major, kWt): a K block is 128 elements,
@@ -1188,7 +1270,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             }
                             const int col0 = n0 + (h * 4 + i) * 32;
                             if (p.oz_fast) fast.tb = p.oz_tb + col0;  // 256-byte aligned: col0 % 32 == 0
-                            if (row_ok && col0 < p.N)
+                            if (col0 + 32 <= p.N)
+                                ozaki_accumulate_block_staged(
+                                    C + static_cast<int64_t>(m0) * p.ld_out + col0, p.ld_out, min(32, p.M - m0),
+                                    p.oz_cb + col0, e_pair, r, pair == 0, fast,
+                                    reinterpret_cast<double*>(gbase + (sOut - base)) + (q * 2 + h) * 512, lane);
+                            else if (row_ok && col0 < p.N)
                                 ozaki_accumulate_block(C + static_cast<int64_t>(row) * p.ld_out + col0,
                                                        p.oz_cb + col0, min(32, p.N - col0), e_pair, r,
                                                        pair == 0, fast);

@@ -363,7 +363,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         if (i == 3) release_acc(acc);  // the accumulator is no longer needed
                         const int col0 = n0 + (h * 4 + i) * 32;
                         if (p.oz_fast) fast.tb = p.oz_tb + col0;  // 256-byte aligned: col0 % 32 == 0
-                        if (row_ok && col0 < p.N)
+                        if (col0 + 32 <= p.N)
+                            ozaki_accumulate_block_staged(
+                                C + static_cast<int64_t>(m0) * p.ld_out + col0, p.ld_out, min(32, p.M - m0),
+                                p.oz_cb + col0, e_pair, r, pair == 0, fast,
+                                reinterpret_cast<double*>(smem_raw + (sOut - base)) + (q * 2 + h) * 512, lane);
+                        else if (row_ok && col0 < p.N)
                             ozaki_accumulate_block(C + static_cast<int64_t>(row) * p.ld_out + col0, p.oz_cb + col0,
                                                    min(32, p.N - col0), e_pair, r, pair == 0, fast);
                     }
