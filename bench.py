@@ -261,7 +261,7 @@ def kernel_source_hash() -> str:
     kernel, so it does not make an ncu capture stale."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("kernels.cuh", "ptx.cuh", "ozaki.cuh", "skinny.cuh", "bigemm.cu"):
+    for f in ("kernels.cuh", "ptx.cuh", "ozaki.cuh", "skinny.cuh", "pair.cuh", "bigemm.cu"):
         with open(os.path.join(ROOT, "deterministic_invariant_gemm_gb300", "csrc", f),
                   encoding="utf-8") as fh:
             h.update(code_only(fh.read()).encode("utf-8"))
@@ -759,14 +759,17 @@ def run_single(name, args, world, rank, dev, peaks, peak_src):
         tens = dig.bigemm_ozaki_pairs(s_, s_) * flops
         peak = peaks["bf16_tflops"]
         line["config"]["slices"] = s_
-        line["roofline"] = {"kernel": "ozaki split kernels + bigemm_tc_kernel<kOutOzaki>",
+        line["roofline"] = {"kernel": "ozaki split kernels + slice-pair kernel (%s)" % (
+                                "bigemm_pair_kernel<kOutOzaki>" if (M >= 256 and K <= 4096)
+                                else "bigemm_tc_kernel<kOutOzaki>"),
                             "bound": "tensor", "achieved": round(tens / per / 1e12, 1), "peak": peak,
                             "peak_source": peak_src, "unit": "TFLOP/s",
                             "frac": round(tens / per / 1e12 / peak, 4), "traffic": None}
     elif bound in ("tensor", "tensor_fp8"):
         # an 8-bit product takes the measured bf16 peak times the nominal ratio 2
         peak = peaks["bf16_tflops"] * (2.0 if bound == "tensor_fp8" else 1.0)
-        line["roofline"] = {"kernel": "bigemm_tc_kernel", "bound": "tensor",
+        line["roofline"] = {"kernel": "bigemm_pair_kernel" if dig.bigemm_uses_pair(M, N, K, S, bound == "tensor_fp8")
+                            else "bigemm_tc_kernel", "bound": "tensor",
                             "achieved": round(flops / per / 1e12, 1), "peak": peak,
                             "peak_source": peak_src, "unit": "TFLOP/s",
                             "frac": round(flops / per / 1e12 / peak, 4), "traffic": None}
@@ -900,7 +903,8 @@ def run_other_workloads(dev, peaks) -> dict:
         out[name] = {"tflops": round(tflops, 2), "frac_of_bf16_peak": round(tflops / bf16_peak, 4),
                      "ms": round(secs * 1e3 / iters, 4), "split_k": S,
                      "out": "bf16" if bf16 else "fp32", "input_copies": copies,
-                     "launches": dig.bigemm_last_launch_count(), "clocks": clocks}
+                     "launches": dig.bigemm_last_launch_count(), "clocks": clocks,
+                     "cta_pairs": bool(dig.bigemm_uses_pair(M, N, K, S))}
         del AB, C, ws
         torch.cuda.empty_cache()
     # The small product (64 x 256 x 512, split_k 1, FP32 out): a latency case
@@ -965,7 +969,8 @@ def run_other_workloads(dev, peaks) -> dict:
         out[name] = {"tflops": round(tflops, 2), "frac_of_peak": round(tflops / peak, 4),
                      "peak": peak, "peak_note": "measured bf16 x 2 (nominal fp8/bf16 ratio)"
                      if fp8 else "measured bf16", "ms": round(secs * 1e3 / iters, 4),
-                     "out": "bf16", "inputs": "fp8 e4m3" if fp8 else "bf16"}
+                     "out": "bf16", "inputs": "fp8 e4m3" if fp8 else "bf16",
+                     "cta_pairs": bool(dig.bigemm_uses_pair(n, n, n, 1, fp8))}
         del x, w, C
         torch.cuda.empty_cache()
     return out
@@ -1102,11 +1107,13 @@ def compact_workloads(detail: dict, peaks: dict, peak_src: str):
               "square_8192_split16_folded", "prefill_1024x4096x4096_split8_folded"):
         d = detail.get(k)
         if d:
-            out[k] = {"tflops": d["tflops"], "frac": d["frac_of_bf16_peak"], "ms": d["ms"]}
+            out[k] = {"tflops": d["tflops"], "frac": d["frac_of_bf16_peak"], "ms": d["ms"],
+                      "pairs": d.get("cta_pairs", False)}
     for k in ("linear_bf16_8192", "linear_fp8_e4m3_16384"):
         d = detail.get(k)
         if d:
-            out[k] = {"tflops": d["tflops"], "frac": d["frac_of_peak"], "ms": d["ms"]}
+            out[k] = {"tflops": d["tflops"], "frac": d["frac_of_peak"], "ms": d["ms"],
+                      "pairs": d.get("cta_pairs", False)}
     lk = detail.get("longk_256x256x65536")
     if lk:
         out["longk_256x256x65536"] = {
@@ -1135,7 +1142,9 @@ def compact_workloads(detail: dict, peaks: dict, peak_src: str):
     big = detail.get("large_16384_bf16out")
     roof = None
     if big:
-        roof = {"kernel": "bigemm_tc_kernel<kOutBF16> (16384^3, bf16 out)", "bound": "tensor",
+        kname = ("bigemm_pair_kernel<kOutBF16> (16384^3 on CTA pairs, bf16 out)" if big.get("cta_pairs")
+                 else "bigemm_tc_kernel<kOutBF16> (16384^3, bf16 out)")
+        roof = {"kernel": kname, "bound": "tensor",
                 "achieved": big["tflops"], "peak": peaks["bf16_tflops"], "peak_source": peak_src,
                 "peak_kind": "burst (the product is timed alone)", "unit": "TFLOP/s",
                 "frac": round(big["tflops"] / peaks["bf16_tflops"], 4), "traffic": None,
