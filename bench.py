@@ -1164,6 +1164,10 @@ def main():
                     help="skip the other shapes, e2e and the CPU baseline")
     ap.add_argument("--workload", default="decode", choices=("decode",) + tuple(SINGLE),
                     help="decode (the headline step) or one of the other workload shapes")
+    ap.add_argument("--pair-mode", default="auto", choices=("never", "auto", "always"),
+                    help="when products run on CTA pairs (the 2-SM kernel): the library's rule "
+                         "(auto, the default), never, or whenever they can -- for comparisons and "
+                         "profiles; the arithmetic is the same either way")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -1180,6 +1184,9 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
+    if args.pair_mode != "auto":
+        import deterministic_invariant_gemm_gb300 as dig
+        dig.bigemm_set_pair_mode({"never": dig.PAIR_NEVER, "always": dig.PAIR_ALWAYS}[args.pair_mode])
     if args.workload != "decode":
         run_single(args.workload, args, world, rank, dev, peaks, peak_src)
         if world > 1:

@@ -749,6 +749,12 @@ __device__ __forceinline__ void ozaki_accumulate_block(double* crow, const int* 
     }
 }
 
+// C rows at least this many elements apart take the staged form below: at
+// 8192^3 (rows 64 KiB apart) it took 31.9 against 33.7 ms; at 4096^3 (32
+// KiB) it was no faster and read 17.3 against 9.6 GB from DRAM, so narrower
+// rows keep the direct per-lane accesses.
+constexpr int64_t kOzStagedMinLd = 8192;
+
 // ozaki_accumulate_block for a warp's full 32 x 32 block (32 columns inside
 // N), with the loads and stores of C coalesced through the warp's 4 KiB of
 // shared memory: per half of 16 columns, the warp reads the block's rows four
@@ -1270,7 +1276,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             }
                             const int col0 = n0 + (h * 4 + i) * 32;
                             if (p.oz_fast) fast.tb = p.oz_tb + col0;  // 256-byte aligned: col0 % 32 == 0
-                            if (col0 + 32 <= p.N)
+                            if (col0 + 32 <= p.N && p.ld_out >= kOzStagedMinLd)
                                 ozaki_accumulate_block_staged(
                                     C + static_cast<int64_t>(m0) * p.ld_out + col0, p.ld_out, min(32, p.M - m0),
                                     p.oz_cb + col0, e_pair, r, pair == 0, fast,

@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         if (i == 3) release_acc(acc);  // the accumulator is no longer needed
                         const int col0 = n0 + (h * 4 + i) * 32;
                         if (p.oz_fast) fast.tb = p.oz_tb + col0;  // 256-byte aligned: col0 % 32 == 0
-                        if (col0 + 32 <= p.N)
+                        if (col0 + 32 <= p.N && p.ld_out >= kOzStagedMinLd)
                             ozaki_accumulate_block_staged(
                                 C + static_cast<int64_t>(m0) * p.ld_out + col0, p.ld_out, min(32, p.M - m0),
                                 p.oz_cb + col0, e_pair, r, pair == 0, fast,

@@ -231,6 +231,26 @@ def test_pair_kernel_equals_the_1sm_kernel_and_the_oracle(M, N, K, slices, d):
     assert np.array_equal(pair.view(np.int64), Cref.view(np.int64))
 
 
+@pytest.mark.parametrize("pair_mode", ["never", "always"])
+def test_staged_epilogue_rows_far_apart_equal_the_oracle(pair_mode):
+    """C rows at least 8192 elements apart take the epilogue that reads and
+    writes C through shared memory: a padded ldc puts a small, ragged product
+    on it (single CTAs and CTA pairs); the bits are the oracle's."""
+    M, N, K = 300, 320, 500
+    A = wide((M, K), 97, 12)
+    B = wide((K, N), 98, 12)
+    prev = dig.bigemm_set_pair_mode(dig.PAIR_NEVER if pair_mode == "never" else dig.PAIR_ALWAYS)
+    try:
+        C = run_dgemm(A, B, 0, 0, ldc_pad=8192 - N)
+        Cf = run_dgemm(A, B, 0, -1, ldc_pad=8192 - N)
+    finally:
+        dig.bigemm_set_pair_mode(prev)
+    Cref, _ = oracle.ozaki_gemm(A, B)
+    assert np.array_equal(C.view(np.int64), Cref.view(np.int64))
+    Cref_f, _ = oracle.ozaki_gemm(A, B, d=-1)
+    assert np.array_equal(Cf.view(np.int64), Cref_f.view(np.int64))
+
+
 def test_dgemm_accuracy_against_exact_products():
     """1024^3 normal inputs: rows computed by the oracle match exactly, and
     the error against exact rational products on a sample is binary64's."""
