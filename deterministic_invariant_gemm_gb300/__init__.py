@@ -75,6 +75,7 @@ EXPORTED_SYMBOLS = (
     "bigemm_fp8_effective_split_k", "bigemm_fp8_workspace_bytes", "bigemm_linear_fp8",
     "bigemm_split_is_folded", "bigemm_split_path", "bigemm_tile_n", "bigemm_cluster_capacity",
     "bigemm_uses_pair", "bigemm_set_pair_mode", "bigemm_pair_capacity",
+    "bigemm_fp8_kn_workspace_bytes", "bigemm_run_fp8",
     "bigemm_ozaki_rho", "bigemm_ozaki_default_slices", "bigemm_ozaki_pairs",
     "bigemm_ozaki_workspace_bytes", "bigemm_ozaki_split", "bigemm_ozaki_dgemm",
     "bigemm_selftest_timeout", "bigemm_selftest_ozaki_order_timeout",
@@ -123,6 +124,9 @@ def load():
         "bigemm_uses_pair": ([i64, i64, i64, i32, i32], i32),
         "bigemm_set_pair_mode": ([i32], i32),
         "bigemm_pair_capacity": ([], i32),
+        "bigemm_fp8_kn_workspace_bytes": ([i64, i64, i64, i32], sz),
+        "bigemm_run_fp8": ([vp, vp, i32, i32, ctypes.c_float, vp, vp, i64, i64, i64, i64, i64,
+                            i64, i32, i32, vp, sz, vp], i32),
         "bigemm_ozaki_rho": ([i64], i32),
         "bigemm_selftest_timeout": ([vp], i32),
         "bigemm_selftest_ozaki_order_timeout": ([vp], i32),
@@ -493,6 +497,57 @@ def linear_fp8(x, weight, scale=1.0, bias=None, out_dtype=None, split_k: int = 1
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     bigemm_linear_fp8(x, weight, fmts[x.dtype], fmts[weight.dtype], scale, bias, out, M, N, K, lda,
                       ldw, ldc, split_k, bf16, workspace, wbytes, stream)
+    return out
+
+
+def bigemm_fp8_kn_workspace_bytes(M: int, N: int, K: int, split_k: int) -> int:
+    return int(load().bigemm_fp8_kn_workspace_bytes(M, N, K, split_k))
+
+
+def bigemm_run_fp8(A, B, fmt_a, fmt_b, scale, bias, C, M, N, K, lda, ldb, ldc, split_k, c_is_bf16,
+                   workspace=None, workspace_bytes=0, stream=None, check=True) -> int:
+    st = load().bigemm_run_fp8(_ptr(A), _ptr(B), int(fmt_a), int(fmt_b), float(scale), _ptr(bias),
+                               _ptr(C), M, N, K, lda, ldb, ldc, split_k, int(bool(c_is_bf16)),
+                               _ptr(workspace), workspace_bytes, _stream(stream))
+    if check:
+        _check(st, "bigemm_run_fp8")
+    return st
+
+
+def matmul_fp8(a, b, scale=1.0, bias=None, out_dtype=None, split_k: int = 1, out=None,
+               workspace=None, stream=None):
+    """y = scale * (a @ b) + bias for 8-bit float CUDA tensors a [M, K] and b
+    [K, N] (torch.float8_e4m3fn or torch.float8_e5m2, each), through
+    bigemm_run_fp8 (b is copied transposed into the workspace, then the
+    product is bigemm_linear_fp8's with weight = b^T: the same bits)."""
+    import torch
+    fmts = {torch.float8_e4m3fn: FP8_E4M3, torch.float8_e5m2: FP8_E5M2}
+    if a.dtype not in fmts or b.dtype not in fmts:
+        raise TypeError("a and b must be float8_e4m3fn or float8_e5m2")
+    if bias is not None and (bias.dtype != torch.bfloat16 or bias.dim() != 1 or bias.stride(0) != 1):
+        raise TypeError("bias must be a contiguous bfloat16 vector")
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[0]:
+        raise ValueError("shapes do not compose: %s x %s" % (tuple(a.shape), tuple(b.shape)))
+    if a.stride(1) != 1 or b.stride(1) != 1:
+        raise ValueError("a and b need unit column stride (row-major)")
+    out_dtype = torch.float32 if out_dtype is None else out_dtype
+    M, K = a.shape
+    N = b.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    lda = a.stride(0) if M > 1 else max(K, 16 * ((K + 15) // 16))
+    ldb = b.stride(0) if K > 1 else max(N, 16 * ((N + 15) // 16))
+    ldc = out.stride(0) if M > 1 else max(N, 8 * ((N + 7) // 8))
+    bf16 = out_dtype == torch.bfloat16
+    if lda % 16 or ldb % 16 or ldc % (8 if bf16 else 4):
+        raise ValueError("row strides must be multiples of 16 bytes for a and b and of %d "
+                         "elements for the output; got %d, %d, %d" % (8 if bf16 else 4, lda, ldb, ldc))
+    need = bigemm_fp8_kn_workspace_bytes(M, N, K, split_k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=a.device)
+    wbytes = workspace.numel() * workspace.element_size()
+    bigemm_run_fp8(a, b, fmts[a.dtype], fmts[b.dtype], scale, bias, out, M, N, K, lda, ldb, ldc,
+                   split_k, bf16, workspace, wbytes, stream)
     return out
 
 

@@ -1185,6 +1185,47 @@ bigemm_status bigemm_linear_fp8(const void* A, const void* W, int fmt_a, int fmt
                     fmt_a, fmt_w, scale);
 }
 
+size_t bigemm_fp8_kn_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {
+    if (M < 0 || N < 0 || K < 0 || effective_split(K, split_k, nullptr, 128) == 0) return 0;
+    const size_t bt = static_cast<size_t>(N) * static_cast<size_t>(round_up(K > 0 ? K : 1, 16));
+    return (bt + 255) / 256 * 256 + bigemm_fp8_workspace_bytes(M, N, K, split_k);
+}
+
+bigemm_status bigemm_run_fp8(const void* A, const void* B, int fmt_a, int fmt_b, float scale, const void* bias,
+                             void* C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                             int split_k, int c_is_bf16, void* workspace, size_t workspace_bytes,
+                             bigemm_stream stream) {
+    g_last_launches = 0;
+    if ((fmt_a != BIGEMM_FP8_E4M3 && fmt_a != BIGEMM_FP8_E5M2) ||
+        (fmt_b != BIGEMM_FP8_E4M3 && fmt_b != BIGEMM_FP8_E5M2) || !(scale == scale))
+        return BIGEMM_ERR_ARG;
+    if (M < 0 || N < 0 || K < 0 || M > INT_MAX || N > INT_MAX || K > INT_MAX) return BIGEMM_ERR_ARG;
+    if (effective_split(K, split_k, nullptr, 128) == 0) return BIGEMM_ERR_ARG;
+    if (K > 0 && (B == nullptr || ldb < N)) return BIGEMM_ERR_ARG;
+    if (K > 0 && (!aligned16(B) || ldb % 16 != 0)) return BIGEMM_ERR_ALIGN;
+    const int64_t ldt = round_up(K > 0 ? K : 1, 16);
+    const size_t bt = (static_cast<size_t>(N) * static_cast<size_t>(ldt) + 255) / 256 * 256;
+    const size_t need = bigemm_fp8_kn_workspace_bytes(M, N, K, split_k);
+    if (K > 0 && M > 0 && N > 0 &&
+        (workspace == nullptr || !aligned_to(workspace, 256) || workspace_bytes < need))
+        return BIGEMM_ERR_WORKSPACE;
+    const cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    uint8_t* Bt = static_cast<uint8_t*>(workspace);
+    if (K > 0 && M > 0 && N > 0) {
+        const dim3 g(static_cast<unsigned>(ceil_div(N, kTrTile)), static_cast<unsigned>(ceil_div(ldt, kTrTile)));
+        fp8_transpose_kernel<<<g, kTrThreads, 0, strm>>>(static_cast<const uint8_t*>(B), ldb, Bt, ldt,
+                                                          static_cast<int>(K), static_cast<int>(N));
+        if (cudaGetLastError() != cudaSuccess) return BIGEMM_ERR_CUDA;
+    }
+    unsigned char* ws2 = workspace != nullptr ? static_cast<unsigned char*>(workspace) + bt : nullptr;
+    const size_t ws2_bytes = workspace_bytes > bt ? workspace_bytes - bt : 0;
+    const bigemm_status st = run_impl(c_is_bf16 ? kModeBF16 : kModeF32, A, (K > 0 && M > 0 && N > 0) ? Bt : B, C,
+                                      M, N, K, lda, ldt, ldc, split_k, ws2, ws2_bytes, strm, /*wt=*/true, bias,
+                                      fmt_a, fmt_b, scale);
+    if (st == BIGEMM_OK && K > 0 && M > 0 && N > 0) g_last_launches += 1;
+    return st;
+}
+
 bigemm_status bigemm_run_atomic_splitk(const void* A, const void* B, float* C, int64_t M, int64_t N,
                                        int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int split_k,
                                        bigemm_stream stream) {

@@ -1568,4 +1568,48 @@ __global__ void __launch_bounds__(kReduceThreads)
     }
 }
 
+// Bt[n][k] = B[k][n] for 8-bit operands: B [K, N] (ldb bytes per row) copied
+// K-major into Bt [N, ldt] (ldt a multiple of 16, >= K), the layout the 8-bit
+// tensor-core path reads; columns k in [K, ldt) of Bt are written as zeros.
+// One 64 x 64 byte tile per block through shared memory, 4-byte accesses on
+// both sides (byte accesses at a ragged right edge of B).  A byte copy: the
+// values, and so every product formed from them, are unchanged.
+constexpr int kTrTile = 64;
+constexpr int kTrThreads = 256;
+
+__global__ void __launch_bounds__(kTrThreads)
+    fp8_transpose_kernel(const uint8_t* __restrict__ B, int64_t ldb, uint8_t* __restrict__ Bt, int64_t ldt,
+                         int K, int N) {
+    __shared__ uint8_t tile[kTrTile][kTrTile + 4];
+    const int k0 = static_cast<int>(blockIdx.y) * kTrTile, n0 = static_cast<int>(blockIdx.x) * kTrTile;
+    for (int i = threadIdx.x; i < kTrTile * (kTrTile / 4); i += kTrThreads) {
+        const int r = i / (kTrTile / 4), w = i % (kTrTile / 4);
+        const int k = k0 + r, n = n0 + 4 * w;
+        uint32_t v = 0;
+        if (k < K && n < N) {
+            const uint8_t* src = B + static_cast<int64_t>(k) * ldb + n;
+            if (n + 4 <= N) {
+                v = *reinterpret_cast<const uint32_t*>(src);  // 4-byte aligned: ldb % 16 == 0, n % 4 == 0
+            } else {
+                for (int j = 0; j < N - n; ++j) v |= static_cast<uint32_t>(src[j]) << (8 * j);
+            }
+        }
+        tile[r][4 * w] = static_cast<uint8_t>(v);
+        tile[r][4 * w + 1] = static_cast<uint8_t>(v >> 8);
+        tile[r][4 * w + 2] = static_cast<uint8_t>(v >> 16);
+        tile[r][4 * w + 3] = static_cast<uint8_t>(v >> 24);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kTrTile * (kTrTile / 4); i += kTrThreads) {
+        const int r = i / (kTrTile / 4), w = i % (kTrTile / 4);
+        const int n = n0 + r, k = k0 + 4 * w;
+        if (n < N && k < ldt) {
+            const uint32_t v = static_cast<uint32_t>(tile[4 * w][r]) | (static_cast<uint32_t>(tile[4 * w + 1][r]) << 8) |
+                               (static_cast<uint32_t>(tile[4 * w + 2][r]) << 16) |
+                               (static_cast<uint32_t>(tile[4 * w + 3][r]) << 24);
+            *reinterpret_cast<uint32_t*>(Bt + static_cast<int64_t>(n) * ldt + k) = v;  // ldt % 16 == 0
+        }
+    }
+}
+
 }  // namespace bigemm

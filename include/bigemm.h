@@ -357,6 +357,29 @@ BIGEMM_API bigemm_status bigemm_linear_fp8(const void *A, const void *W, int fmt
                                            void *workspace, size_t workspace_bytes,
                                            bigemm_stream stream);
 
+/* Workspace bytes bigemm_run_fp8 needs: B transposed, N rows of
+ * round_up(K, 16) bytes rounded up to 256, then bigemm_fp8_workspace_bytes.
+ * 0 for invalid arguments. */
+BIGEMM_API size_t bigemm_fp8_kn_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
+
+/* The 8-bit float product with B in the [K, N] layout of bigemm_run:
+ *     C_ij = scale * (sum_{k=0}^{K-1} A_ik * B_kj) + bias_j
+ * B: [K, N] bytes in format fmt_b, ldb >= N a multiple of 16, 16-byte
+ * aligned; everything else as in bigemm_linear_fp8.  The tensor cores read
+ * 8-bit operands K-major, so a first kernel copies B transposed into the
+ * workspace (N rows of round_up(K, 16) bytes, zero past K) and the product
+ * then runs as bigemm_linear_fp8 with W = B^T: the same bits, row i of C a
+ * function of (row i of A, B, formats, scale, bias, K, split_k, output
+ * type).  One launch more than bigemm_linear_fp8 (bigemm_last_launch_count).
+ * Workspace: bigemm_fp8_kn_workspace_bytes, 256-byte aligned. */
+BIGEMM_API bigemm_status bigemm_run_fp8(const void *A, const void *B, int fmt_a, int fmt_b,
+                                        float scale, const void *bias, void *C,
+                                        int64_t M, int64_t N, int64_t K,
+                                        int64_t lda, int64_t ldb, int64_t ldc,
+                                        int split_k, int c_is_bf16,
+                                        void *workspace, size_t workspace_bytes,
+                                        bigemm_stream stream);
+
 /* ------------------------------------------------------------------------
  * Binary64 matrix product by the Ozaki scheme on the bfloat16 tensor cores
  * (cuTile article, "倍精度行列積エミュレーション": "Ozaki Schemeについて",

@@ -127,3 +127,61 @@ def test_fp8_argument_checks():
                                  check=False) == 2
     assert dig.bigemm_fp8_effective_split_k(4096, 8) == 8
     assert dig.bigemm_fp8_effective_split_k(4096, 33) == 0      # 32 blocks of 128
+
+
+@pytest.mark.parametrize("M,N,K,S", [
+    (64, 256, 512, 1),
+    (300, 600, 992, 3),          # ragged rows, columns and K (not a multiple of 128)
+    (7, 45, 96, 1),              # N not a multiple of 4: the transpose's byte edge
+    (1024, 8192, 4096, 4),       # folded split on CTA pairs
+])
+@pytest.mark.parametrize("fa,fb", [(oracle.FMT_E4M3, oracle.FMT_E4M3), (oracle.FMT_E5M2, oracle.FMT_E4M3)])
+def test_fp8_with_b_k_by_n_equals_the_weight_layout(M, N, K, S, fa, fb):
+    """bigemm_run_fp8 takes B [K, N] (copied transposed into the workspace):
+    the bits of bigemm_linear_fp8 with W = B^T, rows computed alone give the
+    same bits, and sampled rows meet the oracle's tolerance."""
+    A, W = fp8_inputs(M, N, K, 61 + M + N, fa, fb)
+    B = W.t().contiguous()                                    # [K, N]
+    b = workloads.normal_bf16((N,), 62).cuda()
+    Ad, Bd, Wd = A.cuda(), B.cuda(), W.cuda()
+    if N % 16:
+        # the [K, N] rows need a 16-byte multiple: pad the leading dimension
+        ldb = round_up(N, 16)
+        Bp = torch.zeros((K, ldb), dtype=torch.uint8, device="cuda")
+        Bp[:, :N] = Bd.view(torch.uint8)
+        Bd = Bp.view(B.dtype)[:, :N]
+    ldc = round_up(N, 4)                                   # fp32 rows: 16-byte multiples
+    out = lambda m: torch.empty((m, ldc), dtype=torch.float32, device="cuda")[:, :N]
+    got = dig.matmul_fp8(Ad, Bd, 0.5, b, split_k=S, out=out(M))
+    assert dig.bigemm_last_launch_count() >= 2             # the transpose, then the product
+    want = dig.linear_fp8(Ad, Wd, 0.5, b, split_k=S, out=out(M))
+    torch.cuda.synchronize()
+    assert bits_equal(got, want)
+    for r in (0, M - 1):
+        one = dig.matmul_fp8(Ad[r:r + 1].contiguous(), Bd, 0.5, b, split_k=S, out=out(1))
+        assert bits_equal(one, got[r:r + 1]), r
+    rows = sorted({0, M // 2, M - 1})
+    Cref, D = oracle.linear8_rows(A, W, fa, fb, M, N, K, 0.5, b.cpu(), rows=rows)
+    check_tolerance(to_f64(got[torch.tensor(rows, device="cuda")]), Cref, D, False, "fp8 B [K, N]")
+
+
+def test_fp8_b_k_by_n_workspace_and_argument_checks():
+    M, N, K = 40, 48, 256
+    up = lambda x: (x + 255) // 256 * 256
+    assert dig.bigemm_fp8_kn_workspace_bytes(M, N, K, 1) == up(N * K)
+    assert dig.bigemm_fp8_kn_workspace_bytes(M, N, 300, 1) == up(N * 304)
+    assert dig.bigemm_fp8_kn_workspace_bytes(M, N, K, 2) == up(N * K) + dig.bigemm_fp8_workspace_bytes(M, N, K, 2)
+    a = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
+    bmat = torch.zeros((K, N), dtype=torch.uint8, device="cuda")
+    c = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    # no workspace (WORKSPACE), a bad format and ldb < N (ARG), ldb not a
+    # multiple of 16 (ALIGN); nothing is launched
+    assert dig.bigemm_run_fp8(a, bmat, 0, 0, 1.0, None, c, M, N, K, K, N, N, 1, 0, None, 0,
+                              check=False) == 3
+    assert dig.bigemm_run_fp8(a, bmat, 2, 0, 1.0, None, c, M, N, K, K, N, N, 1, 0, None, 0,
+                              check=False) == 1
+    assert dig.bigemm_run_fp8(a, bmat, 0, 0, 1.0, None, c, M, N, K, K, N - 8, N, 1, 0, None, 0,
+                              check=False) == 1
+    assert dig.bigemm_run_fp8(a, bmat, 0, 0, 1.0, None, c, M, N, K, K, N + 8, N, 1, 0, None, 0,
+                              check=False) == 2
+    assert dig.bigemm_last_launch_count() == 0
