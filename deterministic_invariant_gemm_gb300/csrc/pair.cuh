@@ -1,5 +1,7 @@
 // pair.cuh -- the 2-SM product: one 256 x 256 output tile per CTA pair,
-// computed by tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16).
+// computed by tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16 for bf16,
+// 32 for 8-bit floats): unsplit and folded split-K products, and the Ozaki
+// scheme's slice-pair products.
 //
 // The two CTAs of a thread-block cluster of 2 form the pair.  CTA r (r = 0,
 // 1) loads rows 128 r .. 128 r + 127 of the tile's A panel and columns
@@ -11,7 +13,8 @@
 // work, and six stages instead of four.
 //
 // Every output element is still one FP32 accumulation chain over the K
-// blocks in ascending order, 16 k per instruction, as in the 1-SM kernel;
+// blocks in ascending order, 16 (or 32) k per instruction, as in the 1-SM
+// kernel;
 // the GPU tests check that both give the same bits (rows of a 2-SM product
 // against the same rows from the 1-SM kernel and from one-row products).
 // (Tencent AI-infra article "腾讯エンジニア：大規模モデルの出力を確定させるため

@@ -160,6 +160,28 @@ def test_fp8_linear_equals_the_1sm_kernel(M, N, K, S, fa, fb, bf16_out):
         assert bits_equal(one, pair[r:r + 1]), r
 
 
+@pytest.mark.parametrize("bf16_out", [False, True])
+def test_folded_linear_with_bias_equals_the_1sm_fold(bf16_out):
+    """A folded split of the weight layout with a bias on pairs (the bias added
+    once after the 0..S-1 sum): the 1-SM fold's bits and the rows alone."""
+    M, N, K, S = 512, 33024, 2048, 4
+    A = workloads.normal_bf16((M, K), 201).cuda()
+    W = workloads.normal_bf16((N, K), 202, 0.02).cuda()
+    b = workloads.normal_bf16((N,), 203).cuda()
+    dt = torch.bfloat16 if bf16_out else torch.float32
+    assert dig.bigemm_split_is_folded(M, N, K, S)
+    dig.bigemm_set_pair_mode(dig.PAIR_ALWAYS)
+    assert dig.bigemm_uses_pair(M, N, K, S) == 1
+    pair = dig.linear(A, W, b, out_dtype=dt, split_k=S)
+    dig.bigemm_set_pair_mode(dig.PAIR_NEVER)
+    single = dig.linear(A, W, b, out_dtype=dt, split_k=S)
+    torch.cuda.synchronize()
+    assert bits_equal(pair, single)
+    for r in (0, 255, 256, M - 1):
+        one = dig.linear(A[r:r + 1].contiguous(), W, b, out_dtype=dt, split_k=S)
+        assert bits_equal(one, pair[r:r + 1]), r
+
+
 @pytest.mark.parametrize("M,N,K", [(256, 512, 1024), (520, 6144, 4096), (768, 1280, 1984)])
 @pytest.mark.parametrize("bf16_out", [False, True])
 def test_linear_with_bias_equals_the_1sm_kernel(M, N, K, bf16_out):
