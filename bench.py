@@ -23,7 +23,7 @@ Also reported (N = 1, rank 0):
   cpu_baseline    the CPU oracle (binary64 triple loop) on one product per M.
   workloads       the other shapes in brief: squares (tensor-core bound), long
                   K, the small product, linear layers, the Ozaki products;
-                  the full record goes to gpurun_out/bench_detail.json.
+                  the full record goes to a side file, bench_detail.json.
   roofline_tensor the 16384^3 product against the dense BF16 peak, with the
                   SM clock sampled during its own timed region.
   clocks          SM clock and throttle reasons sampled during the timed region.
@@ -1016,7 +1016,7 @@ def cpu_baseline(budget_s: float = 10.0) -> dict:
 
 
 def cpu_baseline_configs() -> dict:
-    """The oracle on the other workloads, as SURVEY-style per-config context:
+    """The oracle on the other workloads, as per-config context:
     the small product and long K in full, the squares on a 256-row sample of
     A (every column of C; the full-size time extrapolated by rows).  The
     oracle also forms D = sum |a b| for the tolerance, so it does twice the
