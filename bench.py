@@ -871,14 +871,16 @@ def run_other_workloads(dev, peaks) -> dict:
     import deterministic_invariant_gemm_gb300 as dig
     out = {}
     bf16_peak = peaks["bf16_tflops"]
-    cases = [("square_2048", 2048, 2048, 2048, 1, False, "uniform", 20),
-             ("square_4096", 4096, 4096, 4096, 1, False, "uniform", 10),
+    # (calls per timed region: a few milliseconds of back-to-back products, so
+    # that the region's first launch latency is not a visible share)
+    cases = [("square_2048", 2048, 2048, 2048, 1, False, "uniform", 300),
+             ("square_4096", 4096, 4096, 4096, 1, False, "uniform", 60),
              ("square_8192", 8192, 8192, 8192, 1, False, "uniform", 10),
              ("large_16384_bf16out", 16384, 16384, 16384, 1, True, "normal", 5),
              # split products large enough to fold their segments in the CTA
-             ("square_4096_split8_folded", 4096, 4096, 4096, 8, False, "uniform", 10),
+             ("square_4096_split8_folded", 4096, 4096, 4096, 8, False, "uniform", 60),
              ("square_8192_split16_folded", 8192, 8192, 8192, 16, False, "uniform", 10),
-             ("prefill_1024x4096x4096_split8_folded", 1024, 4096, 4096, 8, False, "normal", 20)]
+             ("prefill_1024x4096x4096_split8_folded", 1024, 4096, 4096, 8, False, "normal", 200)]
     for name, M, N, K, S, bf16, dist_name, iters in cases:
         in_bytes = 2 * (M * K + K * N)
         copies = max(1, min(8, math.ceil(2 * L2_BYTES / in_bytes)))
