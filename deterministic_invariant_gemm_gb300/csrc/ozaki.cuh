@@ -90,14 +90,106 @@ __device__ __forceinline__ float ozaki_unit(int rho) {
     return __int_as_float((127 + rho - 53) << 23);  // 2^(rho - 53), exact in binary32
 }
 
+// The same Q_p through one window per element.  |R| is shifted once so that
+// slice 0's unit sits at bit 96 of a 128-bit word W = |R| 2^(96 - s_0) (held
+// as four 32-bit words); slice p's unit is then bit pos = 96 - p (beta + 1)
+// for every element, and
+//   Q_p = floor(W / 2^pos) + [bit pos-1 of W] * ([W has a 1 below bit pos-1]
+//                                                 or floor(W / 2^pos) odd),
+// round-half-even, with "a 1 below" read off W's trailing zero count.  RNE is
+// odd-symmetric, so the slices of -|R| are the negated slices of |R|.  Exact
+// when no bit of |R| falls below the window (s_0 <= 96) -- the element is
+// not far below the vector's maximum -- and every slice's unit lies in it
+// ((slices - 1)(beta + 1) <= 95); ozaki_window returns false otherwise and
+// the caller keeps the per-slice rounding above.  One variable shift per
+// element instead of one 64-bit rounding per slice.
+struct OzakiWindow {
+    uint32_t w0, w1, w2, w3;  // W, least significant word first
+    int tz;                   // trailing zeros of W (a large value for W = 0)
+    bool neg;
+};
+
+__device__ __forceinline__ bool ozaki_window(double x, int c1, int rho, OzakiWindow& W) {
+    const uint64_t bits = static_cast<uint64_t>(__double_as_longlong(x));
+    const int eb = static_cast<int>((bits >> 52) & 0x7FF);
+    const uint64_t U = (bits & ((1ull << 52) - 1)) | (eb != 0 ? (1ull << 52) : 0ull);
+    const int E = eb != 0 ? eb - 1075 : -1074;
+    const int k = 96 - (c1 + rho - 53 - E);  // W = U 2^k; k <= 96 + beta when |x| <= 2^c1
+    if (k < 0 || k > 104) return false;
+    uint64_t lo, hi;
+    if (k >= 64) {
+        lo = 0;
+        hi = U << (k - 64);
+    } else if (k > 0) {
+        lo = U << k;
+        hi = U >> (64 - k);
+    } else {
+        lo = U;
+        hi = 0;
+    }
+    W.w0 = static_cast<uint32_t>(lo);
+    W.w1 = static_cast<uint32_t>(lo >> 32);
+    W.w2 = static_cast<uint32_t>(hi);
+    W.w3 = static_cast<uint32_t>(hi >> 32);
+    W.tz = lo != 0 ? __ffsll(static_cast<long long>(lo)) - 1
+                   : (hi != 0 ? 63 + __ffsll(static_cast<long long>(hi)) : (1 << 20));
+    W.neg = (bits >> 63) != 0;
+    return true;
+}
+
+// Low 32 bits of Q_p for the slice whose unit is bit pos (1 .. 96) of W.
+__device__ __forceinline__ uint32_t ozaki_window_q(const OzakiWindow& W, int pos) {
+    uint32_t a, h;
+    if (pos >= 64) {
+        a = __funnelshift_rc(W.w2, W.w3, pos - 64);
+        h = pos > 64 ? (W.w2 >> (pos - 65)) : (W.w1 >> 31);
+    } else if (pos >= 32) {
+        a = __funnelshift_rc(W.w1, W.w2, pos - 32);
+        h = pos > 32 ? (W.w1 >> (pos - 33)) : (W.w0 >> 31);
+    } else {
+        a = __funnelshift_r(W.w0, W.w1, pos);
+        h = W.w0 >> (pos - 1);
+    }
+    return a + (h & 1u & ((W.tz < pos - 1 ? 1u : 0u) | a));
+}
+
+// Slice p of two adjacent elements: out[p * plane] and out[p * plane + 1],
+// one 4-byte store when `paired`.
+__device__ __forceinline__ void ozaki_store_two(__nv_bfloat16* out, int64_t plane, int p, int na, int nb,
+                                                float unit, bool paired) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(ozaki_slice_value(na, unit), ozaki_slice_value(nb, unit));
+    __nv_bfloat16* o = out + p * plane;
+    if (paired) {
+        *reinterpret_cast<__nv_bfloat162*>(o) = v;
+    } else {
+        o[0] = __low2bfloat16(v);
+        o[1] = __high2bfloat16(v);
+    }
+}
+
 // Splits two adjacent elements (vector exponents c1a, c1b) into `slices`
 // slices each; slice p of the pair goes to out[p * plane] and out[p * plane
 // + 1], as one 4-byte store when `paired`.  Every value is a bfloat16 exactly.
+// Both elements through their windows when both fit, else both through the
+// per-slice rounding (the same n_p either way).
 __device__ __forceinline__ void ozaki_split_two(double xa, double xb, int c1a, int c1b, int rho,
                                                 int slices, __nv_bfloat16* out, int64_t plane,
                                                 bool paired) {
     const int w = 54 - rho;  // beta + 1
     const float unit = ozaki_unit(rho);
+    OzakiWindow wa, wb;
+    if ((slices - 1) * w <= 95 && ozaki_window(xa, c1a, rho, wa) && ozaki_window(xb, c1b, rho, wb)) {
+        uint32_t pa = 0, pb = 0;
+        for (int p = 0; p < slices; ++p) {
+            const int pos = 96 - p * w;
+            const uint32_t qa = ozaki_window_q(wa, pos), qb = ozaki_window_q(wb, pos);
+            const int na = static_cast<int>(qa - (pa << w)), nb = static_cast<int>(qb - (pb << w));
+            pa = qa;
+            pb = qb;
+            ozaki_store_two(out, plane, p, wa.neg ? -na : na, wb.neg ? -nb : nb, unit, paired);
+        }
+        return;
+    }
     const OzakiElem a = ozaki_elem(xa), b = ozaki_elem(xb);
     int sa = c1a + rho - 53 - a.E, sb = c1b + rho - 53 - b.E;
     uint32_t pa = 0, pb = 0;
@@ -106,15 +198,7 @@ __device__ __forceinline__ void ozaki_split_two(double xa, double xb, int c1a, i
         const int na = static_cast<int>(qa - (pa << w)), nb = static_cast<int>(qb - (pb << w));
         pa = qa;
         pb = qb;
-        const __nv_bfloat162 v =
-            __floats2bfloat162_rn(ozaki_slice_value(na, unit), ozaki_slice_value(nb, unit));
-        __nv_bfloat16* o = out + p * plane;
-        if (paired) {
-            *reinterpret_cast<__nv_bfloat162*>(o) = v;
-        } else {
-            o[0] = __low2bfloat16(v);
-            o[1] = __high2bfloat16(v);
-        }
+        ozaki_store_two(out, plane, p, na, nb, unit, paired);
     }
 }
 
@@ -152,15 +236,18 @@ __device__ __forceinline__ unsigned long long ozaki_mass_term(double x, int c1) 
 // kOzakiRowCache; the block finds the row's maximum (integer max of the
 // magnitude bit patterns: exact and order-free), stores c^(1) in exps[row],
 // and splits the row into out[p * plane + row * out_ld + k]; with `mass`
-// not NULL it also stores the row's Fast Mode mass in mass[row].
+// not NULL it also stores the row's Fast Mode mass in mass[row].  A cache
+// of 16 elements (rows up to 4096 read once) keeps three blocks per SM
+// resident: at 4096 x 4096 the kernel took 187 us against 236 us with 32
+// elements and two blocks.
 constexpr int kOzakiRowThreads = 256;
-constexpr int kOzakiRowCache = 32;  // elements per thread kept in registers
+constexpr int kOzakiRowCache = 16;  // elements per thread kept in registers
 
 __device__ __forceinline__ uint64_t ozaki_abs_bits(double x) {
     return static_cast<uint64_t>(__double_as_longlong(x)) & 0x7FFFFFFFFFFFFFFFull;
 }
 
-__global__ void __launch_bounds__(kOzakiRowThreads)
+__global__ void __launch_bounds__(kOzakiRowThreads, 3)
     ozaki_split_rows_kernel(const double* __restrict__ X, int64_t rows, int64_t cols, int64_t ld,
                             int rho, int slices, __nv_bfloat16* __restrict__ out, int64_t out_ld,
                             int64_t plane, int* __restrict__ exps, unsigned long long* __restrict__ mass) {

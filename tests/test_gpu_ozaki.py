@@ -78,7 +78,7 @@ def test_split_rounding_ties_match_the_oracle(axis):
     between two multiples of a slice's unit, where the split rounds to the
     even neighbour: the GPU's slices must still equal the oracle's bit for
     bit, on a row long enough to take the register-cached and the re-read
-    parts of the row kernel (9000 > 8192 columns) and an odd column count."""
+    parts of the row kernel (9000 > 4096 columns) and an odd column count."""
     g = workloads.generator(515)
     rows, cols = (6, 9001) if axis == 0 else (9001, 6)
     X = torch.randint(-1000, 1001, (rows, cols), generator=g).double()
