@@ -934,6 +934,18 @@ int ceil_log2_int(int64_t v) {
 
 bool aligned_to(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
+// The split kernels specialised for the slice width 54 - rho and count that
+// the default slice counts pair with it (1..5), else 0: the general kernels.
+int ozaki_split_shape(int rho, int slices) {
+    const int w = 54 - rho;
+    if (w == 9 && slices == 6) return 1;
+    if (w == 8 && slices == 7) return 2;
+    if (w == 7 && slices == 8) return 3;
+    if (w == 6 && slices == 9) return 4;
+    if (w == 5 && slices == 11) return 5;
+    return 0;
+}
+
 // mass: Fast Mode's vector masses (zeroed here for the columns), or nullptr.
 cudaError_t launch_ozaki_split(const DeviceInfo& d, const double* X, int64_t rows, int64_t cols,
                                int64_t ld, int axis, int rho, int slices, __nv_bfloat16* out,
@@ -943,8 +955,16 @@ cudaError_t launch_ozaki_split(const DeviceInfo& d, const double* X, int64_t row
         // one block per row, at most 16 resident blocks' worth per SM at a time
         int64_t blocks = rows;
         if (blocks > 16 * static_cast<int64_t>(d.sm_count)) blocks = 16 * static_cast<int64_t>(d.sm_count);
-        ozaki_split_rows_kernel<<<static_cast<unsigned>(blocks), kOzakiRowThreads, 0, stream>>>(
-            X, rows, cols, ld, rho, slices, out, out_ld, rows * out_ld, exps, mass);
+        const dim3 g(static_cast<unsigned>(blocks)), blk(kOzakiRowThreads);
+        const int64_t plane = rows * out_ld;
+        switch (ozaki_split_shape(rho, slices)) {
+        case 1: ozaki_split_rows_kernel<9, 6><<<g, blk, 0, stream>>>(X, rows, cols, ld, rho, slices, out, out_ld, plane, exps, mass); break;
+        case 2: ozaki_split_rows_kernel<8, 7><<<g, blk, 0, stream>>>(X, rows, cols, ld, rho, slices, out, out_ld, plane, exps, mass); break;
+        case 3: ozaki_split_rows_kernel<7, 8><<<g, blk, 0, stream>>>(X, rows, cols, ld, rho, slices, out, out_ld, plane, exps, mass); break;
+        case 4: ozaki_split_rows_kernel<6, 9><<<g, blk, 0, stream>>>(X, rows, cols, ld, rho, slices, out, out_ld, plane, exps, mass); break;
+        case 5: ozaki_split_rows_kernel<5, 11><<<g, blk, 0, stream>>>(X, rows, cols, ld, rho, slices, out, out_ld, plane, exps, mass); break;
+        default: ozaki_split_rows_kernel<><<<g, blk, 0, stream>>>(X, rows, cols, ld, rho, slices, out, out_ld, plane, exps, mass);
+        }
         return cudaGetLastError();
     }
     // column maxima: every exponent starts below any c^(1), then chunks of
@@ -969,8 +989,16 @@ cudaError_t launch_ozaki_split(const DeviceInfo& d, const double* X, int64_t row
     if (by > out_rows) by = out_rows;
     if (by > 65535) by = 65535;
     if (by < 1) by = 1;
-    ozaki_split_cols_kernel<<<dim3(static_cast<unsigned>(bx), static_cast<unsigned>(by)), 256, 0, stream>>>(
-        X, rows, cols, ld, out_rows, rho, slices, out, out_ld, out_rows * out_ld, exps, mass);
+    const dim3 g(static_cast<unsigned>(bx), static_cast<unsigned>(by));
+    const int64_t plane = out_rows * out_ld;
+    switch (ozaki_split_shape(rho, slices)) {
+    case 1: ozaki_split_cols_kernel<9, 6><<<g, 256, 0, stream>>>(X, rows, cols, ld, out_rows, rho, slices, out, out_ld, plane, exps, mass); break;
+    case 2: ozaki_split_cols_kernel<8, 7><<<g, 256, 0, stream>>>(X, rows, cols, ld, out_rows, rho, slices, out, out_ld, plane, exps, mass); break;
+    case 3: ozaki_split_cols_kernel<7, 8><<<g, 256, 0, stream>>>(X, rows, cols, ld, out_rows, rho, slices, out, out_ld, plane, exps, mass); break;
+    case 4: ozaki_split_cols_kernel<6, 9><<<g, 256, 0, stream>>>(X, rows, cols, ld, out_rows, rho, slices, out, out_ld, plane, exps, mass); break;
+    case 5: ozaki_split_cols_kernel<5, 11><<<g, 256, 0, stream>>>(X, rows, cols, ld, out_rows, rho, slices, out, out_ld, plane, exps, mass); break;
+    default: ozaki_split_cols_kernel<><<<g, 256, 0, stream>>>(X, rows, cols, ld, out_rows, rho, slices, out, out_ld, plane, exps, mass);
+    }
     return cudaGetLastError();
 }
 

@@ -202,6 +202,40 @@ __device__ __forceinline__ void ozaki_split_two(double xa, double xb, int c1a, i
     }
 }
 
+// ozaki_split_two for the slice width kW = beta + 1 = 54 - rho and slice
+// count kS fixed at compile time (the common (K, slices) choices): the loop
+// over slices unrolls and every window position is a constant.
+template <int kW, int kS>
+__device__ __forceinline__ void ozaki_split_two_fixed(double xa, double xb, int c1a, int c1b, int rho,
+                                                      __nv_bfloat16* out, int64_t plane, bool paired) {
+    static_assert(kW >= 1 && kS >= 1 && (kS - 1) * kW <= 95, "every slice's unit inside the window");
+    OzakiWindow wa, wb;
+    if (ozaki_window(xa, c1a, rho, wa) && ozaki_window(xb, c1b, rho, wb)) {
+        const float unit = ozaki_unit(rho);
+        uint32_t pa = 0, pb = 0;
+#pragma unroll
+        for (int p = 0; p < kS; ++p) {
+            const uint32_t qa = ozaki_window_q(wa, 96 - p * kW), qb = ozaki_window_q(wb, 96 - p * kW);
+            const int na = static_cast<int>(qa - (pa << kW)), nb = static_cast<int>(qb - (pb << kW));
+            pa = qa;
+            pb = qb;
+            ozaki_store_two(out, plane, p, wa.neg ? -na : na, wb.neg ? -nb : nb, unit, paired);
+        }
+        return;
+    }
+    ozaki_split_two(xa, xb, c1a, c1b, rho, kS, out, plane, paired);
+}
+
+// kW = 0: the slice width and count from rho and slices at run time.
+template <int kW, int kS>
+__device__ __forceinline__ void ozaki_split_two_as(double xa, double xb, int c1a, int c1b, int rho, int slices,
+                                                   __nv_bfloat16* out, int64_t plane, bool paired) {
+    if constexpr (kW > 0)
+        ozaki_split_two_fixed<kW, kS>(xa, xb, c1a, c1b, rho, out, plane, paired);
+    else
+        ozaki_split_two(xa, xb, c1a, c1b, rho, slices, out, plane, paired);
+}
+
 // One element alone (an odd vector's last element).
 __device__ __forceinline__ void ozaki_split_one(double x, int c1, int rho, int slices,
                                                 __nv_bfloat16* out, int64_t plane) {
@@ -239,7 +273,7 @@ __device__ __forceinline__ unsigned long long ozaki_mass_term(double x, int c1) 
 // not NULL it also stores the row's Fast Mode mass in mass[row].  A cache
 // of 16 elements (rows up to 4096 read once) keeps three blocks per SM
 // resident: at 4096 x 4096 the kernel took 187 us against 236 us with 32
-// elements and two blocks.
+// elements and two blocks, and 128 us with the slice shape fixed (kW, kS).
 constexpr int kOzakiRowThreads = 256;
 constexpr int kOzakiRowCache = 16;  // elements per thread kept in registers
 
@@ -247,6 +281,7 @@ __device__ __forceinline__ uint64_t ozaki_abs_bits(double x) {
     return static_cast<uint64_t>(__double_as_longlong(x)) & 0x7FFFFFFFFFFFFFFFull;
 }
 
+template <int kW = 0, int kS = 0>
 __global__ void __launch_bounds__(kOzakiRowThreads, 3)
     ozaki_split_rows_kernel(const double* __restrict__ X, int64_t rows, int64_t cols, int64_t ld,
                             int rho, int slices, __nv_bfloat16* __restrict__ out, int64_t out_ld,
@@ -308,12 +343,13 @@ __global__ void __launch_bounds__(kOzakiRowThreads, 3)
         for (int i = 0; i < kOzakiRowCache / 2; ++i) {
             const int64_t pr = tid + static_cast<int64_t>(i) * kOzakiRowThreads;
             if (pr < pairs)
-                ozaki_split_two(cache[2 * i], cache[2 * i + 1], c1, c1, rho, slices, orow + 2 * pr, plane,
+                ozaki_split_two_as<kW, kS>(cache[2 * i], cache[2 * i + 1], c1, c1, rho, slices, orow + 2 * pr, plane,
                                 paired);
         }
         for (int64_t pr = tid + static_cast<int64_t>(kOzakiRowCache / 2) * kOzakiRowThreads; pr < pairs;
              pr += kOzakiRowThreads)
-            ozaki_split_two(x[2 * pr], x[2 * pr + 1], c1, c1, rho, slices, orow + 2 * pr, plane, paired);
+            ozaki_split_two_as<kW, kS>(x[2 * pr], x[2 * pr + 1], c1, c1, rho, slices, orow + 2 * pr, plane,
+                                       paired);
         if ((cols & 1) && tid == 0) ozaki_split_one(x[cols - 1], c1, rho, slices, orow + cols - 1, plane);
     }
 }
@@ -359,6 +395,7 @@ __global__ void __launch_bounds__(256)
 // turn an all-zero column's kOzakiNoExp into its c^(1) = 0.  With `mass` not
 // NULL (zero beforehand) every thread adds its rows' Fast Mode mass terms
 // into mass[j] with one integer atomic addition per column: order-free.
+template <int kW = 0, int kS = 0>
 __global__ void __launch_bounds__(256)
     ozaki_split_cols_kernel(const double* __restrict__ X, int64_t rows, int64_t cols, int64_t ld,
                             int64_t out_rows, int rho, int slices, __nv_bfloat16* __restrict__ out,
@@ -382,7 +419,7 @@ __global__ void __launch_bounds__(256)
         if (two) {
             const double xa = r < rows ? X[r * ld + j] : 0.0;
             const double xb = r < rows ? X[r * ld + j + 1] : 0.0;
-            ozaki_split_two(xa, xb, ea, eb, rho, slices, o, plane, paired);
+            ozaki_split_two_as<kW, kS>(xa, xb, ea, eb, rho, slices, o, plane, paired);
             if (mass != nullptr) {
                 ta += ozaki_mass_term(xa, ea);
                 tb += ozaki_mass_term(xb, eb);

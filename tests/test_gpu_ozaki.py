@@ -49,7 +49,14 @@ def gpu_split(X, axis, rho, slices, out_rows=None):
 
 
 @pytest.mark.parametrize("axis", [0, 1])
-@pytest.mark.parametrize("rows,cols,K", [(37, 300, 300), (300, 37, 4096), (5, 8, 1 << 20)])
+@pytest.mark.parametrize("rows,cols,K", [
+    (37, 300, 256),      # rho 45: 6 slices of width 9 (the split kernels' fixed shapes)
+    (70, 64, 512),       # rho 46: 7 x 8
+    (300, 37, 4096),     # rho 47: 8 x 7
+    (64, 70, 8192),      # rho 48: 9 x 6
+    (40, 33, 65536),     # rho 49: 11 x 5
+    (5, 8, 1 << 20),     # rho 51: 18 slices, the general kernels
+])
 def test_split_matches_the_oracle_bit_for_bit(axis, rows, cols, K):
     X = wide((rows, cols), rows * cols + axis)
     X[0, 0] = -0.0
