@@ -1461,20 +1461,22 @@ static bigemm_status ozaki_dgemm_impl(const double* A, const double* B, double* 
     p.oz_ta = ta;
     p.oz_tb = tb;
     p.oz_need0 = 134 + ceil_log2_int(slices) + ceil_log2_int(K);
+    p.oz_c32 = (aligned_to(C, 32) && ldc % 4 == 0) ? 1 : 0;
     p.a_rows = kBM;
     // On CTA pairs: the same items over 256-row tiles, each CTA adding its 128
     // rows under the count of its 128 x 256 tile; a cooperative launch of
     // clusters of two.  The rule (pair mode 1): the (slice pair, tile) items
-    // fill two waves of pairs and K is at most 4096.  Measured at 4096^3 the
-    // pairs take 4 % less time; at 8192^3 14 % more -- there the binary64
-    // read-add-write of C, not the loads, paces each item, and a pair waits
-    // for the slower of its two CTAs.
+    // fill two waves of pairs and K is below 4096.  Measured with 32-byte C
+    // accesses in the epilogue: pairs 2-3 % faster at 2048^3 and 3072^3, 6 %
+    // slower at 4096^3, 13 % at 6144^3 and 3 % at 8192^3 -- with the shorter
+    // products the loads pace an item, with the longer ones the binary64
+    // read-add-write of C, and a pair waits for the slower of its two CTAs.
     {
         const int mode = g_pair_mode.load(std::memory_order_relaxed);
         const int64_t pm_tiles = ceil_div(M, kPairBM);
         const int64_t pitems = pm_tiles * n_tiles * pairs;
         if (mode != 0 && M >= kPairBM && dev->pair_clusters > 0 &&
-            (mode == 2 || (pitems >= 2 * static_cast<int64_t>(dev->pair_clusters) && K <= 4096))) {
+            (mode == 2 || (pitems >= 2 * static_cast<int64_t>(dev->pair_clusters) && K < 4096))) {
             GemmParams q = p;
             q.m_tiles = static_cast<int>(pm_tiles);
             q.units = static_cast<int>(pm_tiles * n_tiles);

@@ -198,6 +198,7 @@ struct GemmParams {
     const unsigned long long* oz_ta;  // mass of every row of A
     const unsigned long long* oz_tb;  // mass of every column of B
     int oz_fast, oz_need0;
+    int oz_c32;             // 1: C and its row stride are 32-byte aligned (wide C accesses)
     int selftest_stall;     // 1 (the failure self-test only): the producer issues no
                             //    loads, so the MMA issuer's bounded wait must give up
     int a_rows;             // rows of A each stage loads (32, 64 or 128: the batch
@@ -686,7 +687,7 @@ __device__ __forceinline__ bool ozaki_takes(const OzakiFastRow& f, int j) {
 
 __device__ __forceinline__ void ozaki_accumulate_block(double* crow, const int* cb, int valid,
                                                        int e_pair, const uint32_t (&r)[32],
-                                                       bool first, const OzakiFastRow& fast) {
+                                                       bool first, const OzakiFastRow& fast, bool c32) {
     if (valid == 32) {
         // all loads first (C and the column exponents), then the arithmetic,
         // then the stores: 32 independent memory operations in flight
@@ -703,6 +704,12 @@ __device__ __forceinline__ void ozaki_accumulate_block(double* crow, const int* 
         if (first) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) c[j] = make_double2(0.0, 0.0);
+        } else if (c32) {
+            // 32 bytes per lane and instruction: a whole sector, half the
+            // instructions (each lane's row is another line)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                ld_global_v4f64(crow + 4 * j, c[2 * j].x, c[2 * j].y, c[2 * j + 1].x, c[2 * j + 1].y);
         } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j) c[j] = *reinterpret_cast<const double2*>(crow + 2 * j);
@@ -739,8 +746,14 @@ __device__ __forceinline__ void ozaki_accumulate_block(double* crow, const int* 
                 if (ozaki_takes(fast, 2 * j + 1)) c[j].y = ozaki_term(c[j].y, r[2 * j + 1], e[2 * j + 1]);
             }
         }
+        if (c32) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) *reinterpret_cast<double2*>(crow + 2 * j) = c[j];
+            for (int j = 0; j < 8; ++j)
+                st_global_v4f64(crow + 4 * j, c[2 * j].x, c[2 * j].y, c[2 * j + 1].x, c[2 * j + 1].y);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) *reinterpret_cast<double2*>(crow + 2 * j) = c[j];
+        }
     } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
@@ -1284,7 +1297,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             else if (row_ok && col0 < p.N)
                                 ozaki_accumulate_block(C + static_cast<int64_t>(row) * p.ld_out + col0,
                                                        p.oz_cb + col0, min(32, p.N - col0), e_pair, r,
-                                                       pair == 0, fast);
+                                                       pair == 0, fast, p.oz_c32 != 0);
                         }
                     } else {
                         tc_fence_before();

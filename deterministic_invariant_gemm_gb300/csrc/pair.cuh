@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                 reinterpret_cast<double*>(smem_raw + (sOut - base)) + (q * 2 + h) * 512, lane);
                         else if (row_ok && col0 < p.N)
                             ozaki_accumulate_block(C + static_cast<int64_t>(row) * p.ld_out + col0, p.oz_cb + col0,
-                                                   min(32, p.N - col0), e_pair, r, pair == 0, fast);
+                                                   min(32, p.N - col0), e_pair, r, pair == 0, fast, p.oz_c32 != 0);
                     }
                 } else {
                     release_acc(acc);

@@ -47,6 +47,21 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 // A 32-bit global load with acquire semantics at GPU scope: the writes that
 // the releasing thread made before its matching store or atomic are visible
 // to this thread's later reads.
+// 32-byte global accesses (one sector per lane): four binary64 values at a
+// 32-byte-aligned address.  Volatile, so that they stay after an acquire
+// load and before a release fence issued as inline PTX around them.
+__device__ __forceinline__ void ld_global_v4f64(const double* p, double& a, double& b, double& c, double& d) {
+    asm volatile("ld.global.v4.f64 {%0, %1, %2, %3}, [%4];"
+                 : "=d"(a), "=d"(b), "=d"(c), "=d"(d)
+                 : "l"(p)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_global_v4f64(double* p, double a, double b, double c, double d) {
+    asm volatile("st.global.v4.f64 [%0], {%1, %2, %3, %4};" ::"l"(p), "d"(a), "d"(b), "d"(c), "d"(d)
+                 : "memory");
+}
+
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

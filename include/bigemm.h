@@ -460,7 +460,7 @@ BIGEMM_API bigemm_status bigemm_ozaki_split(const double *X, int64_t rows, int64
  * the pairs of one tile may run on different SMs at once; each element of C
  * still takes its pairs' terms one after another in the fixed pair order (a
  * tile's epilogue waits, bounded, for its count to show the previous pair).
- * With at least 256 rows and K <= 4096 (and enough items for two waves) the
+ * With at least 256 rows and K < 4096 (and enough items for two waves) the
  * products run on CTA pairs (256 x 256 tiles, tcgen05.mma.cta_group::2; see
  * bigemm_uses_pair and bigemm_set_pair_mode), each CTA adding its 128 rows
  * under its 128 x 256 tile's count -- the same additions in the same order.
